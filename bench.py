@@ -1,0 +1,517 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode-attention step on GB300.
+
+Workload (multi-stream paged decode): 4 streams with cached lengths
+{1000, 3000, 6000, 9000}, shuffled through one arena by random permutation
+page tables; 16 query / 2 KV heads of 256, indexer keys of 128; one new
+token per stream is stored, then its query attends the stream's keys
+(split-KV partials and their combine).  A step runs 13 layer slots (the
+pages' Flash Next pool: 12 attention layers plus the MTP head's cache) at
+each swept page size {16, 48, 128, 256, 512}; each page size's 13 layers
+stream ~506 MB of K/V, well above the 129 MB L2, so no flush is needed.
+The same streams in contiguous buffers are timed beside it for the
+paged/contiguous ratio.
+
+Metric: algorithmic HBM bytes / device time, in GB/s, and query-heads/s.
+`--impl reference` times the CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from paged_kv_cache_pg_gb300 import synth  # noqa: E402
+
+METRIC = ("paged decode attn HBM GB/s (% of peak) & query-heads/s at 9k ctx; "
+          "paged/contig ratio")
+LENS = [1000, 3000, 6000, 9000]          # cached before the new token
+N_LAYERS, HQ, HKV, D, DI = 13, 16, 2, 256, 128
+PAGES = [16, 48, 128, 256, 512]
+NOMINAL_HBM = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def config_desc():
+    return {"workload": "multi-stream paged decode", "streams": len(LENS),
+            "cached_lengths": LENS, "new_tokens_per_stream": 1, "layers": N_LAYERS,
+            "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "idx_dim": DI,
+            "page_sizes": PAGES, "tables": "random permutations of one arena",
+            "l2": "inputs larger than L2 (about 506 MB of K/V per page size per step)",
+            "step": "13 layer slots x (store new token + split-KV decode + combine) at every page size"}
+
+
+# ---- accounting ------------------------------------------------------------------
+
+def layer_bytes(lens_after, n_pages_used):
+    """Algorithmic HBM bytes of one layer's store + decode for the batch."""
+    kv = sum(lens_after) * HKV * D * 2 * 2          # every K and V row read once
+    qo = len(lens_after) * HQ * D * 2 * 2           # queries read, outputs written
+    store = len(lens_after) * (2 * HKV * D + DI) * 2 * 2  # new rows read and written
+    tables = n_pages_used * 4
+    return kv + qo + store + tables
+
+
+def decode_bytes(lens_after):
+    """Bytes one decode call must move: K/V rows, queries, outputs."""
+    return sum(lens_after) * HKV * D * 2 * 2 + len(lens_after) * HQ * D * 2 * 2
+
+
+def row_credit_bytes(length):
+    """Algorithmic bytes credited to one (stream, query head) row: its share of
+    the stream's K/V read (the G heads of a KV head share each row)."""
+    return length * HKV * D * 2 * 2 / HQ
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---- clocks ----------------------------------------------------------------------
+
+class Clocks:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- distributed -------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- the CPU oracle (baseline and reference arm) ------------------------------------
+
+def oracle_rows(seconds: float, max_rows: int = 1 << 30):
+    """Time oracle rows of the workload's layer 0 round-robin over (stream, head)
+    until `seconds` pass; returns (credited bytes, rows, elapsed, sample)."""
+    import oracle as orc
+    orc.build()
+    shape = orc.Shape(1, HKV, D, DI)
+    caches, qs = [], []
+    for i, L in enumerate(LENS):
+        s = synth.make_stream(i, 1, L + 1, HKV, D, DI)
+        c = orc.contiguous(shape, -(-(L + 1) // 4) * 4)
+        orc.put_rows(shape, c, 0, orc.K, 0, s.k[0])
+        orc.put_rows(shape, c, 0, orc.V, 0, s.v[0])
+        caches.append(c)
+        qs.append(synth.queries(100 + i, 1, HQ, D))
+    credited, rows = 0.0, 0
+    order = [(i, h) for h in range(HQ) for i in range(len(LENS))]
+    t0 = time.perf_counter()
+    while rows < max_rows:
+        i, h = order[rows % len(order)]
+        orc.attend_row(shape, caches[i], 0, HQ, h, LENS[i], qs[i][0, h])
+        credited += row_credit_bytes(LENS[i] + 1)
+        rows += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return credited, rows, el
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    # each step: one (stream, head) row of the workload, a bounded sample
+    import oracle as orc
+    orc.build()
+    for _ in range(args.warmup):
+        oracle_rows(0.0, max_rows=1)
+    credited, rows, el = oracle_rows(1e9, max_rows=args.steps)
+    gbs = credited / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / rows * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_desc(),
+            "query_heads_per_s": rows / el,
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"{rows} (stream, query head) rows of layer 0, one a step, "
+                                       "round-robin over the 4 streams and 16 heads"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---- our arm -----------------------------------------------------------------------
+
+def main_ours(args):
+    import torch
+    from paged_kv_cache_pg_gb300 import build, pkv
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    pkv.load()
+
+    lay = pkv.layout(N_LAYERS, HKV, D, DI)
+    lens_after = [L + 1 for L in LENS]
+    S = len(LENS)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    # data: per layer, every stream's positions 0..L (the last one is the new token)
+    streams = [synth.make_stream(rank * 100 + i, N_LAYERS, L + 1, HKV, D, DI)
+               for i, L in enumerate(LENS)]
+    q_host = [np.concatenate([synth.queries(rank * 100 + 50 + l * S + i, 1, HQ, D)
+                              for i in range(S)]) for l in range(N_LAYERS)]
+    k_new = [up(np.concatenate([s.k[l][-1:] for s in streams])) for l in range(N_LAYERS)]
+    v_new = [up(np.concatenate([s.v[l][-1:] for s in streams])) for l in range(N_LAYERS)]
+    ik_new = [up(np.concatenate([s.ik[l][-1:] for s in streams])) for l in range(N_LAYERS)]
+    q_dev = [up(q) for q in q_host]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # caches: one arena per page size, and contiguous buffers
+    confs = {}
+    for p in PAGES + [None]:
+        if p is None:
+            pgs, mems = [], []
+            for L in lens_after:
+                cap = -(-L // 4) * 4
+                ps = pkv.page_elems(lay, cap)
+                m = torch.empty(ps, dtype=torch.int16, device=dev)
+                mems.append(m)
+                pgs.append(pkv.pg(m, None, ps, cap))
+            tables, used = [], 0
+        else:
+            ps = pkv.page_elems(lay, p)
+            counts = [synth.pages_for(L, p) for L in lens_after]
+            n_pages = sum(counts) + 8
+            tabs = synth.shuffled_tables(rank * 1000 + p, n_pages, counts)
+            m = torch.empty(n_pages * ps, dtype=torch.int16, device=dev)
+            mems = [m]
+            tables = [torch.from_numpy(t).to(dev) for t in tabs]
+            pgs = [pkv.pg(m, t, ps, p, n_pages, t.numel()) for t in tables]
+            used = sum(counts)
+        confs[p] = {"mems": mems, "tables": tables, "pgs": pgs, "pages_used": used}
+
+    for l in range(N_LAYERS):
+        kc = up(np.concatenate([s.k[l][:-1] for s in streams]))
+        vc = up(np.concatenate([s.v[l][:-1] for s in streams]))
+        ic = up(np.concatenate([s.ik[l][:-1] for s in streams]))
+        for p, cf in confs.items():
+            pkv.store(lay, [pkv.seq(g, L, L) for g, L in zip(cf["pgs"], LENS)], l, kc, vc, ic,
+                      status=status)
+        del kc, vc, ic
+    torch.cuda.synchronize()
+    del streams
+
+    step_seqs = {p: [pkv.seq(g, L, 1) for g, L in zip(cf["pgs"], lens_after)]
+                 for p, cf in confs.items()}
+    for p, cf in confs.items():
+        n = pkv.decode_ws_size(lay, step_seqs[p], HQ)
+        cf["ws"] = torch.empty(max(64, n // 4 + 64), dtype=torch.float32, device=dev)
+        cf["launches_per_layer"] = 2 + (1 if n > 0 else 0)
+        cf["out"] = [torch.empty_like(q_dev[0]) for _ in range(N_LAYERS)]
+
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext = True
+    except TypeError:
+        ext = False
+
+    def capture(p, events):
+        cf = confs[p]
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):  # settle lazy set-up before capture
+                for l in range(N_LAYERS):
+                    pkv.store(lay, step_seqs[p], l, k_new[l], v_new[l], ik_new[l], status=status)
+                    pkv.decode(lay, step_seqs[p], l, HQ, q_dev[l], cf["out"][l], cf["ws"],
+                               status=status)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for l in range(N_LAYERS):
+                pkv.store(lay, step_seqs[p], l, k_new[l], v_new[l], ik_new[l], status=status)
+                if events:
+                    events[l][0].record()
+                pkv.decode(lay, step_seqs[p], l, HQ, q_dev[l], cf["out"][l], cf["ws"],
+                           status=status)
+                if events:
+                    events[l][1].record()
+        return g
+
+    graphs, dec_events = {}, {}
+    for p in confs:
+        ev = ([(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+               for _ in range(N_LAYERS)] if ext else None)
+        dec_events[p] = ev
+        graphs[p] = capture(p, ev)
+
+    # correctness guard: paged outputs equal contiguous outputs bit for bit
+    for p in confs:
+        graphs[p].replay()
+    torch.cuda.synchronize()
+    same = all(torch.equal(confs[p]["out"][l], confs[None]["out"][l])
+               for p in PAGES for l in range(N_LAYERS))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status word {int(status.item())}")
+
+    for _ in range(args.warmup):
+        for p in confs:
+            graphs[p].replay()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    step_ms = {p: [] for p in confs}
+    dec_ms = {p: [] for p in confs}
+    ev0 = {p: torch.cuda.Event(enable_timing=True) for p in confs}
+    ev1 = {p: torch.cuda.Event(enable_timing=True) for p in confs}
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        for p in PAGES:
+            ev0[p].record()
+            graphs[p].replay()
+            ev1[p].record()
+        ev1[PAGES[-1]].synchronize()
+        for p in PAGES:
+            step_ms[p].append(ev0[p].elapsed_time(ev1[p]))
+            if dec_events[p]:
+                try:
+                    dec_ms[p].extend(a.elapsed_time(b) for a, b in dec_events[p])
+                except Exception:
+                    dec_events[p] = None
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    barrier(world)
+    clk = clocks.stop()
+
+    # contiguous baseline (same workload, own buffers), timed the same way
+    cont_ms, cont_dec = [], []
+    for _ in range(args.steps):
+        ev0[None].record()
+        graphs[None].replay()
+        ev1[None].record()
+        ev1[None].synchronize()
+        cont_ms.append(ev0[None].elapsed_time(ev1[None]))
+        if dec_events[None]:
+            try:
+                cont_dec.extend(a.elapsed_time(b) for a, b in dec_events[None])
+            except Exception:
+                dec_events[None] = None
+    torch.cuda.synchronize()
+
+    # ---- results ----
+    per_step_ms = sum(statistics.fmean(step_ms[p]) for p in PAGES)
+    max_ms = max_over_ranks(per_step_ms * args.steps, world, dev)
+    step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in PAGES)
+    value = world * step_bytes * args.steps / (max_ms / 1e3) / 1e9
+    qh_per_step = len(PAGES) * N_LAYERS * S * HQ
+    per_page = {}
+    for p in PAGES:
+        ms = statistics.fmean(step_ms[p])
+        per_page[str(p)] = {
+            "GBps": round(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) / ms / 1e6, 1),
+            "ms_13_layers": round(ms, 4),
+            "paged_over_contig": round(ms / statistics.fmean(cont_ms), 4)}
+    cont_gbs = N_LAYERS * layer_bytes(lens_after, 0) / statistics.fmean(cont_ms) / 1e6
+    peak, peak_kind = peaks()
+
+    roof = None
+    all_dec = [x for p in PAGES for x in dec_ms[p]]
+    if all_dec:
+        dur = statistics.fmean(all_dec) / 1e3
+        achieved = decode_bytes(lens_after) / dur / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "pkv_decode (split-KV partial + combine), one layer, 4 streams",
+                "avg_launch_us": round(dur * 1e6, 3), "peak_kind": peak_kind,
+                "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM, 4)}
+
+    # end to end through the public API with host buffers
+    e2e = e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, status,
+                  lens_after, dev, args)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        credited, rows, el = oracle_rows(args.cpu_seconds)
+        cpu = {"value": round(credited / el / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{rows} (stream, query head) rows of layer 0 of the workload "
+                         f"({el:.1f} s, one thread)"}
+
+    launches = args.steps * sum(N_LAYERS * confs[p]["launches_per_layer"] for p in PAGES)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_desc(),
+            "pct_of_measured_peak": round(100 * value / world / peak, 2),
+            "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM, 2),
+            "query_heads_per_s": round(world * qh_per_step * args.steps / (max_ms / 1e3), 1),
+            "per_page_size": per_page,
+            "contiguous": {"GBps": round(cont_gbs, 1), "ms_13_layers": round(statistics.fmean(cont_ms), 4)},
+            "paged_contig_ratio_worst": max(v["paged_over_contig"] for v in per_page.values()),
+            "paged_equals_contiguous": bool(same),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk, "timed_wall_s": round(wall, 3)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, status, lens_after,
+            dev, args):
+    """Same step through the public calls, inputs from pinned host memory and
+    outputs back to it, copies inside the timed region."""
+    S = len(lens_after)
+    h_q = torch.from_numpy(np.stack(q_host).view(np.int16)).pin_memory()
+    kv_rows = torch.stack([torch.stack([k.cpu(), v.cpu()]) for k, v in zip(k_new, v_new)]).pin_memory()
+    ik_rows = torch.stack([i.cpu() for i in ik_new]).pin_memory()
+    d_q = torch.empty(h_q.shape, dtype=torch.int16, device=dev)
+    d_kv = torch.empty(kv_rows.shape, dtype=torch.int16, device=dev)
+    d_ik = torch.empty(ik_rows.shape, dtype=torch.int16, device=dev)
+    h_out = torch.empty(h_q.shape, dtype=torch.int16).pin_memory()
+    d_out = torch.empty(h_q.shape, dtype=torch.int16, device=dev)
+    graphs = {}
+    for p in PAGES:
+        cf = confs[p]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            d_q.copy_(h_q, non_blocking=True)
+            d_kv.copy_(kv_rows, non_blocking=True)
+            d_ik.copy_(ik_rows, non_blocking=True)
+            for l in range(N_LAYERS):
+                pkv.store(lay, step_seqs[p], l, d_kv[l, 0], d_kv[l, 1], d_ik[l], status=status)
+                pkv.decode(lay, step_seqs[p], l, HQ, d_q[l], d_out[l], cf["ws"], status=status)
+            h_out.copy_(d_out, non_blocking=True)
+        graphs[p] = g
+    for _ in range(max(3, args.warmup)):
+        for p in PAGES:
+            graphs[p].replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(10, args.steps // 4)
+    total = 0.0
+    for _ in range(n):
+        e0.record()
+        for p in PAGES:
+            graphs[p].replay()
+        e1.record()
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in PAGES)
+    h2d = len(PAGES) * (h_q.numel() + kv_rows.numel() + ik_rows.numel()) * 2
+    d2h = len(PAGES) * h_out.numel() * 2
+    return {"value": round(step_bytes / (total / n / 1e3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": n, "ms_per_step": round(total / n, 4)}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return main_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,246 @@
+/*
+ * pkv.h - paged KV-cache attention on one GB300 (sm_103a), C ABI.
+ *
+ * What is paged (TensorFold PR #1169 "fn-paged-kv", What this changes; PR
+ * #1170 "the streams beside the first take KV pages from the core pool",
+ * commit 3f5b87d): each stream's attention caches are n-position pages of
+ * one device arena, found through an int page table.  A page of n positions
+ * holds, for every attention layer, the keys, values and indexer keys of its
+ * n positions and the pooled rows of their n/4 blocks, so n is a multiple of
+ * 4.  Row lookup (pg_at): with no table, the old contiguous expression ("cap
+ * rows a head"); with a table, the start of the page holding the position
+ * plus the row inside that page.  Only addresses change and no sum changes
+ * order, so paged results are bit-identical to contiguous ones.
+ *
+ * Layout of one page, in bf16 elements (page_pos = n positions, D = head_dim,
+ * Di = idx_dim, H = n_kv_heads), repeated for layer 0 .. n_layers-1:
+ *     K  [H][n][D]   V  [H][n][D]   IK [n][Di]   P [n/4][Di]
+ * A contiguous stream buffer is the same layout with one page of n = cap.
+ * page_elems = n_layers * (2*H*n*D + n*Di + (n/4)*Di).
+ *
+ * Conventions for every call:
+ *   - Returns PKV_OK (0) or a PKV_E* code; nothing else crosses the ABI (no
+ *     C++ exceptions).  Argument checks happen before anything is launched.
+ *   - Device pointers are the caller's (allocated by the caller, e.g. with
+ *     PyTorch).  The library allocates no device memory.  Work buffers are
+ *     sized by the *_ws_size calls and passed in.
+ *   - Every launch goes on the caller's `stream`; no call synchronizes.
+ *   - A multi-stream launch takes one pkv_seq per stream, each with its own
+ *     page table (PR #2244 "the grouped draft head's lanes carry their page
+ *     table": a grouped launch built without each stream's table read and
+ *     wrote other streams' pages).
+ *   - Kernels never trap.  A table entry outside [0, n_pages) is reported by
+ *     OR-ing PKV_DEV_* bits into *dev_status (a device int32 owned by the
+ *     caller; NULL disables reporting) and the access is skipped or replaced
+ *     by a read of page 0; results are then unspecified.
+ *   - Data types: K, V, IK, P, queries and outputs are bf16; scores float32;
+ *     ids int32.  Head dim 256 and indexer dim 128 (or 0) are supported.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define PKV_OK 0
+#define PKV_EINVAL 1  /* an argument is malformed or unsupported            */
+#define PKV_EAGAIN 2  /* not enough free pages right now; retry after give   */
+#define PKV_ECUDA 3   /* a CUDA runtime call failed                          */
+#define PKV_EDEVICE 4 /* reserved: a device-side check failed                */
+
+/* ---- bits a kernel ORs into *dev_status ---------------------------------- */
+#define PKV_DEV_BAD_PAGE 1u /* a table entry was outside [0, n_pages)     */
+#define PKV_DEV_TIMEOUT 2u  /* a pipeline wait ran past its time limit     */
+
+/* kinds of rows (pkv_pg_row, pkv_gather) */
+#define PKV_K 0
+#define PKV_V 1
+#define PKV_IK 2
+#define PKV_P 3 /* pooled rows: `pos` counts blocks of 4 positions */
+
+#define PKV_MAX_SEQS 64 /* streams in one launch */
+
+/* Shape of a model's caches; the same for every stream. */
+typedef struct pkv_layout {
+    int32_t n_layers;   /* attention layer slots in one page (>= 1)           */
+    int32_t n_kv_heads; /* key/value heads (>= 1)                              */
+    int32_t head_dim;   /* elements in a key or value row (256)                */
+    int32_t idx_dim;    /* elements in an indexer-key / pooled row (128, or 0) */
+} pkv_layout;
+
+/*
+ * Pg: where one stream's caches live (#1169: "an int page table, the
+ * elements in a page, and the positions in a page").
+ */
+typedef struct pkv_pg {
+    void *base;            /* device, 16-byte aligned: page 0 of the arena, or the
+                              stream's own contiguous buffer when table == NULL      */
+    const int32_t *table;  /* device: page id of each logical page; NULL = contiguous */
+    int64_t page_elems;    /* elements (bf16) in one page over all layers             */
+    int32_t page_pos;      /* positions in one page (cap when table == NULL); %4 == 0 */
+    int32_t n_pages;       /* pages in the arena; table entries must be below it;
+                              1 when table == NULL                                    */
+    int32_t n_table;       /* entries in table (positions must be < n_table*page_pos);
+                              1 when table == NULL                                    */
+    int32_t reserved;      /* set to 0 */
+} pkv_pg;
+
+/*
+ * One stream in a launch.  Positions 0 .. len-1 are valid after this call's
+ * new tokens; the last n_new of them (len-n_new .. len-1) are this call's new
+ * tokens.  New-token rows (k_new, v_new, ik_new, q, out) are packed in stream
+ * order: stream s owns rows sum_{t<s} n_new[t] .. + n_new[s]-1.
+ */
+typedef struct pkv_seq {
+    pkv_pg pg;
+    int32_t len;
+    int32_t n_new;
+} pkv_seq;
+
+/* ---- layout ------------------------------------------------------------- */
+
+/* Elements in one page of `page_pos` positions.  EINVAL: bad layout or
+ * page_pos <= 0 or not a multiple of 4 (#1170: "n must be a multiple of 4"). */
+int pkv_layout_page_elems(const pkv_layout *layout, int32_t page_pos, int64_t *out);
+
+/*
+ * pg_at on the host (#1169 What this changes; #1170 commit 3f5b87d kv_row):
+ * element offset from pg->base of row (layer, kind, head, pos).  host_table
+ * is a host copy of pg->table (ignored when pg->table == NULL).  For PKV_P,
+ * pos is a block index.  EINVAL if the row lies outside the cache.
+ */
+int pkv_pg_row(const pkv_layout *layout, const pkv_pg *pg, const int32_t *host_table,
+               int32_t layer, int32_t kind, int32_t head, int32_t pos, int64_t *out);
+
+/* ---- arena: the page pool (#1170 What this changes; commit 1ac2075) ------
+ * The arena is caller-owned device memory cut into pages.  Free pages are
+ * handed out lowest id first ("the free stack hands out KV pages from the
+ * bottom").  Pages given back with a stream become free again only once the
+ * work already queued on that stream has finished ("a lane's pages go back
+ * once the engine's stream drains"); the arena polls with an event, never
+ * blocks.  A request that finds too few free pages gets PKV_EAGAIN and waits
+ * (LaneMemory in the pages): it is not an error.  Not thread-safe per arena.
+ */
+typedef struct pkv_arena pkv_arena;
+
+/* Cut [dev_base, dev_base+bytes) into pages of page_pos positions.  The
+ * memory stays the caller's; destroy before freeing it.  EINVAL on a bad
+ * layout, a misaligned base or room for no page. */
+int pkv_arena_create(const pkv_layout *layout, int32_t page_pos, void *dev_base, size_t bytes,
+                     pkv_arena **out);
+/* Forget the arena (pending releases are dropped with their events). */
+int pkv_arena_destroy(pkv_arena *arena);
+/* Pages in the arena, pages free now (after polling pending releases), and
+ * elements a page. Any pointer may be NULL. */
+int pkv_arena_info(pkv_arena *arena, int32_t *n_pages, int32_t *n_free, int64_t *page_elems);
+/* Take n pages (lowest free ids, ascending) into host ids_out[n].
+ * EAGAIN if fewer than n are free; nothing is taken then. */
+int pkv_pages_take(pkv_arena *arena, int32_t n, int32_t *ids_out);
+/* Give pages back.  With `defer` nonzero the pages return once the work
+ * queued on `stream` so far has finished (an event is recorded); with defer
+ * == 0 they return now and the caller asserts the stream has drained.
+ * EINVAL for an id outside the arena or not taken (nothing changes then). */
+int pkv_pages_give(pkv_arena *arena, const int32_t *ids, int32_t n, cudaStream_t stream,
+                   int32_t defer);
+/* Fill a pkv_pg for a stream of this arena; dev_table holds n_table ids. */
+int pkv_arena_pg(const pkv_arena *arena, const int32_t *dev_table, int32_t n_table,
+                 pkv_pg *out);
+
+/* Event operations used for deferred release; the default is CUDA events.
+ * record: 0 and *ev set on success; query: 0 done, 1 pending, <0 failed. */
+typedef struct pkv_event_ops {
+    int (*record)(void *ctx, cudaStream_t stream, void **ev);
+    int (*query)(void *ctx, void *ev);
+    void (*destroy)(void *ctx, void *ev);
+    void *ctx;
+} pkv_event_ops;
+/* Replace the event operations (NULL restores CUDA events).  For hosts that
+ * track completion themselves, and for tests without a GPU. */
+int pkv_arena_set_event_ops(pkv_arena *arena, const pkv_event_ops *ops);
+
+/* ---- cache store (#1169: fn_attn_prep writes key, value and indexer-key
+ * rows through pg_at; #1170 commit 3f5b87d: rope's store through kv_row) ---
+ * Copy each stream's n_new new tokens into positions len-n_new .. len-1 of
+ * `layer`: k_new, v_new [tokens][H][D] bf16; ik_new [tokens][Di] bf16 (NULL
+ * iff idx_dim == 0).  Bytes move unchanged. */
+int pkv_store(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+              const void *k_new, const void *v_new, const void *ik_new, int32_t *dev_status,
+              cudaStream_t stream);
+
+/* ---- gather (prompt-cache save: #1169 "saves and restores copy page runs
+ * in the contiguous layout") -----------------------------------------------
+ * Copy rows of `kind` for positions 0 .. len-1 of every stream into `out`,
+ * packed in stream order: K/V [sum len][H][D]; IK [sum len][Di]; P
+ * [sum len/4][Di].  Restoring is pkv_store with n_new = len. */
+int pkv_gather(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+               int32_t kind, void *out, int32_t *dev_status, cudaStream_t stream);
+
+/* ---- pooling (#1169: fn_qsa_pool reads indexer keys once per block of
+ * four and writes pooled rows through the table) ------------------------------
+ * For every block b completed by this call's new tokens (4b+3 in
+ * [len-n_new, len)): P[b] = bf16_rn(((ik[4b]+ik[4b+1])+ik[4b+2])+ik[4b+3]) * 0.25)
+ * with float32 sums.  EINVAL if idx_dim == 0. */
+int pkv_pool(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+             int32_t *dev_status, cudaStream_t stream);
+
+/* ---- decode attention with split-KV partials and their combine (#1169:
+ * fn_attn_chunks(_ahead) reads key and value tiles through key_at, one
+ * lookup per key per tile; #1170 commit ce5b78d: tf_q35_attn_partial reads
+ * rows through the table, the contiguous path branches once) ---------------
+ * Causal attention of each stream's n_new queries: query j (position
+ * len-n_new+j) of head h reads keys 0 .. len-n_new+j of KV head
+ * h / (n_q_heads/H), softmax(q.k / sqrt(D)) . v.  q, out: [tokens][n_q_heads][D]
+ * bf16.  Float32 accumulation.  n_new * (n_q_heads/H) <= 32 per stream.
+ * The split of each stream's keys depends only on its length and the GPU's
+ * SM count, never on page size, so paged output equals contiguous output
+ * bit for bit and a stream's output does not depend on the other streams.
+ * The split partials go to ws and a second kernel combines them, splits in
+ * ascending order.  ws: device, >= pkv_decode_ws_size bytes (0 when no
+ * stream needs more than one split), 256-byte aligned, no initialization;
+ * one ws per in-flight call.  q and out 16-byte aligned. */
+int pkv_decode_ws_size(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
+                       int32_t n_q_heads, size_t *bytes);
+int pkv_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+               int32_t n_q_heads, const void *q, void *out, void *ws, size_t ws_bytes,
+               int32_t *dev_status, cudaStream_t stream);
+
+/* ---- block scores (#1169: fn_qsa_scores reads pooled rows) ---------------
+ * For each stream's one decode query (n_new == 1), head h and complete block
+ * b < len/4: scores[s][h][b] = sum_d qi[h][d] * P[b][d], float32, as the
+ * chain acc = fmaf(qi[d], P[b][d], acc) for d = 0 .. Di-1 from acc = 0.
+ * qi [tokens][n_q_heads][Di] bf16; scores [n_seqs][n_q_heads][ld] float32,
+ * entries b >= len/4 set to -infinity.  EINVAL if ld < len/4. */
+int pkv_block_scores(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
+                     int32_t layer, int32_t n_q_heads, const void *qi, float *scores,
+                     int32_t ld, int32_t *dev_status, cudaStream_t stream);
+
+/* ---- top-k block selection ------------------------------------------------
+ * Per (stream, head): the min(k, len/4) blocks with the highest scores, an
+ * exact tie going to the lower block id (+0 == -0), written in ascending id
+ * order to ids [n_seqs][n_q_heads][k] and padded with -1.  1 <= k <= 256. */
+int pkv_topk(const pkv_seq *seqs, int32_t n_seqs, int32_t n_q_heads, const float *scores,
+             int32_t ld, int32_t k, int32_t *ids, cudaStream_t stream);
+
+/* ---- block-sparse decode (#1169 Receipt: "sparse attention rows") -------
+ * Each stream's one decode query, head h, reads only the keys of its selected
+ * blocks ids[s][h][0..k-1] (ascending, -1 = none), softmax(q.k/sqrt(D)) . v
+ * over them; no selected block gives a zero row.  Blocks must be < len/4.
+ * q, out [tokens][n_q_heads][D] bf16; ws as for pkv_decode. */
+int pkv_sparse_ws_size(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
+                       int32_t n_q_heads, int32_t k, size_t *bytes);
+int pkv_sparse_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
+                      int32_t layer, int32_t n_q_heads, const void *q, const int32_t *ids,
+                      int32_t k, void *out, void *ws, size_t ws_bytes, int32_t *dev_status,
+                      cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,178 @@
+// Cache store, gather and block pooling.  Rows are located with pg_at once
+// per row (store, gather) or once per block of four positions (pool: a page
+// holds whole blocks because its size is a multiple of 4), never per load.
+#include "pkv_dev.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunk = 8;  // bf16 elements in a 16-byte chunk
+
+// Offset of the page holding `pos`, or -1 for a table entry outside the
+// arena (reported); row is the row inside the page.
+__device__ __forceinline__ int64_t page_or_bad(const SeqDev &s, int32_t pos, int32_t *row,
+                                               uint32_t *status) {
+    if (s.table == nullptr) {
+        *row = pos;
+        return 0;
+    }
+    int32_t page = pos / s.ptok;
+    *row = pos - page * s.ptok;
+    int32_t id = __ldg(s.table + page);
+    if (static_cast<uint32_t>(id) >= static_cast<uint32_t>(s.n_pages)) {
+        if (status) atomicOr(status, PKV_DEV_BAD_PAGE);
+        return -1;
+    }
+    return (int64_t)id * s.ps;
+}
+
+// One thread per 16-byte chunk of a new token's rows: 2*H rows of 256
+// (K then V) and, with indexer keys, one row of 128.
+__global__ void __launch_bounds__(kThreads) store_kernel(const __grid_constant__ Common c,
+                                                         int64_t total_chunks,
+                                                         const uint16_t *__restrict__ k_new,
+                                                         const uint16_t *__restrict__ v_new,
+                                                         const uint16_t *__restrict__ ik_new) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = c.n_kv_heads;
+    const int row_chunks = kHeadDim / kChunk;  // 32
+    const int ik_chunks = c.idx_dim / kChunk;  // 16 or 0
+    const int per_tok = 2 * H * row_chunks + ik_chunks;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total_chunks;
+         i += (int64_t)gridDim.x * kThreads) {
+        const int32_t tok = static_cast<int32_t>(i / per_tok);
+        const int32_t r = static_cast<int32_t>(i % per_tok);
+        const int s = find_seq(c.n_seqs, tok, [&](int t) { return c.seq[t].tok_off; });
+        const SeqDev &sd = c.seq[s];
+        const int32_t pos = sd.len - sd.n_new + (tok - sd.tok_off);
+        int32_t row;
+        const int64_t page = page_or_bad(sd, pos, &row, c.status);
+        if (page < 0) continue;
+        const uint16_t *src;
+        int64_t dst;
+        if (r < 2 * H * row_chunks) {
+            const int kind = r / (H * row_chunks);  // 0 = K, 1 = V
+            const int head = (r / row_chunks) % H;
+            const int ch = r % row_chunks;
+            src = (kind ? v_new : k_new) + ((int64_t)tok * H + head) * kHeadDim + ch * kChunk;
+            dst = page + (kind ? off_v(H, sd.ptok, head, row) : off_k(sd.ptok, head, row)) +
+                  ch * kChunk;
+        } else {
+            const int ch = r - 2 * H * row_chunks;
+            src = ik_new + (int64_t)tok * c.idx_dim + ch * kChunk;
+            dst = page + off_ik(H, c.idx_dim, sd.ptok, row) + ch * kChunk;
+        }
+        uint16_t *base = const_cast<uint16_t *>(sd.layer_base);
+        *reinterpret_cast<uint4 *>(base + dst) = __ldg(reinterpret_cast<const uint4 *>(src));
+    }
+}
+
+// One thread per 16-byte chunk of an output row.  work_off holds each
+// stream's first output row.
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ Common c,
+                                                          int32_t kind, int64_t total_chunks,
+                                                          uint16_t *__restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = c.n_kv_heads;
+    const bool kv = kind == PKV_K || kind == PKV_V;
+    const int row_chunks = (kv ? kHeadDim : c.idx_dim) / kChunk;
+    const int per_row = (kv ? H : 1) * row_chunks;  // chunks of one output row
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total_chunks;
+         i += (int64_t)gridDim.x * kThreads) {
+        const int32_t orow = static_cast<int32_t>(i / per_row);
+        const int32_t r = static_cast<int32_t>(i % per_row);
+        const int s = find_seq(c.n_seqs, orow, [&](int t) { return c.seq[t].work_off; });
+        const SeqDev &sd = c.seq[s];
+        const int32_t idx = orow - sd.work_off;  // position, or block for PKV_P
+        const int32_t pos = kind == PKV_P ? 4 * idx : idx;
+        int32_t row;
+        int64_t page = page_or_bad(sd, pos, &row, c.status);
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (page >= 0) {
+            int64_t src;
+            const int ch = r % row_chunks;
+            if (kind == PKV_K) src = off_k(sd.ptok, r / row_chunks, row);
+            else if (kind == PKV_V) src = off_v(H, sd.ptok, r / row_chunks, row);
+            else if (kind == PKV_IK) src = off_ik(H, c.idx_dim, sd.ptok, row);
+            else src = off_p(H, c.idx_dim, sd.ptok, row / 4);
+            val = *reinterpret_cast<const uint4 *>(sd.layer_base + page + src + ch * kChunk);
+        }
+        *reinterpret_cast<uint4 *>(out + (int64_t)orow * per_row * kChunk + (int64_t)r * kChunk) =
+            val;
+    }
+}
+
+// One thread per (block, 8 dims): P[b] = bf16_rn((((k0 + k1) + k2) + k3) * 0.25f),
+// float32 sums in position order.  work_off holds each stream's first block item.
+__global__ void __launch_bounds__(kThreads) pool_kernel(const __grid_constant__ Common c,
+                                                        int64_t total_chunks) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = c.n_kv_heads;
+    const int per_block = c.idx_dim / kChunk;  // 16
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total_chunks;
+         i += (int64_t)gridDim.x * kThreads) {
+        const int32_t item = static_cast<int32_t>(i / per_block);
+        const int ch = static_cast<int>(i % per_block);
+        const int s = find_seq(c.n_seqs, item, [&](int t) { return c.seq[t].work_off; });
+        const SeqDev &sd = c.seq[s];
+        const int32_t b = (sd.len - sd.n_new) / 4 + (item - sd.work_off);
+        int32_t row;
+        const int64_t page = page_or_bad(sd, 4 * b, &row, c.status);  // one lookup a block
+        if (page < 0) continue;
+        uint16_t *lb = const_cast<uint16_t *>(sd.layer_base) + page;
+        const uint16_t *ik = lb + off_ik(H, c.idx_dim, sd.ptok, row) + ch * kChunk;
+        float sum[kChunk];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            uint4 u = *reinterpret_cast<const uint4 *>(ik + (int64_t)r * c.idx_dim);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < kChunk; ++e) {
+                const uint32_t half = (e & 1) ? (w[e / 2] & 0xffff0000u) : (w[e / 2] << 16);
+                const float x = __uint_as_float(half);
+                sum[e] = r == 0 ? x : __fadd_rn(sum[e], x);
+            }
+        }
+        uint32_t packed[4];
+#pragma unroll
+        for (int e = 0; e < kChunk; e += 2)
+            packed[e / 2] = pack_bf16(__fmul_rn(sum[e], 0.25f), __fmul_rn(sum[e + 1], 0.25f));
+        *reinterpret_cast<uint4 *>(lb + off_p(H, c.idx_dim, sd.ptok, row / 4) + ch * kChunk) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+}
+
+unsigned grid_for(int64_t work) {
+    int64_t g = (work + kThreads - 1) / kThreads;
+    return static_cast<unsigned>(g < 1 ? 1 : (g > 65535 * 4 ? 65535 * 4 : g));
+}
+
+}  // namespace
+
+int launch_store(const Common &c, int32_t total_tokens, const uint16_t *k_new,
+                 const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream) {
+    const int64_t per_tok = 2 * c.n_kv_heads * (kHeadDim / kChunk) + c.idx_dim / kChunk;
+    const int64_t total = per_tok * total_tokens;
+    return launch_status(launch_pdl(store_kernel, grid_for(total), kThreads, 0, stream, c, total,
+                                    k_new, v_new, ik_new));
+}
+
+int launch_gather(const Common &c, int32_t kind, int64_t total_rows, uint16_t *out,
+                  cudaStream_t stream) {
+    const bool kv = kind == PKV_K || kind == PKV_V;
+    const int64_t per_row = (kv ? c.n_kv_heads : 1) * ((kv ? kHeadDim : c.idx_dim) / kChunk);
+    const int64_t total = per_row * total_rows;
+    return launch_status(
+        launch_pdl(gather_kernel, grid_for(total), kThreads, 0, stream, c, kind, total, out));
+}
+
+int launch_pool(const Common &c, int32_t total_blocks, cudaStream_t stream) {
+    const int64_t total = (int64_t)total_blocks * (c.idx_dim / kChunk);
+    return launch_status(launch_pdl(pool_kernel, grid_for(total), kThreads, 0, stream, c, total));
+}
+
+}  // namespace pkv

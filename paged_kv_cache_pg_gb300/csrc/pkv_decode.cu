@@ -1,0 +1,430 @@
+// Decode attention over paged caches: split-KV partials and their combine.
+//
+// Work unit: (stream, KV head, split) for dense decode, where the G query
+// heads of the KV head (times the stream's n_new queries) share every staged
+// key/value tile; (stream, query head, split) for block-sparse decode, whose
+// keys are the positions of that head's selected blocks.
+//
+// One CTA = one producer warp + four consumer warps.  The producer looks each
+// key's row up once per tile (#1169: key_at once per key per tile, beside the
+// key ids; kept here as the ids in shared memory and the row addresses in the
+// producer lanes) and stages the tile's K and V rows with bulk async copies
+// into a ring of shared-memory stages.  The consumers compute S^T = K Q^T and
+// O^T += V^T P^T with warp MMAs (bf16 in, float32 accumulate), keep an online
+// softmax per query column, and merge their key slices in a fixed order.
+// Splits have a fixed length set by the stream's key count and the SM count,
+// so paged and contiguous caches give the same bits.
+#include <cfloat>
+
+#include "pkv_dev.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kTile = 16;                    // keys a stage
+constexpr int kRowBytes = 528;               // staged row stride: 512 + 16 (bank spread)
+constexpr int kStageBytes = 2 * kTile * kRowBytes;
+constexpr int kStages = 6;
+constexpr int kCons = 4;                     // consumer warps
+constexpr int kThreads = (kCons + 1) * 32;
+constexpr int kMaxCols = 32;                 // query columns of one unit
+constexpr int kMinSplitDense = 128;          // keys
+constexpr int kMinSplitSparse = 64;
+constexpr int kMaxSplits = 512;
+constexpr int kCombThreads = 256;
+constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
+
+constexpr size_t kSmemBytes = kStages * kStageBytes + kStages * kTile * 4 + 2 * kStages * 8 + 16;
+static_assert(kCons * 8 * kHeadDim * 4 + kCons * 8 * 2 * 4 <= kStages * kStageBytes,
+              "merge buffers reuse the stages");
+
+struct DecodeArgs {
+    const uint16_t *q;
+    uint16_t *out;
+    float *ws;
+    const int32_t *ids;  // sparse: [n_seqs][n_q_heads][k]
+    int32_t k;
+};
+
+__device__ __forceinline__ float warp_max_lanes(float v) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum_lanes(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    return v;
+}
+
+struct Unit {
+    int s, unit, split, kvh;
+    int key0, key1, ntiles;
+};
+
+template <bool kSparse>
+__device__ __forceinline__ Unit locate(const Common &c, const DecodeArgs &a) {
+    Unit u;
+    u.s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].work_off; });
+    const SeqDev &sd = c.seq[u.s];
+    const int r = blockIdx.x - sd.work_off;
+    u.unit = r / sd.nsplit;
+    u.split = r - u.unit * sd.nsplit;
+    u.kvh = kSparse ? u.unit / c.group : u.unit;
+    const int nkeys = kSparse ? 4 * a.k : sd.len;
+    u.key0 = u.split * sd.split_len;
+    u.key1 = min(nkeys, u.key0 + sd.split_len);
+    u.ntiles = (u.key1 - u.key0 + kTile - 1) / kTile;
+    return u;
+}
+
+// Packed row of query column `col` of the unit.
+template <bool kSparse>
+__device__ __forceinline__ int64_t q_row(const Common &c, const SeqDev &sd, const Unit &u,
+                                         int col) {
+    if (kSparse) return (int64_t)sd.tok_off * c.n_q_heads + u.unit;
+    const int j = col / c.group;
+    return ((int64_t)sd.tok_off + j) * c.n_q_heads + u.kvh * c.group + (col - j * c.group);
+}
+
+template <bool kSparse>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_partial(const __grid_constant__ Common c, const DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *stages = smem;
+    int32_t *kpos = reinterpret_cast<int32_t *>(smem + kStages * kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(kpos + kStages * kTile);
+    uint64_t *empty = full + kStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Unit u = locate<kSparse>(c, a);
+    const SeqDev &sd = c.seq[u.s];
+    const int ncols = sd.ncols;
+    const int ncg = (ncols + 7) >> 3;
+    const int ks_n = kCons / ncg;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], ncg);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    const int cg = warp % ncg, ks = warp / ncg;
+
+    if (warp == kCons) {
+        // ---------------- producer ----------------
+        const uint64_t pol = policy_evict_first();
+        int issued = 0;
+        bool ok = true;
+        const int32_t *ids = kSparse ? a.ids + ((int64_t)u.s * c.n_q_heads + u.unit) * a.k : nullptr;
+        const int nb = sd.len / 4;
+        for (int t = 0; t < u.ntiles; ++t) {
+            const int st = t % kStages, use = t / kStages;
+            if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, c.status)) {
+                ok = false;
+                break;
+            }
+            if (*abort_flag) break;
+            const uint16_t *kr = nullptr, *vr = nullptr;
+            if (lane < kTile) {
+                const int i = u.key0 + t * kTile + lane;
+                int pos = -1;
+                if (i < u.key1) {
+                    if (kSparse) {
+                        const int b = __ldg(ids + (i >> 2));
+                        if (b >= 0 && b < nb) pos = 4 * b + (i & 3);
+                        else if (b >= nb && c.status) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                    } else {
+                        pos = i;
+                    }
+                }
+                kpos[st * kTile + lane] = pos;
+                // a masked key still stages a real row, so every stage byte is finite data
+                const int src = pos >= 0 ? pos : (kSparse ? 0 : u.key0);
+                kr = k_row(sd, c.n_kv_heads, u.kvh, src, c.status);
+                vr = v_row(sd, c.n_kv_heads, u.kvh, src, c.status);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], kTile * 2 * 512);
+            __syncwarp();
+            if (lane < kTile) {
+                uint8_t *sk = stages + st * kStageBytes + lane * kRowBytes;
+                bulk_g2s(sk, kr, 512, &full[st], pol);
+                bulk_g2s(sk + kTile * kRowBytes, vr, 512, &full[st], pol);
+            }
+            issued = t + 1;
+        }
+        if (!ok) *abort_flag = 1;
+        if (*abort_flag) {
+            // let every copy already issued land before the CTA's memory is released
+            for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+                mbar_wait(&full[t % kStages], (t / kStages) & 1, nullptr);
+        }
+    } else if (ks < ks_n) {
+        // ---------------- consumer ----------------
+        const int bcol = cg * 8 + (lane >> 2);
+        uint32_t qf[16][2];
+        {
+            const uint16_t *qr =
+                bcol < ncols ? a.q + q_row<kSparse>(c, sd, u, bcol) * kHeadDim : nullptr;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                const int d = kk * 16 + 2 * (lane & 3);
+                qf[kk][0] = qr ? __ldg(reinterpret_cast<const uint32_t *>(qr + d)) : 0u;
+                qf[kk][1] = qr ? __ldg(reinterpret_cast<const uint32_t *>(qr + d + 8)) : 0u;
+            }
+        }
+        // the two columns this lane owns in S^T and O^T fragments, and the
+        // last key position each may read (causal; -1 for a padding column)
+        const int c0 = cg * 8 + 2 * (lane & 3), c1 = c0 + 1;
+        const int qbase = sd.len - sd.n_new;
+        const int lim0 = c0 < ncols ? (kSparse ? INT32_MAX : qbase + c0 / c.group) : -1;
+        const int lim1 = c1 < ncols ? (kSparse ? INT32_MAX : qbase + c1 / c.group) : -1;
+
+        const uint32_t s_base = smem_u32(stages);
+        const uint32_t k_lane = ((lane & 7) + 8 * ((lane >> 3) & 1)) * kRowBytes + 16 * (lane >> 4);
+        const uint32_t v_lane = ((lane & 7) + 8 * (lane >> 4)) * kRowBytes + 16 * ((lane >> 3) & 1);
+
+        for (int t = ks; t < u.ntiles; t += ks_n) {
+            const int st = t % kStages, use = t / kStages;
+            if (!mbar_wait(&full[st], use & 1, c.status)) {
+                *abort_flag = 1;
+                break;
+            }
+            const uint32_t kb = s_base + st * kStageBytes;
+            const uint32_t vb = kb + kTile * kRowBytes;
+            // S^T[16 keys x 8 cols] = K Q^T, two accumulator chains
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 16; kk += 2) {
+                uint32_t x0, x1, x2, x3;
+                ldsm_x4(kb + k_lane + kk * 32, x0, x1, x2, x3);
+                mma_bf16(sa, x0, x1, x2, x3, qf[kk][0], qf[kk][1]);
+                ldsm_x4(kb + k_lane + (kk + 1) * 32, x0, x1, x2, x3);
+                mma_bf16(sb, x0, x1, x2, x3, qf[kk + 1][0], qf[kk + 1][1]);
+            }
+            const int kp0 = kpos[st * kTile + (lane >> 2)];
+            const int kp1 = kpos[st * kTile + (lane >> 2) + 8];
+            const float x0 = (kp0 >= 0 && kp0 <= lim0) ? (sa[0] + sb[0]) * kScaleLog2 : -INFINITY;
+            const float x1 = (kp0 >= 0 && kp0 <= lim1) ? (sa[1] + sb[1]) * kScaleLog2 : -INFINITY;
+            const float x2 = (kp1 >= 0 && kp1 <= lim0) ? (sa[2] + sb[2]) * kScaleLog2 : -INFINITY;
+            const float x3 = (kp1 >= 0 && kp1 <= lim1) ? (sa[3] + sb[3]) * kScaleLog2 : -INFINITY;
+            const float n0 = fmaxf(m0, warp_max_lanes(fmaxf(x0, x2)));
+            const float n1 = fmaxf(m1, warp_max_lanes(fmaxf(x1, x3)));
+            const float b0 = n0 == -INFINITY ? 0.f : n0;
+            const float b1 = n1 == -INFINITY ? 0.f : n1;
+            const float al0 = ex2(m0 - b0), al1 = ex2(m1 - b1);
+            const float p0 = ex2(x0 - b0), p1 = ex2(x1 - b1);
+            const float p2 = ex2(x2 - b0), p3 = ex2(x3 - b1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            m0 = n0;
+            m1 = n1;
+            const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+            // O^T[16 dims x 8 cols] += V^T P^T for the 16 dim tiles
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al1;
+                acc[i][2] *= al0;
+                acc[i][3] *= al1;
+                uint32_t y0, y1, y2, y3;
+                ldsm_x4_t(vb + v_lane + i * 32, y0, y1, y2, y3);
+                mma_bf16(acc[i], y0, y1, y2, y3, pb0, pb1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        l0 = warp_sum_lanes(l0);
+        l1 = warp_sum_lanes(l1);
+    }
+
+    __syncthreads();
+    if (*abort_flag) return;
+
+    // ---- merge the key slices (ks = 0, 1, ...) in order, inside the CTA ----
+    const int NC = ncg * 8;
+    float *mbuf = reinterpret_cast<float *>(stages);     // [ks][NC][256]
+    float *mlb = mbuf + ks_n * NC * kHeadDim;             // [ks][NC][2]
+    if (warp < kCons && ks < ks_n) {
+        const int c0 = cg * 8 + 2 * (lane & 3);
+        float *b0 = mbuf + (ks * NC + c0) * kHeadDim;
+        float *b1 = b0 + kHeadDim;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int d = i * 16 + (lane >> 2);
+            b0[d] = acc[i][0];
+            b1[d] = acc[i][1];
+            b0[d + 8] = acc[i][2];
+            b1[d + 8] = acc[i][3];
+        }
+        if ((lane >> 2) == 0) {
+            mlb[(ks * NC + c0) * 2 + 0] = m0;
+            mlb[(ks * NC + c0) * 2 + 1] = l0;
+            mlb[(ks * NC + c0 + 1) * 2 + 0] = m1;
+            mlb[(ks * NC + c0 + 1) * 2 + 1] = l1;
+        }
+    }
+    __syncthreads();
+
+    const bool single = sd.nsplit == 1;
+    const int units = kSparse ? c.n_q_heads : c.n_kv_heads;
+    float *part_acc = a.ws + sd.ws_off;
+    float *part_ml = part_acc + (int64_t)units * sd.nsplit * ncols * kHeadDim;
+    const int64_t pidx = ((int64_t)u.unit * sd.nsplit + u.split) * ncols;
+    for (int idx = tid; idx < ncols * kHeadDim; idx += kThreads) {
+        const int col = idx / kHeadDim, d = idx - col * kHeadDim;
+        float M = -INFINITY;
+        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + col) * 2]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+            for (int k = 0; k < ks_n; ++k) {
+                const float w = ex2(mlb[(k * NC + col) * 2] - M);
+                L += w * mlb[(k * NC + col) * 2 + 1];
+                O += w * mbuf[(k * NC + col) * kHeadDim + d];
+            }
+        }
+        if (single) {
+            const float o = L > 0.f ? O / L : 0.f;
+            a.out[q_row<kSparse>(c, sd, u, col) * kHeadDim + d] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        } else {
+            part_acc[(pidx + col) * kHeadDim + d] = O;
+            if (d == 0) {
+                part_ml[(pidx + col) * 2 + 0] = M;
+                part_ml[(pidx + col) * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// Combine a unit's split partials for one query column, splits in order:
+// M = max m_i, L = sum 2^(m_i-M) l_i, O = sum 2^(m_i-M) acc_i, out = O / L.
+template <bool kSparse>
+__global__ void __launch_bounds__(kCombThreads)
+    decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
+    __shared__ float w[kMaxSplits];
+    __shared__ float inv_l;
+    pdl_wait();
+    pdl_trigger();
+    const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
+    const SeqDev &sd = c.seq[s];
+    const int r = blockIdx.x - sd.comb_off;
+    const int unit = r / sd.ncols, col = r - unit * sd.ncols;
+    const int ns = sd.nsplit;
+    const int units = kSparse ? c.n_q_heads : c.n_kv_heads;
+    const float *part_acc = a.ws + sd.ws_off;
+    const float *part_ml = part_acc + (int64_t)units * ns * sd.ncols * kHeadDim;
+    const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
+    for (int i = threadIdx.x; i < ns; i += kCombThreads)
+        w[i] = __ldcg(part_ml + (p0 + (int64_t)i * sd.ncols) * 2);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float M = -INFINITY;
+        for (int i = 0; i < ns; ++i) M = fmaxf(M, w[i]);
+        float L = 0.f;
+        for (int i = 0; i < ns; ++i) {
+            const float wi = M == -INFINITY ? 0.f : ex2(w[i] - M);
+            L += wi * __ldcg(part_ml + (p0 + (int64_t)i * sd.ncols) * 2 + 1);
+            w[i] = wi;
+        }
+        inv_l = L;
+    }
+    __syncthreads();
+    const float L = inv_l;
+    const int d = threadIdx.x;  // kCombThreads == head dim
+    float O = 0.f;
+    for (int i = 0; i < ns; ++i) O += w[i] * __ldcg(part_acc + (p0 + (int64_t)i * sd.ncols) * kHeadDim + d);
+    const float o = L > 0.f ? O / L : 0.f;
+    Unit u;
+    u.unit = unit;
+    u.kvh = kSparse ? unit / c.group : unit;
+    a.out[q_row<kSparse>(c, sd, u, col) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+}
+static_assert(kCombThreads == kHeadDim, "one combine thread per dim");
+
+}  // namespace
+
+// Splits: a fixed number of keys per split, a multiple of the tile, at least
+// the minimum, and enough splits for about two CTAs per SM from one stream.
+int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
+    int32_t items = 0, comb = 0;
+    int64_t floats = 0;
+    const int units = sparse ? c.n_q_heads : c.n_kv_heads;
+    for (int s = 0; s < c.n_seqs; ++s) {
+        SeqDev &d = c.seq[s];
+        d.work_off = items;
+        d.comb_off = comb;
+        d.ws_off = floats;
+        const int nkeys = sparse ? 4 * k : d.len;
+        d.ncols = sparse ? 1 : d.n_new * c.group;
+        if (d.ncols > kMaxCols) return PKV_EINVAL;
+        if (d.n_new == 0 || nkeys == 0) {
+            d.nsplit = 1;
+            d.split_len = kTile;
+            d.ncols = 0;
+            continue;  // no queries: nothing to launch for this stream
+        }
+        const int max_splits = std::max(1, 2 * nsm / units);
+        int sl = (nkeys + max_splits - 1) / max_splits;
+        sl = (sl + kTile - 1) / kTile * kTile;
+        sl = std::max(sl, sparse ? kMinSplitSparse : kMinSplitDense);
+        int ns = (nkeys + sl - 1) / sl;
+        while (ns > kMaxSplits) {
+            sl += kTile;
+            ns = (nkeys + sl - 1) / sl;
+        }
+        d.nsplit = ns;
+        d.split_len = sl;
+        items += units * ns;
+        if (ns > 1) {
+            comb += units * d.ncols;
+            floats += (int64_t)units * ns * d.ncols * (kHeadDim + 2);
+            floats = (floats + 63) / 64 * 64;
+        }
+    }
+    plan->total_items = items;
+    plan->total_comb = comb;
+    plan->ws_bytes = static_cast<size_t>(floats) * 4;
+    return PKV_OK;
+}
+
+int launch_decode(const Common &c, const DecodePlan &plan, bool sparse, const uint16_t *q,
+                  const int32_t *ids, int32_t k, uint16_t *out, float *ws, cudaStream_t stream) {
+    DecodeArgs a{q, out, ws, ids, k};
+    // streams with no queries own no CTAs: give them an empty range
+    Common cc = c;
+    auto part = sparse ? decode_partial<true> : decode_partial<false>;
+    auto comb = sparse ? decode_combine<true> : decode_combine<false>;
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[sparse]) {
+        if (cudaFuncSetAttribute(part, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
+            return PKV_ECUDA;
+        attr_set[sparse] = true;
+    }
+    cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, a);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    if (plan.total_comb > 0) {
+        e = launch_pdl(comb, plan.total_comb, kCombThreads, 0, stream, cc, a);
+        if (e != cudaSuccess) return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
+}  // namespace pkv

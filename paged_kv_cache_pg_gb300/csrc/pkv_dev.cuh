@@ -1,0 +1,204 @@
+// Device helpers: pg_at row translation, inline-PTX wrappers for sm_103a
+// (mbarrier, bulk async copies, ldmatrix, warp MMA, movmatrix), bounded
+// waits and programmatic dependent launch control.
+#pragma once
+
+#include <cstdint>
+#include <utility>
+
+#include <cuda_bf16.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// ---- pg_at (#1169 What this changes; #1170 commit ce5b78d) -----------------
+// With no table the old contiguous expression; with a table the start of the
+// page holding the position plus the row inside that page.  The branch is
+// uniform for a stream, taken once per key per tile by the caller, never per
+// load.  A table entry outside [0, n_pages) is reported and replaced by page
+// 0, so the read stays inside the arena.
+__device__ __forceinline__ int64_t page_start(const SeqDev &s, int32_t pos, int32_t *row,
+                                              uint32_t *status) {
+    if (s.table == nullptr) {
+        *row = pos;
+        return 0;
+    }
+    int32_t page = pos / s.ptok;
+    *row = pos - page * s.ptok;
+    int32_t id = __ldg(s.table + page);
+    if (static_cast<uint32_t>(id) >= static_cast<uint32_t>(s.n_pages)) {
+        if (status) atomicOr(status, PKV_DEV_BAD_PAGE);
+        id = 0;
+    }
+    return (int64_t)id * s.ps;
+}
+
+__device__ __forceinline__ const uint16_t *k_row(const SeqDev &s, int32_t h_kv, int32_t head,
+                                                 int32_t pos, uint32_t *status) {
+    int32_t row;
+    int64_t p = page_start(s, pos, &row, status);
+    return s.layer_base + p + off_k(s.ptok, head, row);
+}
+
+__device__ __forceinline__ const uint16_t *v_row(const SeqDev &s, int32_t h_kv, int32_t head,
+                                                 int32_t pos, uint32_t *status) {
+    int32_t row;
+    int64_t p = page_start(s, pos, &row, status);
+    return s.layer_base + p + off_v(h_kv, s.ptok, head, row);
+}
+
+// ---- small PTX wrappers -----------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// A wait that gives up after about a second: it reports PKV_DEV_TIMEOUT and
+// returns false instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_ns();
+    for (uint32_t spin = 0;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) {
+            if (status) atomicOr(status, PKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// One bulk async copy global -> shared, completing on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).  Streamed rows are read once: evict first.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                        uint32_t &a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &a0, uint32_t &a1,
+                                          uint32_t &a2, uint32_t &a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+
+// D (16x8 f32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Programmatic dependent launch: wait for the previous grid's results, and
+// let the next grid start its prologue early.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Stream of the work item / token: the last s with off(s) <= i.
+template <typename F>
+__device__ __forceinline__ int find_seq(int n, int32_t i, F off) {
+    int s = 0;
+    for (int t = 1; t < n; ++t)
+        if (off(t) <= i) s = t;
+    return s;
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream drains; it calls pdl_wait() before
+// touching memory that kernel writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace pkv

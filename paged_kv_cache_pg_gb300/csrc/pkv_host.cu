@@ -1,0 +1,497 @@
+// Host side of the C ABI: argument checks, the page arena (free pages, lowest
+// id first; deferred release on a stream event), host pg_at, and the entry
+// points that pack kernel parameters and launch.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ECUDA; }
+
+int validate_layout(const pkv_layout *L) {
+    if (!L) return PKV_EINVAL;
+    if (L->n_layers < 1 || L->n_kv_heads < 1 || L->n_kv_heads > 64) return PKV_EINVAL;
+    if (L->head_dim != kHeadDim) return PKV_EINVAL;
+    if (L->idx_dim != 0 && L->idx_dim != kIdxDim) return PKV_EINVAL;
+    return PKV_OK;
+}
+
+static bool page_pos_ok(int32_t page_pos) { return page_pos > 0 && page_pos % 4 == 0; }
+
+int sm_count(int *out) {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ECUDA;
+    if (dev < 0 || dev >= 64) return PKV_ECUDA;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PKV_ECUDA;
+        cached[dev] = n;
+    }
+    *out = cached[dev];
+    return PKV_OK;
+}
+
+// Check one stream's descriptor against the layout.
+static int validate_pg(const pkv_layout *L, const pkv_pg &pg) {
+    if (!pg.base || (reinterpret_cast<uintptr_t>(pg.base) & 15u)) return PKV_EINVAL;
+    if (!page_pos_ok(pg.page_pos)) return PKV_EINVAL;
+    int64_t want = (int64_t)L->n_layers * layer_elems(L->n_kv_heads, L->idx_dim, pg.page_pos);
+    if (pg.page_elems != want) return PKV_EINVAL;
+    if (pg.table) {
+        if (pg.n_pages < 1 || pg.n_table < 1) return PKV_EINVAL;
+    }
+    return PKV_OK;
+}
+
+static int64_t capacity(const pkv_pg &pg) {
+    return pg.table ? (int64_t)pg.n_table * pg.page_pos : pg.page_pos;
+}
+
+int fill_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                int32_t n_q_heads, int32_t *dev_status, Common *c) {
+    int rc = validate_layout(L);
+    if (rc) return rc;
+    if (n_seqs < 0 || n_seqs > PKV_MAX_SEQS || (n_seqs > 0 && !seqs)) return PKV_EINVAL;
+    if (layer < 0 || layer >= L->n_layers) return PKV_EINVAL;
+    if (n_q_heads < 1 || n_q_heads % L->n_kv_heads != 0) return PKV_EINVAL;
+    std::memset(c, 0, sizeof(*c));
+    c->n_seqs = n_seqs;
+    c->n_kv_heads = L->n_kv_heads;
+    c->idx_dim = L->idx_dim;
+    c->layer = layer;
+    c->n_q_heads = n_q_heads;
+    c->group = n_q_heads / L->n_kv_heads;
+    c->status = reinterpret_cast<uint32_t *>(dev_status);
+    int32_t tok = 0;
+    for (int32_t s = 0; s < n_seqs; ++s) {
+        const pkv_seq &q = seqs[s];
+        rc = validate_pg(L, q.pg);
+        if (rc) return rc;
+        if (q.len < 0 || q.n_new < 0 || q.n_new > q.len || q.len > capacity(q.pg))
+            return PKV_EINVAL;
+        SeqDev &d = c->seq[s];
+        const uint16_t *base = static_cast<const uint16_t *>(q.pg.base);
+        d.layer_base = base + (int64_t)layer * layer_elems(L->n_kv_heads, L->idx_dim,
+                                                           q.pg.page_pos);
+        d.table = q.pg.table;
+        d.ps = q.pg.page_elems;
+        d.ptok = q.pg.page_pos;
+        d.n_pages = q.pg.table ? q.pg.n_pages : 1;
+        d.len = q.len;
+        d.n_new = q.n_new;
+        d.tok_off = tok;
+        if ((int64_t)tok + q.n_new > INT32_MAX / 2) return PKV_EINVAL;
+        tok += q.n_new;
+    }
+    return PKV_OK;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int total_new(const Common &c) {
+    int t = 0;
+    for (int s = 0; s < c.n_seqs; ++s) t += c.seq[s].n_new;
+    return t;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+// ============================================================================
+// layout and host pg_at
+// ============================================================================
+
+extern "C" int pkv_layout_page_elems(const pkv_layout *layout, int32_t page_pos, int64_t *out) {
+    if (validate_layout(layout) || !page_pos_ok(page_pos) || !out) return PKV_EINVAL;
+    *out = (int64_t)layout->n_layers * layer_elems(layout->n_kv_heads, layout->idx_dim, page_pos);
+    return PKV_OK;
+}
+
+extern "C" int pkv_pg_row(const pkv_layout *L, const pkv_pg *pg, const int32_t *host_table,
+                          int32_t layer, int32_t kind, int32_t head, int32_t pos, int64_t *out) {
+    if (validate_layout(L) || !pg || !out || validate_pg(L, *pg)) return PKV_EINVAL;
+    if (layer < 0 || layer >= L->n_layers || pos < 0) return PKV_EINVAL;
+    if (kind < PKV_K || kind > PKV_P) return PKV_EINVAL;
+    if ((kind == PKV_K || kind == PKV_V) && (head < 0 || head >= L->n_kv_heads))
+        return PKV_EINVAL;
+    if ((kind == PKV_IK || kind == PKV_P) && L->idx_dim == 0) return PKV_EINVAL;
+    if (pg->table && !host_table) return PKV_EINVAL;
+    const int32_t ptok = pg->page_pos;
+    const int64_t position = kind == PKV_P ? 4 * (int64_t)pos : pos;
+    if (position >= capacity(*pg)) return PKV_EINVAL;
+    int64_t page_off = 0;
+    int32_t row = static_cast<int32_t>(position);
+    if (pg->table) {
+        int32_t page = static_cast<int32_t>(position / ptok);
+        int32_t id = host_table[page];
+        if (id < 0 || id >= pg->n_pages) return PKV_EINVAL;
+        page_off = (int64_t)id * pg->page_elems;
+        row = static_cast<int32_t>(position % ptok);
+    }
+    int64_t in_layer;
+    const int32_t H = L->n_kv_heads;
+    switch (kind) {
+    case PKV_K: in_layer = off_k(ptok, head, row); break;
+    case PKV_V: in_layer = off_v(H, ptok, head, row); break;
+    case PKV_IK: in_layer = off_ik(H, L->idx_dim, ptok, row); break;
+    default: in_layer = off_p(H, L->idx_dim, ptok, row / 4); break;
+    }
+    *out = page_off + (int64_t)layer * layer_elems(H, L->idx_dim, ptok) + in_layer;
+    return PKV_OK;
+}
+
+// ============================================================================
+// arena
+// ============================================================================
+
+struct pkv_arena {
+    pkv_layout layout;
+    int32_t page_pos = 0;
+    int64_t page_elems = 0;
+    int32_t n_pages = 0;
+    void *base = nullptr;
+    std::vector<uint8_t> taken;  // 1 = held by a stream or pending release
+    int32_t n_free = 0;
+    int32_t low = 0;  // no free page below this id
+    struct Pending {
+        void *ev;
+        std::vector<int32_t> ids;
+    };
+    std::vector<Pending> pending;
+    pkv_event_ops ops{};
+    bool custom_ops = false;
+    std::mutex mu;
+};
+
+namespace {
+
+int cuda_record(void *, cudaStream_t stream, void **ev) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return -1;
+    if (cudaEventRecord(e, stream) != cudaSuccess) {
+        cudaEventDestroy(e);
+        return -1;
+    }
+    *ev = e;
+    return 0;
+}
+int cuda_query(void *, void *ev) {
+    cudaError_t r = cudaEventQuery(static_cast<cudaEvent_t>(ev));
+    if (r == cudaSuccess) return 0;
+    if (r == cudaErrorNotReady) {
+        cudaGetLastError();  // not-ready is not sticky; clear it
+        return 1;
+    }
+    return -1;
+}
+void cuda_destroy(void *, void *ev) { cudaEventDestroy(static_cast<cudaEvent_t>(ev)); }
+
+const pkv_event_ops kCudaOps = {cuda_record, cuda_query, cuda_destroy, nullptr};
+
+void free_page(pkv_arena *a, int32_t id) {
+    a->taken[id] = 0;
+    a->n_free++;
+    if (id < a->low) a->low = id;
+}
+
+// Move releases whose stream work has finished back to the free pages.
+int poll_pending(pkv_arena *a) {
+    int rc = PKV_OK;
+    size_t keep = 0;
+    for (size_t i = 0; i < a->pending.size(); ++i) {
+        auto &p = a->pending[i];
+        int q = a->ops.query(a->ops.ctx, p.ev);
+        if (q == 0) {
+            a->ops.destroy(a->ops.ctx, p.ev);
+            for (int32_t id : p.ids) free_page(a, id);
+        } else {
+            if (q < 0) rc = PKV_ECUDA;
+            if (keep != i) a->pending[keep] = std::move(p);
+            ++keep;
+        }
+    }
+    a->pending.resize(keep);
+    return rc;
+}
+
+}  // namespace
+
+extern "C" int pkv_arena_create(const pkv_layout *layout, int32_t page_pos, void *dev_base,
+                                size_t bytes, pkv_arena **out) {
+    if (!out) return PKV_EINVAL;
+    *out = nullptr;
+    if (validate_layout(layout) || !page_pos_ok(page_pos) || !dev_base) return PKV_EINVAL;
+    if (reinterpret_cast<uintptr_t>(dev_base) & 15u) return PKV_EINVAL;
+    int64_t ps = (int64_t)layout->n_layers *
+                 layer_elems(layout->n_kv_heads, layout->idx_dim, page_pos);
+    int64_t n = static_cast<int64_t>(bytes / 2) / ps;
+    if (n < 1 || n > INT32_MAX) return PKV_EINVAL;
+    pkv_arena *a = new (std::nothrow) pkv_arena;
+    if (!a) return PKV_EINVAL;
+    a->layout = *layout;
+    a->page_pos = page_pos;
+    a->page_elems = ps;
+    a->n_pages = static_cast<int32_t>(n);
+    a->base = dev_base;
+    a->taken.assign(static_cast<size_t>(n), 0);
+    a->n_free = a->n_pages;
+    a->ops = kCudaOps;
+    *out = a;
+    return PKV_OK;
+}
+
+extern "C" int pkv_arena_destroy(pkv_arena *a) {
+    if (!a) return PKV_EINVAL;
+    for (auto &p : a->pending) a->ops.destroy(a->ops.ctx, p.ev);
+    delete a;
+    return PKV_OK;
+}
+
+extern "C" int pkv_arena_set_event_ops(pkv_arena *a, const pkv_event_ops *ops) {
+    if (!a) return PKV_EINVAL;
+    std::lock_guard<std::mutex> g(a->mu);
+    if (!a->pending.empty()) return PKV_EINVAL;  // events of one kind at a time
+    if (ops && (!ops->record || !ops->query || !ops->destroy)) return PKV_EINVAL;
+    a->ops = ops ? *ops : kCudaOps;
+    a->custom_ops = ops != nullptr;
+    return PKV_OK;
+}
+
+extern "C" int pkv_arena_info(pkv_arena *a, int32_t *n_pages, int32_t *n_free,
+                              int64_t *page_elems) {
+    if (!a) return PKV_EINVAL;
+    std::lock_guard<std::mutex> g(a->mu);
+    int rc = poll_pending(a);
+    if (n_pages) *n_pages = a->n_pages;
+    if (n_free) *n_free = a->n_free;
+    if (page_elems) *page_elems = a->page_elems;
+    return rc;
+}
+
+extern "C" int pkv_pages_take(pkv_arena *a, int32_t n, int32_t *ids_out) {
+    if (!a || n < 0 || (n > 0 && !ids_out)) return PKV_EINVAL;
+    std::lock_guard<std::mutex> g(a->mu);
+    int rc = poll_pending(a);
+    if (rc) return rc;
+    if (n > a->n_free) return PKV_EAGAIN;
+    int32_t got = 0;
+    for (int32_t id = a->low; id < a->n_pages && got < n; ++id) {
+        if (!a->taken[id]) {
+            a->taken[id] = 1;
+            ids_out[got++] = id;
+        }
+    }
+    a->n_free -= got;
+    a->low = got ? ids_out[got - 1] + 1 : a->low;
+    return PKV_OK;
+}
+
+extern "C" int pkv_pages_give(pkv_arena *a, const int32_t *ids, int32_t n, cudaStream_t stream,
+                              int32_t defer) {
+    if (!a || n < 0 || (n > 0 && !ids)) return PKV_EINVAL;
+    std::lock_guard<std::mutex> g(a->mu);
+    // every id must be in range, held, and listed once
+    std::vector<int32_t> v(ids, ids + n);
+    std::sort(v.begin(), v.end());
+    for (int32_t i = 0; i < n; ++i) {
+        if (v[i] < 0 || v[i] >= a->n_pages || !a->taken[v[i]]) return PKV_EINVAL;
+        if (i && v[i] == v[i - 1]) return PKV_EINVAL;
+    }
+    for (auto &p : a->pending)
+        for (int32_t id : p.ids)
+            if (std::binary_search(v.begin(), v.end(), id)) return PKV_EINVAL;
+    if (n == 0) return PKV_OK;
+    if (!defer) {
+        for (int32_t id : v) free_page(a, id);
+        return PKV_OK;
+    }
+    void *ev = nullptr;
+    if (a->ops.record(a->ops.ctx, stream, &ev) != 0) return PKV_ECUDA;
+    a->pending.push_back({ev, std::move(v)});
+    return PKV_OK;
+}
+
+extern "C" int pkv_arena_pg(const pkv_arena *a, const int32_t *dev_table, int32_t n_table,
+                            pkv_pg *out) {
+    if (!a || !dev_table || n_table < 1 || !out) return PKV_EINVAL;
+    out->base = a->base;
+    out->table = dev_table;
+    out->page_elems = a->page_elems;
+    out->page_pos = a->page_pos;
+    out->n_pages = a->n_pages;
+    out->n_table = n_table;
+    out->reserved = 0;
+    return PKV_OK;
+}
+
+// ============================================================================
+// kernel entry points
+// ============================================================================
+
+extern "C" int pkv_store(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                         const void *k_new, const void *v_new, const void *ik_new,
+                         int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    int rc = fill_common(L, seqs, n_seqs, layer, L ? L->n_kv_heads : 1, dev_status, &c);
+    if (rc) return rc;
+    int tok = total_new(c);
+    if (tok == 0) return PKV_OK;
+    if (!k_new || !v_new || (L->idx_dim && !ik_new)) return PKV_EINVAL;
+    if (!aligned16(k_new) || !aligned16(v_new) || (L->idx_dim && !aligned16(ik_new)))
+        return PKV_EINVAL;
+    return launch_store(c, tok, static_cast<const uint16_t *>(k_new),
+                        static_cast<const uint16_t *>(v_new),
+                        static_cast<const uint16_t *>(ik_new), stream);
+}
+
+extern "C" int pkv_gather(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                          int32_t kind, void *out, int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    int rc = fill_common(L, seqs, n_seqs, layer, L ? L->n_kv_heads : 1, dev_status, &c);
+    if (rc) return rc;
+    if (kind < PKV_K || kind > PKV_P) return PKV_EINVAL;
+    if ((kind == PKV_IK || kind == PKV_P) && L->idx_dim == 0) return PKV_EINVAL;
+    int64_t rows = 0;
+    for (int s = 0; s < c.n_seqs; ++s) {
+        c.seq[s].work_off = static_cast<int32_t>(rows);
+        rows += kind == PKV_P ? c.seq[s].len / 4 : c.seq[s].len;
+    }
+    if (rows == 0) return PKV_OK;
+    if (!out || !aligned16(out) || rows > INT32_MAX / 2) return PKV_EINVAL;
+    return launch_gather(c, kind, rows, static_cast<uint16_t *>(out), stream);
+}
+
+extern "C" int pkv_pool(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                        int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    int rc = fill_common(L, seqs, n_seqs, layer, L ? L->n_kv_heads : 1, dev_status, &c);
+    if (rc) return rc;
+    if (L->idx_dim == 0) return PKV_EINVAL;
+    int32_t blocks = 0;
+    for (int s = 0; s < c.n_seqs; ++s) {
+        SeqDev &d = c.seq[s];
+        d.work_off = blocks;
+        blocks += d.len / 4 - (d.len - d.n_new) / 4;
+    }
+    if (blocks == 0) return PKV_OK;
+    return launch_pool(c, blocks, stream);
+}
+
+static int decode_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
+                         int32_t layer, int32_t n_q_heads, bool sparse, int32_t k,
+                         int32_t *dev_status, Common *c, DecodePlan *plan) {
+    int rc = fill_common(L, seqs, n_seqs, layer, n_q_heads, dev_status, c);
+    if (rc) return rc;
+    if (sparse) {
+        if (k < 1 || k > 256) return PKV_EINVAL;
+        for (int s = 0; s < c->n_seqs; ++s)
+            if (c->seq[s].n_new != 1) return PKV_EINVAL;
+    } else {
+        for (int s = 0; s < c->n_seqs; ++s)
+            if (c->seq[s].n_new * c->group > 32) return PKV_EINVAL;  // query columns of a unit
+    }
+    int nsm = 0;
+    rc = sm_count(&nsm);
+    if (rc) return rc;
+    return plan_decode(*c, sparse, k, nsm, plan);
+}
+
+extern "C" int pkv_decode_ws_size(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
+                                  int32_t n_q_heads, size_t *bytes) {
+    if (!bytes) return PKV_EINVAL;
+    Common c;
+    DecodePlan plan;
+    int rc = decode_common(L, seqs, n_seqs, 0, n_q_heads, false, 0, nullptr, &c, &plan);
+    if (rc) return rc;
+    *bytes = plan.ws_bytes;
+    return PKV_OK;
+}
+
+extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                          int32_t n_q_heads, const void *q, void *out, void *ws,
+                          size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    DecodePlan plan;
+    int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, false, 0, dev_status, &c, &plan);
+    if (rc) return rc;
+    if (plan.total_items == 0) return PKV_OK;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) return PKV_EINVAL;
+    if (plan.ws_bytes > 0 &&
+        (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return PKV_EINVAL;
+    return launch_decode(c, plan, false, static_cast<const uint16_t *>(q), nullptr, 0,
+                         static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
+}
+
+extern "C" int pkv_sparse_ws_size(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
+                                  int32_t n_q_heads, int32_t k, size_t *bytes) {
+    if (!bytes) return PKV_EINVAL;
+    Common c;
+    DecodePlan plan;
+    int rc = decode_common(L, seqs, n_seqs, 0, n_q_heads, true, k, nullptr, &c, &plan);
+    if (rc) return rc;
+    *bytes = plan.ws_bytes;
+    return PKV_OK;
+}
+
+extern "C" int pkv_sparse_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
+                                 int32_t layer, int32_t n_q_heads, const void *q,
+                                 const int32_t *ids, int32_t k, void *out, void *ws,
+                                 size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    DecodePlan plan;
+    int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, true, k, dev_status, &c, &plan);
+    if (rc) return rc;
+    if (plan.total_items == 0) return PKV_OK;
+    if (!q || !out || !ids || !aligned16(q) || !aligned16(out)) return PKV_EINVAL;
+    if (plan.ws_bytes > 0 &&
+        (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return PKV_EINVAL;
+    return launch_decode(c, plan, true, static_cast<const uint16_t *>(q), ids, k,
+                         static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
+}
+
+extern "C" int pkv_block_scores(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
+                                int32_t layer, int32_t n_q_heads, const void *qi, float *scores,
+                                int32_t ld, int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    int rc = fill_common(L, seqs, n_seqs, layer, n_q_heads, dev_status, &c);
+    if (rc) return rc;
+    if (L->idx_dim == 0) return PKV_EINVAL;
+    int32_t max_nb = 0;
+    for (int s = 0; s < c.n_seqs; ++s) {
+        if (c.seq[s].n_new != 1) return PKV_EINVAL;
+        max_nb = std::max(max_nb, c.seq[s].len / 4);
+    }
+    if (ld < max_nb || ld < 0) return PKV_EINVAL;
+    if (c.n_seqs == 0 || ld == 0) return PKV_OK;
+    if (!qi || !scores) return PKV_EINVAL;
+    return launch_scores(c, scores, ld, static_cast<const uint16_t *>(qi), max_nb, stream);
+}
+
+extern "C" int pkv_topk(const pkv_seq *seqs, int32_t n_seqs, int32_t n_q_heads,
+                        const float *scores, int32_t ld, int32_t k, int32_t *ids,
+                        cudaStream_t stream) {
+    if (n_seqs < 0 || n_seqs > PKV_MAX_SEQS || (n_seqs > 0 && !seqs)) return PKV_EINVAL;
+    if (n_q_heads < 1 || k < 1 || k > 256) return PKV_EINVAL;
+    Common c;
+    std::memset(&c, 0, sizeof(c));
+    c.n_seqs = n_seqs;
+    c.n_q_heads = n_q_heads;
+    for (int s = 0; s < n_seqs; ++s) {
+        if (seqs[s].len < 0) return PKV_EINVAL;
+        if (seqs[s].len / 4 > ld) return PKV_EINVAL;
+        c.seq[s].len = seqs[s].len;
+    }
+    if (n_seqs == 0) return PKV_OK;
+    if (!scores || !ids || ld < 0) return PKV_EINVAL;
+    return launch_topk(c, scores, ld, k, ids, stream);
+}

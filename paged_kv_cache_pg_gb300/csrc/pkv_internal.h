@@ -1,0 +1,99 @@
+// Internal declarations shared by the host entry points and the kernels.
+// Nothing here is part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Supported row widths (the pages' head_dim 256 and indexer keys of 128).
+constexpr int kHeadDim = 256;
+constexpr int kIdxDim = 128;
+
+// One stream as a kernel sees it.  `layer_base` is the stream's base plus
+// the layer's part of page 0 (#1169: "a cache pointer is its layer's part of
+// page 0"); every row of that layer is layer_base + page offset + the row's
+// place inside the page's layer part.
+struct SeqDev {
+    const uint16_t *layer_base;
+    const int32_t *table;  // nullptr: contiguous (one page of ptok = cap rows)
+    int64_t ps;            // elements in a page
+    int32_t ptok;          // positions in a page
+    int32_t n_pages;       // arena pages (table entries must be below)
+    int32_t len;           // valid positions after the new tokens
+    int32_t n_new;         // new tokens (queries) of this call
+    int32_t tok_off;       // first packed row of this stream's new tokens
+    int32_t work_off;      // first CTA (work item) of this stream in a launch
+    int32_t nsplit;        // splits of each unit's key range (decode)
+    int32_t split_len;     // keys in a split (multiple of the key tile)
+    int32_t comb_off;      // first CTA of this stream in the combine launch
+    int32_t ncols;         // query columns of one unit: n_new * group (decode)
+    int64_t ws_off;        // float offset of this stream's partials in ws
+};
+
+struct Common {
+    int32_t n_seqs;
+    int32_t n_kv_heads;
+    int32_t idx_dim;
+    int32_t layer;
+    int32_t n_q_heads;
+    int32_t group;  // n_q_heads / n_kv_heads
+    uint32_t *status;
+    SeqDev seq[PKV_MAX_SEQS];
+};
+
+// Row offsets inside one layer's part of a page of `ptok` positions.
+__host__ __device__ inline int64_t off_k(int32_t ptok, int32_t head, int32_t row) {
+    return (int64_t)head * ptok * kHeadDim + (int64_t)row * kHeadDim;
+}
+__host__ __device__ inline int64_t off_v(int32_t h_kv, int32_t ptok, int32_t head, int32_t row) {
+    return (int64_t)h_kv * ptok * kHeadDim + off_k(ptok, head, row);
+}
+__host__ __device__ inline int64_t off_ik(int32_t h_kv, int32_t idx_dim, int32_t ptok,
+                                          int32_t row) {
+    return 2 * (int64_t)h_kv * ptok * kHeadDim + (int64_t)row * idx_dim;
+}
+__host__ __device__ inline int64_t off_p(int32_t h_kv, int32_t idx_dim, int32_t ptok,
+                                         int32_t block_row) {
+    return 2 * (int64_t)h_kv * ptok * kHeadDim + (int64_t)ptok * idx_dim +
+           (int64_t)block_row * idx_dim;
+}
+__host__ __device__ inline int64_t layer_elems(int32_t h_kv, int32_t idx_dim, int32_t ptok) {
+    return 2 * (int64_t)h_kv * ptok * kHeadDim + (int64_t)ptok * idx_dim +
+           (int64_t)(ptok / 4) * idx_dim;
+}
+
+// Host helpers (pkv_host.cu).
+int validate_layout(const pkv_layout *layout);
+int fill_common(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                int32_t n_q_heads, int32_t *dev_status, Common *c);
+int sm_count(int *out);
+int launch_status(cudaError_t e);
+
+// Kernel launchers (one per kernel file); all return PKV_OK or PKV_ECUDA.
+int launch_store(const Common &c, int32_t total_tokens, const uint16_t *k_new,
+                 const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream);
+int launch_gather(const Common &c, int32_t kind, int64_t total_rows, uint16_t *out,
+                  cudaStream_t stream);
+int launch_pool(const Common &c, int32_t total_blocks, cudaStream_t stream);
+
+struct DecodePlan {
+    int32_t total_items;   // CTAs of the partial kernel
+    int32_t total_comb;    // CTAs of the combine kernel
+    size_t ws_bytes;       // counters + partials
+};
+int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan);
+int launch_decode(const Common &c, const DecodePlan &plan, bool sparse, const uint16_t *q,
+                  const int32_t *ids, int32_t k, uint16_t *out, float *ws,
+                  cudaStream_t stream);
+int launch_scores(const Common &c, float *scores, int32_t ld, const uint16_t *qi,
+                  int32_t max_nb, cudaStream_t stream);
+int launch_topk(const Common &c, const float *scores, int32_t ld, int32_t k, int32_t *ids,
+                cudaStream_t stream);
+
+}  // namespace pkv

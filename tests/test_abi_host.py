@@ -1,0 +1,251 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load and export every function ``include/pkv.h`` declares;
+host pg_at must agree with the oracle's translation bit for bit; argument
+checks must refuse malformed descriptors before anything is launched; the
+page arena must hand out the lowest free pages, refuse over-asks with
+PKV_EAGAIN, and return pages only after the stream's work is done (checked
+with fake event operations, so no GPU is involved).
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_pg_gb300 import build, pkv, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pkv.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*int\s+(pkv_\w+)\s*\(", txt, re.M))
+    return names
+
+
+def test_library_exports_every_declared_function(lib):
+    declared = _declared()
+    assert len(declared) >= 18
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(pkv.EXPORTS) <= declared
+
+
+def test_page_elems_match_oracle(lib, orc):
+    for hkv, di, ptok in [(2, 128, 256), (1, 128, 16), (4, 0, 48), (2, 128, 4)]:
+        lay = pkv.layout(13, hkv, 256, di)
+        assert pkv.page_elems(lay, ptok) == orc.page_elems(orc.Shape(13, hkv, 256, di), ptok)
+
+
+@pytest.mark.parametrize("ptok", [4, 16, 48, 128, 256, 512])
+def test_host_pg_at_equals_oracle(lib, orc, ptok):
+    lay = pkv.layout(3, 2, 256, 128)
+    shape = orc.Shape(3, 2, 256, 128)
+    ps = pkv.page_elems(lay, ptok)
+    n_pages = 40
+    table = synth.shuffled_tables(ptok, n_pages, [7])[0]
+    arena = np.zeros(1, np.uint16)
+    oc = orc.Cache(arena, ptok, ps, table, n_pages)
+    g = pkv.pg(0x10000, 0x20000, ps, ptok, n_pages, table.size)
+    rng = np.random.default_rng(ptok)
+    for _ in range(400):
+        layer = int(rng.integers(3)); kind = int(rng.integers(4)); head = int(rng.integers(2))
+        limit = 7 * ptok // 4 if kind == 3 else 7 * ptok
+        pos = int(rng.integers(limit))
+        if kind >= 2:
+            head = 0
+        assert pkv.pg_row(lay, g, table, layer, kind, head, pos) == \
+            orc.row(shape, oc, layer, kind, head, pos)
+    # contiguous: one page of cap rows
+    cap = 7 * ptok
+    cont = pkv.pg(0x10000, None, pkv.page_elems(lay, cap), cap)
+    occ = orc.Cache(arena, cap, pkv.page_elems(lay, cap), None, 1)
+    for pos in (0, 1, cap - 1):
+        for kind in range(4):
+            p = pos // 4 if kind == 3 else pos
+            assert pkv.pg_row(lay, cont, None, 2, kind, 0, p) == orc.row(shape, occ, 2, kind, 0, p)
+
+
+def test_pg_at_refuses_rows_outside(lib):
+    lay = pkv.layout(1, 1, 256, 128)
+    ps = pkv.page_elems(lay, 16)
+    table = np.array([3, 9], np.int32)
+    g = pkv.pg(0x10000, 0x20000, ps, 16, 5, 2)
+    with pytest.raises(pkv.PkvError):
+        pkv.pg_row(lay, g, table, 0, pkv.K, 0, 16)   # page id 9 >= 5 pages
+    with pytest.raises(pkv.PkvError):
+        pkv.pg_row(lay, g, table, 0, pkv.K, 0, 32)   # past the table
+    with pytest.raises(pkv.PkvError):
+        pkv.pg_row(lay, g, table, 1, pkv.K, 0, 0)    # no layer 1
+
+
+@pytest.mark.parametrize("page_pos", [0, -4, 6, 17])
+def test_page_size_must_be_a_multiple_of_four(lib, page_pos):
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.page_elems(pkv.layout(1, 1), page_pos)
+    assert e.value.code == pkv.EINVAL
+
+
+def _seq(lay, ptok=16, length=10, n_new=1, base=0x10000, table=None, n_table=4, n_pages=8):
+    ps = pkv.page_elems(lay, ptok)
+    if table is None:
+        return pkv.seq(pkv.pg(base, None, ps, ptok), length, n_new)
+    return pkv.seq(pkv.Pg(base, table, ps, ptok, n_pages, n_table, 0), length, n_new)
+
+
+def _store(lay, seqs, layer=0):
+    lib = pkv.load()
+    arr, n = pkv._seqs(seqs)
+    return lib.pkv_store(ctypes.byref(lay), arr, n, layer, 0x1000, 0x1000, 0x1000, None, None)
+
+
+def test_kernels_refuse_malformed_descriptors_before_launch(lib):
+    lay = pkv.layout(2, 2)
+    good = _seq(lay, table=0x30000)
+    assert _store(pkv.layout(2, 2, 128, 128), [good]) == pkv.EINVAL       # head dim
+    assert _store(pkv.layout(2, 2, 256, 64), [good]) == pkv.EINVAL        # indexer dim
+    assert _store(lay, [good], layer=2) == pkv.EINVAL                      # no such layer
+    bad_ps = _seq(lay, table=0x30000); bad_ps.pg.page_elems += 1
+    assert _store(lay, [bad_ps]) == pkv.EINVAL
+    assert _store(lay, [_seq(lay, base=0x10008, table=0x30000)]) == pkv.EINVAL  # misaligned
+    assert _store(lay, [_seq(lay, length=65, table=0x30000)]) == pkv.EINVAL    # past 4 pages
+    assert _store(lay, [_seq(lay, length=17)]) == pkv.EINVAL                   # past cap 16
+    assert _store(lay, [_seq(lay, n_new=11)]) == pkv.EINVAL                    # n_new > len
+    odd = _seq(lay, table=0x30000); odd.pg.page_pos = 18
+    assert _store(lay, [odd]) == pkv.EINVAL                                    # 18 % 4
+    assert _store(lay, [_seq(lay, table=0x30000, n_pages=0)]) == pkv.EINVAL
+    arr = (pkv.Seq * 65)(*([good] * 65))
+    assert pkv.load().pkv_store(ctypes.byref(lay), arr, 65, 0, 1, 1, 1, None, None) == pkv.EINVAL
+
+
+def test_garbage_descriptor_is_refused(lib):
+    # A descriptor left uninitialized must not be read as a valid table
+    # (#1170: a test's undefined Cache.paged read as a page table on x86).
+    lay = pkv.layout(1, 1)
+    raw = (ctypes.c_uint8 * ctypes.sizeof(pkv.Seq))(*([0xAA] * ctypes.sizeof(pkv.Seq)))
+    s = pkv.Seq.from_buffer_copy(raw)
+    assert _store(lay, [s]) == pkv.EINVAL
+
+
+def test_decode_refuses_too_many_query_columns(lib):
+    lay = pkv.layout(1, 2)
+    s = _seq(lay, length=100, n_new=5, ptok=128)
+    arr, n = pkv._seqs([s])
+    out = ctypes.c_size_t()
+    # 5 queries x 8 heads a KV head = 40 columns > 32; checked before any device query
+    rc = pkv.load().pkv_decode(ctypes.byref(lay), arr, n, 0, 16, 1, 1, None, 0, None, None)
+    assert rc == pkv.EINVAL
+
+
+# ---- arena -------------------------------------------------------------------
+
+@pytest.fixture
+def arena(lib):
+    lay = pkv.layout(2, 2)
+    ps = pkv.page_elems(lay, 16)
+    a = pkv.Arena(lay, 16, 0x100000, nbytes=ps * 2 * 10 + 100)
+    yield a
+    a.close()
+
+
+def test_arena_counts_pages_and_hands_out_lowest_first(arena):
+    n, free, ps = arena.info()
+    assert n == 10 and free == 10
+    assert arena.take(3).tolist() == [0, 1, 2]
+    assert arena.take(2).tolist() == [3, 4]
+    arena.give([1, 3], defer=False)
+    assert arena.take(3).tolist() == [1, 3, 5]
+    assert arena.info()[1] == 4
+
+
+def test_arena_short_of_pages_says_wait(arena):
+    arena.take(8)
+    with pytest.raises(pkv.PkvError) as e:
+        arena.take(3)
+    assert e.value.code == pkv.EAGAIN
+    assert arena.info()[1] == 2          # nothing was taken by the refused call
+
+
+def test_arena_refuses_foreign_or_double_give(arena):
+    ids = arena.take(2)
+    for bad in ([7], [0, 0], [-1], [10]):
+        with pytest.raises(pkv.PkvError):
+            arena.give(bad, defer=False)
+    arena.give(ids, defer=False)
+    with pytest.raises(pkv.PkvError):
+        arena.give(ids, defer=False)
+
+
+class FakeEvents:
+    """Event operations whose completion the test controls."""
+
+    def __init__(self):
+        self.done = set()
+        self.fail = set()
+        self.live = set()
+        self.n = 0
+
+        def record(ctx, stream, ev):
+            self.n += 1
+            ev[0] = self.n
+            self.live.add(self.n)
+            return 0
+
+        def query(ctx, ev):
+            if ev in self.fail:
+                return -1
+            return 0 if ev in self.done else 1
+
+        def destroy(ctx, ev):
+            self.live.discard(ev)
+
+        self.ops = pkv.EventOps(pkv.EventOps.RECORD(record), pkv.EventOps.QUERY(query),
+                                pkv.EventOps.DESTROY(destroy), None)
+
+
+def test_given_pages_return_only_after_the_stream_drains(arena):
+    ev = FakeEvents()
+    arena.set_event_ops(ev.ops)
+    ids = arena.take(10)
+    arena.give(ids[:4], stream=0x1234, defer=True)
+    assert arena.info()[1] == 0                # still in flight on the stream
+    with pytest.raises(pkv.PkvError) as e:
+        arena.take(1)
+    assert e.value.code == pkv.EAGAIN
+    with pytest.raises(pkv.PkvError):
+        arena.give(ids[:1], stream=0x1234)     # already pending: not held any more
+    ev.done.add(1)
+    assert arena.info()[1] == 4
+    assert ev.live == set()                    # the event was destroyed once done
+    assert arena.take(4).tolist() == [0, 1, 2, 3]
+
+
+def test_failed_event_query_is_reported_and_pages_stay_out(arena):
+    ev = FakeEvents()
+    arena.set_event_ops(ev.ops)
+    ids = arena.take(3)
+    arena.give(ids, stream=0x1, defer=True)
+    ev.fail.add(1)
+    with pytest.raises(pkv.PkvError) as e:
+        arena.take(1)
+    assert e.value.code == pkv.ECUDA
+    ev.fail.clear(); ev.done.add(1)
+    assert arena.take(1).tolist() == [0]
+
+
+def test_arena_pg_describes_the_pool(arena):
+    g = arena.pg(0x5000, n_table=3)
+    n, _, ps = arena.info()
+    assert (g.base, g.table, g.page_elems, g.page_pos, g.n_pages, g.n_table) == \
+        (0x100000, 0x5000, ps, 16, n, 3)
