@@ -364,6 +364,7 @@ def main_ours(args):
     torch.cuda.synchronize()
     clocks.start()
     t_wall = time.perf_counter()
+    torch.cuda.profiler.start()   # the profiler's capture range is the timed region
     for _ in range(args.steps):
         for p in PAGES:
             ev0[p].record()
@@ -378,6 +379,7 @@ def main_ours(args):
                 except Exception:
                     dec_events[p] = None
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     wall = time.perf_counter() - t_wall
     barrier(world)
     clk = clocks.stop()

@@ -234,8 +234,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             l1 = l1 * al1 + (p1 + p3);
             m0 = n0;
             m1 = n1;
-            const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
-            const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+            // P as a bf16 pair hi + lo (lo = p - hi is exact in float32), so the
+            // weights reach the float32 accumulator with ~16 significant bits
+            const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+            const uint32_t l01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+            const uint32_t l23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+            const uint32_t pb0 = movmatrix_t(h01), pb1 = movmatrix_t(h23);
+            const uint32_t pc0 = movmatrix_t(l01), pc1 = movmatrix_t(l23);
             // O^T[16 dims x 8 cols] += V^T P^T for the 16 dim tiles
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t y0, y1, y2, y3;
                 ldsm_x4_t(vb + v_lane + i * 32, y0, y1, y2, y3);
                 mma_bf16(acc[i], y0, y1, y2, y3, pb0, pb1);
+                mma_bf16(acc[i], y0, y1, y2, y3, pc0, pc1);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
@@ -313,13 +319,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// Combine a unit's split partials for one query column, splits in order:
+// Combine a unit's split partials for one query column:
 // M = max m_i, L = sum 2^(m_i-M) l_i, O = sum 2^(m_i-M) acc_i, out = O / L.
+// Every sum runs in a fixed order (lanes over splits i = lane + 32j, then a
+// butterfly; warps over splits i = w + 8j, then warps 0..7), so the result
+// depends only on the partials.
 template <bool kSparse>
 __global__ void __launch_bounds__(kCombThreads)
     decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
+    constexpr int kWarps = kCombThreads / 32;
     __shared__ float w[kMaxSplits];
-    __shared__ float inv_l;
+    __shared__ float lsum[kMaxSplits];
+    __shared__ float4 part[kWarps][kHeadDim / 4];
+    __shared__ float sh_m, sh_l;
     pdl_wait();
     pdl_trigger();
     const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
@@ -331,25 +343,64 @@ __global__ void __launch_bounds__(kCombThreads)
     const float *part_acc = a.ws + sd.ws_off;
     const float *part_ml = part_acc + (int64_t)units * ns * sd.ncols * kHeadDim;
     const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
-    for (int i = threadIdx.x; i < ns; i += kCombThreads)
-        w[i] = __ldcg(part_ml + (p0 + (int64_t)i * sd.ncols) * 2);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int i = 0; i < ns; ++i) M = fmaxf(M, w[i]);
-        float L = 0.f;
-        for (int i = 0; i < ns; ++i) {
-            const float wi = M == -INFINITY ? 0.f : ex2(w[i] - M);
-            L += wi * __ldcg(part_ml + (p0 + (int64_t)i * sd.ncols) * 2 + 1);
-            w[i] = wi;
-        }
-        inv_l = L;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < ns; i += kCombThreads) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part_ml + (p0 + (int64_t)i * sd.ncols) * 2));
+        w[i] = ml.x;
+        lsum[i] = ml.y;
     }
     __syncthreads();
-    const float L = inv_l;
-    const int d = threadIdx.x;  // kCombThreads == head dim
+    if (warp == 0) {
+        float M = -INFINITY;
+        for (int i = lane; i < ns; i += 32) M = fmaxf(M, w[i]);
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        for (int i = lane; i < ns; i += 32) {
+            const float wi = M == -INFINITY ? 0.f : ex2(w[i] - M);
+            w[i] = wi;
+            L += wi * lsum[i];
+        }
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) sh_l = L;
+    }
+    __syncthreads();
+    // warp `warp` sums splits warp, warp+8, ...; lane owns dims 4*lane.. and 128+4*lane..
+    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+    const float *base = part_acc + p0 * kHeadDim + 4 * lane;
+    const int64_t stride = (int64_t)sd.ncols * kHeadDim;
+    int i = warp;
+    for (; i + 3 * kWarps < ns; i += 4 * kWarps) {
+        float4 x[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float *src = base + (int64_t)(i + u * kWarps) * stride;
+            x[u][0] = __ldcg(reinterpret_cast<const float4 *>(src));
+            x[u][1] = __ldcg(reinterpret_cast<const float4 *>(src + 128));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float wi = w[i + u * kWarps];
+            o0.x += wi * x[u][0].x; o0.y += wi * x[u][0].y; o0.z += wi * x[u][0].z; o0.w += wi * x[u][0].w;
+            o1.x += wi * x[u][1].x; o1.y += wi * x[u][1].y; o1.z += wi * x[u][1].z; o1.w += wi * x[u][1].w;
+        }
+    }
+    for (; i < ns; i += kWarps) {
+        const float *src = base + (int64_t)i * stride;
+        const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(src));
+        const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(src + 128));
+        const float wi = w[i];
+        o0.x += wi * x0.x; o0.y += wi * x0.y; o0.z += wi * x0.z; o0.w += wi * x0.w;
+        o1.x += wi * x1.x; o1.y += wi * x1.y; o1.z += wi * x1.z; o1.w += wi * x1.w;
+    }
+    part[warp][lane] = o0;
+    part[warp][32 + lane] = o1;
+    __syncthreads();
+    const int d = tid;  // kCombThreads == head dim
+    const float *pf = reinterpret_cast<const float *>(part);
     float O = 0.f;
-    for (int i = 0; i < ns; ++i) O += w[i] * __ldcg(part_acc + (p0 + (int64_t)i * sd.ncols) * kHeadDim + d);
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) O += pf[k * kHeadDim + d];
+    const float L = sh_l;
     const float o = L > 0.f ? O / L : 0.f;
     Unit u;
     u.unit = unit;
