@@ -201,6 +201,14 @@ int pkv_pool(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int3
  * The split of each stream's keys depends only on its length and the GPU's
  * SM count, never on page size, so paged output equals contiguous output
  * bit for bit and a stream's output does not depend on the other streams.
+ * Fused store: with k_new and v_new (and ik_new when idx_dim > 0) non-NULL,
+ * laid out as for pkv_store, the call also writes the new tokens' rows into
+ * the cache (as pkv_store would) and reads them from those inputs; with them
+ * NULL the new rows must already be in the cache.
+ * Ordering: the call may read cached rows (positions below len - n_new)
+ * before the kernel queued just before it on the stream has finished, so that
+ * kernel must not write them; q, k_new, v_new, ik_new, ws and out are only
+ * touched after it finishes.
  * The split partials go to ws and a second kernel combines them, splits in
  * ascending order.  ws: device, >= pkv_decode_ws_size bytes (0 when no
  * stream needs more than one split), 256-byte aligned, no initialization;
@@ -208,8 +216,9 @@ int pkv_pool(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int3
 int pkv_decode_ws_size(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
                        int32_t n_q_heads, size_t *bytes);
 int pkv_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
-               int32_t n_q_heads, const void *q, void *out, void *ws, size_t ws_bytes,
-               int32_t *dev_status, cudaStream_t stream);
+               int32_t n_q_heads, const void *q, const void *k_new, const void *v_new,
+               const void *ik_new, void *out, void *ws, size_t ws_bytes, int32_t *dev_status,
+               cudaStream_t stream);
 
 /* ---- block scores (#1169: fn_qsa_scores reads pooled rows) ---------------
  * For each stream's one decode query (n_new == 1), head h and complete block

@@ -21,21 +21,42 @@
 namespace pkv {
 namespace {
 
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 6
+#endif
+#ifndef PKV_DECODE_MIN_SPLIT
+#define PKV_DECODE_MIN_SPLIT 256
+#endif
+#ifndef PKV_SPARSE_MIN_SPLIT
+#define PKV_SPARSE_MIN_SPLIT 64
+#endif
+#ifndef PKV_DECODE_CTAS_PER_SM
+#define PKV_DECODE_CTAS_PER_SM 2
+#endif
+
 constexpr int kTile = 16;                    // keys a stage
 constexpr int kRowBytes = 528;               // staged row stride: 512 + 16 (bank spread)
 constexpr int kStageBytes = 2 * kTile * kRowBytes;
-constexpr int kStages = 6;
+constexpr int kStages = PKV_DECODE_STAGES;
 constexpr int kCons = 4;                     // consumer warps
 constexpr int kThreads = (kCons + 1) * 32;
 constexpr int kMaxCols = 32;                 // query columns of one unit
-constexpr int kMinSplitDense = 128;          // keys
-constexpr int kMinSplitSparse = 64;
+constexpr int kMinSplitDense = PKV_DECODE_MIN_SPLIT;    // keys
+constexpr int kMinSplitSparse = PKV_SPARSE_MIN_SPLIT;
 constexpr int kMaxSplits = 512;
 constexpr int kCombThreads = 256;
+constexpr int kChunkPages = 64;              // page ids prefetched at a time
+constexpr int kMaxSparseBlocks = 256;        // blocks of one sparse split (k <= 256)
+constexpr int kMergeStride = kHeadDim + 4;   // floats; spreads the 4 column pairs over banks
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 
-constexpr size_t kSmemBytes = kStages * kStageBytes + kStages * kTile * 4 + 2 * kStages * 8 + 16;
-static_assert(kCons * 8 * kHeadDim * 4 + kCons * 8 * 2 * 4 <= kStages * kStageBytes,
+constexpr size_t kOffPos = (size_t)kStages * kStageBytes;
+constexpr size_t kOffPage = kOffPos + kStages * kTile * 4;
+constexpr size_t kOffBar = kOffPage + kMaxSparseBlocks * 8;
+constexpr size_t kSmemBytes = kOffBar + 2 * kStages * 8 + 16;
+static_assert(kMaxSparseBlocks >= kChunkPages, "page-offset buffer holds a chunk");
+static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * (2 + kCons) * 4 + 64 <=
+                  kStages * kStageBytes,
               "merge buffers reuse the stages");
 
 struct DecodeArgs {
@@ -44,6 +65,9 @@ struct DecodeArgs {
     float *ws;
     const int32_t *ids;  // sparse: [n_seqs][n_q_heads][k]
     int32_t k;
+    const uint16_t *k_new;   // fused store of the new tokens (dense), or null
+    const uint16_t *v_new;
+    const uint16_t *ik_new;
 };
 
 __device__ __forceinline__ float warp_max_lanes(float v) {
@@ -90,13 +114,43 @@ __device__ __forceinline__ int64_t q_row(const Common &c, const SeqDev &sd, cons
     return ((int64_t)sd.tok_off + j) * c.n_q_heads + u.kvh * c.group + (col - j * c.group);
 }
 
+__device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
+    const int lo = __shfl_sync(0xffffffffu, static_cast<int>(v), src);
+    const int hi = __shfl_sync(0xffffffffu, static_cast<int>(v >> 32), src);
+    return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
+}
+
+// Offsets of pages first .. first+63 from the stream's layer base (-1: an id
+// outside the arena, reported).  One warp; 2 table entries a lane.
+__device__ __forceinline__ void load_page_chunk(const SeqDev &sd, int first, int n_table,
+                                                int64_t *page_off, int lane, uint32_t *status) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        const int p = first + j;
+        int64_t off = 0;
+        if (p < n_table) {
+            const int id = __ldg(sd.table + p);
+            if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
+                off = (int64_t)id * sd.ps;
+            } else {
+                off = -1;
+                if (status) atomicOr(status, PKV_DEV_BAD_PAGE);
+            }
+        }
+        page_off[j] = off;
+    }
+    __syncwarp();
+}
+
 template <bool kSparse>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
     decode_partial(const __grid_constant__ Common c, const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stages = smem;
-    int32_t *kpos = reinterpret_cast<int32_t *>(smem + kStages * kStageBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(kpos + kStages * kTile);
+    int32_t *kpos = reinterpret_cast<int32_t *>(smem + kOffPos);
+    int64_t *page_off = reinterpret_cast<int64_t *>(smem + kOffPage);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *empty = full + kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
 
@@ -106,6 +160,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int ncols = sd.ncols;
     const int ncg = (ncols + 7) >> 3;
     const int ks_n = kCons / ncg;
+    const int H = c.n_kv_heads;
+    const int qbase = sd.len - sd.n_new;  // first new position
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -116,8 +172,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         fence_mbar_init();
     }
     __syncthreads();
-    pdl_wait();
-    pdl_trigger();
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float acc[16][4];
@@ -127,11 +181,54 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kCons) {
         // ---------------- producer ----------------
+        // Rows of cached positions do not depend on the previous kernel on the
+        // stream: they stream before the grid-dependency wait.  New positions
+        // (and, for sparse decode, the selected block ids) wait for it.
         const uint64_t pol = policy_evict_first();
+        const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;  // V row - K row
+        const bool fuse_store = !kSparse && a.k_new != nullptr;
+        bool waited = false;
+        int chunk_first = -(1 << 30);
+        int64_t fallback = 0;  // sparse: a row that is surely written (position 0)
+        if (kSparse) {
+            pdl_wait();
+            waited = true;
+            // one lookup per selected block of this split: the K row of its first key
+            const int32_t *ids = a.ids + ((int64_t)u.s * c.n_q_heads + u.unit) * a.k;
+            const int nb = sd.len / 4;
+            const int b0 = u.key0 >> 2, nblk = (u.key1 - u.key0 + 3) >> 2;
+            for (int j = lane; j < nblk; j += 32) {
+                const int b = __ldg(ids + b0 + j);
+                int64_t off = -1;
+                if (b >= 0 && b < nb) {
+                    int32_t row;
+                    int64_t pg = 0;
+                    if (sd.table) {
+                        const int page = (4 * b) / sd.ptok;
+                        row = 4 * b - page * sd.ptok;
+                        const int id = __ldg(sd.table + page);
+                        pg = static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)
+                                 ? (int64_t)id * sd.ps
+                                 : -1;
+                    } else {
+                        row = 4 * b;
+                    }
+                    if (pg >= 0) off = pg + off_k(sd.ptok, u.kvh, row);
+                }
+                if ((b >= nb || (b >= 0 && off < 0)) && c.status)
+                    atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                page_off[j] = off;
+            }
+            if (sd.table && lane == 0) {
+                const int id = __ldg(sd.table);
+                if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages))
+                    fallback = (int64_t)id * sd.ps;
+            }
+            fallback = shfl64(fallback, 0) + off_k(sd.ptok, u.kvh, 0);
+            __syncwarp();
+        }
         int issued = 0;
         bool ok = true;
-        const int32_t *ids = kSparse ? a.ids + ((int64_t)u.s * c.n_q_heads + u.unit) * a.k : nullptr;
-        const int nb = sd.len / 4;
         for (int t = 0; t < u.ntiles; ++t) {
             const int st = t % kStages, use = t / kStages;
             if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, c.status)) {
@@ -139,34 +236,96 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             if (*abort_flag) break;
-            const uint16_t *kr = nullptr, *vr = nullptr;
-            if (lane < kTile) {
-                const int i = u.key0 + t * kTile + lane;
-                int pos = -1;
-                if (i < u.key1) {
-                    if (kSparse) {
-                        const int b = __ldg(ids + (i >> 2));
-                        if (b >= 0 && b < nb) pos = 4 * b + (i & 3);
-                        else if (b >= nb && c.status) atomicOr(c.status, PKV_DEV_BAD_PAGE);
-                    } else {
+            const int i = u.key0 + t * kTile + lane;  // key index of this lane (lane < 16)
+            const bool mine = lane < kTile && i < u.key1;
+            int pos = -1;            // live key position, or -1 (masked)
+            int64_t krow = 0;        // element offset of the K row from layer_base
+            bool bad = false;        // its page id was outside the arena
+            bool fresh = false;      // the row comes from the new-token input
+            if (kSparse) {
+                krow = fallback;
+                if (mine) {
+                    const int64_t off = page_off[(i - u.key0) >> 2];
+                    if (off >= 0) {
                         pos = i;
+                        krow = off + (int64_t)(i & 3) * kHeadDim;
                     }
                 }
-                kpos[st * kTile + lane] = pos;
-                // a masked key still stages a real row, so every stage byte is finite data
-                const int src = pos >= 0 ? pos : (kSparse ? 0 : u.key0);
-                kr = k_row(sd, c.n_kv_heads, u.kvh, src, c.status);
-                vr = v_row(sd, c.n_kv_heads, u.kvh, src, c.status);
+            } else {
+                if (!waited && __any_sync(0xffffffffu, mine && i >= qbase)) {
+                    pdl_wait();
+                    waited = true;
+                }
+                const int key = lane < kTile ? min(i, u.key1 - 1) : u.key0;
+                int row = key;
+                int64_t pg = 0;
+                if (sd.table) {
+                    const int page = key / sd.ptok;
+                    row = key - page * sd.ptok;
+                    const bool out_of_chunk =
+                        lane < kTile && (page < chunk_first || page >= chunk_first + kChunkPages);
+                    if (__any_sync(0xffffffffu, out_of_chunk)) {
+                        chunk_first = __shfl_sync(0xffffffffu, page, 0);
+                        load_page_chunk(sd, chunk_first, sd.n_table, page_off, lane, c.status);
+                    }
+                    if (lane < kTile) pg = page_off[page - chunk_first];
+                    if (pg < 0) {
+                        bad = true;
+                        pg = 0;
+                    }
+                }
+                krow = pg + off_k(sd.ptok, u.kvh, row);
+                if (mine) pos = i;
+                fresh = fuse_store && key >= qbase;
             }
+            const uint16_t *ksrc, *vsrc;
+            if (fresh) {
+                const int key = min(i, u.key1 - 1);
+                const int64_t r = ((int64_t)sd.tok_off + (key - qbase)) * H + u.kvh;
+                ksrc = a.k_new + r * kHeadDim;
+                vsrc = a.v_new + r * kHeadDim;
+            } else {
+                ksrc = sd.layer_base + krow;
+                vsrc = ksrc + v_gap;
+            }
+            if (lane < kTile) kpos[st * kTile + lane] = pos;
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[st], kTile * 2 * 512);
             __syncwarp();
             if (lane < kTile) {
                 uint8_t *sk = stages + st * kStageBytes + lane * kRowBytes;
-                bulk_g2s(sk, kr, 512, &full[st], pol);
-                bulk_g2s(sk + kTile * kRowBytes, vr, 512, &full[st], pol);
+                bulk_g2s(sk, ksrc, 512, &full[st], pol);
+                bulk_g2s(sk + kTile * kRowBytes, vsrc, 512, &full[st], pol);
             }
             issued = t + 1;
+            // fused store: this tile's new rows go to the cache as well
+            if (fuse_store) {
+                unsigned todo = __ballot_sync(0xffffffffu, fresh && pos >= 0 && !bad);
+                while (todo) {
+                    const int src = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const int p = __shfl_sync(0xffffffffu, pos, src);
+                    const int64_t kr = shfl64(krow, src);
+                    const int64_t r = (int64_t)sd.tok_off + (p - qbase);
+                    uint16_t *dst = const_cast<uint16_t *>(sd.layer_base) + kr;
+                    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(
+                                               a.k_new + (r * H + u.kvh) * kHeadDim) + lane);
+                    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
+                                               a.v_new + (r * H + u.kvh) * kHeadDim) + lane);
+                    reinterpret_cast<uint4 *>(dst)[lane] = kv;
+                    reinterpret_cast<uint4 *>(dst + v_gap)[lane] = vv;
+                    if (u.kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
+                        // the indexer-key row of the same position, written once (KV head 0)
+                        const int64_t page_start = kr - off_k(sd.ptok, 0, 0) -
+                                                   (int64_t)(sd.table ? p % sd.ptok : p) * kHeadDim;
+                        const int prow = sd.table ? p % sd.ptok : p;
+                        uint16_t *idst = const_cast<uint16_t *>(sd.layer_base) + page_start +
+                                         off_ik(H, c.idx_dim, sd.ptok, prow);
+                        reinterpret_cast<uint4 *>(idst)[lane] = __ldg(
+                            reinterpret_cast<const uint4 *>(a.ik_new + r * c.idx_dim) + lane);
+                    }
+                }
+            }
         }
         if (!ok) *abort_flag = 1;
         if (*abort_flag) {
@@ -174,8 +333,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
                 mbar_wait(&full[t % kStages], (t / kStages) & 1, nullptr);
         }
+        if (!waited) pdl_wait();
     } else if (ks < ks_n) {
         // ---------------- consumer ----------------
+        pdl_wait();  // queries come from the previous kernel
         const int bcol = cg * 8 + (lane >> 2);
         uint32_t qf[16][2];
         {
@@ -191,7 +352,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         // the two columns this lane owns in S^T and O^T fragments, and the
         // last key position each may read (causal; -1 for a padding column)
         const int c0 = cg * 8 + 2 * (lane & 3), c1 = c0 + 1;
-        const int qbase = sd.len - sd.n_new;
         const int lim0 = c0 < ncols ? (kSparse ? INT32_MAX : qbase + c0 / c.group) : -1;
         const int lim1 = c1 < ncols ? (kSparse ? INT32_MAX : qbase + c1 / c.group) : -1;
 
@@ -258,19 +418,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         l0 = warp_sum_lanes(l0);
         l1 = warp_sum_lanes(l1);
+    } else {
+        pdl_wait();
     }
 
     __syncthreads();
+    pdl_trigger();  // every thread has passed its grid-dependency wait
     if (*abort_flag) return;
 
     // ---- merge the key slices (ks = 0, 1, ...) in order, inside the CTA ----
     const int NC = ncg * 8;
-    float *mbuf = reinterpret_cast<float *>(stages);     // [ks][NC][256]
-    float *mlb = mbuf + ks_n * NC * kHeadDim;             // [ks][NC][2]
+    float *mbuf = reinterpret_cast<float *>(stages);               // [ks][NC][kMergeStride]
+    float *mlb = mbuf + ks_n * NC * kMergeStride;                   // [ks][NC][2]
+    float *wts = mlb + ks_n * NC * 2;                               // [ks][NC]
+    float *lt = wts + ks_n * NC;                                    // [NC]
     if (warp < kCons && ks < ks_n) {
         const int c0 = cg * 8 + 2 * (lane & 3);
-        float *b0 = mbuf + (ks * NC + c0) * kHeadDim;
-        float *b1 = b0 + kHeadDim;
+        float *b0 = mbuf + (ks * NC + c0) * kMergeStride;
+        float *b1 = b0 + kMergeStride;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int d = i * 16 + (lane >> 2);
@@ -287,6 +452,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     __syncthreads();
+    float *mout = lt + NC;  // [NC]: the merged maximum of each column
+    if (tid < NC) {
+        float M = -INFINITY;
+        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + tid) * 2]);
+        float L = 0.f;
+        for (int k = 0; k < ks_n; ++k) {
+            const float w = M == -INFINITY ? 0.f : ex2(mlb[(k * NC + tid) * 2] - M);
+            wts[k * NC + tid] = w;
+            L += w * mlb[(k * NC + tid) * 2 + 1];
+        }
+        lt[tid] = L;
+        mout[tid] = M;
+    }
+    __syncthreads();
 
     const bool single = sd.nsplit == 1;
     const int units = kSparse ? c.n_q_heads : c.n_kv_heads;
@@ -295,16 +474,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t pidx = ((int64_t)u.unit * sd.nsplit + u.split) * ncols;
     for (int idx = tid; idx < ncols * kHeadDim; idx += kThreads) {
         const int col = idx / kHeadDim, d = idx - col * kHeadDim;
-        float M = -INFINITY;
-        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + col) * 2]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-            for (int k = 0; k < ks_n; ++k) {
-                const float w = ex2(mlb[(k * NC + col) * 2] - M);
-                L += w * mlb[(k * NC + col) * 2 + 1];
-                O += w * mbuf[(k * NC + col) * kHeadDim + d];
-            }
-        }
+        float O = 0.f;
+        for (int k = 0; k < ks_n; ++k) O += wts[k * NC + col] * mbuf[(k * NC + col) * kMergeStride + d];
+        const float L = lt[col];
         if (single) {
             const float o = L > 0.f ? O / L : 0.f;
             a.out[q_row<kSparse>(c, sd, u, col) * kHeadDim + d] =
@@ -312,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         } else {
             part_acc[(pidx + col) * kHeadDim + d] = O;
             if (d == 0) {
-                part_ml[(pidx + col) * 2 + 0] = M;
+                part_ml[(pidx + col) * 2 + 0] = mout[col];
                 part_ml[(pidx + col) * 2 + 1] = L;
             }
         }
@@ -456,8 +628,10 @@ int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
 }
 
 int launch_decode(const Common &c, const DecodePlan &plan, bool sparse, const uint16_t *q,
-                  const int32_t *ids, int32_t k, uint16_t *out, float *ws, cudaStream_t stream) {
-    DecodeArgs a{q, out, ws, ids, k};
+                  const int32_t *ids, int32_t k, uint16_t *out, float *ws,
+                  const uint16_t *k_new, const uint16_t *v_new, const uint16_t *ik_new,
+                  cudaStream_t stream) {
+    DecodeArgs a{q, out, ws, ids, k, k_new, v_new, ik_new};
     // streams with no queries own no CTAs: give them an empty range
     Common cc = c;
     auto part = sparse ? decode_partial<true> : decode_partial<false>;

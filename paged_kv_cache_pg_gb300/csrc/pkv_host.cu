@@ -84,6 +84,7 @@ int fill_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_
         d.ps = q.pg.page_elems;
         d.ptok = q.pg.page_pos;
         d.n_pages = q.pg.table ? q.pg.n_pages : 1;
+        d.n_table = q.pg.table ? q.pg.n_table : 1;
         d.len = q.len;
         d.n_new = q.n_new;
         d.tok_off = tok;
@@ -416,19 +417,27 @@ extern "C" int pkv_decode_ws_size(const pkv_layout *L, const pkv_seq *seqs, int3
 }
 
 extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
-                          int32_t n_q_heads, const void *q, void *out, void *ws,
-                          size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+                          int32_t n_q_heads, const void *q, const void *k_new, const void *v_new,
+                          const void *ik_new, void *out, void *ws, size_t ws_bytes,
+                          int32_t *dev_status, cudaStream_t stream) {
     Common c;
     DecodePlan plan;
     int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, false, 0, dev_status, &c, &plan);
     if (rc) return rc;
     if (plan.total_items == 0) return PKV_OK;
     if (!q || !out || !aligned16(q) || !aligned16(out)) return PKV_EINVAL;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_EINVAL;
+    if (k_new) {
+        if (!aligned16(k_new) || !aligned16(v_new)) return PKV_EINVAL;
+        if (L->idx_dim && (!ik_new || !aligned16(ik_new))) return PKV_EINVAL;
+    }
     if (plan.ws_bytes > 0 &&
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
     return launch_decode(c, plan, false, static_cast<const uint16_t *>(q), nullptr, 0,
-                         static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
+                         static_cast<uint16_t *>(out), static_cast<float *>(ws),
+                         static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+                         k_new ? static_cast<const uint16_t *>(ik_new) : nullptr, stream);
 }
 
 extern "C" int pkv_sparse_ws_size(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
@@ -456,7 +465,8 @@ extern "C" int pkv_sparse_decode(const pkv_layout *L, const pkv_seq *seqs, int32
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
     return launch_decode(c, plan, true, static_cast<const uint16_t *>(q), ids, k,
-                         static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
+                         static_cast<uint16_t *>(out), static_cast<float *>(ws), nullptr, nullptr,
+                         nullptr, stream);
 }
 
 extern "C" int pkv_block_scores(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,

@@ -25,6 +25,7 @@ struct SeqDev {
     int64_t ps;            // elements in a page
     int32_t ptok;          // positions in a page
     int32_t n_pages;       // arena pages (table entries must be below)
+    int32_t n_table;       // table entries (1 when contiguous)
     int32_t len;           // valid positions after the new tokens
     int32_t n_new;         // new tokens (queries) of this call
     int32_t tok_off;       // first packed row of this stream's new tokens
@@ -90,6 +91,7 @@ struct DecodePlan {
 int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan);
 int launch_decode(const Common &c, const DecodePlan &plan, bool sparse, const uint16_t *q,
                   const int32_t *ids, int32_t k, uint16_t *out, float *ws,
+                  const uint16_t *k_new, const uint16_t *v_new, const uint16_t *ik_new,
                   cudaStream_t stream);
 int launch_scores(const Common &c, float *scores, int32_t ld, const uint16_t *qi,
                   int32_t max_nb, cudaStream_t stream);

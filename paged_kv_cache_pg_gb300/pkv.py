@@ -91,7 +91,7 @@ def load(path: Optional[str] = None):
         "pkv_gather": [LP, SP, i32, i32, i32, vp, vp, vp],
         "pkv_pool": [LP, SP, i32, i32, vp, vp],
         "pkv_decode_ws_size": [LP, SP, i32, i32, ctypes.POINTER(sz)],
-        "pkv_decode": [LP, SP, i32, i32, i32, vp, vp, vp, sz, vp, vp],
+        "pkv_decode": [LP, SP, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp],
         "pkv_block_scores": [LP, SP, i32, i32, i32, vp, vp, i32, vp, vp],
         "pkv_topk": [SP, i32, i32, vp, i32, i32, vp, vp],
         "pkv_sparse_ws_size": [LP, SP, i32, i32, i32, ctypes.POINTER(sz)],
@@ -251,11 +251,14 @@ def decode_ws_size(lay, seqs, n_q_heads) -> int:
     return out.value
 
 
-def decode(lay, seqs, layer, n_q_heads, q, out, ws, status=None, stream=None):
+def decode(lay, seqs, layer, n_q_heads, q, out, ws, status=None, stream=None, k_new=None,
+           v_new=None, ik_new=None):
+    """Decode attention; with k_new/v_new (and ik_new) the new rows are stored too."""
     arr, n = _seqs(seqs)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-    _check(load().pkv_decode(ctypes.byref(lay), arr, n, layer, n_q_heads, _ptr(q), _ptr(out),
-                             _ptr(ws), ws_bytes, _ptr(status), _stream(stream)), "pkv_decode")
+    _check(load().pkv_decode(ctypes.byref(lay), arr, n, layer, n_q_heads, _ptr(q), _ptr(k_new),
+                             _ptr(v_new), _ptr(ik_new), _ptr(out), _ptr(ws), ws_bytes,
+                             _ptr(status), _stream(stream)), "pkv_decode")
 
 
 def block_scores(lay, seqs, layer, n_q_heads, qi, scores, ld, status=None, stream=None):

@@ -144,7 +144,8 @@ def test_decode_refuses_too_many_query_columns(lib):
     arr, n = pkv._seqs([s])
     out = ctypes.c_size_t()
     # 5 queries x 8 heads a KV head = 40 columns > 32; checked before any device query
-    rc = pkv.load().pkv_decode(ctypes.byref(lay), arr, n, 0, 16, 1, 1, None, 0, None, None)
+    rc = pkv.load().pkv_decode(ctypes.byref(lay), arr, n, 0, 16, 16, None, None, None, 16, None,
+                               0, None, None)
     assert rc == pkv.EINVAL
 
 

@@ -157,3 +157,52 @@ def test_status_word_stays_clear_on_good_input(multi):
     out = decode(pl, 1, 16, q, status=status)
     assert int(status.item()) == 0
     assert np.array_equal(out, base)
+
+
+@pytest.mark.parametrize("ptok", [16, 48, None])
+def test_fused_store_decode_equals_store_then_decode(ptok):
+    # Lengths put a split boundary (multiples of 256 keys) inside the 4-token
+    # window of the first stream; the second stream's window starts a split.
+    from gpu_setup import CANARY
+    t = torch()
+    lay = pkv.layout(2, 2, 256, 128)
+    lens = [258, 516, 1000, 37]
+    nq, layer = 4, 1
+    full = _streams(lens, 2, 2, seed=900)
+    q = [synth.queries(950 + i, nq, 16, 256) for i in range(len(lens))]
+    kn = dev_u16(np.concatenate([s.k[layer][-nq:] for s in full]))
+    vn = dev_u16(np.concatenate([s.v[layer][-nq:] for s in full]))
+    ikn = dev_u16(np.concatenate([s.ik[layer][-nq:] for s in full]))
+    dq = dev_u16(np.concatenate(q))
+    canary = int(np.array([CANARY], np.uint16).view(np.int16)[0])
+    outs, bodies = [], []
+    for fused in (False, True):
+        pl = place(lay, full, ptok, seed=7)
+        # blank the window rows: the call itself must write them
+        for i, T in enumerate(lens):
+            body = pl.body(0 if ptok else i)
+            tab = pl.tables[i] if ptok else None
+            for p in range(T - nq, T):
+                for kind, heads, width in ((pkv.K, 2, 256), (pkv.V, 2, 256), (pkv.IK, 1, 128)):
+                    for h in range(heads):
+                        off = pkv.pg_row(lay, pl.pgs[i], tab, layer, kind, h, p)
+                        body[off:off + width] = canary
+        seqs = pl.seqs(lens, [nq] * len(lens))
+        out = t.zeros_like(dq)
+        ws = t.zeros(pkv.decode_ws_size(lay, seqs, 16) // 4 + 64, dtype=t.float32, device="cuda")
+        if fused:
+            pkv.decode(lay, seqs, layer, 16, dq, out, ws, k_new=kn, v_new=vn, ik_new=ikn)
+        else:
+            pkv.store(lay, seqs, layer, kn, vn, ikn)
+            pkv.decode(lay, seqs, layer, 16, dq, out, ws)
+        t.cuda.synchronize()
+        outs.append(host_u16(out))
+        bodies.append([host_u16(pl.body(i)) for i in range(len(pl.buffers))])
+        # the stored bytes are the oracle's placement of the full streams
+        for i in range(len(pl.buffers)):
+            assert np.array_equal(bodies[-1][i], pl.oarenas[i])
+        assert pl.guards_intact()
+    assert np.array_equal(outs[0], outs[1])
+    ref_pl = place(lay, full, None)
+    ok, worst = within_tol(outs[1], oracle_decode(ref_pl, layer, 16, q))
+    assert ok, worst
