@@ -266,7 +266,7 @@ def main_ours(args):
         if p is None:
             pgs, mems = [], []
             for L in lens_after:
-                cap = -(-L // 4) * 4
+                cap = -(-L // 256) * 256   # a reserved window, rounded to 256 positions
                 ps = pkv.page_elems(lay, cap)
                 m = torch.empty(ps, dtype=torch.int16, device=dev)
                 mems.append(m)

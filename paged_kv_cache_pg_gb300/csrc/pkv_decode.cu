@@ -35,8 +35,9 @@ namespace {
 #endif
 
 constexpr int kTile = 16;                    // keys a stage
-constexpr int kRowBytes = 528;               // staged row stride: 512 + 16 (bank spread)
-constexpr int kStageBytes = 2 * kTile * kRowBytes;
+constexpr int kPlane = 2048;                 // one 64-dim column chunk of 16 rows (bytes)
+constexpr int kHalfStage = 4 * kPlane;       // the K (or V) tile: 16 rows x 512 B, swizzled
+constexpr int kStageBytes = 2 * kHalfStage;
 constexpr int kStages = PKV_DECODE_STAGES;
 constexpr int kCons = 4;                     // consumer warps
 constexpr int kThreads = (kCons + 1) * 32;
@@ -53,7 +54,7 @@ constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(2
 constexpr size_t kOffPos = (size_t)kStages * kStageBytes;
 constexpr size_t kOffPage = kOffPos + kStages * kTile * 4;
 constexpr size_t kOffBar = kOffPage + kMaxSparseBlocks * 8;
-constexpr size_t kSmemBytes = kOffBar + 2 * kStages * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + kOffBar + 2 * kStages * 8 + 16;  // + alignment slack
 static_assert(kMaxSparseBlocks >= kChunkPages, "page-offset buffer holds a chunk");
 static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * (2 + kCons) * 4 + 64 <=
                   kStages * kStageBytes,
@@ -69,6 +70,14 @@ struct DecodeArgs {
     const uint16_t *v_new;
     const uint16_t *ik_new;
 };
+
+// Byte offset of 16-byte chunk c (0..31 along the 512-byte row) of row r
+// (0..15) inside a K or V tile.  The tile is four 2 KB planes (one per 64
+// dims), each 16 rows of 128 B with the TMA 128-byte swizzle: chunk c & 7 of
+// row r sits at position (c & 7) ^ (r & 7).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return (c >> 3) * kPlane + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
 
 __device__ __forceinline__ float warp_max_lanes(float v) {
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
@@ -145,8 +154,11 @@ __device__ __forceinline__ void load_page_chunk(const SeqDev &sd, int first, int
 
 template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
-    decode_partial(const __grid_constant__ Common c, const DecodeArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    decode_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
+                   const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
     int32_t *kpos = reinterpret_cast<int32_t *>(smem + kOffPos);
     int64_t *page_off = reinterpret_cast<int64_t *>(smem + kOffPage);
@@ -184,9 +196,15 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
         // Rows of cached positions do not depend on the previous kernel on the
         // stream: they stream before the grid-dependency wait.  New positions
         // (and, for sparse decode, the selected block ids) wait for it.
+        // A full tile inside one page whose rows sit on the stream's TMA map
+        // is one 2D tensor copy per 64-dim chunk (8 per tile, K and V); any
+        // other tile (the ragged tail, new rows, pages not a multiple of 16,
+        // selected blocks) is staged key by key with 16-byte cp.async through
+        // the same swizzle, from one row lookup per key.
         const uint64_t pol = policy_evict_first();
         const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;  // V row - K row
         const bool fuse_store = !kSparse && a.k_new != nullptr;
+        const void *map = (!kSparse && sd.tma >= 0) ? &maps.map[sd.tma] : nullptr;
         bool waited = false;
         int chunk_first = -(1 << 30);
         int64_t fallback = 0;  // sparse: a row that is surely written (position 0)
@@ -278,24 +296,49 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
                 if (mine) pos = i;
                 fresh = fuse_store && key >= qbase;
             }
-            const uint16_t *ksrc, *vsrc;
-            if (fresh) {
-                const int key = min(i, u.key1 - 1);
-                const int64_t r = ((int64_t)sd.tok_off + (key - qbase)) * H + u.kvh;
-                ksrc = a.k_new + r * kHeadDim;
-                vsrc = a.v_new + r * kHeadDim;
-            } else {
-                ksrc = sd.layer_base + krow;
-                vsrc = ksrc + v_gap;
-            }
             if (lane < kTile) kpos[st * kTile + lane] = pos;
+            uint8_t *kst = stages + st * kStageBytes;
+            uint8_t *vst = kst + kHalfStage;
+            // a whole tile of cached rows inside one page goes by TMA
+            const bool tile_tma = map != nullptr &&
+                                  __all_sync(0xffffffffu, lane >= kTile || (pos >= 0 && !fresh));
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&full[st], kTile * 2 * 512);
-            __syncwarp();
-            if (lane < kTile) {
-                uint8_t *sk = stages + st * kStageBytes + lane * kRowBytes;
-                bulk_g2s(sk, ksrc, 512, &full[st], pol);
-                bulk_g2s(sk + kTile * kRowBytes, vsrc, 512, &full[st], pol);
+            if (tile_tma) {
+                if (lane == 0) {
+                    // rows of 256 elements from the map base: krow is row-aligned
+                    const int y = static_cast<int>(sd.layer_row + krow / kHeadDim);
+                    const int yv = y + static_cast<int>(v_gap / kHeadDim);
+                    mbar_arrive_expect_tx(&full[st], kTile * 2 * 512);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        tma_load_2d(kst + j * kPlane, map, 64 * j, y, &full[st], pol);
+                        tma_load_2d(vst + j * kPlane, map, 64 * j, yv, &full[st], pol);
+                    }
+                }
+            } else {
+                const uint16_t *ksrc, *vsrc;
+                if (fresh) {
+                    const int key = min(i, u.key1 - 1);
+                    const int64_t r = ((int64_t)sd.tok_off + (key - qbase)) * H + u.kvh;
+                    ksrc = a.k_new + r * kHeadDim;
+                    vsrc = a.v_new + r * kHeadDim;
+                } else {
+                    ksrc = sd.layer_base + krow;
+                    vsrc = ksrc + v_gap;
+                }
+                // key r's row comes from lane r's address: one lookup per key per tile
+                const int64_t kp = reinterpret_cast<int64_t>(ksrc);
+                const int64_t vp = reinterpret_cast<int64_t>(vsrc);
+#pragma unroll 4
+                for (int r = 0; r < kTile; ++r) {
+                    const uint16_t *kr = reinterpret_cast<const uint16_t *>(shfl64(kp, r));
+                    const uint16_t *vr = reinterpret_cast<const uint16_t *>(shfl64(vp, r));
+                    cp_async16(kst + swz(r, lane), kr + lane * 8, pol);
+                    cp_async16(vst + swz(r, lane), vr + lane * 8, pol);
+                }
+                cp_async_mbar_arrive(&full[st]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[st]);
             }
             issued = t + 1;
             // fused store: this tile's new rows go to the cache as well
@@ -316,9 +359,8 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
                     reinterpret_cast<uint4 *>(dst + v_gap)[lane] = vv;
                     if (u.kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
                         // the indexer-key row of the same position, written once (KV head 0)
-                        const int64_t page_start = kr - off_k(sd.ptok, 0, 0) -
-                                                   (int64_t)(sd.table ? p % sd.ptok : p) * kHeadDim;
                         const int prow = sd.table ? p % sd.ptok : p;
+                        const int64_t page_start = kr - (int64_t)prow * kHeadDim;
                         uint16_t *idst = const_cast<uint16_t *>(sd.layer_base) + page_start +
                                          off_ik(H, c.idx_dim, sd.ptok, prow);
                         reinterpret_cast<uint4 *>(idst)[lane] = __ldg(
@@ -356,8 +398,10 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
         const int lim1 = c1 < ncols ? (kSparse ? INT32_MAX : qbase + c1 / c.group) : -1;
 
         const uint32_t s_base = smem_u32(stages);
-        const uint32_t k_lane = ((lane & 7) + 8 * ((lane >> 3) & 1)) * kRowBytes + 16 * (lane >> 4);
-        const uint32_t v_lane = ((lane & 7) + 8 * (lane >> 4)) * kRowBytes + 16 * ((lane >> 3) & 1);
+        // ldmatrix rows: K fragments take keys (lane & 7) + 8 * bit 3, V^T fragments
+        // keys (lane & 7) + 8 * bit 4; column chunk bit from bit 4 (K) or bit 3 (V)
+        const int kr_ = (lane & 7) + 8 * ((lane >> 3) & 1), kcb = lane >> 4;
+        const int vr_ = (lane & 7) + 8 * (lane >> 4), vcb = (lane >> 3) & 1;
 
         for (int t = ks; t < u.ntiles; t += ks_n) {
             const int st = t % kStages, use = t / kStages;
@@ -366,15 +410,15 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
                 break;
             }
             const uint32_t kb = s_base + st * kStageBytes;
-            const uint32_t vb = kb + kTile * kRowBytes;
+            const uint32_t vb = kb + kHalfStage;
             // S^T[16 keys x 8 cols] = K Q^T, two accumulator chains
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < 16; kk += 2) {
                 uint32_t x0, x1, x2, x3;
-                ldsm_x4(kb + k_lane + kk * 32, x0, x1, x2, x3);
+                ldsm_x4(kb + swz(kr_, 2 * kk + kcb), x0, x1, x2, x3);
                 mma_bf16(sa, x0, x1, x2, x3, qf[kk][0], qf[kk][1]);
-                ldsm_x4(kb + k_lane + (kk + 1) * 32, x0, x1, x2, x3);
+                ldsm_x4(kb + swz(kr_, 2 * (kk + 1) + kcb), x0, x1, x2, x3);
                 mma_bf16(sb, x0, x1, x2, x3, qf[kk + 1][0], qf[kk + 1][1]);
             }
             const int kp0 = kpos[st * kTile + (lane >> 2)];
@@ -409,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
                 acc[i][2] *= al0;
                 acc[i][3] *= al1;
                 uint32_t y0, y1, y2, y3;
-                ldsm_x4_t(vb + v_lane + i * 32, y0, y1, y2, y3);
+                ldsm_x4_t(vb + swz(vr_, 2 * i + vcb), y0, y1, y2, y3);
                 mma_bf16(acc[i], y0, y1, y2, y3, pb0, pb1);
                 mma_bf16(acc[i], y0, y1, y2, y3, pc0, pc1);
             }
@@ -432,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
     float *mlb = mbuf + ks_n * NC * kMergeStride;                   // [ks][NC][2]
     float *wts = mlb + ks_n * NC * 2;                               // [ks][NC]
     float *lt = wts + ks_n * NC;                                    // [NC]
+    float *mout = lt + NC;                                          // [NC]
     if (warp < kCons && ks < ks_n) {
         const int c0 = cg * 8 + 2 * (lane & 3);
         float *b0 = mbuf + (ks * NC + c0) * kMergeStride;
@@ -452,7 +497,6 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
         }
     }
     __syncthreads();
-    float *mout = lt + NC;  // [NC]: the merged maximum of each column
     if (tid < NC) {
         float M = -INFINITY;
         for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + tid) * 2]);
@@ -627,8 +671,8 @@ int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
     return PKV_OK;
 }
 
-int launch_decode(const Common &c, const DecodePlan &plan, bool sparse, const uint16_t *q,
-                  const int32_t *ids, int32_t k, uint16_t *out, float *ws,
+int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &maps, bool sparse,
+                  const uint16_t *q, const int32_t *ids, int32_t k, uint16_t *out, float *ws,
                   const uint16_t *k_new, const uint16_t *v_new, const uint16_t *ik_new,
                   cudaStream_t stream) {
     DecodeArgs a{q, out, ws, ids, k, k_new, v_new, ik_new};
@@ -643,7 +687,7 @@ int launch_decode(const Common &c, const DecodePlan &plan, bool sparse, const ui
             return PKV_ECUDA;
         attr_set[sparse] = true;
     }
-    cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, a);
+    cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;
     if (plan.total_comb > 0) {
         e = launch_pdl(comb, plan.total_comb, kCombThreads, 0, stream, cc, a);

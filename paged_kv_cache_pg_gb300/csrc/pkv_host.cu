@@ -7,6 +7,9 @@
 #include <new>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -95,6 +98,84 @@ int fill_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- TMA row maps ------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+namespace {
+struct MapKey {
+    uintptr_t base;
+    uint64_t rows;
+};
+std::mutex g_map_mu;
+std::vector<std::pair<MapKey, RowMap>> g_maps;  // encoded maps, most recent last
+}  // namespace
+
+int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows) {
+    if (rows == 0 || rows > (1ull << 31) || !aligned16(base)) return -1;
+    RowMap m;
+    bool have = false;
+    {
+        std::lock_guard<std::mutex> g(g_map_mu);
+        for (auto &e : g_maps)
+            if (e.first.base == reinterpret_cast<uintptr_t>(base) && e.first.rows == rows) {
+                m = e.second;
+                have = true;
+                break;
+            }
+    }
+    if (!have) {
+        auto fn = encode_fn();
+        if (!fn) return -1;
+        cuuint64_t dims[2] = {256, rows};
+        cuuint64_t strides[1] = {512};
+        cuuint32_t box[2] = {64, 16};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = fn(reinterpret_cast<CUtensorMap *>(m.bytes), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return -1;
+        std::lock_guard<std::mutex> g(g_map_mu);
+        if (g_maps.size() >= 256) g_maps.erase(g_maps.begin());
+        g_maps.push_back({{reinterpret_cast<uintptr_t>(base), rows}, m});
+    }
+    for (int i = 0; i < n_maps; ++i)
+        if (std::memcmp(maps.map[i].bytes, m.bytes, sizeof(m.bytes)) == 0) return i;
+    if (n_maps >= kMaxMaps) return -1;
+    maps.map[n_maps] = m;
+    return n_maps++;
+}
+
+void plan_maps(Common &c, const pkv_layout *L, const pkv_seq *seqs, DecodeMaps &maps) {
+    int n_maps = 0;
+    for (int s = 0; s < c.n_seqs; ++s) {
+        SeqDev &d = c.seq[s];
+        d.tma = -1;
+        const pkv_pg &pg = seqs[s].pg;
+        const int64_t layer_off =
+            (int64_t)c.layer * layer_elems(L->n_kv_heads, L->idx_dim, pg.page_pos);
+        if (pg.page_pos % 16 != 0 || pg.page_elems % 256 != 0 || layer_off % 256 != 0) continue;
+        const uint64_t rows = (uint64_t)(pg.table ? pg.n_pages : 1) * pg.page_elems / 256;
+        d.tma = row_map(maps, n_maps, pg.base, rows);
+        d.layer_row = layer_off / 256;
+        d.page_rows = pg.page_elems / 256;
+    }
+}
 
 static int total_new(const Common &c) {
     int t = 0;
@@ -434,7 +515,9 @@ extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
     if (plan.ws_bytes > 0 &&
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
-    return launch_decode(c, plan, false, static_cast<const uint16_t *>(q), nullptr, 0,
+    DecodeMaps maps;  // copied into the launch's parameters
+    plan_maps(c, L, seqs, maps);
+    return launch_decode(c, plan, maps, false, static_cast<const uint16_t *>(q), nullptr, 0,
                          static_cast<uint16_t *>(out), static_cast<float *>(ws),
                          static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
                          k_new ? static_cast<const uint16_t *>(ik_new) : nullptr, stream);
@@ -464,7 +547,9 @@ extern "C" int pkv_sparse_decode(const pkv_layout *L, const pkv_seq *seqs, int32
     if (plan.ws_bytes > 0 &&
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
-    return launch_decode(c, plan, true, static_cast<const uint16_t *>(q), ids, k,
+    for (int s = 0; s < c.n_seqs; ++s) c.seq[s].tma = -1;  // selected blocks: cp.async path
+    DecodeMaps maps;
+    return launch_decode(c, plan, maps, true, static_cast<const uint16_t *>(q), ids, k,
                          static_cast<uint16_t *>(out), static_cast<float *>(ws), nullptr, nullptr,
                          nullptr, stream);
 }

@@ -35,7 +35,25 @@ struct SeqDev {
     int32_t comb_off;      // first CTA of this stream in the combine launch
     int32_t ncols;         // query columns of one unit: n_new * group (decode)
     int64_t ws_off;        // float offset of this stream's partials in ws
+    int32_t tma;           // decode: index of the stream's row tensor map, or -1
+    int32_t pad_;
+    int64_t layer_row;     // row (256 elements) of layer_base from the map's base
+    int64_t page_rows;     // rows in a page (page_elems / 256)
 };
+
+// A 2D TMA view of a buffer as rows of 256 bf16 (512 B), boxes of 64 x 16
+// elements with 128-byte swizzle: one box is 16 consecutive key (or value)
+// rows of one 64-element column chunk.
+constexpr int kMaxMaps = 16;
+struct alignas(64) RowMap {
+    unsigned char bytes[128];  // CUtensorMap
+};
+struct DecodeMaps {
+    RowMap map[kMaxMaps];
+};
+// Index of the map for [base, base + rows*512 B) in `maps` (added if new),
+// or -1 when none can be made (no driver entry point, or maps full).
+int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows);
 
 struct Common {
     int32_t n_seqs;
@@ -89,8 +107,11 @@ struct DecodePlan {
     size_t ws_bytes;       // counters + partials
 };
 int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan);
-int launch_decode(const Common &c, const DecodePlan &plan, bool sparse, const uint16_t *q,
-                  const int32_t *ids, int32_t k, uint16_t *out, float *ws,
+// Give each eligible dense stream its row map (page size a multiple of 16,
+// rows of 256 elements aligned to the buffer base).
+void plan_maps(Common &c, const pkv_layout *layout, const pkv_seq *seqs, DecodeMaps &maps);
+int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &maps, bool sparse,
+                  const uint16_t *q, const int32_t *ids, int32_t k, uint16_t *out, float *ws,
                   const uint16_t *k_new, const uint16_t *v_new, const uint16_t *ik_new,
                   cudaStream_t stream);
 int launch_scores(const Common &c, float *scores, int32_t ld, const uint16_t *qi,
