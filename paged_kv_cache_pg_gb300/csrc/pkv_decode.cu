@@ -21,8 +21,8 @@
 namespace pkv {
 namespace {
 
-#ifndef PKV_DECODE_STAGES
-#define PKV_DECODE_STAGES 6
+#ifndef PKV_DECODE_SLOTS
+#define PKV_DECODE_SLOTS 12
 #endif
 #ifndef PKV_DECODE_MIN_SPLIT
 #define PKV_DECODE_MIN_SPLIT 256
@@ -30,34 +30,33 @@ namespace {
 #ifndef PKV_SPARSE_MIN_SPLIT
 #define PKV_SPARSE_MIN_SPLIT 64
 #endif
-#ifndef PKV_DECODE_CTAS_PER_SM
-#define PKV_DECODE_CTAS_PER_SM 2
-#endif
 
-constexpr int kTile = 16;                    // keys a stage
+constexpr int kTile = 16;                    // keys a stage slot
 constexpr int kPlane = 2048;                 // one 64-dim column chunk of 16 rows (bytes)
 constexpr int kHalfStage = 4 * kPlane;       // the K (or V) tile: 16 rows x 512 B, swizzled
 constexpr int kStageBytes = 2 * kHalfStage;
-constexpr int kStages = PKV_DECODE_STAGES;
-constexpr int kCons = 4;                     // consumer warps
-constexpr int kThreads = (kCons + 1) * 32;
+constexpr int kSlots = PKV_DECODE_SLOTS;     // stage slots of a CTA, shared by its key slices
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCols = 32;                 // query columns of one unit
 constexpr int kMinSplitDense = PKV_DECODE_MIN_SPLIT;    // keys
 constexpr int kMinSplitSparse = PKV_SPARSE_MIN_SPLIT;
-constexpr int kMaxSplits = 512;
+constexpr int kMaxSplitLen = 1024;           // keys of one split (bounds the page list)
+constexpr int kMaxSplits = 2048;
 constexpr int kCombThreads = 256;
-constexpr int kChunkPages = 64;              // page ids prefetched at a time
-constexpr int kMaxSparseBlocks = 256;        // blocks of one sparse split (k <= 256)
+constexpr int kMaxPages = kMaxSplitLen / 4 + 2;  // pages one split can touch
+constexpr int kMaxSparseBlocks = kMaxSplitLen / 4;
 constexpr int kMergeStride = kHeadDim + 4;   // floats; spreads the 4 column pairs over banks
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 
-constexpr size_t kOffPos = (size_t)kStages * kStageBytes;
-constexpr size_t kOffPage = kOffPos + kStages * kTile * 4;
-constexpr size_t kOffBar = kOffPage + kMaxSparseBlocks * 8;
-constexpr size_t kSmemBytes = 1024 + kOffBar + 2 * kStages * 8 + 16;  // + alignment slack
-static_assert(kMaxSparseBlocks >= kChunkPages, "page-offset buffer holds a chunk");
-static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * (2 + kCons) * 4 + 64 <=
-                  kStages * kStageBytes,
+constexpr size_t kOffPos = (size_t)kSlots * kStageBytes;
+constexpr size_t kOffPage = kOffPos + kSlots * kTile * 4;
+constexpr size_t kOffBar = kOffPage + ((kMaxPages + 1) & ~1) * 8;
+constexpr size_t kSmemBytes = 1024 + kOffBar + 2 * kSlots * 8 + 16;  // + alignment slack
+static_assert(kMaxPages >= kMaxSparseBlocks, "the page list also holds block rows");
+static_assert(kSlots % kWarps == 0, "every key slice gets the same number of slots");
+static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * (2 + kWarps) * 4 + 64 <=
+                  kSlots * kStageBytes,
               "merge buffers reuse the stages");
 
 struct DecodeArgs {
@@ -129,256 +128,252 @@ __device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
     return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
 }
 
-// Offsets of pages first .. first+63 from the stream's layer base (-1: an id
-// outside the arena, reported).  One warp; 2 table entries a lane.
-__device__ __forceinline__ void load_page_chunk(const SeqDev &sd, int first, int n_table,
-                                                int64_t *page_off, int lane, uint32_t *status) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int j = lane + 32 * h;
-        const int p = first + j;
-        int64_t off = 0;
-        if (p < n_table) {
-            const int id = __ldg(sd.table + p);
-            if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
-                off = (int64_t)id * sd.ps;
-            } else {
-                off = -1;
-                if (status) atomicOr(status, PKV_DEV_BAD_PAGE);
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The state one CTA shares between its warps.
+struct Ctx {
+    uint8_t *stages;
+    int32_t *kpos;       // [slot][16] key positions (-1 masked)
+    int64_t *rows;       // dense: offsets of the split's pages; sparse: K rows of its blocks
+    uint64_t *full;      // [slot]
+    uint64_t *empty;     // [slot]
+    volatile int *abort_flag;
+    int first_page;      // dense: page of the split's first key
+    int64_t fallback;    // sparse: a row surely written (position 0)
+};
+
+// Stage tile t of the unit into `slot` (one warp).  A whole tile of cached
+// rows inside one page whose rows sit on the stream's TMA map is one 2D tensor
+// copy per 64-dim chunk (8 per tile, K and V); any other tile (the ragged
+// tail, new rows, pages not a multiple of 16, selected blocks) goes key by key
+// with 16-byte cp.async through the same swizzle, from one row lookup per key.
+// With a fused store, new rows come from k_new/v_new and are written to the
+// cache here as well.
+template <bool kSparse>
+__device__ __forceinline__ void stage_tile(const Common &c, const DecodeArgs &a,
+                                           const DecodeMaps &maps, const SeqDev &sd,
+                                           const Unit &u, const Ctx &x, int t, int slot,
+                                           int lane, uint64_t pol) {
+    const int H = c.n_kv_heads;
+    const int qbase = sd.len - sd.n_new;
+    const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;  // V row - K row
+    const bool fuse_store = !kSparse && a.k_new != nullptr;
+    const int i = u.key0 + t * kTile + lane;  // key index of this lane (lane < 16)
+    const bool mine = lane < kTile && i < u.key1;
+    int pos = -1;            // live key position, or -1 (masked)
+    int64_t krow = 0;        // element offset of the K row from layer_base
+    bool bad = false;        // its page id was outside the arena
+    bool fresh = false;      // the row comes from the new-token input
+    if (kSparse) {
+        krow = x.fallback;
+        if (mine) {
+            const int64_t off = x.rows[(i - u.key0) >> 2];
+            if (off >= 0) {
+                pos = i;
+                krow = off + (int64_t)(i & 3) * kHeadDim;
             }
         }
-        page_off[j] = off;
+    } else {
+        const int key = lane < kTile ? min(i, u.key1 - 1) : u.key0;
+        int row = key;
+        int64_t pg = 0;
+        if (sd.table) {
+            const int page = key / sd.ptok;
+            row = key - page * sd.ptok;
+            pg = x.rows[page - x.first_page];
+            if (pg < 0) {
+                bad = true;
+                pg = 0;
+            }
+        }
+        krow = pg + off_k(sd.ptok, u.kvh, row);
+        if (mine) pos = i;
+        fresh = fuse_store && key >= qbase;
     }
+    if (lane < kTile) x.kpos[slot * kTile + lane] = pos;
+    uint8_t *kst = x.stages + slot * kStageBytes;
+    uint8_t *vst = kst + kHalfStage;
+    const void *map = (!kSparse && sd.tma >= 0) ? &maps.map[sd.tma] : nullptr;
+    const bool tile_tma =
+        map != nullptr && __all_sync(0xffffffffu, lane >= kTile || (pos >= 0 && !fresh));
     __syncwarp();
+    if (tile_tma) {
+        if (lane == 0) {
+            const int y = static_cast<int>(sd.layer_row + krow / kHeadDim);  // row-aligned
+            const int yv = y + static_cast<int>(v_gap / kHeadDim);
+            mbar_arrive_expect_tx(&x.full[slot], kTile * 2 * 512);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                tma_load_2d(kst + j * kPlane, map, 64 * j, y, &x.full[slot], pol);
+                tma_load_2d(vst + j * kPlane, map, 64 * j, yv, &x.full[slot], pol);
+            }
+        }
+    } else {
+        const uint16_t *ksrc, *vsrc;
+        if (fresh) {
+            const int key = min(i, u.key1 - 1);
+            const int64_t r = ((int64_t)sd.tok_off + (key - qbase)) * H + u.kvh;
+            ksrc = a.k_new + r * kHeadDim;
+            vsrc = a.v_new + r * kHeadDim;
+        } else {
+            ksrc = sd.layer_base + krow;
+            vsrc = ksrc + v_gap;
+        }
+        const int64_t kp = reinterpret_cast<int64_t>(ksrc);
+        const int64_t vp = reinterpret_cast<int64_t>(vsrc);
+#pragma unroll 4
+        for (int r = 0; r < kTile; ++r) {
+            const uint16_t *kr = reinterpret_cast<const uint16_t *>(shfl64(kp, r));
+            const uint16_t *vr = reinterpret_cast<const uint16_t *>(shfl64(vp, r));
+            cp_async16(kst + swz(r, lane), kr + lane * 8, pol);
+            cp_async16(vst + swz(r, lane), vr + lane * 8, pol);
+        }
+        cp_async_mbar_arrive(&x.full[slot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&x.full[slot]);
+    }
+    if (fuse_store) {
+        unsigned todo = __ballot_sync(0xffffffffu, fresh && pos >= 0 && !bad);
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int p = __shfl_sync(0xffffffffu, pos, src);
+            const int64_t kr = shfl64(krow, src);
+            const int64_t r = (int64_t)sd.tok_off + (p - qbase);
+            uint16_t *dst = const_cast<uint16_t *>(sd.layer_base) + kr;
+            const uint4 kv =
+                __ldg(reinterpret_cast<const uint4 *>(a.k_new + (r * H + u.kvh) * kHeadDim) + lane);
+            const uint4 vv =
+                __ldg(reinterpret_cast<const uint4 *>(a.v_new + (r * H + u.kvh) * kHeadDim) + lane);
+            reinterpret_cast<uint4 *>(dst)[lane] = kv;
+            reinterpret_cast<uint4 *>(dst + v_gap)[lane] = vv;
+            if (u.kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
+                // the indexer-key row of the same position, written once (KV head 0)
+                const int prow = sd.table ? p % sd.ptok : p;
+                const int64_t page_start = kr - (int64_t)prow * kHeadDim;
+                uint16_t *idst = const_cast<uint16_t *>(sd.layer_base) + page_start +
+                                 off_ik(H, c.idx_dim, sd.ptok, prow);
+                reinterpret_cast<uint4 *>(idst)[lane] =
+                    __ldg(reinterpret_cast<const uint4 *>(a.ik_new + r * c.idx_dim) + lane);
+            }
+        }
+    }
 }
 
 template <bool kSparse>
-__global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
                    const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *stages = smem;
-    int32_t *kpos = reinterpret_cast<int32_t *>(smem + kOffPos);
-    int64_t *page_off = reinterpret_cast<int64_t *>(smem + kOffPage);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *empty = full + kStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    Ctx x;
+    x.stages = smem;
+    x.kpos = reinterpret_cast<int32_t *>(smem + kOffPos);
+    x.rows = reinterpret_cast<int64_t *>(smem + kOffPage);
+    x.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    x.empty = x.full + kSlots;
+    x.abort_flag = reinterpret_cast<volatile int *>(x.empty + kSlots);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Unit u = locate<kSparse>(c, a);
     const SeqDev &sd = c.seq[u.s];
     const int ncols = sd.ncols;
-    const int ncg = (ncols + 7) >> 3;
-    const int ks_n = kCons / ncg;
-    const int H = c.n_kv_heads;
-    const int qbase = sd.len - sd.n_new;  // first new position
+    const int ncg = (ncols + 7) >> 3;           // column groups: warps sharing a tile
+    const int ks_n = kWarps / ncg;              // key slices
+    const int S = kSlots / ks_n;                // slots of one key slice
+    const int cg = warp % ncg, ks = warp / ncg;
+    const bool active = ks < ks_n;
+    const bool leader = active && cg == 0;      // stages the slice's tiles
+    const int qbase = sd.len - sd.n_new;
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], ncg);
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&x.full[i], 1);
+            mbar_init(&x.empty[i], ncg);
         }
-        *abort_flag = 0;
+        *x.abort_flag = 0;
         fence_mbar_init();
     }
+    // one row lookup per page (dense) or per selected block (sparse) of the split
+    x.first_page = 0;
+    x.fallback = 0;
+    if (kSparse) {
+        pdl_wait();  // the selected ids come from the previous kernel
+        const int32_t *ids = a.ids + ((int64_t)u.s * c.n_q_heads + u.unit) * a.k;
+        const int nb = sd.len / 4;
+        const int b0 = u.key0 >> 2, nblk = (u.key1 - u.key0 + 3) >> 2;
+        for (int j = tid; j < nblk; j += kThreads) {
+            const int b = __ldg(ids + b0 + j);
+            int64_t off = -1;
+            if (b >= 0 && b < nb) {
+                int32_t row;
+                int64_t pg = 0;
+                if (sd.table) {
+                    const int page = (4 * b) / sd.ptok;
+                    row = 4 * b - page * sd.ptok;
+                    const int id = __ldg(sd.table + page);
+                    pg = static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)
+                             ? (int64_t)id * sd.ps
+                             : -1;
+                } else {
+                    row = 4 * b;
+                }
+                if (pg >= 0) off = pg + off_k(sd.ptok, u.kvh, row);
+            }
+            if ((b >= nb || (b >= 0 && off < 0)) && c.status) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+            x.rows[j] = off;
+        }
+        int64_t fb = 0;
+        if (sd.table) {
+            const int id = __ldg(sd.table);
+            if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) fb = (int64_t)id * sd.ps;
+        }
+        x.fallback = fb + off_k(sd.ptok, u.kvh, 0);
+    } else if (sd.table) {
+        x.first_page = u.key0 / sd.ptok;
+        const int npages = (u.key1 - 1) / sd.ptok - x.first_page + 1;
+        for (int j = tid; j < npages; j += kThreads) {
+            const int p = x.first_page + j;
+            int64_t off = -1;
+            if (p < sd.n_table) {
+                const int id = __ldg(sd.table + p);
+                if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages))
+                    off = (int64_t)id * sd.ps;
+            }
+            if (off < 0 && c.status) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+            x.rows[j] = off;
+        }
+    }
     __syncthreads();
+
+    const uint64_t pol = policy_evict_first();
+    // Rows of cached positions do not depend on the previous kernel on the
+    // stream: the first tiles stream before the grid-dependency wait.  Tiles
+    // holding new positions, the queries and every write wait for it.
+    const int my_tiles = active ? (u.ntiles - ks + ks_n - 1) / ks_n : 0;  // tiles ks, ks+ks_n, ...
+    bool waited = kSparse;
+    int issued = 0;
+    if (leader) {
+        for (; issued < S && issued < my_tiles; ++issued) {
+            const int t = ks + issued * ks_n;
+            if (!waited && u.key0 + t * kTile + kTile > qbase) {
+                pdl_wait();
+                waited = true;
+            }
+            stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, lane, pol);
+        }
+    }
+    if (!waited) pdl_wait();
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float acc[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    const int cg = warp % ncg, ks = warp / ncg;
 
-    if (warp == kCons) {
-        // ---------------- producer ----------------
-        // Rows of cached positions do not depend on the previous kernel on the
-        // stream: they stream before the grid-dependency wait.  New positions
-        // (and, for sparse decode, the selected block ids) wait for it.
-        // A full tile inside one page whose rows sit on the stream's TMA map
-        // is one 2D tensor copy per 64-dim chunk (8 per tile, K and V); any
-        // other tile (the ragged tail, new rows, pages not a multiple of 16,
-        // selected blocks) is staged key by key with 16-byte cp.async through
-        // the same swizzle, from one row lookup per key.
-        const uint64_t pol = policy_evict_first();
-        const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;  // V row - K row
-        const bool fuse_store = !kSparse && a.k_new != nullptr;
-        const void *map = (!kSparse && sd.tma >= 0) ? &maps.map[sd.tma] : nullptr;
-        bool waited = false;
-        int chunk_first = -(1 << 30);
-        int64_t fallback = 0;  // sparse: a row that is surely written (position 0)
-        if (kSparse) {
-            pdl_wait();
-            waited = true;
-            // one lookup per selected block of this split: the K row of its first key
-            const int32_t *ids = a.ids + ((int64_t)u.s * c.n_q_heads + u.unit) * a.k;
-            const int nb = sd.len / 4;
-            const int b0 = u.key0 >> 2, nblk = (u.key1 - u.key0 + 3) >> 2;
-            for (int j = lane; j < nblk; j += 32) {
-                const int b = __ldg(ids + b0 + j);
-                int64_t off = -1;
-                if (b >= 0 && b < nb) {
-                    int32_t row;
-                    int64_t pg = 0;
-                    if (sd.table) {
-                        const int page = (4 * b) / sd.ptok;
-                        row = 4 * b - page * sd.ptok;
-                        const int id = __ldg(sd.table + page);
-                        pg = static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)
-                                 ? (int64_t)id * sd.ps
-                                 : -1;
-                    } else {
-                        row = 4 * b;
-                    }
-                    if (pg >= 0) off = pg + off_k(sd.ptok, u.kvh, row);
-                }
-                if ((b >= nb || (b >= 0 && off < 0)) && c.status)
-                    atomicOr(c.status, PKV_DEV_BAD_PAGE);
-                page_off[j] = off;
-            }
-            if (sd.table && lane == 0) {
-                const int id = __ldg(sd.table);
-                if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages))
-                    fallback = (int64_t)id * sd.ps;
-            }
-            fallback = shfl64(fallback, 0) + off_k(sd.ptok, u.kvh, 0);
-            __syncwarp();
-        }
-        int issued = 0;
-        bool ok = true;
-        for (int t = 0; t < u.ntiles; ++t) {
-            const int st = t % kStages, use = t / kStages;
-            if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, c.status)) {
-                ok = false;
-                break;
-            }
-            if (*abort_flag) break;
-            const int i = u.key0 + t * kTile + lane;  // key index of this lane (lane < 16)
-            const bool mine = lane < kTile && i < u.key1;
-            int pos = -1;            // live key position, or -1 (masked)
-            int64_t krow = 0;        // element offset of the K row from layer_base
-            bool bad = false;        // its page id was outside the arena
-            bool fresh = false;      // the row comes from the new-token input
-            if (kSparse) {
-                krow = fallback;
-                if (mine) {
-                    const int64_t off = page_off[(i - u.key0) >> 2];
-                    if (off >= 0) {
-                        pos = i;
-                        krow = off + (int64_t)(i & 3) * kHeadDim;
-                    }
-                }
-            } else {
-                if (!waited && __any_sync(0xffffffffu, mine && i >= qbase)) {
-                    pdl_wait();
-                    waited = true;
-                }
-                const int key = lane < kTile ? min(i, u.key1 - 1) : u.key0;
-                int row = key;
-                int64_t pg = 0;
-                if (sd.table) {
-                    const int page = key / sd.ptok;
-                    row = key - page * sd.ptok;
-                    const bool out_of_chunk =
-                        lane < kTile && (page < chunk_first || page >= chunk_first + kChunkPages);
-                    if (__any_sync(0xffffffffu, out_of_chunk)) {
-                        chunk_first = __shfl_sync(0xffffffffu, page, 0);
-                        load_page_chunk(sd, chunk_first, sd.n_table, page_off, lane, c.status);
-                    }
-                    if (lane < kTile) pg = page_off[page - chunk_first];
-                    if (pg < 0) {
-                        bad = true;
-                        pg = 0;
-                    }
-                }
-                krow = pg + off_k(sd.ptok, u.kvh, row);
-                if (mine) pos = i;
-                fresh = fuse_store && key >= qbase;
-            }
-            if (lane < kTile) kpos[st * kTile + lane] = pos;
-            uint8_t *kst = stages + st * kStageBytes;
-            uint8_t *vst = kst + kHalfStage;
-            // a whole tile of cached rows inside one page goes by TMA
-            const bool tile_tma = map != nullptr &&
-                                  __all_sync(0xffffffffu, lane >= kTile || (pos >= 0 && !fresh));
-            __syncwarp();
-            if (tile_tma) {
-                if (lane == 0) {
-                    // rows of 256 elements from the map base: krow is row-aligned
-                    const int y = static_cast<int>(sd.layer_row + krow / kHeadDim);
-                    const int yv = y + static_cast<int>(v_gap / kHeadDim);
-                    mbar_arrive_expect_tx(&full[st], kTile * 2 * 512);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        tma_load_2d(kst + j * kPlane, map, 64 * j, y, &full[st], pol);
-                        tma_load_2d(vst + j * kPlane, map, 64 * j, yv, &full[st], pol);
-                    }
-                }
-            } else {
-                const uint16_t *ksrc, *vsrc;
-                if (fresh) {
-                    const int key = min(i, u.key1 - 1);
-                    const int64_t r = ((int64_t)sd.tok_off + (key - qbase)) * H + u.kvh;
-                    ksrc = a.k_new + r * kHeadDim;
-                    vsrc = a.v_new + r * kHeadDim;
-                } else {
-                    ksrc = sd.layer_base + krow;
-                    vsrc = ksrc + v_gap;
-                }
-                // key r's row comes from lane r's address: one lookup per key per tile
-                const int64_t kp = reinterpret_cast<int64_t>(ksrc);
-                const int64_t vp = reinterpret_cast<int64_t>(vsrc);
-#pragma unroll 4
-                for (int r = 0; r < kTile; ++r) {
-                    const uint16_t *kr = reinterpret_cast<const uint16_t *>(shfl64(kp, r));
-                    const uint16_t *vr = reinterpret_cast<const uint16_t *>(shfl64(vp, r));
-                    cp_async16(kst + swz(r, lane), kr + lane * 8, pol);
-                    cp_async16(vst + swz(r, lane), vr + lane * 8, pol);
-                }
-                cp_async_mbar_arrive(&full[st]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[st]);
-            }
-            issued = t + 1;
-            // fused store: this tile's new rows go to the cache as well
-            if (fuse_store) {
-                unsigned todo = __ballot_sync(0xffffffffu, fresh && pos >= 0 && !bad);
-                while (todo) {
-                    const int src = __ffs(todo) - 1;
-                    todo &= todo - 1;
-                    const int p = __shfl_sync(0xffffffffu, pos, src);
-                    const int64_t kr = shfl64(krow, src);
-                    const int64_t r = (int64_t)sd.tok_off + (p - qbase);
-                    uint16_t *dst = const_cast<uint16_t *>(sd.layer_base) + kr;
-                    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(
-                                               a.k_new + (r * H + u.kvh) * kHeadDim) + lane);
-                    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(
-                                               a.v_new + (r * H + u.kvh) * kHeadDim) + lane);
-                    reinterpret_cast<uint4 *>(dst)[lane] = kv;
-                    reinterpret_cast<uint4 *>(dst + v_gap)[lane] = vv;
-                    if (u.kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
-                        // the indexer-key row of the same position, written once (KV head 0)
-                        const int prow = sd.table ? p % sd.ptok : p;
-                        const int64_t page_start = kr - (int64_t)prow * kHeadDim;
-                        uint16_t *idst = const_cast<uint16_t *>(sd.layer_base) + page_start +
-                                         off_ik(H, c.idx_dim, sd.ptok, prow);
-                        reinterpret_cast<uint4 *>(idst)[lane] = __ldg(
-                            reinterpret_cast<const uint4 *>(a.ik_new + r * c.idx_dim) + lane);
-                    }
-                }
-            }
-        }
-        if (!ok) *abort_flag = 1;
-        if (*abort_flag) {
-            // let every copy already issued land before the CTA's memory is released
-            for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
-                mbar_wait(&full[t % kStages], (t / kStages) & 1, nullptr);
-        }
-        if (!waited) pdl_wait();
-    } else if (ks < ks_n) {
-        // ---------------- consumer ----------------
-        pdl_wait();  // queries come from the previous kernel
+    if (active) {
         const int bcol = cg * 8 + (lane >> 2);
         uint32_t qf[16][2];
         {
@@ -397,19 +392,19 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
         const int lim0 = c0 < ncols ? (kSparse ? INT32_MAX : qbase + c0 / c.group) : -1;
         const int lim1 = c1 < ncols ? (kSparse ? INT32_MAX : qbase + c1 / c.group) : -1;
 
-        const uint32_t s_base = smem_u32(stages);
+        const uint32_t s_base = smem_u32(x.stages);
         // ldmatrix rows: K fragments take keys (lane & 7) + 8 * bit 3, V^T fragments
         // keys (lane & 7) + 8 * bit 4; column chunk bit from bit 4 (K) or bit 3 (V)
         const int kr_ = (lane & 7) + 8 * ((lane >> 3) & 1), kcb = lane >> 4;
         const int vr_ = (lane & 7) + 8 * (lane >> 4), vcb = (lane >> 3) & 1;
 
-        for (int t = ks; t < u.ntiles; t += ks_n) {
-            const int st = t % kStages, use = t / kStages;
-            if (!mbar_wait(&full[st], use & 1, c.status)) {
-                *abort_flag = 1;
+        for (int j = 0; j < my_tiles; ++j) {
+            const int slot = ks * S + j % S;
+            if (!mbar_wait(&x.full[slot], (j / S) & 1, c.status)) {
+                *x.abort_flag = 1;
                 break;
             }
-            const uint32_t kb = s_base + st * kStageBytes;
+            const uint32_t kb = s_base + slot * kStageBytes;
             const uint32_t vb = kb + kHalfStage;
             // S^T[16 keys x 8 cols] = K Q^T, two accumulator chains
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -421,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
                 ldsm_x4(kb + swz(kr_, 2 * (kk + 1) + kcb), x0, x1, x2, x3);
                 mma_bf16(sb, x0, x1, x2, x3, qf[kk + 1][0], qf[kk + 1][1]);
             }
-            const int kp0 = kpos[st * kTile + (lane >> 2)];
-            const int kp1 = kpos[st * kTile + (lane >> 2) + 8];
+            const int kp0 = x.kpos[slot * kTile + (lane >> 2)];
+            const int kp1 = x.kpos[slot * kTile + (lane >> 2) + 8];
             const float x0 = (kp0 >= 0 && kp0 <= lim0) ? (sa[0] + sb[0]) * kScaleLog2 : -INFINITY;
             const float x1 = (kp0 >= 0 && kp0 <= lim1) ? (sa[1] + sb[1]) * kScaleLog2 : -INFINITY;
             const float x2 = (kp1 >= 0 && kp1 <= lim0) ? (sa[2] + sb[2]) * kScaleLog2 : -INFINITY;
@@ -457,27 +452,40 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_CTAS_PER_SM)
                 mma_bf16(acc[i], y0, y1, y2, y3, pb0, pb1);
                 mma_bf16(acc[i], y0, y1, y2, y3, pc0, pc1);
             }
+            // release the slot; its leader refills it with the slice's tile j + S
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (ncg > 1 && lane == 0) mbar_arrive(&x.empty[slot]);
+            if (leader && issued < my_tiles) {
+                if (ncg > 1 && !mbar_wait(&x.empty[slot], (j / S) & 1, c.status)) {
+                    *x.abort_flag = 1;
+                    break;
+                }
+                fence_proxy_async_smem();  // this slot's reads come before the next tile's writes
+                stage_tile<kSparse>(c, a, maps, sd, u, x, ks + issued * ks_n, slot, lane, pol);
+                ++issued;
+            }
         }
         l0 = warp_sum_lanes(l0);
         l1 = warp_sum_lanes(l1);
-    } else {
-        pdl_wait();
+    }
+    if (leader && *x.abort_flag) {
+        // let every copy this slice issued land before the CTA's memory is released
+        for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+            mbar_wait(&x.full[ks * S + j % S], (j / S) & 1, nullptr);
     }
 
     __syncthreads();
     pdl_trigger();  // every thread has passed its grid-dependency wait
-    if (*abort_flag) return;
+    if (*x.abort_flag) return;
 
     // ---- merge the key slices (ks = 0, 1, ...) in order, inside the CTA ----
     const int NC = ncg * 8;
-    float *mbuf = reinterpret_cast<float *>(stages);               // [ks][NC][kMergeStride]
-    float *mlb = mbuf + ks_n * NC * kMergeStride;                   // [ks][NC][2]
-    float *wts = mlb + ks_n * NC * 2;                               // [ks][NC]
-    float *lt = wts + ks_n * NC;                                    // [NC]
-    float *mout = lt + NC;                                          // [NC]
-    if (warp < kCons && ks < ks_n) {
+    float *mbuf = reinterpret_cast<float *>(x.stages);            // [ks][NC][kMergeStride]
+    float *mlb = mbuf + ks_n * NC * kMergeStride;                  // [ks][NC][2]
+    float *wts = mlb + ks_n * NC * 2;                              // [ks][NC]
+    float *lt = wts + ks_n * NC;                                   // [NC]
+    float *mout = lt + NC;                                         // [NC]
+    if (active) {
         const int c0 = cg * 8 + 2 * (lane & 3);
         float *b0 = mbuf + (ks * NC + c0) * kMergeStride;
         float *b1 = b0 + kMergeStride;
@@ -651,11 +659,9 @@ int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
         int sl = (nkeys + max_splits - 1) / max_splits;
         sl = (sl + kTile - 1) / kTile * kTile;
         sl = std::max(sl, sparse ? kMinSplitSparse : kMinSplitDense);
-        int ns = (nkeys + sl - 1) / sl;
-        while (ns > kMaxSplits) {
-            sl += kTile;
-            ns = (nkeys + sl - 1) / sl;
-        }
+        sl = std::min(sl, kMaxSplitLen);
+        const int ns = (nkeys + sl - 1) / sl;
+        if (ns > kMaxSplits) return PKV_EINVAL;  // more than 2M keys in one stream
         d.nsplit = ns;
         d.split_len = sl;
         items += units * ns;
