@@ -303,13 +303,7 @@ def main_ours(args):
         cf["launches_per_layer"] = 1 + (1 if n > 0 else 0)
         cf["out"] = [torch.empty_like(q_dev[0]) for _ in range(N_LAYERS)]
 
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        ext = True
-    except TypeError:
-        ext = False
-
-    def capture(p, events):
+    def capture(p):
         cf = confs[p]
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(device=dev)
@@ -323,22 +317,12 @@ def main_ours(args):
         torch.cuda.synchronize()
         with torch.cuda.graph(g):
             for l in range(N_LAYERS):
-                if events:
-                    events[l][0].record()
                 # the new token's store is fused into the decode call
                 pkv.decode(lay, step_seqs[p], l, HQ, q_dev[l], cf["out"][l], cf["ws"],
                            status=status, k_new=k_new[l], v_new=v_new[l], ik_new=ik_new[l])
-                if events:
-                    events[l][1].record()
         return g
 
-    graphs, dec_events = {}, {}
-    for p in confs:
-        ev = ([(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True))
-               for _ in range(N_LAYERS)] if ext else None)
-        dec_events[p] = ev
-        graphs[p] = capture(p, ev)
+    graphs = {p: capture(p) for p in confs}
 
     # correctness guard: paged outputs equal contiguous outputs bit for bit
     for p in confs:
@@ -356,7 +340,6 @@ def main_ours(args):
 
     clocks = Clocks(local)
     step_ms = {p: [] for p in confs}
-    dec_ms = {p: [] for p in confs}
     ev0 = {p: torch.cuda.Event(enable_timing=True) for p in confs}
     ev1 = {p: torch.cuda.Event(enable_timing=True) for p in confs}
     barrier(world)
@@ -372,11 +355,6 @@ def main_ours(args):
         ev1[PAGES[-1]].synchronize()
         for p in PAGES:
             step_ms[p].append(ev0[p].elapsed_time(ev1[p]))
-            if dec_events[p]:
-                try:
-                    dec_ms[p].extend(a.elapsed_time(b) for a, b in dec_events[p])
-                except Exception:
-                    dec_events[p] = None
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
     wall = time.perf_counter() - t_wall
@@ -384,18 +362,13 @@ def main_ours(args):
     clk = clocks.stop()
 
     # contiguous baseline (same workload, own buffers), timed the same way
-    cont_ms, cont_dec = [], []
+    cont_ms = []
     for _ in range(args.steps):
         ev0[None].record()
         graphs[None].replay()
         ev1[None].record()
         ev1[None].synchronize()
         cont_ms.append(ev0[None].elapsed_time(ev1[None]))
-        if dec_events[None]:
-            try:
-                cont_dec.extend(a.elapsed_time(b) for a, b in dec_events[None])
-            except Exception:
-                dec_events[None] = None
     torch.cuda.synchronize()
 
     # ---- results ----
@@ -414,16 +387,15 @@ def main_ours(args):
     cont_gbs = N_LAYERS * layer_bytes(lens_after, 0) / statistics.fmean(cont_ms) / 1e6
     peak, peak_kind = peaks()
 
-    roof = None
-    all_dec = [x for p in PAGES for x in dec_ms[p]]
-    if all_dec:
-        dur = statistics.fmean(all_dec) / 1e3
-        achieved = decode_bytes(lens_after) / dur / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": "pkv_decode (split-KV partial with fused store + combine), one layer, 4 streams",
-                "avg_launch_us": round(dur * 1e6, 3), "peak_kind": peak_kind,
-                "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM, 4)}
+    # one pkv_decode call (partial kernel with the fused store + combine kernel) per
+    # layer; its average duration is the timed graph time over its 13 calls
+    dur = statistics.fmean(x for p in PAGES for x in step_ms[p]) / N_LAYERS / 1e3
+    achieved = decode_bytes(lens_after) / dur / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "kernel": "pkv_decode (split-KV partial with fused store + combine), one layer, 4 streams",
+            "avg_launch_us": round(dur * 1e6, 3), "peak_kind": peak_kind,
+            "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM, 4)}
 
     # end to end through the public API with host buffers
     e2e = e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, status,

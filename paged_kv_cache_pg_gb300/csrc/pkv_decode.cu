@@ -545,17 +545,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Combine a unit's split partials for one query column:
 // M = max m_i, L = sum 2^(m_i-M) l_i, O = sum 2^(m_i-M) acc_i, out = O / L.
-// Every sum runs in a fixed order (lanes over splits i = lane + 32j, then a
-// butterfly; warps over splits i = w + 8j, then warps 0..7), so the result
-// depends only on the partials.
+// Thread d owns dim d and loads acc_i[d] for up to 32 splits at once while
+// the split maxima load, so one memory round trip covers a column of up to
+// 32 splits.  Every sum runs in split order.
 template <bool kSparse>
 __global__ void __launch_bounds__(kCombThreads)
     decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
-    constexpr int kWarps = kCombThreads / 32;
+    constexpr int kBatch = 32;
     __shared__ float w[kMaxSplits];
     __shared__ float lsum[kMaxSplits];
-    __shared__ float4 part[kWarps][kHeadDim / 4];
-    __shared__ float sh_m, sh_l;
+    __shared__ float sh_l;
     pdl_wait();
     pdl_trigger();
     const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
@@ -567,7 +566,13 @@ __global__ void __launch_bounds__(kCombThreads)
     const float *part_acc = a.ws + sd.ws_off;
     const float *part_ml = part_acc + (int64_t)units * ns * sd.ncols * kHeadDim;
     const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
+    const int64_t stride = (int64_t)sd.ncols * kHeadDim;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = tid;  // kCombThreads == head dim
+    const float *col_acc = part_acc + p0 * kHeadDim + d;
+    float xs[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) xs[j] = j < ns ? __ldcg(col_acc + j * stride) : 0.f;
     for (int i = tid; i < ns; i += kCombThreads) {
         const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part_ml + (p0 + (int64_t)i * sd.ncols) * 2));
         w[i] = ml.x;
@@ -588,42 +593,17 @@ __global__ void __launch_bounds__(kCombThreads)
         if (lane == 0) sh_l = L;
     }
     __syncthreads();
-    // warp `warp` sums splits warp, warp+8, ...; lane owns dims 4*lane.. and 128+4*lane..
-    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
-    const float *base = part_acc + p0 * kHeadDim + 4 * lane;
-    const int64_t stride = (int64_t)sd.ncols * kHeadDim;
-    int i = warp;
-    for (; i + 3 * kWarps < ns; i += 4 * kWarps) {
-        float4 x[4][2];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float *src = base + (int64_t)(i + u * kWarps) * stride;
-            x[u][0] = __ldcg(reinterpret_cast<const float4 *>(src));
-            x[u][1] = __ldcg(reinterpret_cast<const float4 *>(src + 128));
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float wi = w[i + u * kWarps];
-            o0.x += wi * x[u][0].x; o0.y += wi * x[u][0].y; o0.z += wi * x[u][0].z; o0.w += wi * x[u][0].w;
-            o1.x += wi * x[u][1].x; o1.y += wi * x[u][1].y; o1.z += wi * x[u][1].z; o1.w += wi * x[u][1].w;
-        }
-    }
-    for (; i < ns; i += kWarps) {
-        const float *src = base + (int64_t)i * stride;
-        const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(src));
-        const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(src + 128));
-        const float wi = w[i];
-        o0.x += wi * x0.x; o0.y += wi * x0.y; o0.z += wi * x0.z; o0.w += wi * x0.w;
-        o1.x += wi * x1.x; o1.y += wi * x1.y; o1.z += wi * x1.z; o1.w += wi * x1.w;
-    }
-    part[warp][lane] = o0;
-    part[warp][32 + lane] = o1;
-    __syncthreads();
-    const int d = tid;  // kCombThreads == head dim
-    const float *pf = reinterpret_cast<const float *>(part);
     float O = 0.f;
 #pragma unroll
-    for (int k = 0; k < kWarps; ++k) O += pf[k * kHeadDim + d];
+    for (int j = 0; j < kBatch; ++j)
+        if (j < ns) O += w[j] * xs[j];
+    for (int b = kBatch; b < ns; b += kBatch) {
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) xs[j] = b + j < ns ? __ldcg(col_acc + (b + j) * stride) : 0.f;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (b + j < ns) O += w[b + j] * xs[j];
+    }
     const float L = sh_l;
     const float o = L > 0.f ? O / L : 0.f;
     Unit u;
