@@ -14,6 +14,7 @@
 // softmax per query column, and merge their key slices in a fixed order.
 // Splits have a fixed length set by the stream's key count and the SM count,
 // so paged and contiguous caches give the same bits.
+#include <algorithm>
 #include <cfloat>
 
 #include "pkv_dev.cuh"
@@ -36,7 +37,7 @@ constexpr int kPlane = 2048;                 // one 64-dim column chunk of 16 ro
 constexpr int kHalfStage = 4 * kPlane;       // the K (or V) tile: 16 rows x 512 B, swizzled
 constexpr int kStageBytes = 2 * kHalfStage;
 constexpr int kSlots = PKV_DECODE_SLOTS;     // stage slots of a CTA, shared by its key slices
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;                    // 2 per tile share the dims (halves)
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCols = 32;                 // query columns of one unit
 constexpr int kMinSplitDense = PKV_DECODE_MIN_SPLIT;    // keys
@@ -54,8 +55,8 @@ constexpr size_t kOffPage = kOffPos + kSlots * kTile * 4;
 constexpr size_t kOffBar = kOffPage + ((kMaxPages + 1) & ~1) * 8;
 constexpr size_t kSmemBytes = 1024 + kOffBar + 2 * kSlots * 8 + 16;  // + alignment slack
 static_assert(kMaxPages >= kMaxSparseBlocks, "the page list also holds block rows");
-static_assert(kSlots % kWarps == 0, "every key slice gets the same number of slots");
-static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * (2 + kWarps) * 4 + 64 <=
+static_assert(kSlots % (kWarps / 2) == 0, "every key slice gets the same number of slots");
+static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * (2 + kWarps / 2) * 4 + 64 <=
                   kSlots * kStageBytes,
               "merge buffers reuse the stages");
 
@@ -277,22 +278,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.empty = x.full + kSlots;
     x.abort_flag = reinterpret_cast<volatile int *>(x.empty + kSlots);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int dh = (tid >> 5) & 1;              // which half of the 256 dims this warp sums
+    const int warp = tid >> 6;                  // warp pair: one column group of one key slice
     const Unit u = locate<kSparse>(c, a);
     const SeqDev &sd = c.seq[u.s];
     const int ncols = sd.ncols;
-    const int ncg = (ncols + 7) >> 3;           // column groups: warps sharing a tile
-    const int ks_n = kWarps / ncg;              // key slices
+    const int ncg = (ncols + 7) >> 3;           // column groups
+    const int ks_n = (kWarps / 2) / ncg;        // key slices
     const int S = kSlots / ks_n;                // slots of one key slice
     const int cg = warp % ncg, ks = warp / ncg;
     const bool active = ks < ks_n;
-    const bool leader = active && cg == 0;      // stages the slice's tiles
+    const bool leader = active && cg == 0 && dh == 0;  // stages the slice's tiles
     const int qbase = sd.len - sd.n_new;
 
     if (tid == 0) {
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&x.full[i], 1);
-            mbar_init(&x.empty[i], ncg);
+            mbar_init(&x.empty[i], 2 * ncg);
         }
         *x.abort_flag = 0;
         fence_mbar_init();
@@ -369,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!waited) pdl_wait();
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float acc[16][4];
+    float acc[8][4];  // O^T for dims 128*dh .. 128*dh+127
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
     if (active) {
         const int bcol = cg * 8 + (lane >> 2);
@@ -440,23 +443,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t l23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
             const uint32_t pb0 = movmatrix_t(h01), pb1 = movmatrix_t(h23);
             const uint32_t pc0 = movmatrix_t(l01), pc1 = movmatrix_t(l23);
-            // O^T[16 dims x 8 cols] += V^T P^T for the 16 dim tiles
+            // O^T[16 dims x 8 cols] += V^T P^T for this warp's 8 dim tiles
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 acc[i][0] *= al0;
                 acc[i][1] *= al1;
                 acc[i][2] *= al0;
                 acc[i][3] *= al1;
                 uint32_t y0, y1, y2, y3;
-                ldsm_x4_t(vb + swz(vr_, 2 * i + vcb), y0, y1, y2, y3);
+                ldsm_x4_t(vb + swz(vr_, 2 * (8 * dh + i) + vcb), y0, y1, y2, y3);
                 mma_bf16(acc[i], y0, y1, y2, y3, pb0, pb1);
                 mma_bf16(acc[i], y0, y1, y2, y3, pc0, pc1);
             }
             // release the slot; its leader refills it with the slice's tile j + S
             __syncwarp();
-            if (ncg > 1 && lane == 0) mbar_arrive(&x.empty[slot]);
+            if (lane == 0) mbar_arrive(&x.empty[slot]);
             if (leader && issued < my_tiles) {
-                if (ncg > 1 && !mbar_wait(&x.empty[slot], (j / S) & 1, c.status)) {
+                if (!mbar_wait(&x.empty[slot], (j / S) & 1, c.status)) {
                     *x.abort_flag = 1;
                     break;
                 }
@@ -490,14 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *b0 = mbuf + (ks * NC + c0) * kMergeStride;
         float *b1 = b0 + kMergeStride;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int d = i * 16 + (lane >> 2);
+        for (int i = 0; i < 8; ++i) {
+            const int d = (8 * dh + i) * 16 + (lane >> 2);
             b0[d] = acc[i][0];
             b1[d] = acc[i][1];
             b0[d + 8] = acc[i][2];
             b1[d + 8] = acc[i][3];
         }
-        if ((lane >> 2) == 0) {
+        if (dh == 0 && (lane >> 2) == 0) {
             mlb[(ks * NC + c0) * 2 + 0] = m0;
             mlb[(ks * NC + c0) * 2 + 1] = l0;
             mlb[(ks * NC + c0 + 1) * 2 + 0] = m1;
@@ -524,17 +527,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *part_acc = a.ws + sd.ws_off;
     float *part_ml = part_acc + (int64_t)units * sd.nsplit * ncols * kHeadDim;
     const int64_t pidx = ((int64_t)u.unit * sd.nsplit + u.split) * ncols;
-    for (int idx = tid; idx < ncols * kHeadDim; idx += kThreads) {
-        const int col = idx / kHeadDim, d = idx - col * kHeadDim;
-        float O = 0.f;
-        for (int k = 0; k < ks_n; ++k) O += wts[k * NC + col] * mbuf[(k * NC + col) * kMergeStride + d];
+    // four consecutive dims a thread: O = sum over slices in order
+    for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
+        const int col = idx / (kHeadDim / 4), d = 4 * (idx - col * (kHeadDim / 4));
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < ks_n; ++k) {
+            const float w = wts[k * NC + col];
+            const float4 v = *reinterpret_cast<const float4 *>(mbuf + (k * NC + col) * kMergeStride + d);
+            O.x += w * v.x;
+            O.y += w * v.y;
+            O.z += w * v.z;
+            O.w += w * v.w;
+        }
         const float L = lt[col];
         if (single) {
-            const float o = L > 0.f ? O / L : 0.f;
-            a.out[q_row<kSparse>(c, sd, u, col) * kHeadDim + d] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            const float inv = L > 0.f ? 1.f : 0.f;
+            const float lz = L > 0.f ? L : 1.f;
+            uint2 pk;
+            pk.x = pack_bf16(inv * (O.x / lz), inv * (O.y / lz));
+            pk.y = pack_bf16(inv * (O.z / lz), inv * (O.w / lz));
+            *reinterpret_cast<uint2 *>(a.out + q_row<kSparse>(c, sd, u, col) * kHeadDim + d) = pk;
         } else {
-            part_acc[(pidx + col) * kHeadDim + d] = O;
+            *reinterpret_cast<float4 *>(part_acc + (pidx + col) * kHeadDim + d) = O;
             if (d == 0) {
                 part_ml[(pidx + col) * 2 + 0] = mout[col];
                 part_ml[(pidx + col) * 2 + 1] = L;
@@ -551,9 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kSparse>
 __global__ void __launch_bounds__(kCombThreads)
     decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
-    constexpr int kBatch = 32;
-    __shared__ float w[kMaxSplits];
-    __shared__ float lsum[kMaxSplits];
+    constexpr int kBatch = 64;
+    extern __shared__ float comb_smem[];  // w[ns], lsum[ns]
     __shared__ float sh_l;
     pdl_wait();
     pdl_trigger();
@@ -562,6 +575,7 @@ __global__ void __launch_bounds__(kCombThreads)
     const int r = blockIdx.x - sd.comb_off;
     const int unit = r / sd.ncols, col = r - unit * sd.ncols;
     const int ns = sd.nsplit;
+    float *w = comb_smem, *lsum = comb_smem + ns;
     const int units = kSparse ? c.n_q_heads : c.n_kv_heads;
     const float *part_acc = a.ws + sd.ws_off;
     const float *part_ml = part_acc + (int64_t)units * ns * sd.ncols * kHeadDim;
@@ -676,7 +690,9 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;
     if (plan.total_comb > 0) {
-        e = launch_pdl(comb, plan.total_comb, kCombThreads, 0, stream, cc, a);
+        int max_ns = 1;
+        for (int s = 0; s < cc.n_seqs; ++s) max_ns = std::max(max_ns, cc.seq[s].nsplit);
+        e = launch_pdl(comb, plan.total_comb, kCombThreads, 2 * max_ns * sizeof(float), stream, cc, a);
         if (e != cudaSuccess) return PKV_ECUDA;
     }
     return PKV_OK;
