@@ -263,27 +263,6 @@ __device__ __forceinline__ void stage_tile(const Common &c, const DecodeArgs &a,
     }
 }
 
-// Warm L2 with the K and V rows of cached tile t (one warp, one row a lane):
-// the slots hold the first tiles of each key slice, and the rest are read
-// from L2 once their slots free up after the grid-dependency wait.
-__device__ __forceinline__ void prefetch_tile_l2(const SeqDev &sd, const Unit &u, const Ctx &x,
-                                                 int h_kv, int t, int lane) {
-    const int i = u.key0 + t * kTile + lane;
-    const int qbase = sd.len - sd.n_new;
-    if (lane >= kTile || i >= u.key1 || i >= qbase) return;
-    int row = i;
-    int64_t pg = 0;
-    if (sd.table) {
-        const int page = i / sd.ptok;
-        row = i - page * sd.ptok;
-        pg = x.rows[page - x.first_page];
-        if (pg < 0) return;
-    }
-    const uint16_t *k = sd.layer_base + pg + off_k(sd.ptok, u.kvh, row);
-    prefetch_l2(k, 512);
-    prefetch_l2(k + (int64_t)h_kv * sd.ptok * kHeadDim, 512);
-}
-
 template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
@@ -389,8 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, lane, pol);
         }
-        if (!kSparse)
-            for (int j = issued; j < my_tiles; ++j) prefetch_tile_l2(sd, u, x, c.n_kv_heads, ks + j * ks_n, lane);
     }
     if (!waited) pdl_wait();
 

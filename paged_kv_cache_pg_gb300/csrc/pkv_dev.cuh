@@ -127,11 +127,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, int x, i
         : "memory");
 }
 
-// Bring [src, src + bytes) into L2 without staging it anywhere (bytes % 16 == 0).
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // 16-byte asynchronous copy global -> shared (L1 bypassed).
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t policy) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
