@@ -220,6 +220,25 @@ int pkv_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, in
                const void *ik_new, void *out, void *ws, size_t ws_bytes, int32_t *dev_status,
                cudaStream_t stream);
 
+/* ---- decode without a caller-provided workspace ------------------------------
+ * No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory, such as plugins inside a host framework that owns every
+ * device allocation, or serving loops that must not call cudaMalloc (it can
+ * synchronize the device and its latency is unbounded).  Same arguments and
+ * result as pkv_decode, but the split partials live in a fixed device array
+ * inside the library (4 MiB; every GPU that loads the library holds it until
+ * the process exits) instead of a workspace.  The call allocates nothing.
+ * EINVAL if the batch needs more than 4 MiB of partials (pkv_decode_ws_size
+ * tells).  The first call on a device looks the array's address up on that
+ * device, so make it before capturing a stream into a graph.  All calls share
+ * the one array: calls that may run at the same time on the GPU (different
+ * streams, or graphs launched concurrently) race on it; issue them in order.
+ * Nothing in the array needs to start at zero. */
+int pkv_decode_static(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
+                      int32_t layer, int32_t n_q_heads, const void *q, const void *k_new,
+                      const void *v_new, const void *ik_new, void *out, int32_t *dev_status,
+                      cudaStream_t stream);
+
 /* ---- block scores (#1169: fn_qsa_scores reads pooled rows) ---------------
  * For each stream's one decode query (n_new == 1), head h and complete block
  * b < len/4: scores[s][h][b] = sum_d qi[h][d] * P[b][d], float32, as the

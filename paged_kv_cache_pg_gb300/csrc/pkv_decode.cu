@@ -16,6 +16,7 @@
 // so paged and contiguous caches give the same bits.
 #include <algorithm>
 #include <cfloat>
+#include <mutex>
 
 #include "pkv_dev.cuh"
 
@@ -628,6 +629,30 @@ __global__ void __launch_bounds__(kCombThreads)
 static_assert(kCombThreads == kHeadDim, "one combine thread per dim");
 
 }  // namespace
+
+// ---- fixed scratch for pkv_decode_static -------------------------------------
+// A file-scope device array holds the split partials for callers that cannot
+// allocate device memory.  Every GPU that loads the library holds it until the
+// process exits.  In host code `g_static_scratch` is only a stand-in for the
+// symbol; the device address is looked up per device below.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+int static_scratch(void **out) {
+    static std::mutex mu;
+    static void *ptrs[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ECUDA;
+    std::lock_guard<std::mutex> g(mu);
+    if (ptrs[dev] == nullptr) {
+        void *p = nullptr;
+        // with `dev` current: the array's address on this device
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+            return PKV_ECUDA;
+        ptrs[dev] = p;
+    }
+    *out = ptrs[dev];
+    return PKV_OK;
+}
 
 // Splits: a fixed number of keys per split, a multiple of the tile, at least
 // the minimum, and enough splits for about two CTAs per SM from one stream.

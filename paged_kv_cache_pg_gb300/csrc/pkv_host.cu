@@ -523,6 +523,33 @@ extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
                          k_new ? static_cast<const uint16_t *>(ik_new) : nullptr, stream);
 }
 
+extern "C" int pkv_decode_static(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
+                                 int32_t layer, int32_t n_q_heads, const void *q,
+                                 const void *k_new, const void *v_new, const void *ik_new,
+                                 void *out, int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    DecodePlan plan;
+    int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, false, 0, dev_status, &c, &plan);
+    if (rc) return rc;
+    if (plan.ws_bytes > kStaticScratchBytes) return PKV_EINVAL;  // over the fixed scratch
+    if (plan.total_items == 0) return PKV_OK;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) return PKV_EINVAL;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_EINVAL;
+    if (k_new) {
+        if (!aligned16(k_new) || !aligned16(v_new)) return PKV_EINVAL;
+        if (L->idx_dim && (!ik_new || !aligned16(ik_new))) return PKV_EINVAL;
+    }
+    void *scratch = nullptr;
+    rc = static_scratch(&scratch);
+    if (rc) return rc;
+    DecodeMaps maps;
+    plan_maps(c, L, seqs, maps);
+    return launch_decode(c, plan, maps, false, static_cast<const uint16_t *>(q), nullptr, 0,
+                         static_cast<uint16_t *>(out), static_cast<float *>(scratch),
+                         static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+                         k_new ? static_cast<const uint16_t *>(ik_new) : nullptr, stream);
+}
+
 extern "C" int pkv_sparse_ws_size(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
                                   int32_t n_q_heads, int32_t k, size_t *bytes) {
     if (!bytes) return PKV_EINVAL;

@@ -114,6 +114,10 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
                   const uint16_t *q, const int32_t *ids, int32_t k, uint16_t *out, float *ws,
                   const uint16_t *k_new, const uint16_t *v_new, const uint16_t *ik_new,
                   cudaStream_t stream);
+// Fixed scratch of pkv_decode_static (pkv_decode.cu): its size, and its
+// device address on the current device (looked up on the first call there).
+constexpr size_t kStaticScratchBytes = 4u << 20;
+int static_scratch(void **out);
 int launch_scores(const Common &c, float *scores, int32_t ld, const uint16_t *qi,
                   int32_t max_nb, cudaStream_t stream);
 int launch_topk(const Common &c, const float *scores, int32_t ld, int32_t k, int32_t *ids,

@@ -58,7 +58,8 @@ EXPORTS = [
     "pkv_layout_page_elems", "pkv_pg_row", "pkv_arena_create", "pkv_arena_destroy",
     "pkv_arena_info", "pkv_pages_take", "pkv_pages_give", "pkv_arena_pg",
     "pkv_arena_set_event_ops", "pkv_store", "pkv_gather", "pkv_pool", "pkv_decode_ws_size",
-    "pkv_decode", "pkv_block_scores", "pkv_topk", "pkv_sparse_ws_size", "pkv_sparse_decode",
+    "pkv_decode", "pkv_decode_static", "pkv_block_scores", "pkv_topk", "pkv_sparse_ws_size",
+    "pkv_sparse_decode",
 ]
 
 
@@ -92,6 +93,7 @@ def load(path: Optional[str] = None):
         "pkv_pool": [LP, SP, i32, i32, vp, vp],
         "pkv_decode_ws_size": [LP, SP, i32, i32, ctypes.POINTER(sz)],
         "pkv_decode": [LP, SP, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp],
+        "pkv_decode_static": [LP, SP, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
         "pkv_block_scores": [LP, SP, i32, i32, i32, vp, vp, i32, vp, vp],
         "pkv_topk": [SP, i32, i32, vp, i32, i32, vp, vp],
         "pkv_sparse_ws_size": [LP, SP, i32, i32, i32, ctypes.POINTER(sz)],
@@ -259,6 +261,20 @@ def decode(lay, seqs, layer, n_q_heads, q, out, ws, status=None, stream=None, k_
     _check(load().pkv_decode(ctypes.byref(lay), arr, n, layer, n_q_heads, _ptr(q), _ptr(k_new),
                              _ptr(v_new), _ptr(ik_new), _ptr(out), _ptr(ws), ws_bytes,
                              _ptr(status), _stream(stream)), "pkv_decode")
+
+
+STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def decode_static(lay, seqs, layer, n_q_heads, q, out, status=None, stream=None, k_new=None,
+                  v_new=None, ik_new=None):
+    """pkv_decode without a workspace: for callers that cannot allocate device
+    memory.  The partials go to a fixed 4 MiB array inside the library; calls
+    that run at the same time on the GPU share it, so issue them in order."""
+    arr, n = _seqs(seqs)
+    _check(load().pkv_decode_static(ctypes.byref(lay), arr, n, layer, n_q_heads, _ptr(q),
+                                    _ptr(k_new), _ptr(v_new), _ptr(ik_new), _ptr(out),
+                                    _ptr(status), _stream(stream)), "pkv_decode_static")
 
 
 def block_scores(lay, seqs, layer, n_q_heads, qi, scores, ld, status=None, stream=None):
