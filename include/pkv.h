@@ -220,6 +220,25 @@ int pkv_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, in
                const void *ik_new, void *out, void *ws, size_t ws_bytes, int32_t *dev_status,
                cudaStream_t stream);
 
+/* ---- chunked prefill on the tensor cores (#1170, maintainer notes on the
+ * Qwen slice: contiguous tensor-core attention for flat batches, a page-run
+ * path for paged or mixed batches; #1169 maintainer reply: the grouped prompt
+ * loop gains the page table) ------------------------------------------------
+ * The same causal attention as pkv_decode for streams whose n_new is large
+ * (a prompt chunk appended to a cached context): query j of head h (position
+ * len-n_new+j) reads keys 0 .. len-n_new+j.  The chunk's rows must be in the
+ * cache already (pkv_store, and pkv_pool for its blocks).  QK^T and PV run as
+ * tcgen05 MMAs with float32 accumulation in tensor memory (P in two bf16
+ * parts).  Whole 16-position page runs are read by TMA when the page size is
+ * a multiple of 16; other tiles key by key.  q, out: [tokens][n_q_heads][D].
+ * ws: device, >= pkv_prefill_ws_size bytes, 256-byte aligned.  Paged output
+ * equals contiguous output bit for bit. */
+int pkv_prefill_ws_size(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
+                        int32_t n_q_heads, size_t *bytes);
+int pkv_prefill(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                int32_t n_q_heads, const void *q, void *out, void *ws, size_t ws_bytes,
+                int32_t *dev_status, cudaStream_t stream);
+
 /* ---- decode without a caller-provided workspace ------------------------------
  * No counterpart on the pages: an addition for callers that cannot allocate
  * device memory, such as plugins inside a host framework that owns every

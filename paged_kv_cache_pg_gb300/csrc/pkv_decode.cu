@@ -124,12 +124,6 @@ __device__ __forceinline__ int64_t q_row(const Common &c, const SeqDev &sd, cons
     return ((int64_t)sd.tok_off + j) * c.n_q_heads + u.kvh * c.group + (col - j * c.group);
 }
 
-__device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
-    const int lo = __shfl_sync(0xffffffffu, static_cast<int>(v), src);
-    const int hi = __shfl_sync(0xffffffffu, static_cast<int>(v >> 32), src);
-    return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -694,6 +688,15 @@ int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
     plan->total_comb = comb;
     plan->ws_bytes = static_cast<size_t>(floats) * 4;
     return PKV_OK;
+}
+
+int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, uint16_t *out,
+                   float *ws, cudaStream_t stream) {
+    DecodeArgs a{q, out, ws, nullptr, 0, nullptr, nullptr, nullptr};
+    int max_ns = 1;
+    for (int s = 0; s < c.n_seqs; ++s) max_ns = std::max(max_ns, c.seq[s].nsplit);
+    return launch_status(launch_pdl(decode_combine<false>, plan.total_comb, kCombThreads,
+                                    2 * max_ns * sizeof(float), stream, c, a));
 }
 
 int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &maps, bool sparse,

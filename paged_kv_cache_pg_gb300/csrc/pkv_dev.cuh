@@ -201,6 +201,13 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// A 64-bit value from lane `src` of the warp.
+__device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
+    const int lo = __shfl_sync(0xffffffffu, static_cast<int>(v), src);
+    const int hi = __shfl_sync(0xffffffffu, static_cast<int>(v >> 32), src);
+    return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
+}
+
 // Stream of the work item / token: the last s with off(s) <= i.
 template <typename F>
 __device__ __forceinline__ int find_seq(int n, int32_t i, F off) {

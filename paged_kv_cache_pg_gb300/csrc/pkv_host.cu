@@ -581,6 +581,45 @@ extern "C" int pkv_sparse_decode(const pkv_layout *L, const pkv_seq *seqs, int32
                          nullptr, stream);
 }
 
+static int prefill_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                          int32_t n_q_heads, int32_t *dev_status, Common *c, DecodePlan *plan) {
+    int rc = fill_common(L, seqs, n_seqs, layer, n_q_heads, dev_status, c);
+    if (rc) return rc;
+    int nsm = 0;
+    rc = sm_count(&nsm);
+    if (rc) return rc;
+    return plan_prefill(*c, nsm, plan);
+}
+
+extern "C" int pkv_prefill_ws_size(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
+                                   int32_t n_q_heads, size_t *bytes) {
+    if (!bytes) return PKV_EINVAL;
+    Common c;
+    DecodePlan plan;
+    int rc = prefill_common(L, seqs, n_seqs, 0, n_q_heads, nullptr, &c, &plan);
+    if (rc) return rc;
+    *bytes = plan.ws_bytes;
+    return PKV_OK;
+}
+
+extern "C" int pkv_prefill(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
+                           int32_t n_q_heads, const void *q, void *out, void *ws, size_t ws_bytes,
+                           int32_t *dev_status, cudaStream_t stream) {
+    Common c;
+    DecodePlan plan;
+    int rc = prefill_common(L, seqs, n_seqs, layer, n_q_heads, dev_status, &c, &plan);
+    if (rc) return rc;
+    if (plan.total_items == 0) return PKV_OK;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) return PKV_EINVAL;
+    if (plan.ws_bytes > 0 &&
+        (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return PKV_EINVAL;
+    DecodeMaps maps;
+    plan_maps(c, L, seqs, maps);
+    return launch_prefill(c, plan, maps, static_cast<const uint16_t *>(q),
+                          static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
+}
+
 extern "C" int pkv_block_scores(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
                                 int32_t layer, int32_t n_q_heads, const void *qi, float *scores,
                                 int32_t ld, int32_t *dev_status, cudaStream_t stream) {

@@ -114,6 +114,14 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
                   const uint16_t *q, const int32_t *ids, int32_t k, uint16_t *out, float *ws,
                   const uint16_t *k_new, const uint16_t *v_new, const uint16_t *ik_new,
                   cudaStream_t stream);
+// Chunked prefill (pkv_prefill.cu): plan and launch; split partials use the
+// decode layout and are merged by the decode combine kernel.
+int plan_prefill(Common &c, int nsm, DecodePlan *plan);
+int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
+                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream);
+int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, uint16_t *out,
+                   float *ws, cudaStream_t stream);
+
 // Fixed scratch of pkv_decode_static (pkv_decode.cu): its size, and its
 // device address on the current device (looked up on the first call there).
 constexpr size_t kStaticScratchBytes = 4u << 20;

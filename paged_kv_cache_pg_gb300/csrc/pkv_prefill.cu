@@ -1,0 +1,517 @@
+// Chunked-prefill attention on the fifth-generation tensor cores (tcgen05).
+//
+// Rows: the (query, head) pairs of one KV head, 128 to an M-tile (16 queries
+// x 8 heads for the pages' 16/2 heads).  A CTA takes one M-tile and one split
+// of the keys and runs, per tile of 32 keys:
+//   S = Q K^T  -> TMEM (128 lanes x 32 columns, two buffers)   [MMA warp]
+//   softmax of S with the causal mask, P = hi + lo bf16 parts   [4 warps]
+//   O += P_hi V + P_lo V -> TMEM (128 lanes x 256 columns)      [MMA warp]
+// Q, K, V and P sit in shared memory in the 128-byte-swizzled layouts the
+// MMA reads through matrix descriptors; K and V tiles arrive by 2D TMA copies
+// of whole 16-row page runs (the rows of 16 consecutive positions are
+// contiguous in a page whose size is a multiple of 16) or, for a ragged tail
+// or other page sizes, by cp.async from one row lookup per key.  The max of a
+// row is rescaled lazily: O in TMEM is corrected only when the running max
+// grows by more than 2^8.  Split partials use the decode layout and its
+// combine kernel.
+#include <algorithm>
+
+#include "pkv_dev.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kM = 128;              // rows of an M-tile
+constexpr int kN = 32;               // keys a tile
+constexpr int kKV = 3;               // K/V tile buffers
+constexpr int kPThreads = 192;       // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr uint32_t kTmemCols = 512;  // S buffers at columns 0 and 32, O at 256
+constexpr uint32_t kOCol = 256;
+constexpr int kQBytes = kM * 512;    // four 64-dim regions of 128 rows x 128 B
+constexpr int kKVBytes = kN * 512;   // four 64-dim regions of 32 rows x 128 B
+constexpr int kRegionQ = kM * 128;   // bytes of one 64-dim region of Q
+constexpr int kRegionKV = kN * 128;  // bytes of one 64-dim region of a K or V tile
+constexpr int kPBytes = kM * 128;    // 128 rows x 128 B (the first 64 B of a row used)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffV = kOffK + kKV * kKVBytes;
+constexpr int kOffP = kOffV + kKV * kKVBytes;  // P hi, then P lo
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+// barriers
+constexpr int kBarKFull = 0, kBarVFull = 3, kBarKVEmpty = 6, kBarSFull = 9, kBarSEmpty = 11;
+constexpr int kBarPFull = 13, kBarODone = 14, kBarQFull = 15, kNumBars = 16;
+constexpr size_t kPSmem = 1024 + kOffBar + kNumBars * 8 + 16;
+constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
+constexpr float kRescale = 8.f;  // rescale O when the max grows by more than 2^8
+
+// Instruction descriptor, kind::f16: D float32, A and B bf16, A K-major, B
+// K-major (S = Q K^T) or MN-major (O += P V), M = 128.
+__host__ __device__ constexpr uint32_t mma_idesc(int n, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// byte offset (MN-major: between 64-element blocks), stride byte offset
+// (between 8-row groups), the fixed version bits.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+struct PrefillArgs {
+    const uint16_t *q;
+    uint16_t *out;
+    float *ws;
+};
+
+// Byte offset of 16-byte chunk c (0..31) of row r in a 128-byte-swizzled
+// operand made of 64-dim regions of `region` bytes.
+__device__ __forceinline__ uint32_t swz128(int region, int r, int c) {
+    return (c >> 3) * region + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
+                    const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].work_off; });
+    const SeqDev &sd = c.seq[s];
+    const int H = c.n_kv_heads, G = c.group;
+    const int mtiles = (sd.ncols + kM - 1) / kM;
+    const int item = blockIdx.x - sd.work_off;
+    const int kvh = item / (mtiles * sd.nsplit);
+    const int mt = (item / sd.nsplit) % mtiles;
+    const int split = item % sd.nsplit;
+    const int col0 = mt * kM;
+    const int rows = min(kM, sd.ncols - col0);
+    const int qbase = sd.len - sd.n_new;
+    const int last_q = qbase + (col0 + rows - 1) / G;  // position of the tile's last query
+    const int key0 = split * sd.split_len;
+    const int key1 = min(min(sd.len, key0 + sd.split_len), last_q + 1);
+    const int ntiles = key1 > key0 ? (key1 - key0 + kN - 1) / kN : 0;
+
+    if (tid == 0) {
+        for (int i = 0; i < kKV; ++i) {
+            mbar_init(&bars[kBarKFull + i], 1);
+            mbar_init(&bars[kBarVFull + i], 1);
+            mbar_init(&bars[kBarKVEmpty + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[kBarSFull + i], 1);
+            mbar_init(&bars[kBarSEmpty + i], kM);
+        }
+        mbar_init(&bars[kBarPFull], kM);
+        mbar_init(&bars[kBarODone], 1);
+        mbar_init(&bars[kBarQFull], kM);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(smem);
+
+    if (warp < 4) {
+        // ---------------- softmax: thread r owns row r (TMEM lane r) ----------------
+        pdl_wait();
+        const int r = tid;
+        const int col = col0 + r;
+        const bool row_ok = r < rows;
+        const int j = row_ok ? col / G : 0;
+        const int qpos = row_ok ? qbase + j : -1;
+        // Q row into the swizzled A operand
+        {
+            uint8_t *qs = smem + kOffQ;
+            if (row_ok) {
+                const uint16_t *src =
+                    a.q + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
+#pragma unroll 8
+                for (int ch = 0; ch < 32; ++ch)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                     smem_u32(qs + swz128(kRegionQ, r, ch))),
+                                 "l"(src + ch * 8)
+                                 : "memory");
+                asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+            } else {
+#pragma unroll 8
+                for (int ch = 0; ch < 32; ++ch)
+                    *reinterpret_cast<uint4 *>(qs + swz128(kRegionQ, r, ch)) = make_uint4(0, 0, 0, 0);
+            }
+            fence_async_smem();
+            mbar_arrive(&bars[kBarQFull]);
+        }
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        uint8_t *p_hi = smem + kOffP, *p_lo = smem + kOffP + kPBytes;
+        for (int n = 0; n < ntiles; ++n) {
+            const int sb = n & 1;
+            if (!mbar_wait(&bars[kBarSFull + sb], (n >> 1) & 1, c.status)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[32];
+            tmem_ld32(lane_base + sb * kN, sv);
+            tc_fence_before();
+            mbar_arrive(&bars[kBarSEmpty + sb]);
+            const int kt = key0 + n * kN;
+            float x[32];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int kp = kt + i;
+                const bool ok = kp < key1 && kp <= qpos;
+                x[i] = ok ? __uint_as_float(sv[i]) * kScaleLog2 : -INFINITY;
+                mx = fmaxf(mx, x[i]);
+            }
+            // P and O are free once the previous tile's P V products are done
+            if (n > 0 && !mbar_wait(&bars[kBarODone], (n - 1) & 1, c.status)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const bool grow = m_used != -INFINITY && mx > m_used + kRescale;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float m_new = fmaxf(m_used, mx);
+                const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
+#pragma unroll 1
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kOCol + ch * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(lane_base + kOCol + ch * 32, o);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                l *= alpha;
+                m_used = m_new;
+            } else if (m_used == -INFINITY) {
+                m_used = mx;  // nothing accumulated yet: O is still zero
+            }
+            float psum = 0.f;
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float p0 = (x[i] == -INFINITY || m_used == -INFINITY) ? 0.f : ex2(x[i] - m_used);
+                const float p1 =
+                    (x[i + 1] == -INFINITY || m_used == -INFINITY) ? 0.f : ex2(x[i + 1] - m_used);
+                psum += p0 + p1;
+                hi[i / 2] = pack_bf16(p0, p1);
+                lo[i / 2] = pack_bf16(p0 - bf16_lo(hi[i / 2]), p1 - bf16_hi(hi[i / 2]));
+            }
+            l += psum;
+            // row r of the P operands: 32 keys = 64 bytes = chunks 0..3
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint32_t off = r * 128 + (((ch ^ (r & 7))) << 4);
+                *reinterpret_cast<uint4 *>(p_hi + off) =
+                    make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
+                *reinterpret_cast<uint4 *>(p_lo + off) =
+                    make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars[kBarPFull]);
+        }
+        // ---------------- epilogue ----------------
+        bool ok = !*abort_flag;
+        if (ok && ntiles > 0 && !mbar_wait(&bars[kBarODone], (ntiles - 1) & 1, c.status)) {
+            *abort_flag = 1;
+            ok = false;
+        }
+        tc_fence_after();
+        if (ok) {
+            const bool single = sd.nsplit == 1;
+            float *part_acc = a.ws + sd.ws_off;
+            float *part_ml = part_acc + (int64_t)H * sd.nsplit * sd.ncols * kHeadDim;
+            const int64_t prow = ((int64_t)kvh * sd.nsplit + split) * sd.ncols + col;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint16_t *orow = a.out + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
+#pragma unroll 1
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t o[32];
+                if (ntiles > 0) {
+                    tmem_ld32(lane_base + kOCol + ch * 32, o);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (!row_ok) continue;
+                if (single) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
+                        v.y = pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+                        v.z = pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
+                        v.w = pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + ch * 32 + i) = v;
+                    }
+                } else {
+                    float *dst = part_acc + prow * kHeadDim + ch * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) =
+                            make_float4(__uint_as_float(o[i]), __uint_as_float(o[i + 1]),
+                                        __uint_as_float(o[i + 2]), __uint_as_float(o[i + 3]));
+                }
+            }
+            if (row_ok && !single) {
+                part_ml[prow * 2 + 0] = m_used;
+                part_ml[prow * 2 + 1] = l;
+            }
+        }
+    } else if (warp == 4) {
+        // ---------------- producer: K and V tiles ----------------
+        pdl_wait();  // the chunk's rows are stored by the previous kernel
+        const void *map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;
+        const uint64_t pol = policy_evict_first();
+        const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;
+        for (int n = 0; n < ntiles && !*abort_flag; ++n) {
+            const int b = n % kKV;
+            if (n >= kKV && !mbar_wait(&bars[kBarKVEmpty + b], ((n / kKV) - 1) & 1, c.status)) {
+                *abort_flag = 1;
+                break;
+            }
+            const int kt = key0 + n * kN;
+            uint8_t *ks = smem + kOffK + b * kKVBytes;
+            uint8_t *vs = smem + kOffV + b * kKVBytes;
+            // this lane's key (one lookup per key per tile): clamped into the split
+            const int key = min(kt + lane, key1 - 1);
+            int row = key;
+            int64_t pg = 0;
+            if (sd.table) {
+                const int page = key / sd.ptok;
+                row = key - page * sd.ptok;
+                const int id = __ldg(sd.table + page);
+                if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
+                    pg = (int64_t)id * sd.ps;
+                } else if (c.status) {
+                    atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                }
+            }
+            const int64_t krow = pg + off_k(sd.ptok, kvh, row);
+            const bool whole = map != nullptr && kt + kN <= key1;
+            if (whole) {
+                // two 16-row page runs, four 64-dim chunks each, for K and for V
+                const int y0 = static_cast<int>(sd.layer_row + shfl64(krow, 0) / kHeadDim);
+                const int y1 = static_cast<int>(sd.layer_row + shfl64(krow, 16) / kHeadDim);
+                const int yv = static_cast<int>(v_gap / kHeadDim);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[kBarKFull + b], kKVBytes);
+                    mbar_arrive_expect_tx(&bars[kBarVFull + b], kKVBytes);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        tma_load_2d(ks + ch * kRegionKV, map, 64 * ch, y0, &bars[kBarKFull + b], pol);
+                        tma_load_2d(ks + ch * kRegionKV + 2048, map, 64 * ch, y1, &bars[kBarKFull + b], pol);
+                        tma_load_2d(vs + ch * kRegionKV, map, 64 * ch, y0 + yv, &bars[kBarVFull + b], pol);
+                        tma_load_2d(vs + ch * kRegionKV + 2048, map, 64 * ch, y1 + yv, &bars[kBarVFull + b], pol);
+                    }
+                }
+            } else {
+                // key r's rows from lane r's lookup; keys past the split repeat its last row
+#pragma unroll 4
+                for (int rr = 0; rr < kN; ++rr) {
+                    const uint16_t *kr = sd.layer_base + shfl64(krow, rr);
+                    cp_async16(ks + swz128(kRegionKV, rr, lane), kr + lane * 8, pol);
+                    cp_async16(vs + swz128(kRegionKV, rr, lane), kr + v_gap + lane * 8, pol);
+                }
+                cp_async_mbar_arrive(&bars[kBarKFull + b]);
+                cp_async_mbar_arrive(&bars[kBarVFull + b]);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[kBarKFull + b]);
+                    mbar_arrive(&bars[kBarVFull + b]);
+                }
+            }
+        }
+    } else if (warp == 5 && lane == 0) {
+        // ---------------- MMA issue ----------------
+        const uint32_t idesc_s = mma_idesc(kN, false);
+        const uint32_t idesc_o = mma_idesc(kHeadDim, true);
+        bool ok = mbar_wait(&bars[kBarQFull], 0, c.status);
+        fence_async_smem();
+        tc_fence_after();
+        auto issue_s = [&](int n) -> bool {
+            const int b = n % kKV, sb = n & 1;
+            if (!mbar_wait(&bars[kBarKFull + b], (n / kKV) & 1, c.status)) return false;
+            if (n >= 2 && !mbar_wait(&bars[kBarSEmpty + sb], ((n - 2) >> 1) & 1, c.status)) return false;
+            fence_async_smem();
+            tc_fence_after();
+            const uint32_t kb = sbase + kOffK + b * kKVBytes;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                const uint32_t qa = sbase + kOffQ + (kk >> 2) * kRegionQ + (kk & 3) * 32;
+                const uint32_t kbb = kb + (kk >> 2) * kRegionKV + (kk & 3) * 32;
+                tc_mma(tmem + sb * kN, smem_desc(qa, 16, 1024), smem_desc(kbb, 16, 1024), idesc_s,
+                       kk > 0);
+            }
+            tc_commit(&bars[kBarSFull + sb]);
+            return true;
+        };
+        if (ok && ntiles > 0) ok = issue_s(0);
+        for (int n = 0; ok && n < ntiles; ++n) {
+            if (n + 1 < ntiles && !issue_s(n + 1)) {
+                ok = false;
+                break;
+            }
+            const int b = n % kKV;
+            if (!mbar_wait(&bars[kBarVFull + b], (n / kKV) & 1, c.status) ||
+                !mbar_wait(&bars[kBarPFull], n & 1, c.status)) {
+                ok = false;
+                break;
+            }
+            fence_async_smem();
+            tc_fence_after();
+            const uint32_t vb = sbase + kOffV + b * kKVBytes;
+#pragma unroll
+            for (int kk = 0; kk < kN / 16; ++kk) {
+                const uint32_t pa = sbase + kOffP + kk * 32;
+                const uint32_t va = vb + kk * 2048;  // 16 keys = two 8-row groups
+                tc_mma(tmem + kOCol, smem_desc(pa, 16, 1024), smem_desc(va, kRegionKV, 1024), idesc_o,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+                tc_mma(tmem + kOCol, smem_desc(pa + kPBytes, 16, 1024), smem_desc(va, kRegionKV, 1024),
+                       idesc_o, 1u);
+            }
+            tc_commit(&bars[kBarODone]);
+            tc_commit(&bars[kBarKVEmpty + b]);
+        }
+        if (!ok) *abort_flag = 1;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    pdl_trigger();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+}  // namespace
+
+// Work items: (KV head, M-tile, split) per stream, splits fastest.  A stream
+// is split only as far as filling the SMs needs, from its own shape alone.
+int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
+    int32_t items = 0, comb = 0;
+    int64_t floats = 0;
+    const int H = c.n_kv_heads;
+    for (int s = 0; s < c.n_seqs; ++s) {
+        SeqDev &d = c.seq[s];
+        d.work_off = items;
+        d.comb_off = comb;
+        d.ws_off = floats;
+        d.ncols = d.n_new * c.group;
+        if (d.ncols == 0) {
+            d.nsplit = 1;
+            d.split_len = kN;
+            continue;
+        }
+        const int mtiles = (d.ncols + kM - 1) / kM;
+        int ns = std::max(1, nsm / (H * mtiles));
+        ns = std::min(ns, std::max(1, d.len / (4 * kN)));
+        int sl = (d.len + ns - 1) / ns;
+        sl = (sl + kN - 1) / kN * kN;
+        ns = (d.len + sl - 1) / sl;
+        if (ns > 2048) return PKV_EINVAL;
+        d.nsplit = ns;
+        d.split_len = sl;
+        items += H * mtiles * ns;
+        if (ns > 1) {
+            comb += H * d.ncols;
+            floats += (int64_t)H * ns * d.ncols * (kHeadDim + 2);
+            floats = (floats + 63) / 64 * 64;
+        }
+    }
+    plan->total_items = items;
+    plan->total_comb = comb;
+    plan->ws_bytes = static_cast<size_t>(floats) * 4;
+    return PKV_OK;
+}
+
+int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
+                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(prefill_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kPSmem)) != cudaSuccess)
+            return PKV_ECUDA;
+        attr_set = true;
+    }
+    PrefillArgs a{q, out, ws};
+    cudaError_t e = launch_pdl(prefill_partial, plan.total_items, kPThreads, kPSmem, stream, c, maps, a);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    if (plan.total_comb > 0) return launch_combine(c, plan, q, out, ws, stream);
+    return PKV_OK;
+}
+
+}  // namespace pkv

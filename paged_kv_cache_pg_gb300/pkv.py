@@ -59,7 +59,7 @@ EXPORTS = [
     "pkv_arena_info", "pkv_pages_take", "pkv_pages_give", "pkv_arena_pg",
     "pkv_arena_set_event_ops", "pkv_store", "pkv_gather", "pkv_pool", "pkv_decode_ws_size",
     "pkv_decode", "pkv_decode_static", "pkv_block_scores", "pkv_topk", "pkv_sparse_ws_size",
-    "pkv_sparse_decode",
+    "pkv_sparse_decode", "pkv_prefill_ws_size", "pkv_prefill",
 ]
 
 
@@ -94,6 +94,8 @@ def load(path: Optional[str] = None):
         "pkv_decode_ws_size": [LP, SP, i32, i32, ctypes.POINTER(sz)],
         "pkv_decode": [LP, SP, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp],
         "pkv_decode_static": [LP, SP, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
+        "pkv_prefill_ws_size": [LP, SP, i32, i32, ctypes.POINTER(sz)],
+        "pkv_prefill": [LP, SP, i32, i32, i32, vp, vp, vp, sz, vp, vp],
         "pkv_block_scores": [LP, SP, i32, i32, i32, vp, vp, i32, vp, vp],
         "pkv_topk": [SP, i32, i32, vp, i32, i32, vp, vp],
         "pkv_sparse_ws_size": [LP, SP, i32, i32, i32, ctypes.POINTER(sz)],
@@ -261,6 +263,22 @@ def decode(lay, seqs, layer, n_q_heads, q, out, ws, status=None, stream=None, k_
     _check(load().pkv_decode(ctypes.byref(lay), arr, n, layer, n_q_heads, _ptr(q), _ptr(k_new),
                              _ptr(v_new), _ptr(ik_new), _ptr(out), _ptr(ws), ws_bytes,
                              _ptr(status), _stream(stream)), "pkv_decode")
+
+
+def prefill_ws_size(lay, seqs, n_q_heads) -> int:
+    arr, n = _seqs(seqs)
+    out = ctypes.c_size_t()
+    _check(load().pkv_prefill_ws_size(ctypes.byref(lay), arr, n, n_q_heads, ctypes.byref(out)),
+           "pkv_prefill_ws_size")
+    return out.value
+
+
+def prefill(lay, seqs, layer, n_q_heads, q, out, ws, status=None, stream=None):
+    """Chunked-prefill attention on the tensor cores (the chunk already stored)."""
+    arr, n = _seqs(seqs)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pkv_prefill(ctypes.byref(lay), arr, n, layer, n_q_heads, _ptr(q), _ptr(out),
+                              _ptr(ws), ws_bytes, _ptr(status), _stream(stream)), "pkv_prefill")
 
 
 STATIC_SCRATCH_BYTES = 4 << 20

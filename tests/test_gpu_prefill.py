@@ -1,0 +1,111 @@
+"""GPU parity: chunked prefill on the tensor cores against the oracle.
+
+A chunk of new positions is stored (pkv_store) and its queries attend the
+cached context plus the chunk, causally.  Every row is checked against the
+float64 oracle where the oracle finishes in seconds; the pages' chunk (512
+queries appended to 31,000 cached positions, pages of 256) is checked on
+sampled rows.  Paged output must equal contiguous output bit for bit, and a
+chunk of a few queries must agree with the decode kernel.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+from paged_kv_cache_pg_gb300 import pkv, synth
+
+from gpu_setup import dev_u16, host_u16, oracle_decode, place, torch, within_tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_pg_gb300 import build
+    build.build()
+    pkv.load()
+
+
+def _prefill(pl, lens, n_new, layer, hq, q_list):
+    t = torch()
+    seqs = pl.seqs(lens, n_new)
+    q = dev_u16(np.concatenate(q_list))
+    out = t.zeros_like(q)
+    ws = t.zeros(max(64, pkv.prefill_ws_size(pl.lay, seqs, hq) // 4 + 64), dtype=t.float32,
+                 device="cuda")
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    pkv.prefill(pl.lay, seqs, layer, hq, q, out, ws, status=status)
+    t.cuda.synchronize()
+    assert int(status.item()) == 0
+    return host_u16(out)
+
+
+@pytest.mark.parametrize("ptok", [16, 48, 256, None, 20])
+def test_small_chunks_match_oracle_and_contiguous(ptok):
+    lay = pkv.layout(2, 2, 256, 128)
+    lens = [140, 77]            # cached + chunk
+    n_new = [40, 77]            # the second stream is all chunk (a prompt from scratch)
+    streams = [synth.make_stream(1200 + i, 2, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q = [synth.queries(1300 + i, n, 16, 256) for i, n in enumerate(n_new)]
+    if ptok is None:
+        pl = place(lay, streams, None)
+    else:
+        pl = place(lay, streams, ptok, seed=ptok)
+    got = _prefill(pl, lens, n_new, 1, 16, q)
+    ok, report = within_tol(got, oracle_decode(pl, 1, 16, q))
+    assert ok, report
+    cont = place(lay, streams, None)
+    assert np.array_equal(_prefill(cont, lens, n_new, 1, 16, q), got)
+
+
+def test_prefill_of_a_short_window_agrees_with_decode():
+    t = torch()
+    lay = pkv.layout(1, 2, 256, 128)
+    lens = [300, 1000]
+    streams = [synth.make_stream(1400 + i, 1, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q = [synth.queries(1500 + i, 4, 16, 256) for i in range(2)]
+    pl = place(lay, streams, 128, seed=3)
+    a = _prefill(pl, lens, [4, 4], 0, 16, q)
+    seqs = pl.seqs(lens, [4, 4])
+    dq = dev_u16(np.concatenate(q))
+    out = t.zeros_like(dq)
+    ws = t.zeros(pkv.decode_ws_size(lay, seqs, 16) // 4 + 64, dtype=t.float32, device="cuda")
+    pkv.decode(lay, seqs, 0, 16, dq, out, ws)
+    t.cuda.synchronize()
+    b = host_u16(out)
+    ref = (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ok, report = within_tol(a, ref)
+    assert ok, report
+    ok, report = within_tol(a, oracle_decode(pl, 0, 16, q))
+    assert ok, report
+
+
+def test_group_sizes_other_than_eight():
+    lay = pkv.layout(1, 4, 256, 0)
+    T, C = 96, 96
+    streams = [synth.Stream(T, synth.normal_bf16(1600, (1, T, 4, 256)),
+                            synth.normal_bf16(1601, (1, T, 4, 256)), np.zeros((1, T, 0), np.uint16))]
+    q = [synth.queries(1602, C, 8, 256)]   # G = 2
+    pl = place(lay, streams, 32, seed=5)
+    got = _prefill(pl, [T], [C], 0, 8, q)
+    ok, report = within_tol(got, oracle_decode(pl, 0, 8, q))
+    assert ok, report
+
+
+def test_pages_chunk_31000_plus_512_sampled():
+    # 1 stream, 512 queries appended to 31,000 cached positions, pages of 256
+    lay = pkv.layout(1, 2, 256, 128)
+    P0, C = 31000, 512
+    T = P0 + C
+    s = synth.make_stream(1700, 1, T, 2, 256, 128)
+    q = synth.queries(1701, C, 16, 256)
+    pl = place(lay, [s], 256, seed=6)
+    got = _prefill(pl, [T], [C], 0, 16, [q]).reshape(C, 16, 256)
+    rng = np.random.default_rng(7)
+    picks = [(0, 0), (C - 1, 15), (255, 7), (256, 8)] + \
+        [(int(rng.integers(C)), int(rng.integers(16))) for _ in range(12)]
+    for j, h in picks:
+        ref = orc.attend_row(pl.shape, pl.ocaches[0], 0, 16, h, P0 + j, q[j, h])
+        ok, report = within_tol(got[j, h], ref)
+        assert ok, (j, h, report)
+    cont = place(lay, [s], None)
+    assert np.array_equal(_prefill(cont, [T], [C], 0, 16, [q]).reshape(C, 16, 256), got)
