@@ -31,15 +31,15 @@ constexpr int kQBytes = kM * 512;    // four 64-dim regions of 128 rows x 128 B
 constexpr int kKVBytes = kN * 512;   // four 64-dim regions of 32 rows x 128 B
 constexpr int kRegionQ = kM * 128;   // bytes of one 64-dim region of Q
 constexpr int kRegionKV = kN * 128;  // bytes of one 64-dim region of a K or V tile
-constexpr int kPBytes = kM * 128;    // 128 rows x 128 B (the first 64 B of a row used)
+constexpr int kPBytes = kM * 128;    // 128 rows x 128 B: tile n's 32 keys in half n & 1
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kKV * kKVBytes;
 constexpr int kOffP = kOffV + kKV * kKVBytes;  // P hi, then P lo
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-// barriers
+// barriers (a pair wherever the producing side may run a tile ahead)
 constexpr int kBarKFull = 0, kBarVFull = 3, kBarKVEmpty = 6, kBarSFull = 9, kBarSEmpty = 11;
-constexpr int kBarPFull = 13, kBarODone = 14, kBarQFull = 15, kNumBars = 16;
+constexpr int kBarPFull = 13, kBarODone = 15, kBarQFull = 17, kNumBars = 18;
 constexpr size_t kPSmem = 1024 + kOffBar + kNumBars * 8 + 16;
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 constexpr float kRescale = 8.f;  // rescale O when the max grows by more than 2^8
@@ -158,9 +158,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[kBarSFull + i], 1);
             mbar_init(&bars[kBarSEmpty + i], kM);
+            mbar_init(&bars[kBarPFull + i], kM);
+            mbar_init(&bars[kBarODone + i], 1);
         }
-        mbar_init(&bars[kBarPFull], kM);
-        mbar_init(&bars[kBarODone], 1);
         mbar_init(&bars[kBarQFull], kM);
         *abort_flag = 0;
         fence_mbar_init();
@@ -231,14 +231,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 x[i] = ok ? __uint_as_float(sv[i]) * kScaleLog2 : -INFINITY;
                 mx = fmaxf(mx, x[i]);
             }
-            // P and O are free once the previous tile's P V products are done
-            if (n > 0 && !mbar_wait(&bars[kBarODone], (n - 1) & 1, c.status)) {
-                *abort_flag = 1;
-                break;
-            }
-            tc_fence_after();
             const bool grow = m_used != -INFINITY && mx > m_used + kRescale;
             if (__any_sync(0xffffffffu, grow)) {
+                // correct O: the previous tile's products must be in it first
+                if (n > 0 && !mbar_wait(&bars[kBarODone + ((n - 1) & 1)], ((n - 1) >> 1) & 1, c.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
                 const float m_new = fmaxf(m_used, mx);
                 const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
 #pragma unroll 1
@@ -267,10 +267,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 lo[i / 2] = pack_bf16(p0 - bf16_lo(hi[i / 2]), p1 - bf16_hi(hi[i / 2]));
             }
             l += psum;
-            // row r of the P operands: 32 keys = 64 bytes = chunks 0..3
+            // this tile's half of the P rows is free once tile n-2's products are done
+            if (n > 1 && !mbar_wait(&bars[kBarODone + (n & 1)], ((n - 2) >> 1) & 1, c.status)) {
+                *abort_flag = 1;
+                break;
+            }
+            // row r of the P operands: 32 keys = 64 bytes = chunks 4h .. 4h+3
+            const int h4 = 4 * (n & 1);
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
-                const uint32_t off = r * 128 + (((ch ^ (r & 7))) << 4);
+                const uint32_t off = r * 128 + ((((ch + h4) ^ (r & 7))) << 4);
                 *reinterpret_cast<uint4 *>(p_hi + off) =
                     make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
                 *reinterpret_cast<uint4 *>(p_lo + off) =
@@ -278,11 +284,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars[kBarPFull]);
+            mbar_arrive(&bars[kBarPFull + (n & 1)]);
         }
         // ---------------- epilogue ----------------
         bool ok = !*abort_flag;
-        if (ok && ntiles > 0 && !mbar_wait(&bars[kBarODone], (ntiles - 1) & 1, c.status)) {
+        if (ok && ntiles > 0 &&
+            !mbar_wait(&bars[kBarODone + ((ntiles - 1) & 1)], ((ntiles - 1) >> 1) & 1, c.status)) {
             *abort_flag = 1;
             ok = false;
         }
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             const int b = n % kKV;
             if (!mbar_wait(&bars[kBarVFull + b], (n / kKV) & 1, c.status) ||
-                !mbar_wait(&bars[kBarPFull], n & 1, c.status)) {
+                !mbar_wait(&bars[kBarPFull + (n & 1)], (n >> 1) & 1, c.status)) {
                 ok = false;
                 break;
             }
@@ -433,14 +440,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t vb = sbase + kOffV + b * kKVBytes;
 #pragma unroll
             for (int kk = 0; kk < kN / 16; ++kk) {
-                const uint32_t pa = sbase + kOffP + kk * 32;
+                const uint32_t pa = sbase + kOffP + (n & 1) * 64 + kk * 32;
                 const uint32_t va = vb + kk * 2048;  // 16 keys = two 8-row groups
                 tc_mma(tmem + kOCol, smem_desc(pa, 16, 1024), smem_desc(va, kRegionKV, 1024), idesc_o,
                        (n > 0 || kk > 0) ? 1u : 0u);
                 tc_mma(tmem + kOCol, smem_desc(pa + kPBytes, 16, 1024), smem_desc(va, kRegionKV, 1024),
                        idesc_o, 1u);
             }
-            tc_commit(&bars[kBarODone]);
+            tc_commit(&bars[kBarODone + (n & 1)]);
             tc_commit(&bars[kBarKVEmpty + b]);
         }
         if (!ok) *abort_flag = 1;
