@@ -341,6 +341,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const void *map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;
         const uint64_t pol = policy_evict_first();
         const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;
+        // page ids in registers: lane i holds pages win + i (cur) and
+        // win + 32 + i (nxt); the window slides by 32 once a tile starts past
+        // its first half, so the next half is loading long before it is read
+        // and no table read waits in the issue loop (a tile spans at most 9
+        // pages, so its pages always lie in the 64-page window)
+        auto page_id = [&](int p) -> int {
+            return (sd.table && p < sd.n_table) ? __ldg(sd.table + p) : 0;
+        };
+        int win = sd.table ? key0 / sd.ptok : 0;
+        int cur = page_id(win + lane), nxt = page_id(win + 32 + lane);
         for (int n = 0; n < ntiles && !*abort_flag; ++n) {
             const int b = n % kKV;
             if (n >= kKV && !mbar_wait(&bars[kBarKVEmpty + b], ((n / kKV) - 1) & 1, c.status)) {
@@ -357,7 +367,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (sd.table) {
                 const int page = key / sd.ptok;
                 row = key - page * sd.ptok;
-                const int id = __ldg(sd.table + page);
+                const int first = __shfl_sync(0xffffffffu, page, 0);  // the tile's lowest page
+                while (first >= win + 32) {
+                    win += 32;
+                    cur = nxt;
+                    nxt = page_id(win + 32 + lane);
+                }
+                const int idx = page - win;  // 0 .. 63
+                const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
+                const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
+                const int id = idx < 32 ? a0 : a1;
                 if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
                     pg = (int64_t)id * sd.ps;
                 } else if (c.status) {
