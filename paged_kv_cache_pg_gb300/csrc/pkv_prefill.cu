@@ -7,14 +7,18 @@
 //   softmax of S with the causal mask, P = hi + lo bf16 parts   [4 warps]
 //   O += P_hi V + P_lo V -> TMEM (128 lanes x 256 columns)      [MMA warp]
 // Q, K, V and P sit in shared memory in the 128-byte-swizzled layouts the
-// MMA reads through matrix descriptors; K and V tiles arrive by 2D TMA copies
-// of whole 16-row page runs (the rows of 16 consecutive positions are
-// contiguous in a page whose size is a multiple of 16) or, for a ragged tail
-// or other page sizes, by cp.async from one row lookup per key.  The max of a
-// row is rescaled lazily: O in TMEM is corrected only when the running max
-// grows by more than 2^8.  Split partials use the decode layout and its
-// combine kernel.
+// MMA reads through matrix descriptors.  K and V tiles have rings of their
+// own, each filled by its own producer warp: a K slot is free as soon as its
+// S product is done, so the next K tiles load while the softmax and the PV
+// product of earlier tiles run (with one ring for both, every tile waited
+// out a whole load latency).  Tiles arrive by 2D TMA copies of whole 16-row
+// page runs (the rows of 16 consecutive positions are contiguous in a page
+// whose size is a multiple of 16) or, for a ragged tail or other page sizes,
+// by cp.async from one row lookup per key.  The max of a row is rescaled
+// lazily: O in TMEM is corrected only when the running max grows by more
+// than 2^8.  Split partials use the decode layout and its combine kernel.
 #include <algorithm>
+#include <climits>
 
 #include "pkv_dev.cuh"
 
@@ -23,8 +27,9 @@ namespace {
 
 constexpr int kM = 128;              // rows of an M-tile
 constexpr int kN = 32;               // keys a tile
-constexpr int kKV = 3;               // K/V tile buffers
-constexpr int kPThreads = 192;       // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kKS = 4;               // K tile buffers
+constexpr int kVS = 4;               // V tile buffers
+constexpr int kPThreads = 224;       // warps 0-3 softmax, 4 K producer, 5 MMA, 6 V producer
 constexpr uint32_t kTmemCols = 512;  // S buffers at columns 0 and 32, O at 256
 constexpr uint32_t kOCol = 256;
 constexpr int kQBytes = kM * 512;    // four 64-dim regions of 128 rows x 128 B
@@ -34,13 +39,16 @@ constexpr int kRegionKV = kN * 128;  // bytes of one 64-dim region of a K or V t
 constexpr int kPBytes = kM * 128;    // 128 rows x 128 B: tile n's 32 keys in half n & 1
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + kKV * kKVBytes;
-constexpr int kOffP = kOffV + kKV * kKVBytes;  // P hi, then P lo
+constexpr int kOffV = kOffK + kKS * kKVBytes;
+constexpr int kOffP = kOffV + kVS * kKVBytes;  // P hi, then P lo
 constexpr int kOffBar = kOffP + 2 * kPBytes;
 // barriers (a pair wherever the producing side may run a tile ahead)
-constexpr int kBarKFull = 0, kBarVFull = 3, kBarKVEmpty = 6, kBarSFull = 9, kBarSEmpty = 11;
-constexpr int kBarPFull = 13, kBarODone = 15, kBarQFull = 17, kNumBars = 18;
+constexpr int kBarKFull = 0, kBarVFull = kBarKFull + kKS, kBarKEmpty = kBarVFull + kVS;
+constexpr int kBarVEmpty = kBarKEmpty + kKS, kBarSFull = kBarVEmpty + kVS, kBarSEmpty = kBarSFull + 2;
+constexpr int kBarPFull = kBarSEmpty + 2, kBarODone = kBarPFull + 2, kBarQFull = kBarODone + 2;
+constexpr int kNumBars = kBarQFull + 1;
 constexpr size_t kPSmem = 1024 + kOffBar + kNumBars * 8 + 16;
+static_assert(kPSmem <= 232448, "prefill shared memory above the 227 KB a CTA may hold");
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 constexpr float kRescale = 8.f;  // rescale O when the max grows by more than 2^8
 
@@ -150,10 +158,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int ntiles = key1 > key0 ? (key1 - key0 + kN - 1) / kN : 0;
 
     if (tid == 0) {
-        for (int i = 0; i < kKV; ++i) {
+        for (int i = 0; i < kKS; ++i) {
             mbar_init(&bars[kBarKFull + i], 1);
+            mbar_init(&bars[kBarKEmpty + i], 1);
+        }
+        for (int i = 0; i < kVS; ++i) {
             mbar_init(&bars[kBarVFull + i], 1);
-            mbar_init(&bars[kBarKVEmpty + i], 1);
+            mbar_init(&bars[kBarVEmpty + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[kBarSFull + i], 1);
@@ -185,7 +196,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int col = col0 + r;
         const bool row_ok = r < rows;
         const int j = row_ok ? col / G : 0;
-        const int qpos = row_ok ? qbase + j : -1;
+        // rows past the M-tile's end take no mask: their Q rows are zero, so
+        // their scores are finite, and their outputs are never written
+        const int qpos = row_ok ? qbase + j : INT_MAX;
         // Q row into the swizzled A operand
         {
             uint8_t *qs = smem + kOffQ;
@@ -212,7 +225,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         uint8_t *p_hi = smem + kOffP, *p_lo = smem + kOffP + kPBytes;
         for (int n = 0; n < ntiles; ++n) {
             const int sb = n & 1;
-            if (!mbar_wait(&bars[kBarSFull + sb], (n >> 1) & 1, c.status)) {
+            // every exit is warp-uniform: the TMEM loads below are .sync.aligned
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarSFull + sb], (n >> 1) & 1, c.status))) {
                 *abort_flag = 1;
                 break;
             }
@@ -222,19 +236,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars[kBarSEmpty + sb]);
             const int kt = key0 + n * kN;
+            // raw scores; the causal and split bounds cut into a tile only near
+            // the diagonal and at the split's end
             float x[32];
-            float mx = -INFINITY;
+            if (__all_sync(0xffffffffu, kt + kN <= key1 && kt + kN - 1 <= qpos)) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int kp = kt + i;
-                const bool ok = kp < key1 && kp <= qpos;
-                x[i] = ok ? __uint_as_float(sv[i]) * kScaleLog2 : -INFINITY;
-                mx = fmaxf(mx, x[i]);
+                for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(sv[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int kp = kt + i;
+                    x[i] = (kp < key1 && kp <= qpos) ? __uint_as_float(sv[i]) : -INFINITY;
+                }
             }
+            float mx = x[0];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) mx = fmaxf(mx, x[i]);
+            mx *= kScaleLog2;  // in log2 units; -inf when the whole tile is masked
             const bool grow = m_used != -INFINITY && mx > m_used + kRescale;
             if (__any_sync(0xffffffffu, grow)) {
                 // correct O: the previous tile's products must be in it first
-                if (n > 0 && !mbar_wait(&bars[kBarODone + ((n - 1) & 1)], ((n - 1) >> 1) & 1, c.status)) {
+                if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + ((n - 1) & 1)],
+                                                                 ((n - 1) >> 1) & 1, c.status))) {
                     *abort_flag = 1;
                     break;
                 }
@@ -255,20 +278,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
             } else if (m_used == -INFINITY) {
                 m_used = mx;  // nothing accumulated yet: O is still zero
             }
+            // p = 2^(s * scale - m); a masked score is -inf and gives 0 (the
+            // offset is 0 while every score so far was masked)
+            const float m_off = m_used == -INFINITY ? 0.f : m_used;
             float psum = 0.f;
             uint32_t hi[16], lo[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                const float p0 = (x[i] == -INFINITY || m_used == -INFINITY) ? 0.f : ex2(x[i] - m_used);
-                const float p1 =
-                    (x[i + 1] == -INFINITY || m_used == -INFINITY) ? 0.f : ex2(x[i + 1] - m_used);
+                const float p0 = ex2(fmaf(x[i], kScaleLog2, -m_off));
+                const float p1 = ex2(fmaf(x[i + 1], kScaleLog2, -m_off));
                 psum += p0 + p1;
-                hi[i / 2] = pack_bf16(p0, p1);
-                lo[i / 2] = pack_bf16(p0 - bf16_lo(hi[i / 2]), p1 - bf16_hi(hi[i / 2]));
+                // p = hi + lo: hi is p's top 16 bits (exact), lo the top 16 bits
+                // of the exact remainder, so hi + lo is p to 2^-15 relative;
+                // bit selects keep the split off the conversion pipe
+                const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+                hi[i / 2] = __byte_perm(u0, u1, 0x7632);
+                const float r0 = p0 - __uint_as_float(u0 & 0xffff0000u);
+                const float r1 = p1 - __uint_as_float(u1 & 0xffff0000u);
+                lo[i / 2] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
             }
             l += psum;
             // this tile's half of the P rows is free once tile n-2's products are done
-            if (n > 1 && !mbar_wait(&bars[kBarODone + (n & 1)], ((n - 2) >> 1) & 1, c.status)) {
+            if (n > 1 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + (n & 1)],
+                                                             ((n - 2) >> 1) & 1, c.status))) {
                 *abort_flag = 1;
                 break;
             }
@@ -287,9 +319,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_arrive(&bars[kBarPFull + (n & 1)]);
         }
         // ---------------- epilogue ----------------
-        bool ok = !*abort_flag;
+        bool ok = __all_sync(0xffffffffu, !*abort_flag);
         if (ok && ntiles > 0 &&
-            !mbar_wait(&bars[kBarODone + ((ntiles - 1) & 1)], ((ntiles - 1) >> 1) & 1, c.status)) {
+            !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + ((ntiles - 1) & 1)],
+                                               ((ntiles - 1) >> 1) & 1, c.status))) {
             *abort_flag = 1;
             ok = false;
         }
@@ -335,12 +368,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 part_ml[prow * 2 + 1] = l;
             }
         }
-    } else if (warp == 4) {
-        // ---------------- producer: K and V tiles ----------------
+    } else if (warp == 4 || warp == 6) {
+        // ---------------- producers: K tiles (warp 4), V tiles (warp 6) ----------------
         pdl_wait();  // the chunk's rows are stored by the previous kernel
+        const bool is_v = warp == 6;
+        const int nbuf = is_v ? kVS : kKS;
+        uint8_t *const ring = smem + (is_v ? kOffV : kOffK);
+        uint64_t *const full = &bars[is_v ? kBarVFull : kBarKFull];
+        uint64_t *const empty = &bars[is_v ? kBarVEmpty : kBarKEmpty];
         const void *map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;
-        const uint64_t pol = policy_evict_first();
-        const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;
+        const uint64_t pol = policy_evict_normal();  // every M-tile of the head reads these rows
+        // V rows sit H * ptok rows after the K rows of the same page
+        const int64_t gap = is_v ? (int64_t)H * sd.ptok * kHeadDim : 0;
         // page ids in registers: lane i holds pages win + i (cur) and
         // win + 32 + i (nxt); the window slides by 32 once a tile starts past
         // its first half, so the next half is loading long before it is read
@@ -351,15 +390,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         };
         int win = sd.table ? key0 / sd.ptok : 0;
         int cur = page_id(win + lane), nxt = page_id(win + 32 + lane);
-        for (int n = 0; n < ntiles && !*abort_flag; ++n) {
-            const int b = n % kKV;
-            if (n >= kKV && !mbar_wait(&bars[kBarKVEmpty + b], ((n / kKV) - 1) & 1, c.status)) {
+        for (int n = 0; n < ntiles; ++n) {
+            const int b = n % nbuf;
+            if (__any_sync(0xffffffffu, *abort_flag) ||
+                (n >= nbuf && !__all_sync(0xffffffffu, mbar_wait(&empty[b], ((n / nbuf) - 1) & 1, c.status)))) {
                 *abort_flag = 1;
                 break;
             }
             const int kt = key0 + n * kN;
-            uint8_t *ks = smem + kOffK + b * kKVBytes;
-            uint8_t *vs = smem + kOffV + b * kKVBytes;
+            uint8_t *dst = ring + b * kKVBytes;
             // this lane's key (one lookup per key per tile): clamped into the split
             const int key = min(kt + lane, key1 - 1);
             int row = key;
@@ -379,43 +418,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const int id = idx < 32 ? a0 : a1;
                 if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
                     pg = (int64_t)id * sd.ps;
-                } else if (c.status) {
+                } else if (c.status && !is_v) {
                     atomicOr(c.status, PKV_DEV_BAD_PAGE);
                 }
             }
-            const int64_t krow = pg + off_k(sd.ptok, kvh, row);
-            const bool whole = map != nullptr && kt + kN <= key1;
-            if (whole) {
-                // two 16-row page runs, four 64-dim chunks each, for K and for V
+            const int64_t krow = pg + off_k(sd.ptok, kvh, row) + gap;
+            if (map != nullptr && kt + kN <= key1) {
+                // two 16-row page runs, four 64-dim chunks each
                 const int y0 = static_cast<int>(sd.layer_row + shfl64(krow, 0) / kHeadDim);
                 const int y1 = static_cast<int>(sd.layer_row + shfl64(krow, 16) / kHeadDim);
-                const int yv = static_cast<int>(v_gap / kHeadDim);
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars[kBarKFull + b], kKVBytes);
-                    mbar_arrive_expect_tx(&bars[kBarVFull + b], kKVBytes);
+                    mbar_arrive_expect_tx(&full[b], kKVBytes);
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
-                        tma_load_2d(ks + ch * kRegionKV, map, 64 * ch, y0, &bars[kBarKFull + b], pol);
-                        tma_load_2d(ks + ch * kRegionKV + 2048, map, 64 * ch, y1, &bars[kBarKFull + b], pol);
-                        tma_load_2d(vs + ch * kRegionKV, map, 64 * ch, y0 + yv, &bars[kBarVFull + b], pol);
-                        tma_load_2d(vs + ch * kRegionKV + 2048, map, 64 * ch, y1 + yv, &bars[kBarVFull + b], pol);
+                        tma_load_2d(dst + ch * kRegionKV, map, 64 * ch, y0, &full[b], pol);
+                        tma_load_2d(dst + ch * kRegionKV + 2048, map, 64 * ch, y1, &full[b], pol);
                     }
                 }
             } else {
-                // key r's rows from lane r's lookup; keys past the split repeat its last row
-#pragma unroll 4
-                for (int rr = 0; rr < kN; ++rr) {
-                    const uint16_t *kr = sd.layer_base + shfl64(krow, rr);
-                    cp_async16(ks + swz128(kRegionKV, rr, lane), kr + lane * 8, pol);
-                    cp_async16(vs + swz128(kRegionKV, rr, lane), kr + v_gap + lane * 8, pol);
-                }
-                cp_async_mbar_arrive(&bars[kBarKFull + b]);
-                cp_async_mbar_arrive(&bars[kBarVFull + b]);
+                // key r's row from lane r's lookup; keys past the split repeat its last row
+#pragma unroll 8
+                for (int rr = 0; rr < kN; ++rr)
+                    cp_async16(dst + swz128(kRegionKV, rr, lane), sd.layer_base + shfl64(krow, rr) + lane * 8,
+                               pol);
+                cp_async_mbar_arrive(&full[b]);
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars[kBarKFull + b]);
-                    mbar_arrive(&bars[kBarVFull + b]);
-                }
+                if (lane == 0) mbar_arrive(&full[b]);
             }
         }
     } else if (warp == 5 && lane == 0) {
@@ -426,8 +454,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         fence_async_smem();
         tc_fence_after();
         auto issue_s = [&](int n) -> bool {
-            const int b = n % kKV, sb = n & 1;
-            if (!mbar_wait(&bars[kBarKFull + b], (n / kKV) & 1, c.status)) return false;
+            const int b = n % kKS, sb = n & 1;
+            if (!mbar_wait(&bars[kBarKFull + b], (n / kKS) & 1, c.status)) return false;
             if (n >= 2 && !mbar_wait(&bars[kBarSEmpty + sb], ((n - 2) >> 1) & 1, c.status)) return false;
             fence_async_smem();
             tc_fence_after();
@@ -440,6 +468,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                        kk > 0);
             }
             tc_commit(&bars[kBarSFull + sb]);
+            tc_commit(&bars[kBarKEmpty + b]);  // the K slot is free once S is computed
             return true;
         };
         if (ok && ntiles > 0) ok = issue_s(0);
@@ -448,8 +477,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 ok = false;
                 break;
             }
-            const int b = n % kKV;
-            if (!mbar_wait(&bars[kBarVFull + b], (n / kKV) & 1, c.status) ||
+            const int b = n % kVS;
+            if (!mbar_wait(&bars[kBarVFull + b], (n / kVS) & 1, c.status) ||
                 !mbar_wait(&bars[kBarPFull + (n & 1)], (n >> 1) & 1, c.status)) {
                 ok = false;
                 break;
@@ -467,7 +496,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                        idesc_o, 1u);
             }
             tc_commit(&bars[kBarODone + (n & 1)]);
-            tc_commit(&bars[kBarKVEmpty + b]);
+            tc_commit(&bars[kBarVEmpty + b]);
         }
         if (!ok) *abort_flag = 1;
     }
