@@ -13,6 +13,15 @@ The same streams in contiguous buffers are timed beside it for the
 paged/contiguous ratio.
 
 Metric: algorithmic HBM bytes / device time, in GB/s, and query-heads/s.
+Every other row of the hot path is measured after the timed region and
+reported beside the headline (`rows`): the chunked prefill of 512 queries on
+31,000 cached positions (store, pool, tensor-core attention), the
+block-sparse decode (block scores, top-64, sparse attention), the serving
+mix (three 4-query draft windows and a 2048-query prefill chunk in one
+arena), and a single decode layer with L2 flushed.  `--only ROW` runs one of
+those alone inside the profiler's capture range (for ncu), `--pages` limits
+the decode sweep.
+
 `--impl reference` times the CPU oracle on the same workload instead.
 """
 from __future__ import annotations
@@ -40,6 +49,15 @@ LENS = [1000, 3000, 6000, 9000]          # cached before the new token
 N_LAYERS, HQ, HKV, D, DI = 13, 16, 2, 256, 128
 PAGES = [16, 48, 128, 256, 512]
 NOMINAL_HBM = 8000.0
+ROWS = ["prefill", "sparse", "mix", "decode_layer"]
+# DRAM bytes (read + write) of one pkv_decode call of the workload (partial +
+# combine kernels), from the ncu capture summarised in
+# profiles/decode_partial_pages256.md, valid while the decode sources hash to
+# the value the capture was taken with; reported as null otherwise.
+DECODE_TRAFFIC = {"bytes": 40438272,
+                  "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
+                  "sha256": "a4aa228c291c2800418f16a30da735c9647cc9f0b068f36b1f9fc1c4e6dc03ee"}
+FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
 def parse():
@@ -50,14 +68,25 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
+    ap.add_argument("--only", choices=ROWS, help="run one hot-path row alone (profiling)")
+    ap.add_argument("--pages", type=str, default=None,
+                    help="comma-separated page sizes to sweep (default: all five)")
+    args = ap.parse_args()
+    if args.pages:
+        args.page_list = [int(x) for x in args.pages.split(",")]
+        if any(p not in PAGES for p in args.page_list):
+            ap.error(f"page sizes must be among {PAGES}")
+    else:
+        args.page_list = list(PAGES)
+    return args
 
 
-def config_desc():
+def config_desc(pages=PAGES):
     return {"workload": "multi-stream paged decode", "streams": len(LENS),
             "cached_lengths": LENS, "new_tokens_per_stream": 1, "layers": N_LAYERS,
             "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "idx_dim": DI,
-            "page_sizes": PAGES, "tables": "random permutations of one arena",
+            "page_sizes": list(pages), "tables": "random permutations of one arena",
             "l2": "inputs larger than L2 (about 506 MB of K/V per page size per step)",
             "step": "13 layer slots x (split-KV decode with the new token's store fused + combine) at every page size"}
 
@@ -82,6 +111,15 @@ def row_credit_bytes(length):
     """Algorithmic bytes credited to one (stream, query head) row: its share of
     the stream's K/V read (the G heads of a KV head share each row)."""
     return length * HKV * D * 2 * 2 / HQ
+
+
+def decode_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, "paged_kv_cache_pg_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return DECODE_TRAFFIC["bytes"] if h.hexdigest() == DECODE_TRAFFIC["sha256"] else None
 
 
 def peaks():
@@ -173,9 +211,10 @@ def barrier(world: int):
 
 # ---- the CPU oracle (baseline and reference arm) ------------------------------------
 
-def oracle_rows(seconds: float, max_rows: int = 1 << 30):
+def oracle_rows(seconds: float, max_rows: int = 1 << 30, part: int = 0, parts: int = 1):
     """Time oracle rows of the workload's layer 0 round-robin over (stream, head)
-    until `seconds` pass; returns (credited bytes, rows, elapsed, sample)."""
+    (this worker's share `part` of `parts`) until `seconds` pass; returns
+    (credited bytes, rows, elapsed)."""
     import oracle as orc
     orc.build()
     shape = orc.Shape(1, HKV, D, DI)
@@ -188,7 +227,7 @@ def oracle_rows(seconds: float, max_rows: int = 1 << 30):
         caches.append(c)
         qs.append(synth.queries(100 + i, 1, HQ, D))
     credited, rows = 0.0, 0
-    order = [(i, h) for h in range(HQ) for i in range(len(LENS))]
+    order = [(i, h) for h in range(HQ) for i in range(len(LENS))][part::parts]
     t0 = time.perf_counter()
     while rows < max_rows:
         i, h = order[rows % len(order)]
@@ -199,6 +238,26 @@ def oracle_rows(seconds: float, max_rows: int = 1 << 30):
             break
     el = time.perf_counter() - t0
     return credited, rows, el
+
+
+def _oracle_worker(args):
+    seconds, part, parts = args
+    return oracle_rows(seconds, part=part, parts=parts)
+
+
+def oracle_rows_all_cores(seconds: float):
+    """The oracle's independent (stream, head) rows split across every host core,
+    one process each (started by spawn, so no CUDA state is inherited)."""
+    import multiprocessing as mp
+    import oracle as orc
+    orc.build()
+    n = max(1, min(os.cpu_count() or 1, len(LENS) * HQ))
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_worker, [(seconds, i, n) for i in range(n)])
+    credited = sum(r[0] for r in res)
+    rows = sum(r[1] for r in res)
+    el = max(r[2] for r in res)
+    return credited, rows, el, n
 
 
 def reference_arm(args):
@@ -227,6 +286,258 @@ def reference_arm(args):
     return 0
 
 
+# ---- the other rows of the hot path ------------------------------------------------
+
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+class FlushTimer:
+    """Median CUDA-event time of a call on the current stream, with a buffer
+    twice the L2 written before every timed call (not timed)."""
+
+    def __init__(self, torch, dev, profile=False):
+        self.torch = torch
+        self.buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.profile = profile
+
+    def ms(self, fn, reps=20, warm=3):
+        t = self.torch
+        for _ in range(warm):
+            self.buf.zero_()
+            fn()
+        t.cuda.synchronize()
+        e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        out = []
+        if self.profile:
+            t.cuda.profiler.start()
+        for _ in range(reps):
+            self.buf.zero_()
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            out.append(e0.elapsed_time(e1))
+        if self.profile:
+            t.cuda.profiler.stop()
+        return statistics.median(out)
+
+
+def _paged(torch, pkv, lay, dev, ptok, lens_total, n_pages, seed):
+    """One arena of n_pages, streams placed by random permutation tables."""
+    ps = pkv.page_elems(lay, ptok)
+    counts = [synth.pages_for(T, ptok) for T in lens_total]
+    tabs = synth.shuffled_tables(seed, n_pages, counts)
+    mem = torch.empty(n_pages * ps, dtype=torch.int16, device=dev)
+    tables = [torch.from_numpy(t).to(dev) for t in tabs]
+    return mem, tables, [pkv.pg(mem, t, ps, ptok, n_pages, t.numel()) for t in tables]
+
+
+def _up(torch, dev, a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+
+def _place(torch, pkv, lay, dev, pg, stream, upto):
+    """Store positions 0 .. upto-1 of a synthetic stream and pool their blocks."""
+    sq = [pkv.seq(pg, upto, upto)]
+    pkv.store(lay, sq, 0, _up(torch, dev, stream.k[0][:upto]), _up(torch, dev, stream.v[0][:upto]),
+              _up(torch, dev, stream.ik[0][:upto]))
+    pkv.pool(lay, sq, 0)
+
+
+def row_prefill(torch, pkv, dev, timer):
+    """512-query chunk on 31,000 cached positions, pages of 256: the chunk's
+    store, its pooled blocks, then the tensor-core attention."""
+    P0, C = 31000, 512
+    T = P0 + C
+    lay = pkv.layout(1, HKV, D, DI)
+    mem, tables, pgs = _paged(torch, pkv, lay, dev, 256, [T], synth.pages_for(T, 256) + 4, 4)
+    s = synth.make_stream(40, 1, T, HKV, D, DI)
+    _place(torch, pkv, lay, dev, pgs[0], s, P0)
+    kc, vc, ic = (_up(torch, dev, x[0][P0:]) for x in (s.k, s.v, s.ik))
+    sq = [pkv.seq(pgs[0], T, C)]
+    q = _up(torch, dev, synth.queries(41, C, HQ, D))
+    out = torch.empty_like(q)
+    ws = torch.empty(pkv.prefill_ws_size(lay, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def store():
+        pkv.store(lay, sq, 0, kc, vc, ic, status=status)
+
+    def pool():
+        pkv.pool(lay, sq, 0, status=status)
+
+    def attend():
+        pkv.prefill(lay, sq, 0, HQ, q, out, ws, status=status)
+
+    def step():
+        store(), pool(), attend()
+
+    t = {"store": timer.ms(store), "pool": timer.ms(pool), "prefill": timer.ms(attend),
+         "step": timer.ms(step)}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"prefill row: device status {int(status.item())}")
+    flop = 4.0 * sum(P0 + j + 1 for j in range(C)) * HQ * D
+    peak, kind = bf16_peak()
+    tf = flop / (t["prefill"] / 1e3) / 1e12
+    return {"workload": "chunked prefill: 512 queries on 31,000 cached positions, pages of 256, "
+                        "16/2 heads", "us": {k: round(v * 1e3, 2) for k, v in t.items()},
+            "flop": flop, "TFLOPs": round(tf, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tf / peak, 4), "peak_kind": kind},
+            "query_heads_per_s": round(C * HQ / (t["step"] / 1e3), 1)}
+
+
+def row_sparse(torch, pkv, dev, timer):
+    """2 streams of 9,000 positions in pages of 128: block scores of the pooled
+    indexer keys, top-64 blocks per head, attention over those blocks."""
+    T, K_SEL = 9000, 64
+    lay = pkv.layout(1, HKV, D, DI)
+    n_pages = 2 * synth.pages_for(T, 128) + 8
+    mem, tables, pgs = _paged(torch, pkv, lay, dev, 128, [T, T], n_pages, 3)
+    for i in range(2):
+        _place(torch, pkv, lay, dev, pgs[i], synth.make_stream(30 + i, 1, T, HKV, D, DI), T)
+    sq = [pkv.seq(g, T, 1) for g in pgs]
+    nb = T // 4
+    qi = _up(torch, dev, np.concatenate([synth.queries(32 + i, 1, HQ, DI) for i in range(2)]))
+    q = _up(torch, dev, np.concatenate([synth.queries(34 + i, 1, HQ, D) for i in range(2)]))
+    scores = torch.empty((2, HQ, nb), dtype=torch.float32, device=dev)
+    ids = torch.empty((2, HQ, K_SEL), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(pkv.sparse_ws_size(lay, sq, HQ, K_SEL) // 4 + 64, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def sc():
+        pkv.block_scores(lay, sq, 0, HQ, qi, scores, nb, status=status)
+
+    def tk():
+        pkv.topk(sq, HQ, scores, nb, K_SEL, ids)
+
+    def att():
+        pkv.sparse_decode(lay, sq, 0, HQ, q, ids, K_SEL, out, ws, status=status)
+
+    def step():
+        sc(), tk(), att()
+
+    t = {"block_scores": timer.ms(sc), "topk": timer.ms(tk), "sparse_decode": timer.ms(att),
+         "step": timer.ms(step)}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"sparse row: device status {int(status.item())}")
+    # algorithmic bytes: pooled rows, scores written and read back, the selected
+    # K and V rows of every query head, queries and outputs
+    b_scores = 2 * (nb * DI * 2 + HQ * DI * 2 + HQ * nb * 4)
+    b_topk = 2 * (HQ * nb * 4 + HQ * K_SEL * 4)
+    b_att = 2 * (HQ * K_SEL * 4 * 2 * D * 2 + 2 * HQ * D * 2 + HQ * K_SEL * 4)
+    peak, kind = peaks()
+    gbs = (b_scores + b_topk + b_att) / (t["step"] / 1e3) / 1e9
+    att_gbs = b_att / (t["sparse_decode"] / 1e3) / 1e9
+    return {"workload": "block-sparse decode: 2 streams of 9,000, pages of 128, top-64 blocks",
+            "us": {k: round(v * 1e3, 2) for k, v in t.items()},
+            "bytes": {"block_scores": b_scores, "topk": b_topk, "sparse_decode": b_att},
+            "GBps_step": round(gbs, 1), "GBps_sparse_decode": round(att_gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind},
+            "query_heads_per_s": round(2 * HQ / (t["step"] / 1e3), 1)}
+
+
+def row_mix(torch, pkv, dev, timer):
+    """Serving mix in one arena of 792 pages of 256: three streams decoding
+    4-query draft windows (the window's rows stored by the call) and one
+    2048-query prefill chunk (store, pool, attention)."""
+    dec_cached = [9000, 24000, 40956]
+    P0, C, W = 16384, 2048, 4
+    totals = [L + W for L in dec_cached] + [P0 + C]
+    lay = pkv.layout(1, HKV, D, DI)
+    mem, tables, pgs = _paged(torch, pkv, lay, dev, 256, totals, 792, 5)
+    streams = [synth.make_stream(50 + i, 1, T, HKV, D, DI) for i, T in enumerate(totals)]
+    for i, L in enumerate(dec_cached + [P0]):
+        _place(torch, pkv, lay, dev, pgs[i], streams[i], L)
+    dsq = [pkv.seq(pgs[i], totals[i], W) for i in range(3)]
+    win = [np.concatenate([getattr(streams[i], f)[0][dec_cached[i]:] for i in range(3)])
+           for f in ("k", "v", "ik")]
+    kn, vn, ikn = (_up(torch, dev, x) for x in win)
+    qd = _up(torch, dev, np.concatenate([synth.queries(60 + i, W, HQ, D) for i in range(3)]))
+    od = torch.empty_like(qd)
+    wsd = torch.empty(pkv.decode_ws_size(lay, dsq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+    psq = [pkv.seq(pgs[3], P0 + C, C)]
+    kc, vc, ic = (_up(torch, dev, x[0][P0:]) for x in (streams[3].k, streams[3].v, streams[3].ik))
+    qp = _up(torch, dev, synth.queries(64, C, HQ, D))
+    op = torch.empty_like(qp)
+    wsp = torch.empty(pkv.prefill_ws_size(lay, psq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    del streams
+
+    def dec():
+        pkv.decode(lay, dsq, 0, HQ, qd, od, wsd, status=status, k_new=kn, v_new=vn, ik_new=ikn)
+
+    def pre():
+        pkv.store(lay, psq, 0, kc, vc, ic, status=status)
+        pkv.pool(lay, psq, 0, status=status)
+        pkv.prefill(lay, psq, 0, HQ, qp, op, wsp, status=status)
+
+    def step():
+        dec(), pre()
+
+    t = {"draft_window_decode": timer.ms(dec), "prefill_lane": timer.ms(pre), "step": timer.ms(step)}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"mix row: device status {int(status.item())}")
+    dec_bytes = sum(totals[:3]) * HKV * D * 2 * 2 + 2 * 3 * W * HQ * D * 2
+    flop = 4.0 * sum(P0 + j + 1 for j in range(C)) * HQ * D
+    peak, kind = peaks()
+    dgbs = dec_bytes / (t["draft_window_decode"] / 1e3) / 1e9
+    return {"workload": "serving mix: 792 x 256 arena; 3 streams {9000, 24000, 40956} with 4-query "
+                        "draft windows; 1 stream with a 2048-query chunk at 16,384",
+            "us": {k: round(v * 1e3, 2) for k, v in t.items()},
+            "draft_window_GBps": round(dgbs, 1), "draft_window_frac": round(dgbs / peak, 4),
+            "prefill_lane_TFLOPs": round(flop / (t["prefill_lane"] / 1e3) / 1e12, 1),
+            "query_heads_per_s": round((3 * W + C) * HQ / (t["step"] / 1e3), 1)}
+
+
+def row_decode_layer(torch, pkv, dev, timer):
+    """One decode layer of the multi-stream workload at pages of 256, L2 flushed."""
+    lens_after = [L + 1 for L in LENS]
+    lay = pkv.layout(1, HKV, D, DI)
+    n_pages = sum(synth.pages_for(L, 256) for L in lens_after) + 8
+    mem, tables, pgs = _paged(torch, pkv, lay, dev, 256, lens_after, n_pages, 6)
+    streams = [synth.make_stream(70 + i, 1, L, HKV, D, DI) for i, L in enumerate(lens_after)]
+    for g, st, L in zip(pgs, streams, LENS):
+        _place(torch, pkv, lay, dev, g, st, L)
+    sq = [pkv.seq(g, L, 1) for g, L in zip(pgs, lens_after)]
+    kn, vn, ikn = (_up(torch, dev, np.concatenate([getattr(st, f)[0][-1:] for st in streams]))
+                   for f in ("k", "v", "ik"))
+    q = _up(torch, dev, np.concatenate([synth.queries(80 + i, 1, HQ, D) for i in range(len(LENS))]))
+    out = torch.empty_like(q)
+    ws = torch.empty(pkv.decode_ws_size(lay, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+
+    def dec():
+        pkv.decode(lay, sq, 0, HQ, q, out, ws, k_new=kn, v_new=vn, ik_new=ikn)
+
+    ms = timer.ms(dec, reps=50)
+    peak, kind = peaks()
+    gbs = decode_bytes(lens_after) / (ms / 1e3) / 1e9
+    return {"workload": "one layer of the multi-stream decode at pages of 256, L2 flushed "
+                        "before every call", "us": round(ms * 1e3, 2), "GBps": round(gbs, 1),
+            "frac": round(gbs / peak, 4), "peak_kind": kind}
+
+
+ROW_FNS = {"prefill": row_prefill, "sparse": row_sparse, "mix": row_mix,
+           "decode_layer": row_decode_layer}
+
+
+def hot_path_rows(torch, pkv, dev, names, profile=False):
+    timer = FlushTimer(torch, dev, profile=profile)
+    out = {}
+    for n in names:
+        out[n] = ROW_FNS[n](torch, pkv, dev, timer)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 # ---- our arm -----------------------------------------------------------------------
 
 def main_ours(args):
@@ -234,6 +545,7 @@ def main_ours(args):
     from paged_kv_cache_pg_gb300 import build, pkv
 
     rank, world, local = dist_env()
+    pages = args.page_list
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -241,6 +553,13 @@ def main_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     build.build()
     pkv.load()
+
+    if args.only:
+        # one hot-path row alone, its timed calls inside the profiler's capture range
+        res = hot_path_rows(torch, pkv, dev, [args.only], profile=True)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "row": res[args.only]}))
+        return 0
 
     lay = pkv.layout(N_LAYERS, HKV, D, DI)
     lens_after = [L + 1 for L in LENS]
@@ -262,7 +581,7 @@ def main_ours(args):
 
     # caches: one arena per page size, and contiguous buffers
     confs = {}
-    for p in PAGES + [None]:
+    for p in pages + [None]:
         if p is None:
             pgs, mems = [], []
             for L in lens_after:
@@ -329,7 +648,7 @@ def main_ours(args):
         graphs[p].replay()
     torch.cuda.synchronize()
     same = all(torch.equal(confs[p]["out"][l], confs[None]["out"][l])
-               for p in PAGES for l in range(N_LAYERS))
+               for p in pages for l in range(N_LAYERS))
     if int(status.item()) != 0:
         raise RuntimeError(f"device status word {int(status.item())}")
 
@@ -348,12 +667,12 @@ def main_ours(args):
     t_wall = time.perf_counter()
     torch.cuda.profiler.start()   # the profiler's capture range is the timed region
     for _ in range(args.steps):
-        for p in PAGES:
+        for p in pages:
             ev0[p].record()
             graphs[p].replay()
             ev1[p].record()
-        ev1[PAGES[-1]].synchronize()
-        for p in PAGES:
+        ev1[pages[-1]].synchronize()
+        for p in pages:
             step_ms[p].append(ev0[p].elapsed_time(ev1[p]))
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
@@ -372,13 +691,13 @@ def main_ours(args):
     torch.cuda.synchronize()
 
     # ---- results ----
-    per_step_ms = sum(statistics.fmean(step_ms[p]) for p in PAGES)
+    per_step_ms = sum(statistics.fmean(step_ms[p]) for p in pages)
     max_ms = max_over_ranks(per_step_ms * args.steps, world, dev)
-    step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in PAGES)
+    step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in pages)
     value = world * step_bytes * args.steps / (max_ms / 1e3) / 1e9
-    qh_per_step = len(PAGES) * N_LAYERS * S * HQ
+    qh_per_step = len(pages) * N_LAYERS * S * HQ
     per_page = {}
-    for p in PAGES:
+    for p in pages:
         ms = statistics.fmean(step_ms[p])
         per_page[str(p)] = {
             "GBps": round(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) / ms / 1e6, 1),
@@ -389,13 +708,16 @@ def main_ours(args):
 
     # one pkv_decode call (partial kernel with the fused store + combine kernel) per
     # layer; its average duration is the timed graph time over its 13 calls
-    dur = statistics.fmean(x for p in PAGES for x in step_ms[p]) / N_LAYERS / 1e3
+    dur = statistics.fmean(x for p in pages for x in step_ms[p]) / N_LAYERS / 1e3
     achieved = decode_bytes(lens_after) / dur / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4), "traffic": decode_traffic(),
+            "algorithmic_bytes": decode_bytes(lens_after),
             "kernel": "pkv_decode (split-KV partial with fused store + combine), one layer, 4 streams",
             "avg_launch_us": round(dur * 1e6, 3), "peak_kind": peak_kind,
             "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM, 4)}
+
+    rows = None if args.no_rows else hot_path_rows(torch, pkv, dev, ROWS)
 
     # end to end through the public API with host buffers
     e2e = e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, status,
@@ -403,17 +725,21 @@ def main_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        credited, rows, el = oracle_rows(args.cpu_seconds)
+        credited, n_rows, el = oracle_rows(args.cpu_seconds)
         cpu = {"value": round(credited / el / 1e9, 4), "unit": "GB/s", "cores": 1,
                "kind": "oracle",
-               "sample": f"{rows} (stream, query head) rows of layer 0 of the workload "
+               "sample": f"{n_rows} (stream, query head) rows of layer 0 of the workload "
                          f"({el:.1f} s, one thread)"}
+        c_all, r_all, el_all, n_all = oracle_rows_all_cores(args.cpu_seconds)
+        cpu["all_cores"] = {"value": round(c_all / el_all / 1e9, 4), "unit": "GB/s", "cores": n_all,
+                            "sample": f"{r_all} rows, the (stream, head) rows split across "
+                                      f"{n_all} processes ({el_all:.1f} s)"}
 
-    launches = args.steps * sum(N_LAYERS * confs[p]["launches_per_layer"] for p in PAGES)
+    launches = args.steps * sum(N_LAYERS * confs[p]["launches_per_layer"] for p in pages)
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step_ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_desc(),
+            "data": "synthetic", "config": config_desc(pages),
             "pct_of_measured_peak": round(100 * value / world / peak, 2),
             "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM, 2),
             "query_heads_per_s": round(world * qh_per_step * args.steps / (max_ms / 1e3), 1),
@@ -422,6 +748,7 @@ def main_ours(args):
             "paged_contig_ratio_worst": max(v["paged_over_contig"] for v in per_page.values()),
             "paged_equals_contiguous": bool(same),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "rows": rows,
             "clocks": clk, "timed_wall_s": round(wall, 3)}
     if rank == 0:
         print(json.dumps(line))
@@ -433,6 +760,7 @@ def main_ours(args):
 
 def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, status, lens_after,
             dev, args):
+    pages = args.page_list
     """Same step through the public calls, inputs from pinned host memory and
     outputs back to it, copies inside the timed region."""
     S = len(lens_after)
@@ -445,7 +773,7 @@ def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, sta
     h_out = torch.empty(h_q.shape, dtype=torch.int16).pin_memory()
     d_out = torch.empty(h_q.shape, dtype=torch.int16, device=dev)
     graphs = {}
-    for p in PAGES:
+    for p in pages:
         cf = confs[p]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -458,7 +786,7 @@ def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, sta
             h_out.copy_(d_out, non_blocking=True)
         graphs[p] = g
     for _ in range(max(3, args.warmup)):
-        for p in PAGES:
+        for p in pages:
             graphs[p].replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -466,14 +794,14 @@ def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, sta
     total = 0.0
     for _ in range(n):
         e0.record()
-        for p in PAGES:
+        for p in pages:
             graphs[p].replay()
         e1.record()
         e1.synchronize()
         total += e0.elapsed_time(e1)
-    step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in PAGES)
-    h2d = len(PAGES) * (h_q.numel() + kv_rows.numel() + ik_rows.numel()) * 2
-    d2h = len(PAGES) * h_out.numel() * 2
+    step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in pages)
+    h2d = len(pages) * (h_q.numel() + kv_rows.numel() + ik_rows.numel()) * 2
+    d2h = len(pages) * h_out.numel() * 2
     return {"value": round(step_bytes / (total / n / 1e3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": n, "ms_per_step": round(total / n, 4)}
