@@ -203,6 +203,14 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def aggregate(step_bytes: float, steps: int, local_ms: float, world: int, device=None):
+    """Whole-job throughput (GB/s) of `world` replicas that each moved
+    step_bytes per step for `steps` steps: every rank's bytes over the slowest
+    rank's time.  Returns (value, max_ms)."""
+    max_ms = max_over_ranks(local_ms, world, device)
+    return world * step_bytes * steps / (max_ms / 1e3) / 1e9, max_ms
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -692,9 +700,8 @@ def main_ours(args):
 
     # ---- results ----
     per_step_ms = sum(statistics.fmean(step_ms[p]) for p in pages)
-    max_ms = max_over_ranks(per_step_ms * args.steps, world, dev)
     step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in pages)
-    value = world * step_bytes * args.steps / (max_ms / 1e3) / 1e9
+    value, max_ms = aggregate(step_bytes, args.steps, per_step_ms * args.steps, world, dev)
     qh_per_step = len(pages) * N_LAYERS * S * HQ
     per_page = {}
     for p in pages:
