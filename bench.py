@@ -370,7 +370,7 @@ def row_prefill(torch, pkv, dev, timer):
     sq = [pkv.seq(pgs[0], T, C)]
     q = _up(torch, dev, synth.queries(41, C, HQ, D))
     out = torch.empty_like(q)
-    ws = torch.empty(pkv.prefill_ws_size(lay, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+    ws = torch.zeros(pkv.prefill_ws_size(lay, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def store():
@@ -416,7 +416,7 @@ def row_sparse(torch, pkv, dev, timer):
     scores = torch.empty((2, HQ, nb), dtype=torch.float32, device=dev)
     ids = torch.empty((2, HQ, K_SEL), dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
-    ws = torch.empty(pkv.sparse_ws_size(lay, sq, HQ, K_SEL) // 4 + 64, dtype=torch.float32, device=dev)
+    ws = torch.zeros(pkv.sparse_ws_size(lay, sq, HQ, K_SEL) // 4 + 64, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def sc():
@@ -470,12 +470,12 @@ def row_mix(torch, pkv, dev, timer):
     kn, vn, ikn = (_up(torch, dev, x) for x in win)
     qd = _up(torch, dev, np.concatenate([synth.queries(60 + i, W, HQ, D) for i in range(3)]))
     od = torch.empty_like(qd)
-    wsd = torch.empty(pkv.decode_ws_size(lay, dsq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+    wsd = torch.zeros(pkv.decode_ws_size(lay, dsq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
     psq = [pkv.seq(pgs[3], P0 + C, C)]
     kc, vc, ic = (_up(torch, dev, x[0][P0:]) for x in (streams[3].k, streams[3].v, streams[3].ik))
     qp = _up(torch, dev, synth.queries(64, C, HQ, D))
     op = torch.empty_like(qp)
-    wsp = torch.empty(pkv.prefill_ws_size(lay, psq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+    wsp = torch.zeros(pkv.prefill_ws_size(lay, psq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     del streams
 
@@ -519,7 +519,7 @@ def row_decode_layer(torch, pkv, dev, timer):
                    for f in ("k", "v", "ik"))
     q = _up(torch, dev, np.concatenate([synth.queries(80 + i, 1, HQ, D) for i in range(len(LENS))]))
     out = torch.empty_like(q)
-    ws = torch.empty(pkv.decode_ws_size(lay, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+    ws = torch.zeros(pkv.decode_ws_size(lay, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
 
     def dec():
         pkv.decode(lay, sq, 0, HQ, q, out, ws, k_new=kn, v_new=vn, ik_new=ikn)
@@ -626,7 +626,7 @@ def main_ours(args):
                  for p, cf in confs.items()}
     for p, cf in confs.items():
         n = pkv.decode_ws_size(lay, step_seqs[p], HQ)
-        cf["ws"] = torch.empty(max(64, n // 4 + 64), dtype=torch.float32, device=dev)
+        cf["ws"] = torch.zeros(max(64, n // 4 + 64), dtype=torch.float32, device=dev)
         cf["launches_per_layer"] = 1 + (1 if n > 0 else 0)
         cf["out"] = [torch.empty_like(q_dev[0]) for _ in range(N_LAYERS)]
 

@@ -556,11 +556,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // M = max m_i, L = sum 2^(m_i-M) l_i, O = sum 2^(m_i-M) acc_i, out = O / L.
 // Thread d owns dim d and loads acc_i[d] for up to 32 splits at once while
 // the split maxima load, so one memory round trip covers a column of up to
-// 32 splits.  Every sum runs in split order.
+// 32 splits.  Every sum runs in split order.  At most 64 registers a thread:
+// a combine CTA then fits on an SM beside a partial CTA of the next call,
+// which can start streaming its keys without waiting for the SM.
 template <bool kSparse>
-__global__ void __launch_bounds__(kCombThreads)
+__global__ void __launch_bounds__(kCombThreads, 4)
     decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
-    constexpr int kBatch = 64;
+    constexpr int kBatch = 32;
     extern __shared__ float comb_smem[];  // w[ns], lsum[ns]
     __shared__ float sh_l;
     pdl_wait();
@@ -690,8 +692,27 @@ int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
     return PKV_OK;
 }
 
+// Every kernel of a decode call asks for the largest shared-memory carveout:
+// an SM configured for a small one (as a kernel using little shared memory
+// would leave it) cannot take a partial CTA of the next call until it drains.
+static int set_carveout() {
+    static bool done = false;
+    if (done) return PKV_OK;
+    const void *fns[] = {reinterpret_cast<const void *>(decode_combine<false>),
+                         reinterpret_cast<const void *>(decode_combine<true>),
+                         reinterpret_cast<const void *>(decode_partial<false>),
+                         reinterpret_cast<const void *>(decode_partial<true>)};
+    for (const void *f : fns)
+        if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return PKV_ECUDA;
+    done = true;
+    return PKV_OK;
+}
+
 int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, uint16_t *out,
                    float *ws, cudaStream_t stream) {
+    if (set_carveout() != PKV_OK) return PKV_ECUDA;
     DecodeArgs a{q, out, ws, nullptr, 0, nullptr, nullptr, nullptr};
     int max_ns = 1;
     for (int s = 0; s < c.n_seqs; ++s) max_ns = std::max(max_ns, c.seq[s].nsplit);
@@ -708,6 +729,7 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     Common cc = c;
     auto part = sparse ? decode_partial<true> : decode_partial<false>;
     auto comb = sparse ? decode_combine<true> : decode_combine<false>;
+    if (set_carveout() != PKV_OK) return PKV_ECUDA;
     static bool attr_set[2] = {false, false};
     if (!attr_set[sparse]) {
         if (cudaFuncSetAttribute(part, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -176,7 +176,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // tcgen05 alloc, dealloc, ld and st are warp-collective (.sync.aligned):
+    // every one below follows a __syncwarp, because a CTA barrier does not
+    // reconverge a warp whose lanes took different paths before it
     if (warp == 5) {
+        __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols)
@@ -337,6 +341,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll 1
             for (int ch = 0; ch < 8; ++ch) {
                 uint32_t o[32];
+                __syncwarp();  // rows past the tile's end skipped the stores below
                 if (ntiles > 0) {
                     tmem_ld32(lane_base + kOCol + ch * 32, o);
                 } else {
@@ -505,6 +510,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     pdl_trigger();
     if (warp == 5) {
+        __syncwarp();  // lane 0 issued the MMAs, lanes 1-31 went straight here
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)

@@ -206,3 +206,28 @@ def test_fused_store_decode_equals_store_then_decode(ptok):
     ref_pl = place(lay, full, None)
     ok, worst = within_tol(outs[1], oracle_decode(ref_pl, layer, 16, q))
     assert ok, worst
+
+
+def test_one_workspace_serves_calls_of_different_shapes(multi):
+    # A workspace holds no state between calls: one workspace serves batches
+    # of different shapes back to back (single tokens, 4-query windows, a
+    # smaller batch) with the bits a fresh workspace gives.
+    t = torch()
+    lay, streams, q, ref, base = multi
+    pl = place(lay, streams, 48, seed=11)
+    lens = [s.length for s in streams]
+    win = [synth.queries(300 + i, 4, 16, 256) for i in range(4)]
+    calls = [(pl.seqs(lens, [1] * 4), q, 1),
+             (pl.seqs(lens, [4] * 4), win, 0),
+             (pl.seqs(lens[:2], [1, 1]), q[:2], 1)]
+    sizes = [pkv.decode_ws_size(lay, sq, 16) for sq, _, _ in calls]
+    shared = t.full((max(sizes) // 4 + 64,), float("nan"), dtype=t.float32, device="cuda")
+    for _ in range(2):
+        for (sq, ql, layer), size in zip(calls, sizes):
+            dq = dev_u16(np.concatenate(ql))
+            fresh = t.empty(size // 4 + 64, dtype=t.float32, device="cuda")
+            a, b = t.zeros_like(dq), t.zeros_like(dq)
+            pkv.decode(lay, sq, layer, 16, dq, a, shared)
+            pkv.decode(lay, sq, layer, 16, dq, b, fresh)
+            t.cuda.synchronize()
+            assert t.equal(a, b)
