@@ -49,14 +49,14 @@ LENS = [1000, 3000, 6000, 9000]          # cached before the new token
 N_LAYERS, HQ, HKV, D, DI = 13, 16, 2, 256, 128
 PAGES = [16, 48, 128, 256, 512]
 NOMINAL_HBM = 8000.0
-ROWS = ["prefill", "sparse", "mix", "decode_layer"]
+ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache"]
 # DRAM bytes (read + write) of one pkv_decode call of the workload (partial +
 # combine kernels), from the ncu capture summarised in
 # profiles/decode_partial_pages256.md, valid while the decode sources hash to
 # the value the capture was taken with; reported as null otherwise.
-DECODE_TRAFFIC = {"bytes": 40438272,
+DECODE_TRAFFIC = {"bytes": 40392192,
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "a4aa228c291c2800418f16a30da735c9647cc9f0b068f36b1f9fc1c4e6dc03ee"}
+                  "sha256": "da119ed2c58a1d2d43310e142b07d883fc12cb5022ac3d32f89134e04a5bc985"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
@@ -532,8 +532,63 @@ def row_decode_layer(torch, pkv, dev, timer):
             "frac": round(gbs / peak, 4), "peak_kind": kind}
 
 
+def row_prompt_cache(torch, pkv, dev, timer):
+    """Prompt-cache save and restore of one 31,512-position stream in pages of
+    256 (one layer): save gathers its K, V, indexer and pooled rows through
+    the table into the contiguous layout; restore stores K, V and indexer rows
+    back into another stream's pages and pools its blocks."""
+    T = 31512
+    lay = pkv.layout(1, HKV, D, DI)
+    n_pages = 2 * synth.pages_for(T, 256) + 4
+    mem, tables, pgs = _paged(torch, pkv, lay, dev, 256, [T, T], n_pages, 7)
+    s = synth.make_stream(90, 1, T, HKV, D, DI)
+    _place(torch, pkv, lay, dev, pgs[0], s, T)
+    del s
+    src, dst = [pkv.seq(pgs[0], T, T)], [pkv.seq(pgs[1], T, T)]
+    k = torch.empty((T, HKV, D), dtype=torch.int16, device=dev)
+    v = torch.empty_like(k)
+    ik = torch.empty((T, DI), dtype=torch.int16, device=dev)
+    pooled = torch.empty((T // 4, DI), dtype=torch.int16, device=dev)
+
+    def save():
+        pkv.gather(lay, src, 0, pkv.K, k)
+        pkv.gather(lay, src, 0, pkv.V, v)
+        pkv.gather(lay, src, 0, pkv.IK, ik)
+        pkv.gather(lay, src, 0, pkv.P, pooled)
+
+    def restore():
+        pkv.store(lay, dst, 0, k, v, ik)
+        pkv.pool(lay, dst, 0)
+
+    t = {"save": timer.ms(save), "restore": timer.ms(restore)}
+    torch.cuda.synchronize()
+    same = all(torch.equal(a, b) for a, b in zip(_gather_all(torch, pkv, lay, dst, T, dev), (k, v, ik, pooled)))
+    row = T * (2 * HKV * D + DI) * 2 + (T // 4) * DI * 2   # bytes of one copy of the stream
+    b_save = 2 * row                                       # read through the table, written packed
+    b_restore = 2 * (T * (2 * HKV * D + DI) * 2) + (T * DI * 2 + (T // 4) * DI * 2)
+    peak, kind = peaks()
+    g_save = b_save / (t["save"] / 1e3) / 1e9
+    g_restore = b_restore / (t["restore"] / 1e3) / 1e9
+    return {"workload": "prompt-cache save/restore: 1 stream of 31,512 positions, pages of 256, "
+                        "one layer (K, V, indexer, pooled rows)",
+            "us": {k_: round(v_ * 1e3, 2) for k_, v_ in t.items()},
+            "GBps": {"save": round(g_save, 1), "restore": round(g_restore, 1)},
+            "frac": {"save": round(g_save / peak, 4), "restore": round(g_restore / peak, 4)},
+            "restored_equals_saved": bool(same)}
+
+
+def _gather_all(torch, pkv, lay, seqs, T, dev):
+    outs = [torch.empty((T, HKV, D), dtype=torch.int16, device=dev),
+            torch.empty((T, HKV, D), dtype=torch.int16, device=dev),
+            torch.empty((T, DI), dtype=torch.int16, device=dev),
+            torch.empty((T // 4, DI), dtype=torch.int16, device=dev)]
+    for kind, o in zip((pkv.K, pkv.V, pkv.IK, pkv.P), outs):
+        pkv.gather(lay, seqs, 0, kind, o)
+    return outs
+
+
 ROW_FNS = {"prefill": row_prefill, "sparse": row_sparse, "mix": row_mix,
-           "decode_layer": row_decode_layer}
+           "decode_layer": row_decode_layer, "prompt_cache": row_prompt_cache}
 
 
 def hot_path_rows(torch, pkv, dev, names, profile=False):
