@@ -5,7 +5,9 @@ CPU-baseline leg may import this package; the library and its binding never
 do.  It wraps ``pkv_oracle.c`` (plain single-threaded C, float64 attention)
 through ctypes and shares no code with the CUDA path.
 
-Caches are numpy ``uint16`` arrays of bf16 bit patterns.  A :class:`Cache`
+Caches are numpy ``uint16`` arrays (bf16 bit patterns; an e4m3-format
+cache keeps its K and V codes and float32 scales in the same buffer, read as
+bytes).  A :class:`Cache`
 says where one stream's rows live: page 0 of an arena plus an int page table,
 or a contiguous buffer of ``cap`` rows a head (``table=None``).
 
@@ -31,7 +33,8 @@ _LIB = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-K, V, IK, P = 0, 1, 2, 3
+K, V, IK, P, KS, VS = 0, 1, 2, 3, 4, 5
+BF16, E4M3 = 0, 1
 
 
 def build(force: bool = False) -> str:
@@ -49,7 +52,8 @@ def build(force: bool = False) -> str:
 
 class _Shape(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("idx_dim", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32)]
 
 
 class _Cache(ctypes.Structure):
@@ -81,6 +85,14 @@ def _load():
                 "orc_scores": (ctypes.c_int, [sh, ca, i32, i32, i32, vp, vp]),
                 "orc_topk": (ctypes.c_int, [i32, i32, vp, i32, i32, vp]),
                 "orc_sparse_attend": (ctypes.c_int, [sh, ca, i32, i32, i32, vp, vp, i32, vp]),
+                "orc_e4m3_to_double": (ctypes.c_double, [ctypes.c_uint8]),
+                "orc_e4m3_from_float": (ctypes.c_uint8, [ctypes.c_float]),
+                "orc_e4m3_decode_n": (None, [vp, i64, vp]),
+                "orc_e4m3_encode_n": (None, [vp, i64, vp]),
+                "orc_quantize_row": (None, [vp, i32, vp, vp]),
+                "orc_row8": (i64, [sh, ca, i32, i32, i32, i32]),
+                "orc_put_rows8": (ctypes.c_int, [sh, ca, i32, i32, i32, i32, vp]),
+                "orc_get_rows8": (ctypes.c_int, [sh, ca, i32, i32, i32, i32, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -95,9 +107,11 @@ class Shape:
     n_kv_heads: int
     head_dim: int = 256
     idx_dim: int = 128
+    kv_format: int = BF16
 
     def c(self) -> _Shape:
-        return _Shape(self.n_layers, self.n_kv_heads, self.head_dim, self.idx_dim)
+        return _Shape(self.n_layers, self.n_kv_heads, self.head_dim, self.idx_dim,
+                      self.kv_format)
 
 
 @dataclass
@@ -242,4 +256,55 @@ def sparse_attend(shape: Shape, cache: Cache, layer: int, n_q_heads: int, length
     _chk(_load().orc_sparse_attend(ctypes.byref(shape.c()), ctypes.byref(cache.c()),
                                    layer, n_q_heads, length, q.ctypes.data,
                                    ids.ctypes.data, k, out.ctypes.data), "sparse_attend")
+    return out
+
+
+# ---- e4m3 K/V (codes + float32 scale per head and row) ---------------------
+
+def e4m3_to_double(codes) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(c.shape, dtype=np.float64)
+    _load().orc_e4m3_decode_n(c.ctypes.data, c.size, out.ctypes.data)
+    return out
+
+
+def e4m3_from_float(x) -> np.ndarray:
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.zeros(f.shape, dtype=np.uint8)
+    _load().orc_e4m3_encode_n(f.ctypes.data, f.size, out.ctypes.data)
+    return out
+
+
+def quantize_row(row_bf16: np.ndarray):
+    """(codes uint8 [n], scale float32) of one bf16 row."""
+    r = np.ascontiguousarray(row_bf16, dtype=np.uint16)
+    codes = np.zeros(r.size, dtype=np.uint8)
+    sc = np.zeros(1, dtype=np.float32)
+    _load().orc_quantize_row(r.ctypes.data, r.size, codes.ctypes.data, sc.ctypes.data)
+    return codes, sc[0]
+
+
+def row8(shape: Shape, cache: Cache, layer: int, kind: int, head: int, pos: int) -> int:
+    """Byte offset of a row of an e4m3-format cache from its base (-1: outside)."""
+    return int(_load().orc_row8(ctypes.byref(shape.c()), ctypes.byref(cache.c()),
+                                layer, kind, head, pos))
+
+
+def put_rows8(shape: Shape, cache: Cache, layer: int, kind: int, pos0: int,
+              rows: np.ndarray) -> None:
+    """Quantize and store bf16 K or V rows [n][heads][head_dim] at pos0.."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint16)
+    n = rows.size // (shape.n_kv_heads * shape.head_dim)
+    _chk(_load().orc_put_rows8(ctypes.byref(shape.c()), ctypes.byref(cache.c()), layer,
+                               kind, pos0, n, rows.ctypes.data), "put_rows8")
+
+
+def get_rows8(shape: Shape, cache: Cache, layer: int, kind: int, pos0: int, n: int) -> np.ndarray:
+    """Codes (K, V: uint8 [n][heads][head_dim]) or scales (KS, VS: float32 [n][heads])."""
+    if kind in (KS, VS):
+        out = np.zeros((n, shape.n_kv_heads), dtype=np.float32)
+    else:
+        out = np.zeros((n, shape.n_kv_heads, shape.head_dim), dtype=np.uint8)
+    _chk(_load().orc_get_rows8(ctypes.byref(shape.c()), ctypes.byref(cache.c()), layer,
+                               kind, pos0, n, out.ctypes.data), "get_rows8")
     return out

@@ -30,12 +30,24 @@
  * the contiguous buffer is the same layout with a single page of ptok = cap.
  * ---------------------------------------------------------------------- */
 
+/* Bytes of one layer's block of a page of ptok positions, either format.
+ * e4m3 (#1170, commit 5c09685: a row's codes and fp32 scale, a layer's block
+ * at ptok rows).  Reading taken for the order inside the block: K codes
+ * [H][ptok][D], V codes [H][ptok][D], K scales [H][ptok], V scales [H][ptok],
+ * then the indexer and pooled rows in bf16 as in the bf16 format. */
+static int64_t layer_bytes(const orc_shape *s, int32_t ptok)
+{
+    int64_t h = s->n_kv_heads, d = s->head_dim;
+    int64_t ik = 2 * (int64_t)ptok * s->idx_dim;
+    int64_t pooled = 2 * (int64_t)(ptok / 4) * s->idx_dim;
+    if (s->kv_format == ORC_E4M3)
+        return 2 * h * ptok * d + 2 * 4 * h * ptok + ik + pooled;
+    return 2 * 2 * h * ptok * d + ik + pooled;
+}
+
 int64_t orc_layer_elems(const orc_shape *s, int32_t ptok)
 {
-    int64_t kv = 2 * (int64_t)s->n_kv_heads * ptok * s->head_dim;
-    int64_t ik = (int64_t)ptok * s->idx_dim;
-    int64_t pooled = (int64_t)(ptok / 4) * s->idx_dim;
-    return kv + ik + pooled;
+    return layer_bytes(s, ptok) / 2; /* 16-bit elements; every block is even */
 }
 
 int64_t orc_page_elems(const orc_shape *s, int32_t ptok)
@@ -82,6 +94,13 @@ int64_t orc_row(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t k
         return -1;
     if ((kind == ORC_IK || kind == ORC_P) && s->idx_dim == 0)
         return -1;
+    if (s->kv_format == ORC_E4M3) {
+        /* only the indexer and pooled rows of an e4m3 cache are bf16 elements */
+        if (kind != ORC_IK && kind != ORC_P)
+            return -1;
+        int64_t b = orc_row8(s, c, layer, kind, head, pos);
+        return b < 0 ? -1 : b / 2;
+    }
     int32_t position = (kind == ORC_P) ? 4 * pos : pos; /* first position of the block */
     int64_t layer_part = (int64_t)layer * orc_layer_elems(s, c->ptok);
     if (c->table == NULL) {
@@ -98,6 +117,59 @@ int64_t orc_row(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t k
         return -1;
     int32_t row = (kind == ORC_P) ? (position % c->ptok) / 4 : position % c->ptok;
     return (int64_t)id * c->ps + layer_part + in_page(s, c->ptok, kind, head, row);
+}
+
+/* Byte offset of a row inside its layer's block of an e4m3-format page. */
+static int64_t in_page8(const orc_shape *s, int32_t ptok, int32_t kind, int32_t head,
+                        int32_t row)
+{
+    int64_t d = s->head_dim, h = s->n_kv_heads;
+    int64_t codes = h * ptok * d;   /* bytes of one kind's codes, all heads */
+    int64_t scales = 4 * h * ptok;  /* bytes of one kind's scales */
+    switch (kind) {
+    case ORC_K:
+        return (int64_t)head * ptok * d + (int64_t)row * d;
+    case ORC_V:
+        return codes + (int64_t)head * ptok * d + (int64_t)row * d;
+    case ORC_KS:
+        return 2 * codes + 4 * ((int64_t)head * ptok + row);
+    case ORC_VS:
+        return 2 * codes + scales + 4 * ((int64_t)head * ptok + row);
+    case ORC_IK:
+        return 2 * codes + 2 * scales + 2 * (int64_t)row * s->idx_dim;
+    default: /* ORC_P: row is the block index inside the page */
+        return 2 * codes + 2 * scales + 2 * (int64_t)ptok * s->idx_dim +
+               2 * (int64_t)row * s->idx_dim;
+    }
+}
+
+int64_t orc_row8(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t kind,
+                 int32_t head, int32_t pos)
+{
+    if (s->kv_format != ORC_E4M3 || layer < 0 || layer >= s->n_layers || pos < 0 || c->ptok <= 0)
+        return -1;
+    if (kind < ORC_K || kind > ORC_VS)
+        return -1;
+    int kv = kind == ORC_K || kind == ORC_V || kind == ORC_KS || kind == ORC_VS;
+    if (kv && (head < 0 || head >= s->n_kv_heads))
+        return -1;
+    if (!kv && s->idx_dim == 0)
+        return -1;
+    int32_t position = (kind == ORC_P) ? 4 * pos : pos;
+    int64_t layer_part = (int64_t)layer * layer_bytes(s, c->ptok);
+    if (c->table == NULL) {
+        if (position >= c->ptok)
+            return -1;
+        return layer_part + in_page8(s, c->ptok, kind, head, pos);
+    }
+    int32_t page = position / c->ptok;
+    if (page >= c->n_table)
+        return -1;
+    int32_t id = c->table[page];
+    if (id < 0 || id >= c->n_pages)
+        return -1;
+    int32_t row = (kind == ORC_P) ? (position % c->ptok) / 4 : position % c->ptok;
+    return (int64_t)id * 2 * c->ps + layer_part + in_page8(s, c->ptok, kind, head, row);
 }
 
 /* Rows per position for a kind: K and V have a row per KV head. */
@@ -172,6 +244,145 @@ uint16_t orc_bf16_round(float x)
 }
 
 /* ------------------------------------------------------------------------
+ * e4m3 codes (#1170, commit 5c09685: a row's e4m3 codes and fp32 scale).
+ * The format: sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent
+ * 0 is subnormal (m * 2^-9); no infinities; S.1111.111 is NaN, so the
+ * largest magnitude is 1.75 * 2^8 = 448.  The pages do not say how a row's
+ * scale is chosen.  Reading taken: scale = max|x| / 448 in float32, each
+ * code the e4m3 value nearest x / scale (float32 division), ties to the even
+ * code, magnitudes from 448 up saturating to 448; an all-zero row has scale
+ * 0 and codes 0.
+ * ---------------------------------------------------------------------- */
+
+double orc_e4m3_to_double(uint8_t code)
+{
+    int e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (code & 0x80) ? -v : v;
+}
+
+uint8_t orc_e4m3_from_float(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x); /* exact */
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; rint rounds half to even */
+        int m = (int)rint(a * 512.0);
+        return sign | (uint8_t)m; /* m == 8 is the smallest normal, code 0x08 */
+    }
+    int ex;
+    frexp(a, &ex); /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1; /* a in [2^e, 2^(e+1)) */
+    int m = (int)rint((ldexp(a, -e) - 1.0) * 8.0); /* exact arguments */
+    if (m == 8) {
+        m = 0;
+        e += 1;
+    }
+    if (e + 7 > 15 || (e + 7 == 15 && m == 7))
+        return sign | 0x7E;
+    return sign | (uint8_t)((e + 7) << 3) | (uint8_t)m;
+}
+
+void orc_e4m3_decode_n(const uint8_t *codes, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = orc_e4m3_to_double(codes[i]);
+}
+
+void orc_e4m3_encode_n(const float *x, int64_t n, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; i++)
+        codes[i] = orc_e4m3_from_float(x[i]);
+}
+
+void orc_quantize_row(const uint16_t *bf16_row, int32_t n, uint8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int32_t i = 0; i < n; i++) {
+        float v = fabsf(bf16_to_float(bf16_row[i]));
+        if (v > amax)
+            amax = v;
+    }
+    float sc = amax / 448.0f;
+    for (int32_t i = 0; i < n; i++) {
+        float q = sc > 0.0f ? bf16_to_float(bf16_row[i]) / sc : 0.0f;
+        codes[i] = orc_e4m3_from_float(q);
+    }
+    *scale = sc;
+}
+
+int orc_put_rows8(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t kind,
+                  int32_t pos0, int32_t n, const uint16_t *rows)
+{
+    if (kind != ORC_K && kind != ORC_V)
+        return -1;
+    int32_t nh = s->n_kv_heads, d = s->head_dim;
+    uint8_t *bytes = (uint8_t *)c->base;
+    for (int32_t i = 0; i < n; i++)
+        for (int32_t h = 0; h < nh; h++) {
+            int64_t off = orc_row8(s, c, layer, kind, h, pos0 + i);
+            int64_t soff = orc_row8(s, c, layer, kind == ORC_K ? ORC_KS : ORC_VS, h, pos0 + i);
+            if (off < 0 || soff < 0)
+                return -1;
+            float sc;
+            orc_quantize_row(rows + ((int64_t)i * nh + h) * d, d, bytes + off, &sc);
+            memcpy(bytes + soff, &sc, 4);
+        }
+    return 0;
+}
+
+int orc_get_rows8(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t kind,
+                  int32_t pos0, int32_t n, void *out)
+{
+    int32_t nh = s->n_kv_heads, d = s->head_dim;
+    int scales = kind == ORC_KS || kind == ORC_VS;
+    if (!scales && kind != ORC_K && kind != ORC_V)
+        return -1;
+    size_t len = scales ? 4 : (size_t)d;
+    const uint8_t *bytes = (const uint8_t *)c->base;
+    for (int32_t i = 0; i < n; i++)
+        for (int32_t h = 0; h < nh; h++) {
+            int64_t off = orc_row8(s, c, layer, kind, h, pos0 + i);
+            if (off < 0)
+                return -1;
+            memcpy((uint8_t *)out + ((int64_t)i * nh + h) * len, bytes + off, len);
+        }
+    return 0;
+}
+
+/* One K or V row as float64: bf16 widened, or e4m3 code x scale (the
+ * dequantization the pages' fp8 reference runs in float64). */
+static int load_row(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t kind,
+                    int32_t head, int32_t pos, double *out)
+{
+    int32_t d_n = s->head_dim;
+    if (s->kv_format == ORC_E4M3) {
+        int64_t off = orc_row8(s, c, layer, kind, head, pos);
+        int64_t soff = orc_row8(s, c, layer, kind == ORC_K ? ORC_KS : ORC_VS, head, pos);
+        if (off < 0 || soff < 0)
+            return -1;
+        const uint8_t *bytes = (const uint8_t *)c->base;
+        float sc;
+        memcpy(&sc, bytes + soff, 4);
+        for (int32_t d = 0; d < d_n; d++)
+            out[d] = orc_e4m3_to_double(bytes[off + d]) * (double)sc;
+        return 0;
+    }
+    int64_t off = orc_row(s, c, layer, kind, head, pos);
+    if (off < 0)
+        return -1;
+    for (int32_t d = 0; d < d_n; d++)
+        out[d] = orc_bf16_to_double(c->base[off + d]);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
  * Pooling (#1169, What this changes: the pool kernel reads indexer keys once
  * per block of four and writes the pooled rows of the n/4 blocks of a page).
  * Readings taken: a pooled row is the mean of its block's four indexer keys,
@@ -230,15 +441,15 @@ static int attend_list(const orc_shape *s, const orc_cache *c, int32_t layer,
     for (int32_t d = 0; d < d_n; d++)
         qd[d] = orc_bf16_to_double(q_row[d]);
     double mx = -INFINITY;
+    double kv[1024];
     for (int32_t j = 0; j < n_keys; j++) {
-        int64_t off = orc_row(s, c, layer, ORC_K, kv_head, pos[j]);
-        if (off < 0) {
+        if (load_row(s, c, layer, ORC_K, kv_head, pos[j], kv) < 0) {
             free(logit);
             return -1;
         }
         double dot = 0.0;
         for (int32_t d = 0; d < d_n; d++)
-            dot += qd[d] * orc_bf16_to_double(c->base[off + d]);
+            dot += qd[d] * kv[d];
         logit[j] = dot * scale;
         if (logit[j] > mx)
             mx = logit[j];
@@ -247,13 +458,12 @@ static int attend_list(const orc_shape *s, const orc_cache *c, int32_t layer,
     for (int32_t j = 0; j < n_keys; j++) {
         double w = exp(logit[j] - mx);
         denom += w;
-        int64_t off = orc_row(s, c, layer, ORC_V, kv_head, pos[j]);
-        if (off < 0) {
+        if (load_row(s, c, layer, ORC_V, kv_head, pos[j], kv) < 0) {
             free(logit);
             return -1;
         }
         for (int32_t d = 0; d < d_n; d++)
-            out_row[d] += w * orc_bf16_to_double(c->base[off + d]);
+            out_row[d] += w * kv[d];
     }
     for (int32_t d = 0; d < d_n; d++)
         out_row[d] /= denom;

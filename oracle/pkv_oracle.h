@@ -18,6 +18,10 @@
  *       commit 3f5b87d: kv_row() with no table is "cap rows a head", with a
  *       table the page holding the position laid out as
  *       [layer][key,value][head][ptok][256].
+ *   #1170, commit 5c09685 ("--kv-cache fp8 through the page table too"):
+ *       a row's e4m3 codes and fp32 scale found through row8(), cap rows a
+ *       head or the row's page laid out as a layer's block at ptok rows; the
+ *       reference dequantizes e4m3 x scale in float64.
  * Where the pages leave the arithmetic open (softmax scale, head grouping,
  * pooling order, score order, top-k ties) the reading taken is stated at the
  * function that takes it.
@@ -37,7 +41,10 @@ typedef struct {
     int32_t n_kv_heads; /* key/value heads                                 */
     int32_t head_dim;   /* elements in a key or value row                  */
     int32_t idx_dim;    /* elements in an indexer-key or pooled row (0: none) */
+    int32_t kv_format;  /* ORC_BF16: bf16 K/V rows; ORC_E4M3: e4m3 codes + fp32 scale */
 } orc_shape;
+
+enum { ORC_BF16 = 0, ORC_E4M3 = 1 };
 
 /* Where one stream's caches live. */
 typedef struct {
@@ -50,7 +57,7 @@ typedef struct {
     int32_t pad_;
 } orc_cache;
 
-enum { ORC_K = 0, ORC_V = 1, ORC_IK = 2, ORC_P = 3 };
+enum { ORC_K = 0, ORC_V = 1, ORC_IK = 2, ORC_P = 3, ORC_KS = 4, ORC_VS = 5 };
 
 int64_t orc_layer_elems(const orc_shape *s, int32_t ptok);
 int64_t orc_page_elems(const orc_shape *s, int32_t ptok);
@@ -65,6 +72,30 @@ int orc_get_rows(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t 
 
 uint16_t orc_bf16_round(float x);
 double orc_bf16_to_double(uint16_t b);
+
+/* e4m3 (4 exponent bits, bias 7, 3 mantissa bits, no infinities, S.1111.111
+ * is NaN): exact value of a code, and the code nearest a float (ties to the
+ * even code, magnitudes from 448 up saturate to +-448). */
+double orc_e4m3_to_double(uint8_t code);
+uint8_t orc_e4m3_from_float(float x);
+void orc_e4m3_decode_n(const uint8_t *codes, int64_t n, double *out);
+void orc_e4m3_encode_n(const float *x, int64_t n, uint8_t *codes);
+/* One row's codes and scale: scale = max|x| / 448 and code_i = e4m3(x_i /
+ * scale), both in float32 (codes 0 for an all-zero row). */
+void orc_quantize_row(const uint16_t *bf16_row, int32_t n, uint8_t *codes, float *scale);
+
+/* Byte offset from c->base of a row of an e4m3-format cache: K and V codes
+ * (head_dim bytes), their scales (ORC_KS, ORC_VS: one float), the indexer
+ * and pooled rows (bf16).  -1 outside the cache. */
+int64_t orc_row8(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t kind,
+                 int32_t head, int32_t pos);
+/* Quantize and store n positions' K or V rows (bf16 [n][heads][head_dim]). */
+int orc_put_rows8(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t kind,
+                  int32_t pos0, int32_t n, const uint16_t *rows);
+/* Read back codes (ORC_K, ORC_V: [n][heads][head_dim] bytes) or scales
+ * (ORC_KS, ORC_VS: [n][heads] floats). */
+int orc_get_rows8(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t kind,
+                  int32_t pos0, int32_t n, void *out);
 
 int orc_pool(const orc_shape *s, const orc_cache *c, int32_t layer, int32_t block0,
              int32_t n_blocks);
