@@ -49,7 +49,7 @@ LENS = [1000, 3000, 6000, 9000]          # cached before the new token
 N_LAYERS, HQ, HKV, D, DI = 13, 16, 2, 256, 128
 PAGES = [16, 48, 128, 256, 512]
 NOMINAL_HBM = 8000.0
-ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache"]
+ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3"]
 # DRAM bytes (read + write) of one pkv_decode call of the workload (partial +
 # combine kernels), from the ncu capture summarised in
 # profiles/decode_partial_pages256.md, valid while the decode sources hash to
@@ -577,6 +577,53 @@ def row_prompt_cache(torch, pkv, dev, timer):
             "restored_equals_saved": bool(same)}
 
 
+def row_decode_e4m3(torch, pkv, dev, timer):
+    """The multi-stream decode with e4m3 K/V (codes + a float32 scale per head
+    and row): 13 layer slots at pages of 256, each a store of the new token
+    (quantized) and a decode call, replayed as one CUDA graph."""
+    lens_after = [L + 1 for L in LENS]
+    lay8 = pkv.layout(N_LAYERS, HKV, D, DI, pkv.KV_E4M3)
+    n_pages = sum(synth.pages_for(L, 256) for L in lens_after) + 8
+    mem, tables, pgs = _paged(torch, pkv, lay8, dev, 256, lens_after, n_pages, 8)
+    streams = [synth.make_stream(110 + i, N_LAYERS, L, HKV, D, DI) for i, L in enumerate(lens_after)]
+    for l in range(N_LAYERS):
+        pkv.store(lay8, [pkv.seq(g, L, L) for g, L in zip(pgs, LENS)], l,
+                  *(_up(torch, dev, np.concatenate([getattr(st, f)[l][:-1] for st in streams]))
+                    for f in ("k", "v", "ik")))
+    new = [[_up(torch, dev, np.concatenate([getattr(st, f)[l][-1:] for st in streams]))
+            for f in ("k", "v", "ik")] for l in range(N_LAYERS)]
+    del streams
+    sq = [pkv.seq(g, L, 1) for g, L in zip(pgs, lens_after)]
+    q = [_up(torch, dev, np.concatenate([synth.queries(120 + l * 4 + i, 1, HQ, D) for i in range(4)]))
+         for l in range(N_LAYERS)]
+    out = [torch.empty_like(x) for x in q]
+    ws = torch.zeros(pkv.decode_ws_size(lay8, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+
+    def step():
+        for l in range(N_LAYERS):
+            pkv.store(lay8, sq, l, *new[l])
+            pkv.decode(lay8, sq, l, HQ, q[l], out[l], ws)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    ms = timer.ms(g.replay, reps=30)
+    row8 = HKV * 2 * (D + 4)                            # K and V codes + scales of a position
+    b_layer = sum(lens_after) * row8 + len(LENS) * HQ * D * 2 * 2 + len(LENS) * (2 * HKV * D + DI) * 2 * 2
+    gbs = N_LAYERS * b_layer / (ms / 1e3) / 1e9
+    peak, kind = peaks()
+    bf16_bytes = N_LAYERS * layer_bytes(lens_after, 0)
+    return {"workload": "multi-stream decode, e4m3 K/V: 4 streams {1000, 3000, 6000, 9000} + 1 new "
+                        "token, 16/2 heads, 13 layer slots, pages of 256 (store + decode a layer)",
+            "us_13_layers": round(ms * 1e3, 2), "us_per_layer": round(ms * 1e3 / N_LAYERS, 2),
+            "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "bf16_equivalent_GBps": round(bf16_bytes / (ms / 1e3) / 1e9, 1),
+            "query_heads_per_s": round(N_LAYERS * len(LENS) * HQ / (ms / 1e3), 1)}
+
+
 def _gather_all(torch, pkv, lay, seqs, T, dev):
     outs = [torch.empty((T, HKV, D), dtype=torch.int16, device=dev),
             torch.empty((T, HKV, D), dtype=torch.int16, device=dev),
@@ -588,7 +635,8 @@ def _gather_all(torch, pkv, lay, seqs, T, dev):
 
 
 ROW_FNS = {"prefill": row_prefill, "sparse": row_sparse, "mix": row_mix,
-           "decode_layer": row_decode_layer, "prompt_cache": row_prompt_cache}
+           "decode_layer": row_decode_layer, "prompt_cache": row_prompt_cache,
+           "decode_e4m3": row_decode_e4m3}
 
 
 def hot_path_rows(torch, pkv, dev, names, profile=False):

@@ -64,6 +64,15 @@ extern "C" {
 #define PKV_V 1
 #define PKV_IK 2
 #define PKV_P 3 /* pooled rows: `pos` counts blocks of 4 positions */
+#define PKV_KS 4 /* e4m3 format only: the float32 scale of a K row */
+#define PKV_VS 5 /* e4m3 format only: the float32 scale of a V row */
+
+/* K/V formats (pkv_layout.kv_format) */
+#define PKV_KV_BF16 0
+#define PKV_KV_E4M3 1 /* #1170, commit 5c09685 ("--kv-cache fp8 through the page
+                         table too"): each K and V row (one head, one position)
+                         is head_dim e4m3 codes and one float32 scale, the row's
+                         value being code x scale */
 
 #define PKV_MAX_SEQS 64 /* streams in one launch */
 
@@ -73,7 +82,24 @@ typedef struct pkv_layout {
     int32_t n_kv_heads; /* key/value heads (>= 1)                              */
     int32_t head_dim;   /* elements in a key or value row (256)                */
     int32_t idx_dim;    /* elements in an indexer-key / pooled row (128, or 0) */
+    int32_t kv_format;  /* PKV_KV_BF16 (0) or PKV_KV_E4M3                         */
 } pkv_layout;
+
+/*
+ * The e4m3 format.  Inside a page, each layer's block holds K codes
+ * [H][n][D] bytes, V codes [H][n][D], K scales [H][n] float32, V scales
+ * [H][n], then the bf16 indexer [n][Di] and pooled [n/4][Di] rows.  Page and
+ * row sizes stay counted in 16-bit elements (page_elems, pkv_layout_page_
+ * elems), and pkv_pg_row gives BYTE offsets for every kind of an e4m3
+ * layout.  Quantization (the pages do not say how a scale is chosen; this is
+ * the plainest reading): scale = max|x| / 448 in float32; code = the e4m3
+ * value nearest x / scale (float32 division), ties to even, saturating at
+ * +-448; an all-zero row has scale 0 and codes 0.  Calls that take the
+ * format: the layout and arena calls, pkv_pg_row, pkv_store (quantizes),
+ * pkv_gather (codes, scales, indexer and pooled rows), pkv_pool,
+ * pkv_block_scores, pkv_topk, and pkv_decode / pkv_decode_static without a
+ * fused store.  pkv_prefill and pkv_sparse_decode answer PKV_EINVAL.
+ */
 
 /*
  * Pg: where one stream's caches live (#1169: "an int page table, the

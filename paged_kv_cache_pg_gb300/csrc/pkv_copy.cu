@@ -1,6 +1,8 @@
 // Cache store, gather and block pooling.  Rows are located with pg_at once
 // per row (store, gather) or once per block of four positions (pool: a page
 // holds whole blocks because its size is a multiple of 4), never per load.
+#include <cuda_fp8.h>
+
 #include "pkv_dev.cuh"
 
 namespace pkv {
@@ -96,8 +98,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
             const int ch = r % row_chunks;
             if (kind == PKV_K) src = off_k(sd.ptok, r / row_chunks, row);
             else if (kind == PKV_V) src = off_v(H, sd.ptok, r / row_chunks, row);
-            else if (kind == PKV_IK) src = off_ik(H, c.idx_dim, sd.ptok, row);
-            else src = off_p(H, c.idx_dim, sd.ptok, row / 4);
+            else if (kind == PKV_IK) src = off_ik_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row);
+            else src = off_p_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row / 4);
             val = *reinterpret_cast<const uint4 *>(sd.layer_base + page + src + ch * kChunk);
         }
         *reinterpret_cast<uint4 *>(out + (int64_t)orow * per_row * kChunk + (int64_t)r * kChunk) =
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const __grid_constant__ 
         const int64_t page = page_or_bad(sd, 4 * b, &row, c.status);  // one lookup a block
         if (page < 0) continue;
         uint16_t *lb = const_cast<uint16_t *>(sd.layer_base) + page;
-        const uint16_t *ik = lb + off_ik(H, c.idx_dim, sd.ptok, row) + ch * kChunk;
+        const uint16_t *ik = lb + off_ik_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row) + ch * kChunk;
         float sum[kChunk];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -141,8 +143,101 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const __grid_constant__ 
 #pragma unroll
         for (int e = 0; e < kChunk; e += 2)
             packed[e / 2] = pack_bf16(__fmul_rn(sum[e], 0.25f), __fmul_rn(sum[e + 1], 0.25f));
-        *reinterpret_cast<uint4 *>(lb + off_p(H, c.idx_dim, sd.ptok, row / 4) + ch * kChunk) =
+        *reinterpret_cast<uint4 *>(lb + off_p_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row / 4) + ch * kChunk) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+}
+
+// e4m3 store: one warp per new row.  K and V rows are quantized (scale =
+// max|x| / 448; code = e4m3 nearest x / scale, ties to even, saturating; the
+// divisions in float32 with IEEE rounding), indexer rows copied.  Items per
+// token: 2H quantized rows, then the indexer row.
+__global__ void __launch_bounds__(kThreads) store8_kernel(const __grid_constant__ Common c,
+                                                          int64_t total_items,
+                                                          const uint16_t *__restrict__ k_new,
+                                                          const uint16_t *__restrict__ v_new,
+                                                          const uint16_t *__restrict__ ik_new) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = c.n_kv_heads, lane = threadIdx.x & 31;
+    const int per_tok = 2 * H + (c.idx_dim ? 1 : 0);
+    const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
+    for (int64_t i = blockIdx.x * (int64_t)(kThreads / 32) + (threadIdx.x >> 5); i < total_items;
+         i += warps) {
+        const int32_t tok = static_cast<int32_t>(i / per_tok);
+        const int32_t r = static_cast<int32_t>(i % per_tok);
+        const int s = find_seq(c.n_seqs, tok, [&](int t) { return c.seq[t].tok_off; });
+        const SeqDev &sd = c.seq[s];
+        const int32_t pos = sd.len - sd.n_new + (tok - sd.tok_off);
+        int32_t row;
+        const int64_t page = page_or_bad(sd, pos, &row, c.status);
+        if (page < 0) continue;  // warp-uniform: one row a warp
+        uint8_t *lb = reinterpret_cast<uint8_t *>(const_cast<uint16_t *>(sd.layer_base)) + 2 * page;
+        if (r < 2 * H) {
+            const bool v = r >= H;
+            const int head = r % H;
+            const uint16_t *src = (v ? v_new : k_new) + ((int64_t)tok * H + head) * kHeadDim;
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src) + lane);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                x[e] = __uint_as_float((e & 1) ? (w[e / 2] & 0xffff0000u) : (w[e / 2] << 16));
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float scale = __fdiv_rn(amax, 448.f);
+            uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float q = scale > 0.f ? __fdiv_rn(x[e], scale) : 0.f;
+                const uint32_t code = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+                packed[e / 4] |= code << (8 * (e & 3));
+            }
+            *reinterpret_cast<uint2 *>(lb + off8_code(v, H, sd.ptok, head, row) + lane * 8) =
+                make_uint2(packed[0], packed[1]);
+            if (lane == 0)
+                *reinterpret_cast<float *>(lb + off8_scale(v, H, sd.ptok, head, row)) = scale;
+        } else if (lane < c.idx_dim / kChunk) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(ik_new + (int64_t)tok * c.idx_dim) + lane);
+            *reinterpret_cast<uint4 *>(lb + 2 * off_ik_f(true, H, c.idx_dim, sd.ptok, row) + 16 * lane) = u;
+        }
+    }
+}
+
+// e4m3 gather: codes (16 bytes a thread, [rows][H][256] out) or scales (a
+// float a thread, [rows][H] out) of positions 0 .. len-1 through the table.
+__global__ void __launch_bounds__(kThreads) gather8_kernel(const __grid_constant__ Common c,
+                                                           int32_t kind, int64_t total,
+                                                           uint8_t *__restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = c.n_kv_heads;
+    const bool codes = kind == PKV_K || kind == PKV_V;
+    const bool v = kind == PKV_V || kind == PKV_VS;
+    const int per_row = codes ? H * (kHeadDim / 16) : H;  // items of one position
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * kThreads) {
+        const int32_t orow = static_cast<int32_t>(i / per_row);
+        const int32_t r = static_cast<int32_t>(i % per_row);
+        const int s = find_seq(c.n_seqs, orow, [&](int t) { return c.seq[t].work_off; });
+        const SeqDev &sd = c.seq[s];
+        int32_t row;
+        const int64_t page = page_or_bad(sd, orow - sd.work_off, &row, c.status);
+        const uint8_t *lb = reinterpret_cast<const uint8_t *>(sd.layer_base) + 2 * page;
+        if (codes) {
+            const int head = r / (kHeadDim / 16), ch = r % (kHeadDim / 16);
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (page >= 0)
+                val = *reinterpret_cast<const uint4 *>(lb + off8_code(v, H, sd.ptok, head, row) + 16 * ch);
+            *reinterpret_cast<uint4 *>(out + i * 16) = val;
+        } else {
+            float val = 0.f;
+            if (page >= 0) val = *reinterpret_cast<const float *>(lb + off8_scale(v, H, sd.ptok, r, row));
+            reinterpret_cast<float *>(out)[i] = val;
+        }
     }
 }
 
@@ -168,6 +263,21 @@ int launch_gather(const Common &c, int32_t kind, int64_t total_rows, uint16_t *o
     const int64_t total = per_row * total_rows;
     return launch_status(
         launch_pdl(gather_kernel, grid_for(total), kThreads, 0, stream, c, kind, total, out));
+}
+
+int launch_store8(const Common &c, int32_t total_tokens, const uint16_t *k_new,
+                  const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream) {
+    const int64_t items = (int64_t)total_tokens * (2 * c.n_kv_heads + (c.idx_dim ? 1 : 0));
+    return launch_status(launch_pdl(store8_kernel, grid_for(items * 32), kThreads, 0, stream, c,
+                                    items, k_new, v_new, ik_new));
+}
+
+int launch_gather8(const Common &c, int32_t kind, int64_t total_rows, void *out,
+                   cudaStream_t stream) {
+    const bool codes = kind == PKV_K || kind == PKV_V;
+    const int64_t total = total_rows * c.n_kv_heads * (codes ? kHeadDim / 16 : 1);
+    return launch_status(launch_pdl(gather8_kernel, grid_for(total), kThreads, 0, stream, c, kind,
+                                    total, static_cast<uint8_t *>(out)));
 }
 
 int launch_pool(const Common &c, int32_t total_blocks, cudaStream_t stream) {

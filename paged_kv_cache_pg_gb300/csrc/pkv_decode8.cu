@@ -1,0 +1,432 @@
+// Decode attention over e4m3 K/V rows (#1170, commit 5c09685: a row's e4m3
+// codes and float32 scale through the page table; the reference dequantizes
+// code x scale).  Same work units, split plan and partial layout as the bf16
+// decode, so the same combine kernel merges the splits, paged output equals
+// contiguous output and a stream's output does not depend on its batch.
+//
+// A CTA is one (stream, KV head, split) unit of 8 warps.  The warps take the
+// split's 16-key tiles round robin (one key slice per warp and column group)
+// and each stages its own tiles, three deep: with codes at half the bytes of
+// bf16 rows, a split of 256 keys is in flight before the grid-dependency
+// wait.  A whole tile of a page whose size is a multiple of 16 is four 2D TMA
+// boxes (16 code rows x 128 bytes, 128-byte swizzle) and two bulk copies of
+// its 16 K and 16 V scales; a ragged tail is copied key by key, clamped into
+// the split, so every staged row is a real row (a masked key's code must not
+// be a NaN pattern).  Per tile a warp computes S^T = K Q^T and
+// O^T += V^T P^T with mma.sync in f16 (an e4m3 code widens to f16 exactly;
+// the queries are converted once), applies the K scale to S in float32,
+// and keeps an online softmax per query column.  The V scale is folded into
+// P relative to the largest V scale the warp has seen (R, rescaled like the
+// running max), so P' = P x scale_v / R stays in [0, 1] where f16 is
+// precise, and P' is split into f16 hi + lo parts; O is multiplied by R at
+// the end.  Dims are permuted inside the MMAs so
+// every operand fragment comes from contiguous 16-byte shared-memory loads:
+// in S thread group c (lane & 3) sums dims 64c .. 64c+63; in O^T row g of
+// M-tile m is dim 32g + 2m and row g+8 is dim 32g + 2m + 1.
+#include <cuda_fp16.h>
+
+#include "pkv_dev.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kT8 = 16;                              // keys a tile
+constexpr int kHalf8 = kT8 * 128;                    // 128-byte halves of 16 code rows (a TMA box)
+constexpr int kCodes8 = 2 * kHalf8;                  // one tile's K (or V) codes, swizzled
+constexpr int kTile8 = 2 * kCodes8;                  // K and V codes (a multiple of 1024 B)
+constexpr int kWarps8 = 8;
+constexpr int kThreads8 = kWarps8 * 32;
+constexpr int kDepth8 = 3;                           // tiles in flight a warp
+constexpr int kSlots8 = kWarps8 * kDepth8;
+constexpr size_t kOffScl8 = (size_t)kSlots8 * kTile8;          // 16 K then 16 V scales a slot
+constexpr size_t kOffBar8 = kOffScl8 + (size_t)kSlots8 * 128;  // a barrier a slot
+constexpr size_t kSmem8 = 1024 + kOffBar8 + kSlots8 * 8 + 16;
+constexpr int kMS8 = kHeadDim + 4;                   // merge row stride (floats)
+constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
+static_assert(64 * kMS8 * 4 + 64 * 4 * 4 + 64 * 4 <= kOffScl8, "merge buffers reuse the stages");
+
+// Byte offset of 16-byte chunk ch (0..15) of code row r (0..15) in a staged
+// tile: two 128-byte halves, each 16 rows with chunk j at j ^ (r & 7).
+__device__ __forceinline__ uint32_t sw8(int r, int ch) {
+    return (ch >> 3) * kHalf8 + r * 128 + ((((ch & 7) ^ (r & 7))) << 4);
+}
+
+struct Decode8Args {
+    const uint16_t *q;
+    uint16_t *out;
+    float *ws;
+};
+
+// Two e4m3 codes (low byte first) to an f16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(r)
+        : "r"(two));
+    return r;
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ float max_over_g(float v) {  // lanes sharing lane & 3
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+    return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+
+__device__ __forceinline__ float sum_over_g(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
+
+__global__ void __launch_bounds__(kThreads8, 1)
+    decode8_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
+                    const Decode8Args a) {
+    extern __shared__ uint8_t sm8_raw[];
+    uint8_t *sm8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm8_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm8 + kOffBar8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + kSlots8);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].work_off; });
+    const SeqDev &sd = c.seq[s];
+    const int r = blockIdx.x - sd.work_off;
+    const int kvh = r / sd.nsplit, split = r - kvh * sd.nsplit;
+    const int H = c.n_kv_heads, G = c.group;
+    const int key0 = split * sd.split_len, key1 = min(sd.len, key0 + sd.split_len);
+    const int ntiles = (key1 - key0 + kT8 - 1) / kT8;
+    const int ncols = sd.ncols, ncg = (ncols + 7) >> 3;
+    const int ks_n = kWarps8 / ncg;  // key slices
+    const int cg = warp % ncg, ks = warp / ncg;
+    const bool active = ks < ks_n;
+    const int qbase = sd.len - sd.n_new;
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(sd.layer_base);
+    const int my_tiles = (active && ks < ntiles) ? (ntiles - ks + ks_n - 1) / ks_n : 0;
+    const uint64_t pol = policy_evict_first();
+    const void *map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;
+
+    if (tid == 0) {
+        for (int i = 0; i < kSlots8; ++i) mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Stage tile t of this warp's slice into its slot: lane i (and i + 16)
+    // looks key i up once; 16 rows of K codes, 16 of V codes, 16 K and 16 V
+    // scales, all completing on the slot's barrier.
+    auto issue = [&](int t) {
+        const int kt = key0 + (ks + t * ks_n) * kT8;
+        const int slot = warp * kDepth8 + t % kDepth8;
+        uint8_t *st = sm8 + (size_t)slot * kTile8;
+        uint8_t *sc = sm8 + kOffScl8 + slot * 128;
+        uint64_t *bar = &bars[slot];
+        const int key = min(kt + (lane & 15), key1 - 1);
+        int64_t pg = 0;
+        int32_t row = key;
+        if (sd.table) {
+            const int page = key / sd.ptok;
+            row = key - page * sd.ptok;
+            const int id = __ldg(sd.table + page);
+            if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages))
+                pg = 2 * (int64_t)id * sd.ps;
+            else if (c.status && lane < 16)
+                atomicOr(c.status, PKV_DEV_BAD_PAGE);
+        }
+        const int64_t kc = pg + off8_code(false, H, sd.ptok, kvh, row);
+        const int64_t vc = pg + off8_code(true, H, sd.ptok, kvh, row);
+        if (map != nullptr && kt + kT8 <= key1) {
+            // one page holds the 16 keys (page size a multiple of 16, tiles
+            // start on 16): their code rows and scales are contiguous runs
+            const int yk = static_cast<int>(sd.layer_row + shfl64(kc, 0) / 256);
+            const int yv = static_cast<int>(sd.layer_row + shfl64(vc, 0) / 256);
+            const int64_t s0 = shfl64(pg, 0) + off8_scale(false, H, sd.ptok, kvh, __shfl_sync(0xffffffffu, row, 0));
+            const int64_t s1 = shfl64(pg, 0) + off8_scale(true, H, sd.ptok, kvh, __shfl_sync(0xffffffffu, row, 0));
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, kTile8 + 128);
+                tma_load_2d(st, map, 0, yk, bar, pol);
+                tma_load_2d(st + kHalf8, map, 128, yk, bar, pol);
+                tma_load_2d(st + kCodes8, map, 0, yv, bar, pol);
+                tma_load_2d(st + kCodes8 + kHalf8, map, 128, yv, bar, pol);
+                bulk_g2s(sc, base + s0, 64, bar, pol);
+                bulk_g2s(sc + 64, base + s1, 64, bar, pol);
+            }
+        } else {
+            // key rr's rows from lane rr's lookup, in the same swizzled layout
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int item = lane + 32 * i, rr = item >> 4, ch = item & 15;
+                cp_async16(st + sw8(rr, ch), base + shfl64(kc, rr) + 16 * ch, pol);
+                cp_async16(st + kCodes8 + sw8(rr, ch), base + shfl64(vc, rr) + 16 * ch, pol);
+            }
+            cp_async4(sc + 4 * lane, base + pg + off8_scale(lane >= 16, H, sd.ptok, kvh, row));
+            cp_async_mbar_arrive(bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+        }
+    };
+
+    // rows of cached positions stream before the grid-dependency wait; a tile
+    // holding a new position (stored by the previous kernel) waits for it
+    int issued = 0;
+    for (; issued < kDepth8 && issued < my_tiles; ++issued) {
+        const int kt = key0 + (ks + issued * ks_n) * kT8;
+        if (kt + kT8 > qbase) break;
+        issue(issued);
+    }
+    pdl_wait();
+    __syncthreads();
+    pdl_trigger();
+    for (; issued < kDepth8 && issued < my_tiles; ++issued) issue(issued);
+
+    // the queries of this thread's B-operand column, in the permuted dim order
+    uint32_t qf[16][2];
+    {
+        const int col = cg * 8 + g;
+        const uint16_t *qr = nullptr;
+        if (active && col < ncols) {
+            const int j = col / G;
+            qr = a.q + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            uint2 u = make_uint2(0u, 0u);
+            if (qr) u = __ldg(reinterpret_cast<const uint2 *>(qr + 64 * c4 + 4 * kk));
+            qf[kk][0] = h2_bits(__floats2half2_rn(bf16_lo(u.x), bf16_hi(u.x)));
+            qf[kk][1] = h2_bits(__floats2half2_rn(bf16_lo(u.y), bf16_hi(u.y)));
+        }
+    }
+    const int colA = cg * 8 + 2 * c4, colB = colA + 1;
+    const int limA = colA < ncols ? qbase + colA / G : -1;
+    const int limB = colB < ncols ? qbase + colB / G : -1;
+
+    float acc[16][4];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    float R = 0.f;  // the largest V scale of the tiles so far
+
+    for (int t = 0; t < my_tiles; ++t) {
+        const int slot = warp * kDepth8 + t % kDepth8;
+        // every lane waits (the barrier makes the async copies visible to it);
+        // a wait that runs out leaves the loop on every lane together
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[slot], (t / kDepth8) & 1, c.status))) {
+            *abort_flag = 1;
+            break;
+        }
+        const uint8_t *st = sm8 + (size_t)slot * kTile8;
+        const float *scl = reinterpret_cast<const float *>(sm8 + kOffScl8 + slot * 128);
+        const int kt = key0 + (ks + t * ks_n) * kT8;
+
+        // ---- S^T = K Q^T: rows keys g and g + 8, columns colA and colB ----
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(st + sw8(g, 4 * c4 + i));
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(st + sw8(g + 8, 4 * c4 + i));
+                const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_f16(sacc, e4m3x2_f16x2(x0[j] & 0xffffu), e4m3x2_f16x2(x1[j] & 0xffffu),
+                            e4m3x2_f16x2(x0[j] >> 16), e4m3x2_f16x2(x1[j] >> 16), qf[4 * i + j][0],
+                            qf[4 * i + j][1]);
+            }
+        }
+        // ---- K scale, causal and split bounds, online softmax ----
+        const int ka = kt + g, kb = kt + g + 8;
+        const float ska = scl[g] * kScaleLog2, skb = scl[g + 8] * kScaleLog2;
+        float x[4];
+        x[0] = (ka < key1 && ka <= limA) ? sacc[0] * ska : -INFINITY;
+        x[1] = (ka < key1 && ka <= limB) ? sacc[1] * ska : -INFINITY;
+        x[2] = (kb < key1 && kb <= limA) ? sacc[2] * skb : -INFINITY;
+        x[3] = (kb < key1 && kb <= limB) ? sacc[3] * skb : -INFINITY;
+        const float nA = fmaxf(mA, max_over_g(fmaxf(x[0], x[2])));
+        const float nB = fmaxf(mB, max_over_g(fmaxf(x[1], x[3])));
+        const float oA = nA == -INFINITY ? 0.f : nA, oB = nB == -INFINITY ? 0.f : nB;
+        const float alA = ex2(mA - oA), alB = ex2(mB - oB);  // 0 while nothing was accumulated
+        float p[4];
+        p[0] = ex2(x[0] - oA);
+        p[1] = ex2(x[1] - oB);
+        p[2] = ex2(x[2] - oA);
+        p[3] = ex2(x[3] - oB);
+        lA = lA * alA + sum_over_g(p[0] + p[2]);
+        lB = lB * alB + sum_over_g(p[1] + p[3]);
+        mA = nA;
+        mB = nB;
+        // the tile's largest V scale (lanes 0 .. 15 hold the 16 keys' scales)
+        float smax = lane < 16 ? scl[16 + lane] : 0.f;
+#pragma unroll
+        for (int o = 8; o; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        smax = __shfl_sync(0xffffffffu, smax, 0);
+        const float Rn = fmaxf(R, smax);
+        const float rho = Rn > 0.f ? R / Rn : 0.f;  // O was accumulated relative to R
+        R = Rn;
+        const float invR = R > 0.f ? 1.f / R : 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            acc[m][0] *= alA * rho;
+            acc[m][1] *= alB * rho;
+            acc[m][2] *= alA * rho;
+            acc[m][3] *= alB * rho;
+        }
+        // ---- P' = P x V scale / R, f16 hi + lo, to the B-operand layout ----
+        const float sva = scl[16 + g] * invR, svb = scl[16 + g + 8] * invR;
+        const float q0 = p[0] * sva, q1 = p[1] * sva, q2 = p[2] * svb, q3 = p[3] * svb;
+        const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+        const __half2 l01 = __floats2half2_rn(q0 - __low2float(h01), q1 - __high2float(h01));
+        const __half2 l23 = __floats2half2_rn(q2 - __low2float(h23), q3 - __high2float(h23));
+        const uint32_t b0h = movmatrix_t(h2_bits(h01)), b1h = movmatrix_t(h2_bits(h23));
+        const uint32_t b0l = movmatrix_t(h2_bits(l01)), b1l = movmatrix_t(h2_bits(l23));
+        // ---- O^T += V^T P'^T: V codes of keys 2c, 2c+1, 2c+8, 2c+9, dims 32g .. 32g+31 ----
+        uint32_t w[4][8];
+        {
+            const uint8_t *vb = st + kCodes8;
+            const int kr[4] = {2 * c4, 2 * c4 + 1, 2 * c4 + 8, 2 * c4 + 9};
+#pragma unroll
+            for (int x4 = 0; x4 < 4; ++x4) {
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(vb + sw8(kr[x4], 2 * g));
+                const uint4 u1 = *reinterpret_cast<const uint4 *>(vb + sw8(kr[x4], 2 * g + 1));
+                w[x4][0] = u0.x;
+                w[x4][1] = u0.y;
+                w[x4][2] = u0.z;
+                w[x4][3] = u0.w;
+                w[x4][4] = u1.x;
+                w[x4][5] = u1.y;
+                w[x4][6] = u1.z;
+                w[x4][7] = u1.w;
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int wi = m >> 1, b = 2 * (m & 1);
+            const uint32_t sel0 = b | ((4 + b) << 4), sel1 = (b + 1) | ((5 + b) << 4);
+            const uint32_t a0 = e4m3x2_f16x2(__byte_perm(w[0][wi], w[1][wi], sel0));
+            const uint32_t a1 = e4m3x2_f16x2(__byte_perm(w[0][wi], w[1][wi], sel1));
+            const uint32_t a2 = e4m3x2_f16x2(__byte_perm(w[2][wi], w[3][wi], sel0));
+            const uint32_t a3 = e4m3x2_f16x2(__byte_perm(w[2][wi], w[3][wi], sel1));
+            mma_f16(acc[m], a0, a1, a2, a3, b0h, b1h);
+            mma_f16(acc[m], a0, a1, a2, a3, b0l, b1l);
+        }
+        __syncwarp();  // every lane is done with the stage before it is refilled
+        if (issued < my_tiles) {
+            fence_proxy_async_smem();  // these reads come before the next copies' writes
+            issue(issued);
+            ++issued;
+        }
+    }
+
+    // ---- merge the key slices of each column group in a fixed order ----
+    __syncthreads();
+    const int NC = ncg * 8;
+    float *mbuf = reinterpret_cast<float *>(sm8);  // [ks][NC][kMS8]
+    float *mlb = mbuf + ks_n * NC * kMS8;          // [ks][NC][2]
+    float *wts = mlb + ks_n * NC * 2;              // [ks][NC]
+    float *lt = wts + ks_n * NC;                   // [NC]
+    float *mo = lt + NC;                           // [NC]
+    if (active) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int d0 = 32 * g + 2 * m;
+            mbuf[(ks * NC + colA) * kMS8 + d0] = acc[m][0] * R;
+            mbuf[(ks * NC + colB) * kMS8 + d0] = acc[m][1] * R;
+            mbuf[(ks * NC + colA) * kMS8 + d0 + 1] = acc[m][2] * R;
+            mbuf[(ks * NC + colB) * kMS8 + d0 + 1] = acc[m][3] * R;
+        }
+        if (g == 0) {
+            mlb[(ks * NC + colA) * 2 + 0] = mA;
+            mlb[(ks * NC + colA) * 2 + 1] = lA;
+            mlb[(ks * NC + colB) * 2 + 0] = mB;
+            mlb[(ks * NC + colB) * 2 + 1] = lB;
+        }
+    }
+    __syncthreads();
+    if (tid < NC) {
+        float M = -INFINITY;
+        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + tid) * 2]);
+        float L = 0.f;
+        for (int k = 0; k < ks_n; ++k) {
+            const float wk = M == -INFINITY ? 0.f : ex2(mlb[(k * NC + tid) * 2] - M);
+            wts[k * NC + tid] = wk;
+            L += wk * mlb[(k * NC + tid) * 2 + 1];
+        }
+        lt[tid] = L;
+        mo[tid] = M;
+    }
+    __syncthreads();
+    const bool single = sd.nsplit == 1;
+    float *part_acc = a.ws + sd.ws_off;
+    float *part_ml = part_acc + (int64_t)H * sd.nsplit * ncols * kHeadDim;
+    const int64_t pidx = ((int64_t)kvh * sd.nsplit + split) * ncols;
+    for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads8) {
+        const int col = idx / (kHeadDim / 4), d = 4 * (idx - col * (kHeadDim / 4));
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < ks_n; ++k) {
+            const float wk = wts[k * NC + col];
+            const float4 v = *reinterpret_cast<const float4 *>(mbuf + (k * NC + col) * kMS8 + d);
+            O.x += wk * v.x;
+            O.y += wk * v.y;
+            O.z += wk * v.z;
+            O.w += wk * v.w;
+        }
+        const float L = lt[col];
+        if (single) {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const int j = col / G;
+            uint2 pk;
+            pk.x = pack_bf16(O.x * inv, O.y * inv);
+            pk.y = pack_bf16(O.z * inv, O.w * inv);
+            *reinterpret_cast<uint2 *>(
+                a.out + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim + d) = pk;
+        } else {
+            *reinterpret_cast<float4 *>(part_acc + (pidx + col) * kHeadDim + d) = O;
+            if (d == 0) {
+                part_ml[(pidx + col) * 2 + 0] = mo[col];
+                part_ml[(pidx + col) * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int launch_decode8(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
+                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(decode8_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmem8)) != cudaSuccess ||
+            cudaFuncSetAttribute(decode8_partial, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return PKV_ECUDA;
+        attr_set = true;
+    }
+    Decode8Args a{q, out, ws};
+    cudaError_t e =
+        launch_pdl(decode8_partial, plan.total_items, kThreads8, kSmem8, stream, c, maps, a);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    if (plan.total_comb > 0) return launch_combine(c, plan, q, out, ws, stream);
+    return PKV_OK;
+}
+
+}  // namespace pkv

@@ -21,8 +21,11 @@ int validate_layout(const pkv_layout *L) {
     if (L->n_layers < 1 || L->n_kv_heads < 1 || L->n_kv_heads > 64) return PKV_EINVAL;
     if (L->head_dim != kHeadDim) return PKV_EINVAL;
     if (L->idx_dim != 0 && L->idx_dim != kIdxDim) return PKV_EINVAL;
+    if (L->kv_format != PKV_KV_BF16 && L->kv_format != PKV_KV_E4M3) return PKV_EINVAL;
     return PKV_OK;
 }
+
+static bool fp8_of(const pkv_layout *L) { return L->kv_format == PKV_KV_E4M3; }
 
 static bool page_pos_ok(int32_t page_pos) { return page_pos > 0 && page_pos % 4 == 0; }
 
@@ -45,7 +48,8 @@ int sm_count(int *out) {
 static int validate_pg(const pkv_layout *L, const pkv_pg &pg) {
     if (!pg.base || (reinterpret_cast<uintptr_t>(pg.base) & 15u)) return PKV_EINVAL;
     if (!page_pos_ok(pg.page_pos)) return PKV_EINVAL;
-    int64_t want = (int64_t)L->n_layers * layer_elems(L->n_kv_heads, L->idx_dim, pg.page_pos);
+    int64_t want =
+        (int64_t)L->n_layers * layer_elems_f(fp8_of(L), L->n_kv_heads, L->idx_dim, pg.page_pos);
     if (pg.page_elems != want) return PKV_EINVAL;
     if (pg.table) {
         if (pg.n_pages < 1 || pg.n_table < 1) return PKV_EINVAL;
@@ -71,6 +75,7 @@ int fill_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_
     c->layer = layer;
     c->n_q_heads = n_q_heads;
     c->group = n_q_heads / L->n_kv_heads;
+    c->kv_fp8 = fp8_of(L);
     c->status = reinterpret_cast<uint32_t *>(dev_status);
     int32_t tok = 0;
     for (int32_t s = 0; s < n_seqs; ++s) {
@@ -81,8 +86,8 @@ int fill_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_
             return PKV_EINVAL;
         SeqDev &d = c->seq[s];
         const uint16_t *base = static_cast<const uint16_t *>(q.pg.base);
-        d.layer_base = base + (int64_t)layer * layer_elems(L->n_kv_heads, L->idx_dim,
-                                                           q.pg.page_pos);
+        d.layer_base = base + (int64_t)layer * layer_elems_f(fp8_of(L), L->n_kv_heads,
+                                                             L->idx_dim, q.pg.page_pos);
         d.table = q.pg.table;
         d.ps = q.pg.page_elems;
         d.ptok = q.pg.page_pos;
@@ -120,19 +125,21 @@ namespace {
 struct MapKey {
     uintptr_t base;
     uint64_t rows;
+    bool bytes8;
 };
 std::mutex g_map_mu;
 std::vector<std::pair<MapKey, RowMap>> g_maps;  // encoded maps, most recent last
 }  // namespace
 
-int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows) {
+int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool bytes8) {
     if (rows == 0 || rows > (1ull << 31) || !aligned16(base)) return -1;
     RowMap m;
     bool have = false;
     {
         std::lock_guard<std::mutex> g(g_map_mu);
         for (auto &e : g_maps)
-            if (e.first.base == reinterpret_cast<uintptr_t>(base) && e.first.rows == rows) {
+            if (e.first.base == reinterpret_cast<uintptr_t>(base) && e.first.rows == rows &&
+                e.first.bytes8 == bytes8) {
                 m = e.second;
                 have = true;
                 break;
@@ -141,18 +148,21 @@ int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows) {
     if (!have) {
         auto fn = encode_fn();
         if (!fn) return -1;
+        // bf16 rows: 256 elements (512 B), boxes of 64 x 16; e4m3 code rows:
+        // 256 bytes, boxes of 128 x 16 (both 128-byte inner boxes)
         cuuint64_t dims[2] = {256, rows};
-        cuuint64_t strides[1] = {512};
-        cuuint32_t box[2] = {64, 16};
+        cuuint64_t strides[1] = {bytes8 ? 256u : 512u};
+        cuuint32_t box[2] = {bytes8 ? 128u : 64u, 16};
         cuuint32_t estr[2] = {1, 1};
-        CUresult r = fn(reinterpret_cast<CUtensorMap *>(m.bytes), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+        CUresult r = fn(reinterpret_cast<CUtensorMap *>(m.bytes),
+                        bytes8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                         const_cast<void *>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return -1;
         std::lock_guard<std::mutex> g(g_map_mu);
         if (g_maps.size() >= 256) g_maps.erase(g_maps.begin());
-        g_maps.push_back({{reinterpret_cast<uintptr_t>(base), rows}, m});
+        g_maps.push_back({{reinterpret_cast<uintptr_t>(base), rows, bytes8}, m});
     }
     for (int i = 0; i < n_maps; ++i)
         if (std::memcmp(maps.map[i].bytes, m.bytes, sizeof(m.bytes)) == 0) return i;
@@ -168,10 +178,21 @@ void plan_maps(Common &c, const pkv_layout *L, const pkv_seq *seqs, DecodeMaps &
         d.tma = -1;
         const pkv_pg &pg = seqs[s].pg;
         const int64_t layer_off =
-            (int64_t)c.layer * layer_elems(L->n_kv_heads, L->idx_dim, pg.page_pos);
+            (int64_t)c.layer * layer_elems_f(fp8_of(L), L->n_kv_heads, L->idx_dim, pg.page_pos);
+        if (fp8_of(L)) {
+            // e4m3 code rows of 256 bytes: whole 16-row runs by TMA when every
+            // page and this layer's block start on a 256-byte row
+            const int64_t page_bytes = 2 * pg.page_elems, layer_bytes = 2 * layer_off;
+            if (pg.page_pos % 16 != 0 || page_bytes % 256 != 0 || layer_bytes % 256 != 0) continue;
+            const uint64_t rows = (uint64_t)(pg.table ? pg.n_pages : 1) * page_bytes / 256;
+            d.tma = row_map(maps, n_maps, pg.base, rows, true);
+            d.layer_row = layer_bytes / 256;
+            d.page_rows = page_bytes / 256;
+            continue;
+        }
         if (pg.page_pos % 16 != 0 || pg.page_elems % 256 != 0 || layer_off % 256 != 0) continue;
         const uint64_t rows = (uint64_t)(pg.table ? pg.n_pages : 1) * pg.page_elems / 256;
-        d.tma = row_map(maps, n_maps, pg.base, rows);
+        d.tma = row_map(maps, n_maps, pg.base, rows, false);
         d.layer_row = layer_off / 256;
         d.page_rows = pg.page_elems / 256;
     }
@@ -193,7 +214,8 @@ using namespace pkv;
 
 extern "C" int pkv_layout_page_elems(const pkv_layout *layout, int32_t page_pos, int64_t *out) {
     if (validate_layout(layout) || !page_pos_ok(page_pos) || !out) return PKV_EINVAL;
-    *out = (int64_t)layout->n_layers * layer_elems(layout->n_kv_heads, layout->idx_dim, page_pos);
+    *out = (int64_t)layout->n_layers *
+           layer_elems_f(fp8_of(layout), layout->n_kv_heads, layout->idx_dim, page_pos);
     return PKV_OK;
 }
 
@@ -201,9 +223,10 @@ extern "C" int pkv_pg_row(const pkv_layout *L, const pkv_pg *pg, const int32_t *
                           int32_t layer, int32_t kind, int32_t head, int32_t pos, int64_t *out) {
     if (validate_layout(L) || !pg || !out || validate_pg(L, *pg)) return PKV_EINVAL;
     if (layer < 0 || layer >= L->n_layers || pos < 0) return PKV_EINVAL;
-    if (kind < PKV_K || kind > PKV_P) return PKV_EINVAL;
-    if ((kind == PKV_K || kind == PKV_V) && (head < 0 || head >= L->n_kv_heads))
-        return PKV_EINVAL;
+    const bool fp8 = fp8_of(L);
+    if (kind < PKV_K || kind > (fp8 ? PKV_VS : PKV_P)) return PKV_EINVAL;
+    const bool per_head = kind == PKV_K || kind == PKV_V || kind == PKV_KS || kind == PKV_VS;
+    if (per_head && (head < 0 || head >= L->n_kv_heads)) return PKV_EINVAL;
     if ((kind == PKV_IK || kind == PKV_P) && L->idx_dim == 0) return PKV_EINVAL;
     if (pg->table && !host_table) return PKV_EINVAL;
     const int32_t ptok = pg->page_pos;
@@ -220,6 +243,19 @@ extern "C" int pkv_pg_row(const pkv_layout *L, const pkv_pg *pg, const int32_t *
     }
     int64_t in_layer;
     const int32_t H = L->n_kv_heads;
+    if (fp8) {
+        // byte offsets for every kind of an e4m3 layout
+        switch (kind) {
+        case PKV_K: in_layer = off8_code(false, H, ptok, head, row); break;
+        case PKV_V: in_layer = off8_code(true, H, ptok, head, row); break;
+        case PKV_KS: in_layer = off8_scale(false, H, ptok, head, row); break;
+        case PKV_VS: in_layer = off8_scale(true, H, ptok, head, row); break;
+        case PKV_IK: in_layer = 2 * off_ik_f(true, H, L->idx_dim, ptok, row); break;
+        default: in_layer = 2 * off_p_f(true, H, L->idx_dim, ptok, row / 4); break;
+        }
+        *out = 2 * page_off + 2 * (int64_t)layer * layer_elems_f(true, H, L->idx_dim, ptok) + in_layer;
+        return PKV_OK;
+    }
     switch (kind) {
     case PKV_K: in_layer = off_k(ptok, head, row); break;
     case PKV_V: in_layer = off_v(H, ptok, head, row); break;
@@ -313,7 +349,7 @@ extern "C" int pkv_arena_create(const pkv_layout *layout, int32_t page_pos, void
     if (validate_layout(layout) || !page_pos_ok(page_pos) || !dev_base) return PKV_EINVAL;
     if (reinterpret_cast<uintptr_t>(dev_base) & 15u) return PKV_EINVAL;
     int64_t ps = (int64_t)layout->n_layers *
-                 layer_elems(layout->n_kv_heads, layout->idx_dim, page_pos);
+                 layer_elems_f(fp8_of(layout), layout->n_kv_heads, layout->idx_dim, page_pos);
     int64_t n = static_cast<int64_t>(bytes / 2) / ps;
     if (n < 1 || n > INT32_MAX) return PKV_EINVAL;
     pkv_arena *a = new (std::nothrow) pkv_arena;
@@ -429,9 +465,9 @@ extern "C" int pkv_store(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seq
     if (!k_new || !v_new || (L->idx_dim && !ik_new)) return PKV_EINVAL;
     if (!aligned16(k_new) || !aligned16(v_new) || (L->idx_dim && !aligned16(ik_new)))
         return PKV_EINVAL;
-    return launch_store(c, tok, static_cast<const uint16_t *>(k_new),
-                        static_cast<const uint16_t *>(v_new),
-                        static_cast<const uint16_t *>(ik_new), stream);
+    auto launch = c.kv_fp8 ? launch_store8 : launch_store;
+    return launch(c, tok, static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+                  static_cast<const uint16_t *>(ik_new), stream);
 }
 
 extern "C" int pkv_gather(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
@@ -439,7 +475,7 @@ extern "C" int pkv_gather(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
     Common c;
     int rc = fill_common(L, seqs, n_seqs, layer, L ? L->n_kv_heads : 1, dev_status, &c);
     if (rc) return rc;
-    if (kind < PKV_K || kind > PKV_P) return PKV_EINVAL;
+    if (kind < PKV_K || kind > (c.kv_fp8 ? PKV_VS : PKV_P)) return PKV_EINVAL;
     if ((kind == PKV_IK || kind == PKV_P) && L->idx_dim == 0) return PKV_EINVAL;
     int64_t rows = 0;
     for (int s = 0; s < c.n_seqs; ++s) {
@@ -448,6 +484,8 @@ extern "C" int pkv_gather(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
     }
     if (rows == 0) return PKV_OK;
     if (!out || !aligned16(out) || rows > INT32_MAX / 2) return PKV_EINVAL;
+    if (c.kv_fp8 && kind != PKV_IK && kind != PKV_P)  // codes or scales
+        return launch_gather8(c, kind, rows, out, stream);
     return launch_gather(c, kind, rows, static_cast<uint16_t *>(out), stream);
 }
 
@@ -517,6 +555,11 @@ extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
         return PKV_EINVAL;
     DecodeMaps maps;  // copied into the launch's parameters
     plan_maps(c, L, seqs, maps);
+    if (c.kv_fp8) {
+        if (k_new) return PKV_EINVAL;  // the e4m3 decode reads rows already stored
+        return launch_decode8(c, plan, maps, static_cast<const uint16_t *>(q),
+                              static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
+    }
     return launch_decode(c, plan, maps, false, static_cast<const uint16_t *>(q), nullptr, 0,
                          static_cast<uint16_t *>(out), static_cast<float *>(ws),
                          static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
@@ -544,6 +587,11 @@ extern "C" int pkv_decode_static(const pkv_layout *L, const pkv_seq *seqs, int32
     if (rc) return rc;
     DecodeMaps maps;
     plan_maps(c, L, seqs, maps);
+    if (c.kv_fp8) {
+        if (k_new) return PKV_EINVAL;
+        return launch_decode8(c, plan, maps, static_cast<const uint16_t *>(q),
+                              static_cast<uint16_t *>(out), static_cast<float *>(scratch), stream);
+    }
     return launch_decode(c, plan, maps, false, static_cast<const uint16_t *>(q), nullptr, 0,
                          static_cast<uint16_t *>(out), static_cast<float *>(scratch),
                          static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
@@ -569,6 +617,7 @@ extern "C" int pkv_sparse_decode(const pkv_layout *L, const pkv_seq *seqs, int32
     DecodePlan plan;
     int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, true, k, dev_status, &c, &plan);
     if (rc) return rc;
+    if (c.kv_fp8) return PKV_EINVAL;
     if (plan.total_items == 0) return PKV_OK;
     if (!q || !out || !ids || !aligned16(q) || !aligned16(out)) return PKV_EINVAL;
     if (plan.ws_bytes > 0 &&
@@ -585,6 +634,7 @@ static int prefill_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
                           int32_t n_q_heads, int32_t *dev_status, Common *c, DecodePlan *plan) {
     int rc = fill_common(L, seqs, n_seqs, layer, n_q_heads, dev_status, c);
     if (rc) return rc;
+    if (c->kv_fp8) return PKV_EINVAL;  // the tensor-core prefill reads bf16 rows
     int nsm = 0;
     rc = sm_count(&nsm);
     if (rc) return rc;

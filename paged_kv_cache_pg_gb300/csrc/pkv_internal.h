@@ -53,7 +53,9 @@ struct DecodeMaps {
 };
 // Index of the map for [base, base + rows*512 B) in `maps` (added if new),
 // or -1 when none can be made (no driver entry point, or maps full).
-int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows);
+// bytes8: rows of 256 bytes (e4m3 codes, boxes of 128 x 16) instead of 256
+// bf16 elements (boxes of 64 x 16).
+int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool bytes8);
 
 struct Common {
     int32_t n_seqs;
@@ -62,6 +64,7 @@ struct Common {
     int32_t layer;
     int32_t n_q_heads;
     int32_t group;  // n_q_heads / n_kv_heads
+    int32_t kv_fp8; // K/V rows are e4m3 codes + float32 scales (PKV_KV_E4M3)
     uint32_t *status;
     SeqDev seq[PKV_MAX_SEQS];
 };
@@ -87,6 +90,38 @@ __host__ __device__ inline int64_t layer_elems(int32_t h_kv, int32_t idx_dim, in
            (int64_t)(ptok / 4) * idx_dim;
 }
 
+// Either K/V format (#1170, commit 5c09685: a row's e4m3 codes and float32
+// scale, a layer's block at ptok rows).  The e4m3 block holds K codes
+// [H][ptok][256] bytes, V codes, K scales [H][ptok] float32, V scales, then
+// the bf16 indexer and pooled rows as in the bf16 format.  Offsets of the
+// bf16 rows are in 16-bit units, of codes and scales in bytes.
+__host__ __device__ inline int64_t kv_part(bool fp8, int32_t h_kv, int32_t ptok) {
+    return fp8 ? (int64_t)h_kv * ptok * kHeadDim + 4 * (int64_t)h_kv * ptok
+               : 2 * (int64_t)h_kv * ptok * kHeadDim;
+}
+__host__ __device__ inline int64_t off_ik_f(bool fp8, int32_t h_kv, int32_t idx_dim, int32_t ptok,
+                                            int32_t row) {
+    return kv_part(fp8, h_kv, ptok) + (int64_t)row * idx_dim;
+}
+__host__ __device__ inline int64_t off_p_f(bool fp8, int32_t h_kv, int32_t idx_dim, int32_t ptok,
+                                           int32_t block_row) {
+    return kv_part(fp8, h_kv, ptok) + (int64_t)ptok * idx_dim + (int64_t)block_row * idx_dim;
+}
+__host__ __device__ inline int64_t layer_elems_f(bool fp8, int32_t h_kv, int32_t idx_dim,
+                                                 int32_t ptok) {
+    return kv_part(fp8, h_kv, ptok) + (int64_t)ptok * idx_dim + (int64_t)(ptok / 4) * idx_dim;
+}
+// byte offsets of an e4m3 code row and of its scale inside a layer block
+__host__ __device__ inline int64_t off8_code(bool v, int32_t h_kv, int32_t ptok, int32_t head,
+                                             int32_t row) {
+    return (v ? (int64_t)h_kv * ptok * kHeadDim : 0) + ((int64_t)head * ptok + row) * kHeadDim;
+}
+__host__ __device__ inline int64_t off8_scale(bool v, int32_t h_kv, int32_t ptok, int32_t head,
+                                              int32_t row) {
+    return 2 * (int64_t)h_kv * ptok * kHeadDim + (v ? 4 * (int64_t)h_kv * ptok : 0) +
+           4 * ((int64_t)head * ptok + row);
+}
+
 // Host helpers (pkv_host.cu).
 int validate_layout(const pkv_layout *layout);
 int fill_common(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
@@ -97,6 +132,13 @@ int launch_status(cudaError_t e);
 // Kernel launchers (one per kernel file); all return PKV_OK or PKV_ECUDA.
 int launch_store(const Common &c, int32_t total_tokens, const uint16_t *k_new,
                  const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream);
+// e4m3 format: quantize the new K and V rows, copy the indexer rows
+int launch_store8(const Common &c, int32_t total_tokens, const uint16_t *k_new,
+                  const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream);
+// e4m3 format: codes (PKV_K, PKV_V: 256 bytes a head and row) or scales
+// (PKV_KS, PKV_VS: a float32 a head and row) of positions 0 .. len-1
+int launch_gather8(const Common &c, int32_t kind, int64_t total_rows, void *out,
+                   cudaStream_t stream);
 int launch_gather(const Common &c, int32_t kind, int64_t total_rows, uint16_t *out,
                   cudaStream_t stream);
 int launch_pool(const Common &c, int32_t total_blocks, cudaStream_t stream);
@@ -121,6 +163,10 @@ int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
                    const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream);
 int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, uint16_t *out,
                    float *ws, cudaStream_t stream);
+// Decode over e4m3 K/V (pkv_decode8.cu): the same plan and partial layout as
+// the bf16 decode, merged by the same combine kernel.
+int launch_decode8(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
+                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream);
 
 // Fixed scratch of pkv_decode_static (pkv_decode.cu): its size, and its
 // device address on the current device (looked up on the first call there).

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kScoreThreads)
             int32_t row;
             const int64_t page = page_start(sd, 4 * b, &row, c.status);
             const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                sd.layer_base + page + off_p(H, Di, sd.ptok, row / 4) + 2 * d2);
+                sd.layer_base + page + off_p_f(c.kv_fp8, H, Di, sd.ptok, row / 4) + 2 * d2);
             lo = __uint_as_float(w << 16);
             hi = __uint_as_float(w & 0xffff0000u);
         }

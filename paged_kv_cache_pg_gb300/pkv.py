@@ -14,7 +14,8 @@ from typing import Optional, Sequence
 
 from . import build as _build
 
-K, V, IK, P = 0, 1, 2, 3
+K, V, IK, P, KS, VS = 0, 1, 2, 3, 4, 5
+KV_BF16, KV_E4M3 = 0, 1
 OK, EINVAL, EAGAIN, ECUDA, EDEVICE = 0, 1, 2, 3, 4
 DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2
 MAX_SEQS = 64
@@ -29,7 +30,8 @@ class PkvError(RuntimeError):
 
 class Layout(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("idx_dim", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32)]
 
 
 class Pg(ctypes.Structure):
@@ -139,8 +141,10 @@ def _seqs(seqs: Sequence[Seq]):
 
 # ---- descriptors ------------------------------------------------------------
 
-def layout(n_layers: int, n_kv_heads: int, head_dim: int = 256, idx_dim: int = 128) -> Layout:
-    return Layout(n_layers, n_kv_heads, head_dim, idx_dim)
+def layout(n_layers: int, n_kv_heads: int, head_dim: int = 256, idx_dim: int = 128,
+           kv_format: int = KV_BF16) -> Layout:
+    """kv_format KV_E4M3: K and V rows are e4m3 codes + a float32 scale each."""
+    return Layout(n_layers, n_kv_heads, head_dim, idx_dim, kv_format)
 
 
 def page_elems(lay: Layout, page_pos: int) -> int:

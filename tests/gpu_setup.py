@@ -106,7 +106,7 @@ def place(lay: pkv.Layout, streams: List[synth.Stream], ptok: Optional[int], see
           spare_pages: int = 3, tables: Optional[list] = None, status=None) -> Placed:
     """Store every position of every stream, on the GPU and in the oracle."""
     t = torch()
-    shape = orc.Shape(lay.n_layers, lay.n_kv_heads, lay.head_dim, lay.idx_dim)
+    shape = orc.Shape(lay.n_layers, lay.n_kv_heads, lay.head_dim, lay.idx_dim, lay.kv_format)
     pl = Placed(lay, shape, streams, ptok)
     if ptok is None:
         for s in streams:
@@ -144,10 +144,11 @@ def place(lay: pkv.Layout, streams: List[synth.Stream], ptok: Optional[int], see
         ik = dev_u16(np.concatenate([s.ik[layer] for s in streams])) if lay.idx_dim else None
         pkv.store(lay, seqs, layer, k, v, ik, status=status)
     # oracle: the same rows through its own translation
+    put_kv = orc.put_rows8 if lay.kv_format == pkv.KV_E4M3 else orc.put_rows
     for oc, s in zip(pl.ocaches, streams):
         for layer in range(lay.n_layers):
-            orc.put_rows(shape, oc, layer, orc.K, 0, s.k[layer])
-            orc.put_rows(shape, oc, layer, orc.V, 0, s.v[layer])
+            put_kv(shape, oc, layer, orc.K, 0, s.k[layer])
+            put_kv(shape, oc, layer, orc.V, 0, s.v[layer])
             if lay.idx_dim:
                 orc.put_rows(shape, oc, layer, orc.IK, 0, s.ik[layer])
     t.cuda.synchronize()

@@ -250,3 +250,45 @@ def test_arena_pg_describes_the_pool(arena):
     n, _, ps = arena.info()
     assert (g.base, g.table, g.page_elems, g.page_pos, g.n_pages, g.n_table) == \
         (0x100000, 0x5000, ps, 16, n, 3)
+
+
+# ---- e4m3 K/V format (#1170, commit 5c09685) -------------------------------
+
+def test_e4m3_page_elems_match_oracle(lib, orc):
+    for hkv, di, ptok in [(2, 128, 256), (4, 0, 256), (1, 128, 16), (2, 128, 4)]:
+        lay = pkv.layout(13, hkv, 256, di, pkv.KV_E4M3)
+        assert pkv.page_elems(lay, ptok) == \
+            orc.page_elems(orc.Shape(13, hkv, 256, di, orc.E4M3), ptok)
+
+
+@pytest.mark.parametrize("ptok", [4, 16, 48, 256])
+def test_host_pg_at_gives_e4m3_byte_offsets_of_the_oracle(lib, orc, ptok):
+    lay = pkv.layout(3, 2, 256, 128, pkv.KV_E4M3)
+    shape = orc.Shape(3, 2, 256, 128, orc.E4M3)
+    ps = pkv.page_elems(lay, ptok)
+    n_pages = 40
+    table = synth.shuffled_tables(ptok + 1, n_pages, [7])[0]
+    oc = orc.Cache(np.zeros(1, np.uint16), ptok, ps, table, n_pages)
+    g = pkv.pg(0x10000, 0x20000, ps, ptok, n_pages, table.size)
+    rng = np.random.default_rng(ptok + 1)
+    for _ in range(400):
+        layer = int(rng.integers(3)); kind = int(rng.integers(6)); head = int(rng.integers(2))
+        if kind in (pkv.IK, pkv.P):
+            head = 0
+        pos = int(rng.integers(7 * ptok // 4 if kind == pkv.P else 7 * ptok))
+        assert pkv.pg_row(lay, g, table, layer, kind, head, pos) == \
+            orc.row8(shape, oc, layer, kind, head, pos)
+
+
+def test_e4m3_refusals_before_launch(lib):
+    lay8 = pkv.layout(1, 2, 256, 128, pkv.KV_E4M3)
+    with pytest.raises(pkv.PkvError) as e:     # the tensor-core prefill reads bf16 rows
+        pkv.prefill_ws_size(lay8, [_seq(lay8, length=64, n_new=8)], 16)
+    assert e.value.code == pkv.EINVAL
+    with pytest.raises(pkv.PkvError) as e:     # scales exist only in the e4m3 format
+        pkv.pg_row(pkv.layout(1, 2), pkv.pg(0x10000, None, pkv.page_elems(pkv.layout(1, 2), 16), 16),
+                   None, 0, pkv.KS, 0, 0)
+    assert e.value.code == pkv.EINVAL
+    with pytest.raises(pkv.PkvError) as e:     # an unknown format
+        pkv.page_elems(pkv.layout(1, 2, 256, 128, 2), 16)
+    assert e.value.code == pkv.EINVAL
