@@ -41,7 +41,9 @@ constexpr int kSlots8 = kWarps8 * kDepth8;
 constexpr size_t kOffScl8 = (size_t)kSlots8 * kTile8;          // 16 K then 16 V scales a slot
 constexpr size_t kOffBar8 = kOffScl8 + (size_t)kSlots8 * 128;  // a barrier a slot
 constexpr size_t kSmem8 = 1024 + kOffBar8 + kSlots8 * 8 + 16;
-constexpr int kMS8 = kHeadDim + 4;                   // merge row stride (floats)
+// merge rows: dim d of a column at d + d / 32 (lanes that differ in g write
+// different banks), columns kMS8 floats apart
+constexpr int kMS8 = kHeadDim + 12;
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 static_assert(64 * kMS8 * 4 + 64 * 4 * 4 + 64 * 4 <= kOffScl8, "merge buffers reuse the stages");
 
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
     if (active) {
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
-            const int d0 = 32 * g + 2 * m;
+            const int d0 = 33 * g + 2 * m;  // dim 32 g + 2 m, skewed by g
             mbuf[(ks * NC + colA) * kMS8 + d0] = acc[m][0] * R;
             mbuf[(ks * NC + colB) * kMS8 + d0] = acc[m][1] * R;
             mbuf[(ks * NC + colA) * kMS8 + d0 + 1] = acc[m][2] * R;
@@ -381,13 +383,14 @@ __global__ void __launch_bounds__(kThreads8, 1)
     for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads8) {
         const int col = idx / (kHeadDim / 4), d = 4 * (idx - col * (kHeadDim / 4));
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int sd0 = d + (d >> 5);  // the four dims share one skew
         for (int k = 0; k < ks_n; ++k) {
             const float wk = wts[k * NC + col];
-            const float4 v = *reinterpret_cast<const float4 *>(mbuf + (k * NC + col) * kMS8 + d);
-            O.x += wk * v.x;
-            O.y += wk * v.y;
-            O.z += wk * v.z;
-            O.w += wk * v.w;
+            const float *v = mbuf + (k * NC + col) * kMS8 + sd0;
+            O.x += wk * v[0];
+            O.y += wk * v[1];
+            O.z += wk * v[2];
+            O.w += wk * v[3];
         }
         const float L = lt[col];
         if (single) {
