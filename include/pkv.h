@@ -288,8 +288,9 @@ int pkv_decode_static(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_s
  * For each stream's one decode query (n_new == 1), head h and complete block
  * b < len/4: scores[s][h][b] = sum_d qi[h][d] * P[b][d], float32, as the
  * chain acc = fmaf(qi[d], P[b][d], acc) for d = 0 .. Di-1 from acc = 0.
- * qi [tokens][n_q_heads][Di] bf16; scores [n_seqs][n_q_heads][ld] float32,
- * entries b >= len/4 set to -infinity.  EINVAL if ld < len/4. */
+ * qi [tokens][n_q_heads][Di] bf16, 16-byte aligned; scores
+ * [n_seqs][n_q_heads][ld] float32, entries b >= len/4 set to -infinity.
+ * EINVAL if ld < len/4 or qi is not 16-byte aligned. */
 int pkv_block_scores(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
                      int32_t layer, int32_t n_q_heads, const void *qi, float *scores,
                      int32_t ld, int32_t *dev_status, cudaStream_t stream);

@@ -684,7 +684,7 @@ extern "C" int pkv_block_scores(const pkv_layout *L, const pkv_seq *seqs, int32_
     }
     if (ld < max_nb || ld < 0) return PKV_EINVAL;
     if (c.n_seqs == 0 || ld == 0) return PKV_OK;
-    if (!qi || !scores) return PKV_EINVAL;
+    if (!qi || !scores || !aligned16(qi)) return PKV_EINVAL;
     return launch_scores(c, scores, ld, static_cast<const uint16_t *>(qi), max_nb, stream);
 }
 

@@ -7,9 +7,12 @@
 // position) and staged in shared memory.
 //
 // Top-k: one CTA per (stream, head) finds the k-th largest score by an 8-bit
-// radix select on order-preserving keys, then writes the selected block ids
-// in ascending order with an ordered compaction; an exact tie at the
-// threshold goes to the lower ids.
+// radix select on order-preserving keys (held in shared memory when the row
+// fits; each pass's digit found by one warp in parallel), then writes the
+// selected block ids in ascending order with an ordered compaction; an exact
+// tie at the threshold goes to the lower ids.
+#include <algorithm>
+
 #include "pkv_dev.cuh"
 
 namespace pkv {
@@ -24,6 +27,7 @@ __global__ void __launch_bounds__(kScoreThreads)
     scores_kernel(const __grid_constant__ Common c, const uint16_t *__restrict__ qi,
                   float *__restrict__ scores, int32_t ld, int32_t tiles_per_seq) {
     __shared__ float ps[kScoreBlocks * kPStride];
+    __shared__ int64_t prow[kScoreBlocks];  // each block's pooled row (-1 past the end)
     extern __shared__ float qs[];  // [n_q_heads][Di]
     pdl_wait();
     pdl_trigger();
@@ -33,44 +37,80 @@ __global__ void __launch_bounds__(kScoreThreads)
     const int nb = sd.len / 4;
     const int H = c.n_kv_heads, Di = c.idx_dim, Hq = c.n_q_heads;
     const int tid = threadIdx.x;
-    // indexer queries of this stream's one decode token
-    for (int i = tid; i < Hq * Di; i += kScoreThreads)
-        qs[i] = __uint_as_float(static_cast<uint32_t>(qi[(int64_t)sd.tok_off * Hq * Di + i]) << 16);
-    // pooled rows of blocks b0 .. b0+63: one lookup per block
-    for (int i = tid; i < kScoreBlocks * (kIdxDim / 2); i += kScoreThreads) {
-        const int bl = i / (kIdxDim / 2), d2 = i - bl * (kIdxDim / 2);
-        const int b = b0 + bl;
-        float lo = 0.f, hi = 0.f;
+    // pooled rows of blocks b0 .. b0+63: one lookup per block, then the rows
+    if (tid < kScoreBlocks) {
+        const int b = b0 + tid;
+        int64_t off = -1;
         if (b < nb) {
             int32_t row;
             const int64_t page = page_start(sd, 4 * b, &row, c.status);
-            const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                sd.layer_base + page + off_p_f(c.kv_fp8, H, Di, sd.ptok, row / 4) + 2 * d2);
-            lo = __uint_as_float(w << 16);
-            hi = __uint_as_float(w & 0xffff0000u);
+            off = page + off_p_f(c.kv_fp8, H, Di, sd.ptok, row / 4);
         }
-        ps[bl * kPStride + 2 * d2] = lo;
-        ps[bl * kPStride + 2 * d2 + 1] = hi;
+        prow[tid] = off;
+    }
+    // indexer queries of this stream's one decode token, 8 a thread and load
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(qi + (int64_t)sd.tok_off * Hq * Di);
+        for (int i = tid; i < Hq * Di / 8; i += kScoreThreads) {
+            const uint4 w = __ldg(src + i);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                qs[8 * i + e] = __uint_as_float((e & 1) ? (u[e / 2] & 0xffff0000u) : (u[e / 2] << 16));
+        }
+    }
+    __syncthreads();
+    // the 64 pooled rows, 16 bytes a load and every load in flight at once
+    constexpr int kLoads = kScoreBlocks * (kIdxDim / 8) / kScoreThreads;  // 4
+    uint4 w[kLoads];
+#pragma unroll
+    for (int it = 0; it < kLoads; ++it) {
+        const int i = tid + it * kScoreThreads, bl = i >> 4, c16 = i & 15;
+        const int64_t off = prow[bl];
+        w[it] = off >= 0 ? __ldg(reinterpret_cast<const uint4 *>(sd.layer_base + off) + c16)
+                         : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int it = 0; it < kLoads; ++it) {
+        const int i = tid + it * kScoreThreads, bl = i >> 4, c16 = i & 15;
+        const uint32_t u[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            ps[bl * kPStride + 8 * c16 + e] =
+                __uint_as_float((e & 1) ? (u[e / 2] & 0xffff0000u) : (u[e / 2] << 16));
     }
     __syncthreads();
     const int lane = tid & 31, warp = tid >> 5;
-    // warps walk heads; each lane owns blocks lane and lane + 32 of the tile
-    for (int h = warp; h < Hq; h += kScoreThreads / 32) {
-        const float *q = qs + h * Di;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int bl = lane + 32 * half;
-            const int b = b0 + bl;
-            if (b >= ld) continue;
-            float acc = 0.f;
-            const float *p = ps + bl * kPStride;
-            for (int d = 0; d < kIdxDim; ++d) acc = __fmaf_rn(q[d], p[d], acc);
-            scores[((int64_t)s * Hq + h) * ld + b] = b < nb ? acc : -INFINITY;
+    // a warp takes heads h and h + 8, each lane blocks lane and lane + 32 of
+    // the tile: four chains side by side, each still summed in d order
+    const float *pa = ps + lane * kPStride, *pb = ps + (lane + 32) * kPStride;
+    for (int h = warp; h < Hq; h += 2 * (kScoreThreads / 32)) {
+        const int h2 = h + kScoreThreads / 32;
+        const bool two = h2 < Hq;
+        const float *qa = qs + h * Di, *qb = qs + (two ? h2 : h) * Di;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < kIdxDim; ++d) {
+            const float x = qa[d], y = qb[d], u = pa[d], v = pb[d];
+            a0 = __fmaf_rn(x, u, a0);
+            a1 = __fmaf_rn(x, v, a1);
+            a2 = __fmaf_rn(y, u, a2);
+            a3 = __fmaf_rn(y, v, a3);
+        }
+        const int ba = b0 + lane, bb = ba + 32;
+        float *row_a = scores + ((int64_t)s * Hq + h) * ld;
+        if (ba < ld) row_a[ba] = ba < nb ? a0 : -INFINITY;
+        if (bb < ld) row_a[bb] = bb < nb ? a1 : -INFINITY;
+        if (two) {
+            float *row_b = scores + ((int64_t)s * Hq + h2) * ld;
+            if (ba < ld) row_b[ba] = ba < nb ? a2 : -INFINITY;
+            if (bb < ld) row_b[bb] = bb < nb ? a3 : -INFINITY;
         }
     }
 }
 
 constexpr int kTopThreads = 256;
+constexpr int kTopSmemKeys = 12288;  // order keys of a row held in shared memory (48 KB)
 
 __device__ __forceinline__ uint32_t order_key(float x) {
     uint32_t u = __float_as_uint(x);
@@ -108,11 +148,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *excl, int *warp_
 
 __global__ void __launch_bounds__(kTopThreads)
     topk_kernel(const __grid_constant__ Common c, const float *__restrict__ scores, int32_t ld,
-                int32_t k, int32_t *__restrict__ ids) {
+                int32_t k, int32_t *__restrict__ ids, int32_t keys_in_smem) {
     __shared__ int hist[256];
     __shared__ int warp_tot[kTopThreads / 32];
     __shared__ uint32_t sh_prefix;
     __shared__ int sh_need;
+    extern __shared__ uint32_t skeys[];  // the row's order keys, when it fits
     pdl_wait();
     pdl_trigger();
     const int s = blockIdx.x / c.n_q_heads, h = blockIdx.x - s * c.n_q_heads;
@@ -120,7 +161,12 @@ __global__ void __launch_bounds__(kTopThreads)
     const int kk = min(k, nb);
     const float *row = scores + ((int64_t)s * c.n_q_heads + h) * ld;
     int32_t *out = ids + ((int64_t)s * c.n_q_heads + h) * k;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool in_smem = keys_in_smem != 0;  // the launch sized the array for every row
+    if (in_smem)
+        for (int b = tid; b < nb; b += kTopThreads) skeys[b] = order_key(row[b]);
+    __syncthreads();
+    auto key_of = [&](int b) -> uint32_t { return in_smem ? skeys[b] : order_key(row[b]); };
 
     // radix select: the key T with count(key > T) < kk <= count(key >= T)
     uint32_t prefix = 0, mask = 0;
@@ -130,18 +176,31 @@ __global__ void __launch_bounds__(kTopThreads)
             for (int i = tid; i < 256; i += kTopThreads) hist[i] = 0;
             __syncthreads();
             for (int b = tid; b < nb; b += kTopThreads) {
-                const uint32_t key = order_key(row[b]);
+                const uint32_t key = key_of(b);
                 if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
             }
             __syncthreads();
-            if (tid == 0) {
-                int acc = 0, digit = 255;
-                for (; digit > 0; --digit) {
-                    if (acc + hist[digit] >= need) break;
-                    acc += hist[digit];
+            if (warp == 0) {
+                // lane l holds digits 8l .. 8l+7; counts above each lane by a suffix sum
+                int own = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) own += hist[8 * lane + i];
+                int incl = own;  // keys with a digit >= 8 * lane
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_down_sync(0xffffffffu, incl, o);
+                    if (lane + o < 32) incl += y;
                 }
-                sh_prefix = prefix | (static_cast<uint32_t>(digit) << shift);
-                sh_need = need - acc;
+                const int above = incl - own;
+                if (above < need && need <= incl) {  // the threshold digit is this lane's
+                    int acc = above, digit = 8 * lane + 7;
+                    for (; digit > 8 * lane; --digit) {
+                        if (acc + hist[digit] >= need) break;
+                        acc += hist[digit];
+                    }
+                    sh_prefix = prefix | (static_cast<uint32_t>(digit) << shift);
+                    sh_need = need - acc;
+                }
             }
             __syncthreads();
             prefix = sh_prefix;
@@ -156,14 +215,14 @@ __global__ void __launch_bounds__(kTopThreads)
     const int lo = min(nb, tid * chunk), hi = min(nb, lo + chunk);
     int eq = 0;
     if (kk > 0)
-        for (int b = lo; b < hi; ++b) eq += order_key(row[b]) == T;
+        for (int b = lo; b < hi; ++b) eq += key_of(b) == T;
     int eq_before;
     block_exclusive_scan(eq, &eq_before, warp_tot);
     int sel = 0;
     if (kk > 0) {
         int e = eq_before;
         for (int b = lo; b < hi; ++b) {
-            const uint32_t key = order_key(row[b]);
+            const uint32_t key = key_of(b);
             if (key > T) ++sel;
             else if (key == T && e++ < need) ++sel;
         }
@@ -173,7 +232,7 @@ __global__ void __launch_bounds__(kTopThreads)
     if (kk > 0) {
         int e = eq_before, o = sel_before;
         for (int b = lo; b < hi; ++b) {
-            const uint32_t key = order_key(row[b]);
+            const uint32_t key = key_of(b);
             if (key > T) out[o++] = b;
             else if (key == T && e++ < need) out[o++] = b;
         }
@@ -203,8 +262,19 @@ int launch_scores(const Common &c, float *scores, int32_t ld, const uint16_t *qi
 
 int launch_topk(const Common &c, const float *scores, int32_t ld, int32_t k, int32_t *ids,
                 cudaStream_t stream) {
-    return launch_status(launch_pdl(topk_kernel, c.n_seqs * c.n_q_heads, kTopThreads, 0, stream,
-                                    c, scores, ld, k, ids));
+    int max_nb = 0;
+    for (int s = 0; s < c.n_seqs; ++s) max_nb = std::max(max_nb, c.seq[s].len / 4);
+    const bool in_smem = max_nb <= kTopSmemKeys;
+    const size_t dyn = in_smem ? static_cast<size_t>(max_nb) * 4 : 0;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kTopSmemKeys * 4) != cudaSuccess)
+            return PKV_ECUDA;
+        attr_set = true;
+    }
+    return launch_status(launch_pdl(topk_kernel, c.n_seqs * c.n_q_heads, kTopThreads, dyn, stream,
+                                    c, scores, ld, k, ids, static_cast<int32_t>(in_smem)));
 }
 
 }  // namespace pkv
