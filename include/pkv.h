@@ -191,6 +191,38 @@ typedef struct pkv_event_ops {
  * track completion themselves, and for tests without a GPU. */
 int pkv_arena_set_event_ops(pkv_arena *arena, const pkv_event_ops *ops);
 
+/* ---- runs (#1170, commit 1ac2075: core kv_pool findRun / claimRun /
+ * releaseRun, Layout.run_bytes and runPages(); commit 51f8354: mapRun) ------
+ * A run is k consecutive pages of the arena leased to one stream for its
+ * state that is not attention cache (recurrent states, convolution tails,
+ * draft buffers).  Runs come from the top of the arena (the highest ids)
+ * while KV pages come from the bottom; a run's pages are never handed out
+ * by pkv_pages_take and cannot be given back by pkv_pages_give.  When no k
+ * consecutive pages are free (too few, or too fragmented) the request gets
+ * PKV_EAGAIN and waits, as one short of pages does.  A run goes back with
+ * the same deferral as pages.  Only addresses are handed out: the library
+ * never touches the run's bytes. */
+
+/* Pages a run of run_bytes needs (runPages): ceil(run_bytes / page bytes),
+ * 0 for 0 bytes. */
+int pkv_run_pages(const pkv_arena *arena, uint64_t run_bytes, int32_t *k_out);
+/* Claim the run of k >= 1 free pages with the highest first id (the first
+ * such window met scanning down from the top) into *first_out.  EAGAIN if
+ * there is none; nothing is taken then. */
+int pkv_run_take(pkv_arena *arena, int32_t k, int32_t *first_out);
+/* Give back the run [first, first + k) exactly as taken, now (defer == 0)
+ * or once the work queued on `stream` has finished.  EINVAL if it is not a
+ * run held now (nothing changes then). */
+int pkv_run_give(pkv_arena *arena, int32_t first, int32_t k, cudaStream_t stream, int32_t defer);
+/* Lay n_parts buffers of part_bytes[i] bytes one after another in the run's
+ * memory, each starting at a device address that is a multiple of `align`
+ * (a power of two, 16 .. 4096), and write their device addresses into
+ * ptrs_out[i] (mapRun).  EINVAL (nothing written) when the parts do not fit
+ * in the run (a run shorter than its parts is refused), or when
+ * [first, first + k) is not a run held now. */
+int pkv_run_map(const pkv_arena *arena, int32_t first, int32_t k, const uint64_t *part_bytes,
+                int32_t n_parts, uint64_t align, void **ptrs_out);
+
 /* ---- cache store (#1169: fn_attn_prep writes key, value and indexer-key
  * rows through pg_at; #1170 commit 3f5b87d: rope's store through kv_row) ---
  * Copy each stream's n_new new tokens into positions len-n_new .. len-1 of

@@ -124,6 +124,9 @@ __host__ __device__ inline int64_t off8_scale(bool v, int32_t h_kv, int32_t ptok
 
 // Host helpers (pkv_host.cu).
 int validate_layout(const pkv_layout *layout);
+inline bool fp8_of(const pkv_layout *L) { return L->kv_format == PKV_KV_E4M3; }
+// page sizes are whole blocks of 4 positions (#1169 What this changes)
+inline bool page_pos_ok(int32_t page_pos) { return page_pos > 0 && page_pos % 4 == 0; }
 int fill_common(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,
                 int32_t n_q_heads, int32_t *dev_status, Common *c);
 int sm_count(int *out);

@@ -59,7 +59,8 @@ _lib = None
 EXPORTS = [
     "pkv_layout_page_elems", "pkv_pg_row", "pkv_arena_create", "pkv_arena_destroy",
     "pkv_arena_info", "pkv_pages_take", "pkv_pages_give", "pkv_arena_pg",
-    "pkv_arena_set_event_ops", "pkv_store", "pkv_gather", "pkv_pool", "pkv_decode_ws_size",
+    "pkv_arena_set_event_ops", "pkv_run_pages", "pkv_run_take", "pkv_run_give", "pkv_run_map",
+    "pkv_store", "pkv_gather", "pkv_pool", "pkv_decode_ws_size",
     "pkv_decode", "pkv_decode_static", "pkv_block_scores", "pkv_topk", "pkv_sparse_ws_size",
     "pkv_sparse_decode", "pkv_prefill_ws_size", "pkv_prefill",
 ]
@@ -90,6 +91,10 @@ def load(path: Optional[str] = None):
         "pkv_pages_give": [vp, vp, i32, vp, i32],
         "pkv_arena_pg": [vp, vp, i32, PP],
         "pkv_arena_set_event_ops": [vp, ctypes.POINTER(EventOps)],
+        "pkv_run_pages": [vp, ctypes.c_uint64, ctypes.POINTER(i32)],
+        "pkv_run_take": [vp, i32, ctypes.POINTER(i32)],
+        "pkv_run_give": [vp, i32, i32, vp, i32],
+        "pkv_run_map": [vp, i32, i32, vp, i32, ctypes.c_uint64, vp],
         "pkv_store": [LP, SP, i32, i32, vp, vp, vp, vp, vp],
         "pkv_gather": [LP, SP, i32, i32, i32, vp, vp, vp],
         "pkv_pool": [LP, SP, i32, i32, vp, vp],
@@ -217,6 +222,29 @@ class Arena:
         st = _stream(stream) if defer else (stream or 0)
         _check(self._lib.pkv_pages_give(self._h, ids.ctypes.data, ids.size, st, int(defer)),
                "pkv_pages_give")
+
+    def run_pages(self, run_bytes: int) -> int:
+        k = ctypes.c_int32()
+        _check(self._lib.pkv_run_pages(self._h, run_bytes, ctypes.byref(k)), "pkv_run_pages")
+        return k.value
+
+    def run_take(self, k: int) -> int:
+        first = ctypes.c_int32()
+        _check(self._lib.pkv_run_take(self._h, k, ctypes.byref(first)), "pkv_run_take")
+        return first.value
+
+    def run_give(self, first: int, k: int, stream=None, defer: bool = True):
+        st = _stream(stream) if defer else (stream or 0)
+        _check(self._lib.pkv_run_give(self._h, first, k, st, int(defer)), "pkv_run_give")
+
+    def run_map(self, first: int, k: int, part_bytes, align: int = 256):
+        """Device addresses of the parts laid one after another in the run."""
+        import numpy as np
+        parts = np.ascontiguousarray(part_bytes, dtype=np.uint64)
+        out = (ctypes.c_void_p * max(1, parts.size))()
+        _check(self._lib.pkv_run_map(self._h, first, k, parts.ctypes.data, parts.size, align,
+                                     out), "pkv_run_map")
+        return [int(out[i] or 0) for i in range(parts.size)]
 
     def pg(self, dev_table, n_table: Optional[int] = None) -> Pg:
         out = Pg()

@@ -252,6 +252,176 @@ def test_arena_pg_describes_the_pool(arena):
         (0x100000, 0x5000, ps, 16, n, 3)
 
 
+# ---- runs (#1170, commit 1ac2075: findRun / claimRun / releaseRun; commit
+# 51f8354: mapRun refuses a run shorter than its parts) ------------------------
+
+def test_runs_come_from_the_top_and_pages_from_the_bottom(arena):
+    assert arena.run_take(3) == 7                 # pages 7, 8, 9
+    assert arena.take(2).tolist() == [0, 1]
+    assert arena.run_take(2) == 5                 # the next window down
+    assert arena.info()[1] == 3
+    assert arena.take(3).tolist() == [2, 3, 4]    # run pages are never handed out
+    with pytest.raises(pkv.PkvError) as e:
+        arena.take(1)
+    assert e.value.code == pkv.EAGAIN
+
+
+def test_fragmented_pool_makes_a_run_wait(arena):
+    ids = arena.take(10)
+    arena.give(ids[1::2], defer=False)            # pages 1, 3, 5, 7, 9 free
+    assert arena.info()[1] == 5
+    with pytest.raises(pkv.PkvError) as e:
+        arena.run_take(2)
+    assert e.value.code == pkv.EAGAIN
+    assert arena.info()[1] == 5                   # nothing was taken
+    assert arena.run_take(1) == 9
+    arena.give([6], defer=False)                  # 5, 6, 7 free now
+    assert arena.run_take(3) == 5
+
+
+def test_run_give_takes_back_exactly_a_run_held(arena):
+    first = arena.run_take(4)                     # 6 .. 9
+    for f, k in ((first, 3), (first + 1, 3), (first, 5), (0, 1)):
+        with pytest.raises(pkv.PkvError):
+            arena.run_give(f, k, defer=False)
+    with pytest.raises(pkv.PkvError):
+        arena.give([first], defer=False)          # a run's page is not a KV page
+    ids = arena.take(2)
+    with pytest.raises(pkv.PkvError):
+        arena.run_give(int(ids[0]), 2, defer=False)   # KV pages are not a run
+    arena.run_give(first, 4, defer=False)
+    with pytest.raises(pkv.PkvError):
+        arena.run_give(first, 4, defer=False)     # not held any more
+    assert arena.info()[1] == 8
+    assert arena.run_take(8) == 2
+
+
+def test_run_returns_only_after_the_stream_drains(arena):
+    ev = FakeEvents()
+    arena.set_event_ops(ev.ops)
+    first = arena.run_take(10)
+    assert first == 0
+    arena.run_give(first, 10, stream=0x77, defer=True)
+    with pytest.raises(pkv.PkvError) as e:
+        arena.run_take(1)
+    assert e.value.code == pkv.EAGAIN
+    with pytest.raises(pkv.PkvError):
+        arena.run_give(first, 10, defer=False)    # pending: not held
+    ev.done.add(1)
+    assert arena.info()[1] == 10
+    assert ev.live == set()
+    assert arena.take(1).tolist() == [0]
+
+
+def test_run_pages_round_up_to_whole_pages(arena):
+    _, _, ps = arena.info()
+    page_bytes = 2 * ps
+    for nbytes, k in ((0, 0), (1, 1), (page_bytes, 1), (page_bytes + 1, 2), (5 * page_bytes, 5)):
+        assert arena.run_pages(nbytes) == k
+
+
+def test_run_map_lays_parts_in_order_and_refuses_a_short_run(arena):
+    _, _, ps = arena.info()
+    page_bytes = 2 * ps
+    first = arena.run_take(2)
+    lo = 0x100000 + first * page_bytes
+    parts = [100, 1000, 7, page_bytes]
+    ptrs = arena.run_map(first, 2, parts, align=256)
+    expect, cur = [], lo
+    for b in parts:
+        cur = -(-cur // 256) * 256
+        expect.append(cur)
+        cur += b
+    assert ptrs == expect
+    assert all(p % 256 == 0 for p in ptrs)
+    assert ptrs[-1] + parts[-1] <= lo + 2 * page_bytes
+    # exactly filling the run is fine; one byte more is refused
+    assert arena.run_map(first, 2, [2 * page_bytes], align=16) == [lo]
+    with pytest.raises(pkv.PkvError):
+        arena.run_map(first, 2, [2 * page_bytes + 1], align=16)
+    with pytest.raises(pkv.PkvError):
+        arena.run_map(first, 2, [page_bytes, page_bytes], align=4096)   # padding pushes it out
+    for align in (8, 24, 8192):
+        with pytest.raises(pkv.PkvError):
+            arena.run_map(first, 2, [16], align=align)
+    with pytest.raises(pkv.PkvError):
+        arena.run_map(first, 1, [16])             # not the run as taken
+
+
+class PoolModel:
+    """Brute-force model of the pool: a set of free ids.  KV pages: the n
+    lowest free ids.  A run: the largest first id whose k pages are all
+    free.  Releases take effect at once (no deferral)."""
+
+    def __init__(self, n):
+        self.n = n
+        self.free = set(range(n))
+        self.runs = {}
+
+    def take(self, k):
+        if k > len(self.free):
+            return None
+        ids = sorted(self.free)[:k]
+        self.free -= set(ids)
+        return ids
+
+    def run_take(self, k):
+        for first in range(self.n - k, -1, -1):
+            if all(i in self.free for i in range(first, first + k)):
+                self.free -= set(range(first, first + k))
+                self.runs[first] = k
+                return first
+        return None
+
+
+def test_pool_follows_the_brute_force_model_over_random_operations(lib):
+    lay = pkv.layout(1, 1, 256, 0)
+    ps = pkv.page_elems(lay, 4)
+    rng = np.random.default_rng(5)
+    for trial in range(6):
+        n = int(rng.integers(5, 60))
+        a = pkv.Arena(lay, 4, 0x200000, nbytes=ps * 2 * n)
+        m = PoolModel(n)
+        held_pages, held_runs = [], []
+        try:
+            for _ in range(400):
+                op = rng.integers(0, 4)
+                if op == 0:
+                    k = int(rng.integers(1, 6))
+                    want = m.take(k)
+                    if want is None:
+                        with pytest.raises(pkv.PkvError) as e:
+                            a.take(k)
+                        assert e.value.code == pkv.EAGAIN
+                    else:
+                        assert a.take(k).tolist() == want
+                        held_pages += want
+                elif op == 1:
+                    k = int(rng.integers(1, 8))
+                    want = m.run_take(k)
+                    if want is None:
+                        with pytest.raises(pkv.PkvError) as e:
+                            a.run_take(k)
+                        assert e.value.code == pkv.EAGAIN
+                    else:
+                        assert a.run_take(k) == want
+                        held_runs.append((want, k))
+                elif op == 2 and held_pages:
+                    pick = rng.permutation(len(held_pages))[: int(rng.integers(1, len(held_pages) + 1))]
+                    ids = [held_pages[i] for i in pick]
+                    a.give(ids, defer=False)
+                    m.free |= set(ids)
+                    held_pages = [x for i, x in enumerate(held_pages) if i not in set(pick.tolist())]
+                elif op == 3 and held_runs:
+                    first, k = held_runs.pop(int(rng.integers(0, len(held_runs))))
+                    a.run_give(first, k, defer=False)
+                    m.free |= set(range(first, first + k))
+                    del m.runs[first]
+                assert a.info()[1] == len(m.free)
+        finally:
+            a.close()
+
+
 # ---- e4m3 K/V format (#1170, commit 5c09685) -------------------------------
 
 def test_e4m3_page_elems_match_oracle(lib, orc):
