@@ -49,14 +49,14 @@ LENS = [1000, 3000, 6000, 9000]          # cached before the new token
 N_LAYERS, HQ, HKV, D, DI = 13, 16, 2, 256, 128
 PAGES = [16, 48, 128, 256, 512]
 NOMINAL_HBM = 8000.0
-ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3"]
+ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3", "allocator"]
 # DRAM bytes (read + write) of one pkv_decode call of the workload (partial +
 # combine kernels), from the ncu capture summarised in
 # profiles/decode_partial_pages256.md, valid while the decode sources hash to
 # the value the capture was taken with; reported as null otherwise.
-DECODE_TRAFFIC = {"bytes": 40392192,
+DECODE_TRAFFIC = {"bytes": 40385280,
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "da119ed2c58a1d2d43310e142b07d883fc12cb5022ac3d32f89134e04a5bc985"}
+                  "sha256": "17e46c324ca08d8d25141ecd6766308bac670ebfa56bcd6dcc330e768629e390"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
@@ -624,6 +624,46 @@ def row_decode_e4m3(torch, pkv, dev, timer):
             "query_heads_per_s": round(N_LAYERS * len(LENS) * HQ / (ms / 1e3), 1)}
 
 
+def row_allocator(torch, pkv, dev, timer):
+    """Host cost of the page pool on the serving-mix arena (792 pages of 256,
+    13 layers): a lane opens (a run of state pages claimed from the top, the
+    KV pages of a 40,960-position stream from the bottom) and closes (both
+    given back, deferred on the stream by an event).  Host work only, timed
+    with the host clock through the Python binding."""
+    import time
+    lay = pkv.layout(N_LAYERS, HKV, D, DI)
+    ps = pkv.page_elems(lay, 256)
+    n_pages = 792
+    mem = torch.empty(n_pages * ps, dtype=torch.int16, device=dev)
+    arena = pkv.Arena(lay, 256, mem)
+    stream = torch.cuda.current_stream(dev)
+    k_run = arena.run_pages(64 << 20)          # 64 MiB of per-stream state
+    n_kv = 40960 // 256
+    busy = arena.take(300)                     # other lanes' pages: the scan starts mid-pool
+    cycles = 2000
+
+    def cycle():
+        first = arena.run_take(k_run)
+        ids = arena.take(n_kv)
+        arena.give(ids, stream=stream, defer=True)
+        arena.run_give(first, k_run, stream=stream, defer=True)
+
+    for _ in range(50):
+        cycle()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(cycles):
+        cycle()
+    us = (time.perf_counter() - t0) / cycles * 1e6
+    torch.cuda.synchronize()
+    ok = arena.info()[1] == n_pages - busy.size
+    arena.close()
+    return {"workload": "page pool: lane open + close on a 792 x 256 arena (run of %d pages from "
+                        "the top, %d KV pages from the bottom, deferred release)" % (k_run, n_kv),
+            "us_per_open_close": round(us, 2), "cycles": cycles, "pages_all_returned": bool(ok),
+            "clock": "host (time.perf_counter), no kernels"}
+
+
 def _gather_all(torch, pkv, lay, seqs, T, dev):
     outs = [torch.empty((T, HKV, D), dtype=torch.int16, device=dev),
             torch.empty((T, HKV, D), dtype=torch.int16, device=dev),
@@ -636,7 +676,7 @@ def _gather_all(torch, pkv, lay, seqs, T, dev):
 
 ROW_FNS = {"prefill": row_prefill, "sparse": row_sparse, "mix": row_mix,
            "decode_layer": row_decode_layer, "prompt_cache": row_prompt_cache,
-           "decode_e4m3": row_decode_e4m3}
+           "decode_e4m3": row_decode_e4m3, "allocator": row_allocator}
 
 
 def hot_path_rows(torch, pkv, dev, names, profile=False):
