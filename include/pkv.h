@@ -25,6 +25,17 @@
  *     PyTorch).  The library allocates no device memory.  Work buffers are
  *     sized by the *_ws_size calls and passed in.
  *   - Every launch goes on the caller's `stream`; no call synchronizes.
+ *   - Kernels launch with programmatic dependent launch: a call's kernels
+ *     may start while the kernel before them on the stream is still running,
+ *     and wait for it before touching anything it may write.  Two things are
+ *     read before that wait: page tables and the rows of cached positions
+ *     (below len - n_new) of pkv_decode / pkv_decode_static.  So those must
+ *     not be written by the kernel immediately before on the stream, unless
+ *     that kernel is one of this library's stores (pkv_store, or pkv_decode
+ *     with k_new), which make their rows visible before letting the next
+ *     kernel start.  Rows, tables and inputs written earlier on the stream,
+ *     or by a copy or a kernel launched without programmatic dependent
+ *     launch, need nothing.
  *   - A multi-stream launch takes one pkv_seq per stream, each with its own
  *     page table (PR #2244 "the grouped draft head's lanes carry their page
  *     table": a grouped launch built without each stream's table read and

@@ -37,7 +37,6 @@ __global__ void __launch_bounds__(kThreads) store_kernel(const __grid_constant__
                                                          const uint16_t *__restrict__ v_new,
                                                          const uint16_t *__restrict__ ik_new) {
     pdl_wait();
-    pdl_trigger();
     const int H = c.n_kv_heads;
     const int row_chunks = kHeadDim / kChunk;  // 32
     const int ik_chunks = c.idx_dim / kChunk;  // 16 or 0
@@ -69,6 +68,7 @@ __global__ void __launch_bounds__(kThreads) store_kernel(const __grid_constant__
         uint16_t *base = const_cast<uint16_t *>(sd.layer_base);
         *reinterpret_cast<uint4 *>(base + dst) = __ldg(reinterpret_cast<const uint4 *>(src));
     }
+    pdl_trigger_after_writes();  // the next decode may read these rows early
 }
 
 // One thread per 16-byte chunk of an output row.  work_off holds each
@@ -158,7 +158,6 @@ __global__ void __launch_bounds__(kThreads) store8_kernel(const __grid_constant_
                                                           const uint16_t *__restrict__ v_new,
                                                           const uint16_t *__restrict__ ik_new) {
     pdl_wait();
-    pdl_trigger();
     const int H = c.n_kv_heads, lane = threadIdx.x & 31;
     const int per_tok = 2 * H + (c.idx_dim ? 1 : 0);
     const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
@@ -205,6 +204,7 @@ __global__ void __launch_bounds__(kThreads) store8_kernel(const __grid_constant_
             *reinterpret_cast<uint4 *>(lb + 2 * off_ik_f(true, H, c.idx_dim, sd.ptok, row) + 16 * lane) = u;
         }
     }
+    pdl_trigger_after_writes();  // the next decode may read these rows early
 }
 
 // e4m3 gather: codes (16 bytes a thread, [rows][H][256] out) or scales (a

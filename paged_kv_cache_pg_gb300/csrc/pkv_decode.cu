@@ -258,6 +258,38 @@ __device__ __forceinline__ void stage_tile(const Common &c, const DecodeArgs &a,
     }
 }
 
+// Prefetch the cached K and V rows of dense tile t into L2 (one warp).  Tiles
+// past a key slice's stage slots are only staged after the slice consumes its
+// first tiles; fetching their rows into L2 while the CTA waits on the previous
+// kernel takes them off that path.  Tiles holding new positions are skipped.
+__device__ __forceinline__ void prefetch_tile(const Common &c, const SeqDev &sd, const Unit &u,
+                                              const Ctx &x, int t, int lane) {
+    const int qbase = sd.len - sd.n_new;
+    const int k0 = u.key0 + t * kTile;
+    if (k0 + kTile > min(u.key1, qbase)) return;  // ragged or holds new rows
+    const int64_t v_gap = (int64_t)c.n_kv_heads * sd.ptok * kHeadDim;
+    const bool run = sd.table == nullptr || sd.ptok % kTile == 0;  // 16 rows in one page
+    const int key = k0 + (run ? 0 : (lane & 15));
+    int row = key;
+    int64_t pg = 0;
+    if (sd.table) {
+        const int page = key / sd.ptok;
+        row = key - page * sd.ptok;
+        pg = x.rows[page - x.first_page];
+        if (pg < 0) return;  // reported when the tile is staged
+    }
+    const uint16_t *kr = sd.layer_base + pg + off_k(sd.ptok, u.kvh, row);
+    if (run) {
+        if (lane == 0) {
+            bulk_prefetch_l2(kr, kTile * 512);
+            bulk_prefetch_l2(kr + v_gap, kTile * 512);
+        }
+    } else if (lane < kTile) {
+        bulk_prefetch_l2(kr, 512);
+        bulk_prefetch_l2(kr + v_gap, 512);
+    }
+}
+
 template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
@@ -363,6 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, lane, pol);
         }
+        if (!kSparse && !waited)
+            for (int j = issued; j < my_tiles && j < 2 * S; ++j)
+                prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
     }
     if (!waited) pdl_wait();
 
@@ -472,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&x.full[ks * S + j % S], (j / S) & 1, nullptr);
     }
 
+    if (a.k_new != nullptr) __threadfence();  // stored rows visible before the next kernel starts
     __syncthreads();
     pdl_trigger();  // every thread has passed its grid-dependency wait
     if (*x.abort_flag) return;
@@ -554,22 +590,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Combine a unit's split partials for one query column:
 // M = max m_i, L = sum 2^(m_i-M) l_i, O = sum 2^(m_i-M) acc_i, out = O / L.
-// Thread d owns dim d and loads acc_i[d] for up to 32 splits at once while
-// the split maxima load, so one memory round trip covers a column of up to
-// 32 splits.  Every sum runs in split order.  At most 64 registers a thread:
-// a combine CTA then fits on an SM beside a partial CTA of the next call,
-// which can start streaming its keys without waiting for the SM.
+// Two CTAs per column, each 128 dims.  The CTA's threads form two groups of
+// 128 (one thread a dim): group 0 sums the first ceil(ns/2) splits, group 1
+// the rest, each in split order, and O = O_0 + O_1.  Every thread loads all
+// its splits' values at once (up to 32) while the split maxima load, so one
+// memory round trip covers a column of up to 64 splits.  At most 64
+// registers a thread: a combine CTA then fits on an SM beside a partial CTA
+// of the next call, which can start streaming its keys without waiting for
+// the SM.
 template <bool kSparse>
 __global__ void __launch_bounds__(kCombThreads, 4)
     decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
     constexpr int kBatch = 32;
+    constexpr int kDims = kHeadDim / 2;   // dims of one CTA
     extern __shared__ float comb_smem[];  // w[ns], lsum[ns]
     __shared__ float sh_l;
+    __shared__ float sh_o[kDims];
     pdl_wait();
     pdl_trigger();
-    const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
+    const int item = blockIdx.x >> 1;  // (unit, column) of the call
+    const int s = find_seq(c.n_seqs, item, [&](int t) { return c.seq[t].comb_off; });
     const SeqDev &sd = c.seq[s];
-    const int r = blockIdx.x - sd.comb_off;
+    const int r = item - sd.comb_off;
     const int unit = r / sd.ncols, col = r - unit * sd.ncols;
     const int ns = sd.nsplit;
     float *w = comb_smem, *lsum = comb_smem + ns;
@@ -579,11 +621,14 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
     const int64_t stride = (int64_t)sd.ncols * kHeadDim;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = tid;  // kCombThreads == head dim
+    const int grp = tid / kDims, dd = tid - grp * kDims;
+    const int d = (blockIdx.x & 1) * kDims + dd;
+    const int half = (ns + 1) >> 1;
+    const int i0 = grp ? half : 0, i1 = grp ? ns : half;  // this group's splits
     const float *col_acc = part_acc + p0 * kHeadDim + d;
     float xs[kBatch];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) xs[j] = j < ns ? __ldcg(col_acc + j * stride) : 0.f;
+    for (int j = 0; j < kBatch; ++j) xs[j] = i0 + j < i1 ? __ldcg(col_acc + (i0 + j) * stride) : 0.f;
     for (int i = tid; i < ns; i += kCombThreads) {
         const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part_ml + (p0 + (int64_t)i * sd.ncols) * 2));
         w[i] = ml.x;
@@ -607,14 +652,18 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     float O = 0.f;
 #pragma unroll
     for (int j = 0; j < kBatch; ++j)
-        if (j < ns) O += w[j] * xs[j];
-    for (int b = kBatch; b < ns; b += kBatch) {
+        if (i0 + j < i1) O += w[i0 + j] * xs[j];
+    for (int b = i0 + kBatch; b < i1; b += kBatch) {
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j) xs[j] = b + j < ns ? __ldcg(col_acc + (b + j) * stride) : 0.f;
+        for (int j = 0; j < kBatch; ++j) xs[j] = b + j < i1 ? __ldcg(col_acc + (b + j) * stride) : 0.f;
 #pragma unroll
         for (int j = 0; j < kBatch; ++j)
-            if (b + j < ns) O += w[b + j] * xs[j];
+            if (b + j < i1) O += w[b + j] * xs[j];
     }
+    if (grp == 1) sh_o[dd] = O;
+    __syncthreads();
+    if (grp == 1) return;
+    O += sh_o[dd];
     const float L = sh_l;
     const float o = L > 0.f ? O / L : 0.f;
     Unit u;
@@ -622,7 +671,7 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     u.kvh = kSparse ? unit / c.group : unit;
     a.out[q_row<kSparse>(c, sd, u, col) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
 }
-static_assert(kCombThreads == kHeadDim, "one combine thread per dim");
+static_assert(kCombThreads == kHeadDim, "two groups of one thread a dim, half the dims a CTA");
 
 }  // namespace
 
@@ -716,7 +765,7 @@ int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, u
     DecodeArgs a{q, out, ws, nullptr, 0, nullptr, nullptr, nullptr};
     int max_ns = 1;
     for (int s = 0; s < c.n_seqs; ++s) max_ns = std::max(max_ns, c.seq[s].nsplit);
-    return launch_status(launch_pdl(decode_combine<false>, plan.total_comb, kCombThreads,
+    return launch_status(launch_pdl(decode_combine<false>, 2 * plan.total_comb, kCombThreads,
                                     2 * max_ns * sizeof(float), stream, c, a));
 }
 
@@ -742,7 +791,7 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     if (plan.total_comb > 0) {
         int max_ns = 1;
         for (int s = 0; s < cc.n_seqs; ++s) max_ns = std::max(max_ns, cc.seq[s].nsplit);
-        e = launch_pdl(comb, plan.total_comb, kCombThreads, 2 * max_ns * sizeof(float), stream, cc, a);
+        e = launch_pdl(comb, 2 * plan.total_comb, kCombThreads, 2 * max_ns * sizeof(float), stream, cc, a);
         if (e != cudaSuccess) return PKV_ECUDA;
     }
     return PKV_OK;

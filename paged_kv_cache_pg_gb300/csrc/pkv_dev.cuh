@@ -117,6 +117,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (bytes % 16 == 0, src 16-byte
+// aligned); nothing lands in shared memory and nothing waits on it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // One 2D TMA tile (64 x 16 bf16 box, 128-byte swizzle) global -> shared.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, int x, int y,
                                             uint64_t *bar, uint64_t policy) {
@@ -205,6 +211,14 @@ __device__ __forceinline__ void pdl_wait() {
 }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Let the next kernel start once this thread's writes are visible device
+// wide: for kernels writing cache rows, which the next kernel may read
+// before its grid-dependency wait.
+__device__ __forceinline__ void pdl_trigger_after_writes() {
+    __threadfence();
+    pdl_trigger();
 }
 
 // A 64-bit value from lane `src` of the warp.

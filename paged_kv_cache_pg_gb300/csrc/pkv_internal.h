@@ -148,7 +148,7 @@ int launch_pool(const Common &c, int32_t total_blocks, cudaStream_t stream);
 
 struct DecodePlan {
     int32_t total_items;   // CTAs of the partial kernel
-    int32_t total_comb;    // CTAs of the combine kernel
+    int32_t total_comb;    // (unit, query column) rows the combine kernel merges
     size_t ws_bytes;       // counters + partials
 };
 int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan);

@@ -208,6 +208,39 @@ def test_fused_store_decode_equals_store_then_decode(ptok):
     assert ok, worst
 
 
+@pytest.mark.parametrize("ptok", [16, 256, None])
+def test_decode_right_after_a_store_of_its_cached_rows(ptok):
+    # A store of every row of the streams and a decode that reads those rows
+    # as cached positions, back to back on one stream: the decode stages
+    # cached rows before its grid-dependency wait, so the store must make its
+    # rows visible before letting the decode start.  The caches are blanked
+    # before each layer's store, so a row read too early shows.
+    from gpu_setup import CANARY
+    t = torch()
+    lay = pkv.layout(4, 2, 256, 128)
+    lens = [L + 1 for L in MULTI_LENS]
+    streams = _streams(lens, 4, 2, seed=1300)
+    q = [synth.queries(1350 + i, 1, 16, 256) for i in range(4)]
+    pl = place(lay, streams, ptok, seed=3)
+    canary = int(np.array([CANARY], np.uint16).view(np.int16)[0])
+    seqs_all = [pkv.seq(g, L, L) for g, L in zip(pl.pgs, lens)]
+    seqs = pl.seqs(lens, [1] * 4)
+    dq = dev_u16(np.concatenate(q))
+    ws = t.zeros(pkv.decode_ws_size(lay, seqs, 16) // 4 + 64, dtype=t.float32, device="cuda")
+    for layer in range(4):
+        k, v, ik = (dev_u16(np.concatenate([getattr(s, f)[layer] for s in streams]))
+                    for f in ("k", "v", "ik"))
+        out = t.zeros_like(dq)
+        for i in range(len(pl.buffers)):
+            pl.body(i).fill_(canary)
+        pkv.store(lay, seqs_all, layer, k, v, ik)
+        pkv.decode(lay, seqs, layer, 16, dq, out, ws)
+        t.cuda.synchronize()
+        ok, worst = within_tol(host_u16(out), oracle_decode(pl, layer, 16, q))
+        assert ok, (layer, worst)
+    assert pl.guards_intact()
+
+
 def test_one_workspace_serves_calls_of_different_shapes(multi):
     # A workspace holds no state between calls: one workspace serves batches
     # of different shapes back to back (single tokens, 4-query windows, a
