@@ -108,8 +108,9 @@ typedef struct pkv_layout {
  * +-448; an all-zero row has scale 0 and codes 0.  Calls that take the
  * format: the layout and arena calls, pkv_pg_row, pkv_store (quantizes),
  * pkv_gather (codes, scales, indexer and pooled rows), pkv_pool,
- * pkv_block_scores, pkv_topk, and pkv_decode / pkv_decode_static without a
- * fused store.  pkv_prefill and pkv_sparse_decode answer PKV_EINVAL.
+ * pkv_block_scores, pkv_topk, and pkv_decode / pkv_decode_static (with k_new
+ * the call quantizes and stores the new rows itself, by the same rule as
+ * pkv_store).  pkv_prefill and pkv_sparse_decode answer PKV_EINVAL.
  */
 
 /*
@@ -272,12 +273,15 @@ int pkv_pool(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int3
  * bit for bit and a stream's output does not depend on the other streams.
  * Fused store: with k_new and v_new (and ik_new when idx_dim > 0) non-NULL,
  * laid out as for pkv_store, the call also writes the new tokens' rows into
- * the cache (as pkv_store would) and reads them from those inputs; with them
- * NULL the new rows must already be in the cache.
+ * the cache (as pkv_store would; quantized by the same rule for an e4m3
+ * layout) and reads them from those inputs; with them NULL the new rows must
+ * already be in the cache.
  * Ordering: the call may read cached rows (positions below len - n_new)
  * before the kernel queued just before it on the stream has finished, so that
- * kernel must not write them; q, k_new, v_new, ik_new, ws and out are only
- * touched after it finishes.
+ * kernel must not write them unless it is a store of this library (pkv_store,
+ * or a pkv_decode with k_new), which makes its rows visible before the next
+ * kernel may start; q, k_new, v_new, ik_new, ws and out are only touched
+ * after it finishes.
  * The split partials go to ws and a second kernel combines them, splits in
  * ascending order.  ws: device, >= pkv_decode_ws_size bytes (0 when no
  * stream needs more than one split), 256-byte aligned, no initialization;

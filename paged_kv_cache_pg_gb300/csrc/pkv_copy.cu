@@ -1,8 +1,6 @@
 // Cache store, gather and block pooling.  Rows are located with pg_at once
 // per row (store, gather) or once per block of four positions (pool: a page
 // holds whole blocks because its size is a multiple of 4), never per load.
-#include <cuda_fp8.h>
-
 #include "pkv_dev.cuh"
 
 namespace pkv {
@@ -176,27 +174,9 @@ __global__ void __launch_bounds__(kThreads) store8_kernel(const __grid_constant_
             const bool v = r >= H;
             const int head = r % H;
             const uint16_t *src = (v ? v_new : k_new) + ((int64_t)tok * H + head) * kHeadDim;
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src) + lane);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                x[e] = __uint_as_float((e & 1) ? (w[e / 2] & 0xffff0000u) : (w[e / 2] << 16));
-            float amax = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float scale = __fdiv_rn(amax, 448.f);
-            uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float q = scale > 0.f ? __fdiv_rn(x[e], scale) : 0.f;
-                const uint32_t code = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
-                packed[e / 4] |= code << (8 * (e & 3));
-            }
-            *reinterpret_cast<uint2 *>(lb + off8_code(v, H, sd.ptok, head, row) + lane * 8) =
-                make_uint2(packed[0], packed[1]);
+            uint2 codes;
+            const float scale = quantize_row8(__ldg(reinterpret_cast<const uint4 *>(src) + lane), &codes);
+            *reinterpret_cast<uint2 *>(lb + off8_code(v, H, sd.ptok, head, row) + lane * 8) = codes;
             if (lane == 0)
                 *reinterpret_cast<float *>(lb + off8_scale(v, H, sd.ptok, head, row)) = scale;
         } else if (lane < c.idx_dim / kChunk) {

@@ -57,6 +57,9 @@ struct Decode8Args {
     const uint16_t *q;
     uint16_t *out;
     float *ws;
+    const uint16_t *k_new;  // fused store of the new tokens (quantized here), or null
+    const uint16_t *v_new;
+    const uint16_t *ik_new;
 };
 
 // Two e4m3 codes (low byte first) to an f16 pair, exactly.
@@ -100,7 +103,7 @@ __device__ __forceinline__ float sum_over_g(float v) {
     return v + __shfl_xor_sync(0xffffffffu, v, 16);
 }
 
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __maxnreg__(192)
     decode8_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
                     const Decode8Args a) {
     extern __shared__ uint8_t sm8_raw[];
@@ -134,9 +137,13 @@ __global__ void __launch_bounds__(kThreads8, 1)
     }
     __syncthreads();
 
+    const bool fuse = a.k_new != nullptr;
+
     // Stage tile t of this warp's slice into its slot: lane i (and i + 16)
     // looks key i up once; 16 rows of K codes, 16 of V codes, 16 K and 16 V
-    // scales, all completing on the slot's barrier.
+    // scales, all completing on the slot's barrier.  With a fused store, the
+    // rows of new positions are quantized here from k_new / v_new (the same
+    // rule as pkv_store), written to the cache and to the stage directly.
     auto issue = [&](int t) {
         const int kt = key0 + (ks + t * ks_n) * kT8;
         const int slot = warp * kDepth8 + t % kDepth8;
@@ -146,18 +153,85 @@ __global__ void __launch_bounds__(kThreads8, 1)
         const int key = min(kt + (lane & 15), key1 - 1);
         int64_t pg = 0;
         int32_t row = key;
+        bool bad = false;
         if (sd.table) {
             const int page = key / sd.ptok;
             row = key - page * sd.ptok;
             const int id = __ldg(sd.table + page);
-            if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages))
+            if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
                 pg = 2 * (int64_t)id * sd.ps;
-            else if (c.status && lane < 16)
-                atomicOr(c.status, PKV_DEV_BAD_PAGE);
+            } else {
+                bad = true;
+                if (c.status && lane < 16) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+            }
         }
         const int64_t kc = pg + off8_code(false, H, sd.ptok, kvh, row);
         const int64_t vc = pg + off8_code(true, H, sd.ptok, kvh, row);
-        if (map != nullptr && kt + kT8 <= key1) {
+        if (fuse && min(kt + kT8, key1) - 1 >= qbase) {
+            // a tile holding new positions: cached rows copied key by key,
+            // new rows quantized by the whole warp, one row at a time
+            const bool fresh = key >= qbase;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int item = lane + 32 * i, rr = item >> 4, ch = item & 15;
+                const int64_t krr = shfl64(kc, rr), vrr = shfl64(vc, rr);
+                const bool frr = __shfl_sync(0xffffffffu, fresh, rr);
+                if (!frr) {
+                    cp_async16(st + sw8(rr, ch), base + krr + 16 * ch, pol);
+                    cp_async16(st + kCodes8 + sw8(rr, ch), base + vrr + 16 * ch, pol);
+                }
+            }
+            if (!fresh) cp_async4(sc + 4 * lane, base + pg + off8_scale(lane >= 16, H, sd.ptok, kvh, row));
+            // rows past the split's end repeat its last key, masked in the
+            // softmax: zero codes and scales keep them finite without work
+            const unsigned past = __ballot_sync(0xffffffffu, lane < 16 && kt + lane >= key1);
+            unsigned todo = __ballot_sync(0xffffffffu, fresh && lane < 16) & ~past;
+            if (past) {
+                for (int rr = __ffs(past) - 1; rr < kT8; ++rr) {
+                    *reinterpret_cast<uint2 *>(st + sw8(rr, lane >> 1) + (lane & 1) * 8) = make_uint2(0u, 0u);
+                    *reinterpret_cast<uint2 *>(st + kCodes8 + sw8(rr, lane >> 1) + (lane & 1) * 8) = make_uint2(0u, 0u);
+                }
+                if (lane < 16 && ((past >> lane) & 1u)) {
+                    reinterpret_cast<float *>(sc)[lane] = 0.f;
+                    reinterpret_cast<float *>(sc)[16 + lane] = 0.f;
+                }
+            }
+            while (todo) {
+                const int rr = __ffs(todo) - 1;
+                todo &= todo - 1;
+                const int p = kt + rr;                           // its position
+                const bool write = !__shfl_sync(0xffffffffu, bad, rr);
+                const int64_t tr = (int64_t)sd.tok_off + (p - qbase);  // its packed input row
+                const int64_t pg_rr = shfl64(pg, rr);
+                const int row_rr = __shfl_sync(0xffffffffu, row, rr);
+                const bool ik_row = write && kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8;
+                // the row's inputs load together: one round trip
+                const uint4 in_k = __ldg(reinterpret_cast<const uint4 *>(a.k_new + (tr * H + kvh) * kHeadDim) + lane);
+                const uint4 in_v = __ldg(reinterpret_cast<const uint4 *>(a.v_new + (tr * H + kvh) * kHeadDim) + lane);
+                const uint4 in_ik = ik_row ? __ldg(reinterpret_cast<const uint4 *>(a.ik_new + tr * c.idx_dim) + lane)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                    uint2 codes;
+                    const float scale = quantize_row8(v ? in_v : in_k, &codes);
+                    *reinterpret_cast<uint2 *>(st + (v ? kCodes8 : 0) + sw8(rr, lane >> 1) + (lane & 1) * 8) = codes;
+                    if (lane == 0) reinterpret_cast<float *>(sc)[16 * v + rr] = scale;
+                    if (write) {
+                        uint8_t *lb = const_cast<uint8_t *>(base) + pg_rr;
+                        *reinterpret_cast<uint2 *>(lb + off8_code(v, H, sd.ptok, kvh, row_rr) + 8 * lane) = codes;
+                        if (lane == 0) *reinterpret_cast<float *>(lb + off8_scale(v, H, sd.ptok, kvh, row_rr)) = scale;
+                    }
+                }
+                if (ik_row) {
+                    // the indexer-key row of the position, written once (KV head 0)
+                    uint8_t *idst = const_cast<uint8_t *>(base) + pg_rr + 2 * off_ik_f(true, H, c.idx_dim, sd.ptok, row_rr);
+                    reinterpret_cast<uint4 *>(idst)[lane] = in_ik;
+                }
+            }
+            cp_async_mbar_arrive(bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+        } else if (map != nullptr && kt + kT8 <= key1) {
             // one page holds the 16 keys (page size a multiple of 16, tiles
             // start on 16): their code rows and scales are contiguous runs
             const int yk = static_cast<int>(sd.layer_row + shfl64(kc, 0) / 256);
@@ -198,7 +272,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
     }
     pdl_wait();
     __syncthreads();
-    pdl_trigger();
+    if (!fuse) pdl_trigger();  // with a fused store: once the new rows are written
     for (; issued < kDepth8 && issued < my_tiles; ++issued) issue(issued);
 
     // the queries of this thread's B-operand column, in the permuted dim order
@@ -339,7 +413,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
     }
 
     // ---- merge the key slices of each column group in a fixed order ----
+    if (fuse) __threadfence();  // stored rows visible before the next kernel starts
     __syncthreads();
+    if (fuse) pdl_trigger();
     const int NC = ncg * 8;
     float *mbuf = reinterpret_cast<float *>(sm8);  // [ks][NC][kMS8]
     float *mlb = mbuf + ks_n * NC * kMS8;          // [ks][NC][2]
@@ -414,7 +490,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
 }  // namespace
 
 int launch_decode8(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
-                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream) {
+                   const uint16_t *q, uint16_t *out, float *ws, const uint16_t *k_new,
+                   const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(decode8_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -424,7 +501,7 @@ int launch_decode8(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
             return PKV_ECUDA;
         attr_set = true;
     }
-    Decode8Args a{q, out, ws};
+    Decode8Args a{q, out, ws, k_new, v_new, ik_new};
     cudaError_t e =
         launch_pdl(decode8_partial, plan.total_items, kThreads8, kSmem8, stream, c, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;

@@ -7,6 +7,7 @@
 #include <utility>
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "pkv_internal.h"
 
@@ -202,6 +203,36 @@ __device__ __forceinline__ float bf16_hi(uint32_t packed) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// e4m3 quantization of one 256-element bf16 row spread over a warp, eight
+// elements a lane in row order (#1170, commit 5c09685: a row's e4m3 codes and
+// float32 scale; the scale rule is the plainest reading): scale = max|x| / 448,
+// code = the e4m3 value nearest x / scale (float32 division with IEEE
+// rounding, ties to even, saturating); an all-zero row has scale 0 and codes 0.
+// Returns the scale (the same on every lane); *codes gets the lane's 8 codes,
+// low byte first.
+__device__ __forceinline__ float quantize_row8(const uint4 u, uint2 *codes) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        x[e] = __uint_as_float((e & 1) ? (w[e / 2] & 0xffff0000u) : (w[e / 2] << 16));
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 448.f);
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float q = scale > 0.f ? __fdiv_rn(x[e], scale) : 0.f;
+        const uint32_t code = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+        packed[e / 4] |= code << (8 * (e & 3));
+    }
+    *codes = make_uint2(packed[0], packed[1]);
+    return scale;
 }
 
 // Programmatic dependent launch: wait for the previous grid's results, and

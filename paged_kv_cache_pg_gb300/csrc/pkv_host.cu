@@ -368,11 +368,12 @@ extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
         return PKV_EINVAL;
     DecodeMaps maps;  // copied into the launch's parameters
     plan_maps(c, L, seqs, maps);
-    if (c.kv_fp8) {
-        if (k_new) return PKV_EINVAL;  // the e4m3 decode reads rows already stored
+    if (c.kv_fp8)
         return launch_decode8(c, plan, maps, static_cast<const uint16_t *>(q),
-                              static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
-    }
+                              static_cast<uint16_t *>(out), static_cast<float *>(ws),
+                              static_cast<const uint16_t *>(k_new),
+                              static_cast<const uint16_t *>(v_new),
+                              k_new ? static_cast<const uint16_t *>(ik_new) : nullptr, stream);
     return launch_decode(c, plan, maps, false, static_cast<const uint16_t *>(q), nullptr, 0,
                          static_cast<uint16_t *>(out), static_cast<float *>(ws),
                          static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
@@ -400,11 +401,12 @@ extern "C" int pkv_decode_static(const pkv_layout *L, const pkv_seq *seqs, int32
     if (rc) return rc;
     DecodeMaps maps;
     plan_maps(c, L, seqs, maps);
-    if (c.kv_fp8) {
-        if (k_new) return PKV_EINVAL;
+    if (c.kv_fp8)
         return launch_decode8(c, plan, maps, static_cast<const uint16_t *>(q),
-                              static_cast<uint16_t *>(out), static_cast<float *>(scratch), stream);
-    }
+                              static_cast<uint16_t *>(out), static_cast<float *>(scratch),
+                              static_cast<const uint16_t *>(k_new),
+                              static_cast<const uint16_t *>(v_new),
+                              k_new ? static_cast<const uint16_t *>(ik_new) : nullptr, stream);
     return launch_decode(c, plan, maps, false, static_cast<const uint16_t *>(q), nullptr, 0,
                          static_cast<uint16_t *>(out), static_cast<float *>(scratch),
                          static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),

@@ -167,9 +167,11 @@ int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
 int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, uint16_t *out,
                    float *ws, cudaStream_t stream);
 // Decode over e4m3 K/V (pkv_decode8.cu): the same plan and partial layout as
-// the bf16 decode, merged by the same combine kernel.
+// the bf16 decode, merged by the same combine kernel; with k_new, the new
+// rows are quantized and stored by the same call.
 int launch_decode8(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
-                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream);
+                   const uint16_t *q, uint16_t *out, float *ws, const uint16_t *k_new,
+                   const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream);
 
 // Fixed scratch of pkv_decode_static (pkv_decode.cu): its size, and its
 // device address on the current device (looked up on the first call there).

@@ -6,8 +6,10 @@ Bars: the store's bytes (codes, scales, indexer rows) equal the oracle's
 quantization bit for bit; gathered codes and scales equal the oracle's;
 decode rows are within |gpu - ref| <= 1e-3 + 2e-3 |ref| (+ half a bf16 ulp)
 of the float64 dequantizing oracle; paged output equals contiguous output
-bit for bit; pooling and block scores on an e4m3 layout equal the oracle's
-bits; calls the format does not support refuse it.
+bit for bit; a decode that stores its new rows itself leaves the bytes of
+the store and gives the outputs of a store and a decode; pooling and block
+scores on an e4m3 layout equal the oracle's bits; calls the format does not
+support refuse it.
 """
 import numpy as np
 import pytest
@@ -157,19 +159,67 @@ def test_e4m3_decode_static_matches_decode(multi8):
     assert np.array_equal(host_u16(out), base)
 
 
-def test_e4m3_refuses_fused_store_and_sparse():
+@pytest.mark.parametrize("ptok", [16, 48, None])
+def test_e4m3_fused_store_decode_equals_store_then_decode(ptok):
+    # The decode call quantizes and stores its new rows itself: the cache
+    # bytes equal the oracle's placement (so pkv_store's quantization, bit for
+    # bit) and the outputs equal a pkv_store followed by a pkv_decode.
+    # Lengths put a split boundary (multiples of 256 keys) inside the
+    # 4-token window of the first stream.
+    t = torch()
+    lay = _lay()
+    lens = [258, 516, 1000, 37]
+    nq, layer = 4, 1
+    full = _streams(lens, seed=3100)
+    q = [synth.queries(3150 + i, nq, 16, 256) for i in range(len(lens))]
+    kn = dev_u16(np.concatenate([s.k[layer][-nq:] for s in full]))
+    vn = dev_u16(np.concatenate([s.v[layer][-nq:] for s in full]))
+    ikn = dev_u16(np.concatenate([s.ik[layer][-nq:] for s in full]))
+    dq = dev_u16(np.concatenate(q))
+    outs = []
+    for fused in (False, True):
+        pl = place(lay, full, ptok, seed=9)
+        # blank the window's K/V codes, scales and indexer rows (0x7f: an
+        # e4m3 NaN code, a huge scale)
+        for i, T in enumerate(lens):
+            body = pl.body(0 if ptok else i)
+            tab = pl.tables[i] if ptok else None
+            b8 = body.view(t.uint8)
+            for p in range(T - nq, T):
+                for kind, heads, nbytes in ((pkv.K, 2, 256), (pkv.V, 2, 256), (pkv.KS, 2, 4),
+                                            (pkv.VS, 2, 4)):
+                    for h in range(heads):
+                        off = pkv.pg_row(lay, pl.pgs[i], tab, layer, kind, h, p)
+                        b8[off:off + nbytes] = 0x7f
+                off = pkv.pg_row(lay, pl.pgs[i], tab, layer, pkv.IK, 0, p)
+                b8[off:off + 256] = 0x7f
+        seqs = pl.seqs(lens, [nq] * len(lens))
+        out = t.zeros_like(dq)
+        ws = t.zeros(pkv.decode_ws_size(lay, seqs, 16) // 4 + 64, dtype=t.float32, device="cuda")
+        if fused:
+            pkv.decode(lay, seqs, layer, 16, dq, out, ws, k_new=kn, v_new=vn, ik_new=ikn)
+        else:
+            pkv.store(lay, seqs, layer, kn, vn, ikn)
+            pkv.decode(lay, seqs, layer, 16, dq, out, ws)
+        t.cuda.synchronize()
+        outs.append(host_u16(out))
+        for i in range(len(pl.buffers)):
+            assert np.array_equal(host_u16(pl.body(i)), pl.oarenas[i])
+        assert pl.guards_intact()
+    assert np.array_equal(outs[0], outs[1])
+    ref_pl = place(lay, full, None)
+    ok, worst = within_tol(outs[1], oracle_decode(ref_pl, layer, 16, q))
+    assert ok, worst
+
+
+def test_e4m3_refuses_sparse():
     t = torch()
     lay = _lay(1, 2, 128)
     streams = _streams([64], 1, seed=3000)
     pl = place(lay, streams, 16, seed=1)
     seqs = pl.seqs([64], [1])
     q = t.zeros((1, 16, 256), dtype=t.int16, device="cuda")
-    rows = t.zeros((1, 2, 256), dtype=t.int16, device="cuda")
     ws = t.zeros(1 << 16, dtype=t.float32, device="cuda")
-    with pytest.raises(pkv.PkvError) as e:
-        pkv.decode(lay, seqs, 0, 16, q, t.zeros_like(q), ws, k_new=rows, v_new=rows,
-                   ik_new=t.zeros((1, 128), dtype=t.int16, device="cuda"))
-    assert e.value.code == pkv.EINVAL
     ids = t.zeros((1, 16, 4), dtype=t.int32, device="cuda")
     with pytest.raises(pkv.PkvError) as e:
         pkv.sparse_decode(lay, seqs, 0, 16, q, ids, 4, t.zeros_like(q), ws)
