@@ -590,30 +590,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Combine a unit's split partials for one query column:
 // M = max m_i, L = sum 2^(m_i-M) l_i, O = sum 2^(m_i-M) acc_i, out = O / L.
-// Two CTAs per column, each 128 dims.  The CTA's threads form two groups of
-// 128 (one thread a dim): group 0 sums the first ceil(ns/2) splits, group 1
-// the rest, each in split order, and O = O_0 + O_1.  Every thread loads all
-// its splits' values at once (up to 32) while the split maxima load, so one
-// memory round trip covers a column of up to 64 splits.  At most 64
-// registers a thread: a combine CTA then fits on an SM beside a partial CTA
-// of the next call, which can start streaming its keys without waiting for
-// the SM.
+// A column of a stream with up to 32 splits is one CTA, a thread a dim; past
+// 32 splits it is two CTAs of 128 dims whose threads form two groups of 128
+// (one thread a dim): group 0 sums the first ceil(ns/2) splits, group 1 the
+// rest, and O = O_0 + O_1 (comb_ctas).  Every sum runs in split order.  A
+// thread loads all its splits' values at once (up to 32) while the split
+// maxima load, so one memory round trip covers a column of up to 64 splits.
+// At most 64 registers a thread: a combine CTA then fits on an SM beside a
+// partial CTA of the next call, which can start streaming its keys without
+// waiting for the SM.
 template <bool kSparse>
 __global__ void __launch_bounds__(kCombThreads, 4)
     decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
     constexpr int kBatch = 32;
-    constexpr int kDims = kHeadDim / 2;   // dims of one CTA
     extern __shared__ float comb_smem[];  // w[ns], lsum[ns]
     __shared__ float sh_l;
-    __shared__ float sh_o[kDims];
+    __shared__ float sh_o[kHeadDim / 2];
     pdl_wait();
     pdl_trigger();
-    const int item = blockIdx.x >> 1;  // (unit, column) of the call
-    const int s = find_seq(c.n_seqs, item, [&](int t) { return c.seq[t].comb_off; });
+    const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
     const SeqDev &sd = c.seq[s];
-    const int r = item - sd.comb_off;
-    const int unit = r / sd.ncols, col = r - unit * sd.ncols;
     const int ns = sd.nsplit;
+    const int halves = comb_ctas(ns);
+    const int r = (blockIdx.x - sd.comb_off) / halves;  // (unit, column) of the stream
+    const int unit = r / sd.ncols, col = r - unit * sd.ncols;
     float *w = comb_smem, *lsum = comb_smem + ns;
     const int units = kSparse ? c.n_q_heads : c.n_kv_heads;
     const float *part_acc = a.ws + sd.ws_off;
@@ -621,10 +621,11 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
     const int64_t stride = (int64_t)sd.ncols * kHeadDim;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int grp = tid / kDims, dd = tid - grp * kDims;
-    const int d = (blockIdx.x & 1) * kDims + dd;
-    const int half = (ns + 1) >> 1;
-    const int i0 = grp ? half : 0, i1 = grp ? ns : half;  // this group's splits
+    // two CTAs: 128 dims each, thread t in group t >> 7; one CTA: all 256 dims, one group
+    const int grp = halves == 2 ? tid >> 7 : 0, dd = halves == 2 ? tid & 127 : tid;
+    const int d = halves == 2 ? (((blockIdx.x - sd.comb_off) & 1) << 7) + dd : dd;
+    const int i0 = halves == 2 && grp ? (ns + 1) >> 1 : 0;  // this group's splits
+    const int i1 = halves == 2 && !grp ? (ns + 1) >> 1 : ns;
     const float *col_acc = part_acc + p0 * kHeadDim + d;
     float xs[kBatch];
 #pragma unroll
@@ -660,10 +661,12 @@ __global__ void __launch_bounds__(kCombThreads, 4)
         for (int j = 0; j < kBatch; ++j)
             if (b + j < i1) O += w[b + j] * xs[j];
     }
-    if (grp == 1) sh_o[dd] = O;
-    __syncthreads();
-    if (grp == 1) return;
-    O += sh_o[dd];
+    if (halves == 2) {
+        if (grp == 1) sh_o[dd] = O;
+        __syncthreads();
+        if (grp == 1) return;
+        O += sh_o[dd];
+    }
     const float L = sh_l;
     const float o = L > 0.f ? O / L : 0.f;
     Unit u;
@@ -671,7 +674,7 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     u.kvh = kSparse ? unit / c.group : unit;
     a.out[q_row<kSparse>(c, sd, u, col) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
 }
-static_assert(kCombThreads == kHeadDim, "two groups of one thread a dim, half the dims a CTA");
+static_assert(kCombThreads == kHeadDim, "a thread a dim (one group), or two groups of half the dims");
 
 }  // namespace
 
@@ -730,7 +733,7 @@ int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
         d.split_len = sl;
         items += units * ns;
         if (ns > 1) {
-            comb += units * d.ncols;
+            comb += units * d.ncols * comb_ctas(ns);
             floats += (int64_t)units * ns * d.ncols * (kHeadDim + 2);
             floats = (floats + 63) / 64 * 64;
         }
@@ -765,7 +768,7 @@ int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, u
     DecodeArgs a{q, out, ws, nullptr, 0, nullptr, nullptr, nullptr};
     int max_ns = 1;
     for (int s = 0; s < c.n_seqs; ++s) max_ns = std::max(max_ns, c.seq[s].nsplit);
-    return launch_status(launch_pdl(decode_combine<false>, 2 * plan.total_comb, kCombThreads,
+    return launch_status(launch_pdl(decode_combine<false>, plan.total_comb, kCombThreads,
                                     2 * max_ns * sizeof(float), stream, c, a));
 }
 
@@ -791,7 +794,7 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     if (plan.total_comb > 0) {
         int max_ns = 1;
         for (int s = 0; s < cc.n_seqs; ++s) max_ns = std::max(max_ns, cc.seq[s].nsplit);
-        e = launch_pdl(comb, 2 * plan.total_comb, kCombThreads, 2 * max_ns * sizeof(float), stream, cc, a);
+        e = launch_pdl(comb, plan.total_comb, kCombThreads, 2 * max_ns * sizeof(float), stream, cc, a);
         if (e != cudaSuccess) return PKV_ECUDA;
     }
     return PKV_OK;

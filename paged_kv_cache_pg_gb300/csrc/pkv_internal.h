@@ -148,7 +148,7 @@ int launch_pool(const Common &c, int32_t total_blocks, cudaStream_t stream);
 
 struct DecodePlan {
     int32_t total_items;   // CTAs of the partial kernel
-    int32_t total_comb;    // (unit, query column) rows the combine kernel merges
+    int32_t total_comb;    // CTAs of the combine kernel
     size_t ws_bytes;       // counters + partials
 };
 int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan);
@@ -164,6 +164,11 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
 int plan_prefill(Common &c, int nsm, DecodePlan *plan);
 int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
                    const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream);
+// CTAs the combine gives one (unit, query column) of a stream with ns splits:
+// two (each half the dims, the splits in two groups) past 32 splits, where
+// one thread would need a second round of loads; one otherwise.  It depends
+// only on the stream's own split count.
+__host__ __device__ inline int comb_ctas(int ns) { return ns > 32 ? 2 : 1; }
 int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, uint16_t *out,
                    float *ws, cudaStream_t stream);
 // Decode over e4m3 K/V (pkv_decode8.cu): the same plan and partial layout as

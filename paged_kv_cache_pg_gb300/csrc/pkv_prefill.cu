@@ -548,7 +548,7 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         d.split_len = sl;
         items += H * mtiles * ns;
         if (ns > 1) {
-            comb += H * d.ncols;
+            comb += H * d.ncols * comb_ctas(ns);
             floats += (int64_t)H * ns * d.ncols * (kHeadDim + 2);
             floats = (floats + 63) / 64 * 64;
         }
