@@ -1,6 +1,9 @@
-// Cache store, gather and block pooling.  Rows are located with pg_at once
-// per row (store, gather) or once per block of four positions (pool: a page
-// holds whole blocks because its size is a multiple of 4), never per load.
+// Cache store, gather and block pooling, for the bf16 and the e4m3 K/V
+// formats (the e4m3 store quantizes each new K and V row).  Rows are located
+// with pg_at once per row (store, gather) or once per block of four positions
+// (pool: a page holds whole blocks because its size is a multiple of 4),
+// never per load.  Stores let the next kernel start only once their rows are
+// visible: a decode may read cached rows before its grid-dependency wait.
 #include "pkv_dev.cuh"
 
 namespace pkv {

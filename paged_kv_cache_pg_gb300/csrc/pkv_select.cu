@@ -1,10 +1,11 @@
 // Block scores over pooled rows and top-k block selection.
 //
-// Scores: one thread per (head, block) runs the float32 chain
-// acc = fmaf(qi[d], P[b][d], acc), d = 0 .. Di-1 (the order is part of the
-// result: a top-k decision downstream must see the same bits on any cache
-// layout).  Pooled rows are looked up once per block (pg_at on its first
-// position) and staged in shared memory.
+// Scores: each (head, block) score is the float32 chain
+// acc = fmaf(qi[d], P[b][d], acc), d = 0 .. Di-1, run by one thread (the
+// order is part of the result: a top-k decision downstream must see the same
+// bits on any cache layout); a thread runs four such chains side by side.
+// Pooled rows are looked up once per block (pg_at on its first position) and
+// staged in shared memory with 16-byte loads.
 //
 // Top-k: one CTA per (stream, head) finds the k-th largest score by an 8-bit
 // radix select on order-preserving keys (held in shared memory when the row
