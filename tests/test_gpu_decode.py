@@ -129,6 +129,23 @@ def test_ragged_lengths(length):
             assert ok, worst
 
 
+def test_sixty_four_streams_in_one_launch():
+    # The most streams a launch takes, every one with its own table and
+    # length (ragged, 1 to 300 positions), pages of 16 through one arena:
+    # each row within the oracle's bound, paged bits equal to contiguous.
+    lay = pkv.layout(1, 2, 256, 128)
+    lens = [1 + (37 * i) % 300 for i in range(64)]
+    streams = _streams(lens, 1, 2, seed=2000)
+    q = [synth.queries(2100 + i, 1, 16, 256) for i in range(64)]
+    paged = place(lay, streams, 16, seed=5)
+    cont = place(lay, streams, None)
+    a = decode(paged, 0, 16, q)
+    assert np.array_equal(a, decode(cont, 0, 16, q))
+    ok, worst = within_tol(a, oracle_decode(cont, 0, 16, q))
+    assert ok, worst
+    assert paged.guards_intact()
+
+
 def test_empty_batch_and_no_query_streams_launch_nothing():
     import oracle as orc
     t = torch()
