@@ -62,8 +62,7 @@ constexpr size_t kOffBar = kOffPage + ((kMaxPages + 1) & ~1) * 8;
 constexpr size_t kSmemBytes = 1024 + kOffBar + 2 * kSlots * 8 + 16;  // + alignment slack
 static_assert(kMaxPages >= kMaxSparseBlocks, "the page list also holds block rows");
 static_assert(kSlots % (kWarps / 2) == 0, "every key slice gets the same number of slots");
-static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * (2 + kWarps / 2) * 4 + 64 <=
-                  kSlots * kStageBytes,
+static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * 2 * 4 <= kSlots * kStageBytes,
               "merge buffers reuse the stages");
 
 struct DecodeArgs {
@@ -521,9 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int NC = ncg * 8;
     float *mbuf = reinterpret_cast<float *>(x.stages);            // [ks][NC][kMergeStride]
     float *mlb = mbuf + ks_n * NC * kMergeStride;                  // [ks][NC][2]
-    float *wts = mlb + ks_n * NC * 2;                              // [ks][NC]
-    float *lt = wts + ks_n * NC;                                   // [NC]
-    float *mout = lt + NC;                                         // [NC]
     if (active) {
         const int c0 = cg * 8 + 2 * (lane & 3);
         float *b0 = mbuf + (ks * NC + c0) * kMergeStride;
@@ -544,38 +540,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    if (tid < NC) {
-        float M = -INFINITY;
-        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + tid) * 2]);
-        float L = 0.f;
-        for (int k = 0; k < ks_n; ++k) {
-            const float w = M == -INFINITY ? 0.f : ex2(mlb[(k * NC + tid) * 2] - M);
-            wts[k * NC + tid] = w;
-            L += w * mlb[(k * NC + tid) * 2 + 1];
-        }
-        lt[tid] = L;
-        mout[tid] = M;
-    }
-    __syncthreads();
 
     const bool single = sd.nsplit == 1;
     const int units = kSparse ? c.n_q_heads : c.n_kv_heads;
     float *part_acc = a.ws + sd.ws_off;
     float *part_ml = part_acc + (int64_t)units * sd.nsplit * ncols * kHeadDim;
     const int64_t pidx = ((int64_t)u.unit * sd.nsplit + u.split) * ncols;
-    // four consecutive dims a thread: O = sum over slices in order
+    // four consecutive dims a thread: the slices' weights of the column
+    // (each thread of a column computes the same ones), O = sum over slices in order
     for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
         const int col = idx / (kHeadDim / 4), d = 4 * (idx - col * (kHeadDim / 4));
+        float M = -INFINITY;
+        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + col) * 2]);
+        float L = 0.f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < ks_n; ++k) {
-            const float w = wts[k * NC + col];
+            const float w = M == -INFINITY ? 0.f : ex2(mlb[(k * NC + col) * 2] - M);
+            L += w * mlb[(k * NC + col) * 2 + 1];
             const float4 v = *reinterpret_cast<const float4 *>(mbuf + (k * NC + col) * kMergeStride + d);
             O.x += w * v.x;
             O.y += w * v.y;
             O.z += w * v.z;
             O.w += w * v.w;
         }
-        const float L = lt[col];
         if (single) {
             const float inv = L > 0.f ? 1.f : 0.f;
             const float lz = L > 0.f ? L : 1.f;
@@ -586,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
             *reinterpret_cast<float4 *>(part_acc + (pidx + col) * kHeadDim + d) = O;
             if (d == 0) {
-                part_ml[(pidx + col) * 2 + 0] = mout[col];
+                part_ml[(pidx + col) * 2 + 0] = M;
                 part_ml[(pidx + col) * 2 + 1] = L;
             }
         }

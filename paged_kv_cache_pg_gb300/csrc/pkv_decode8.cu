@@ -419,9 +419,6 @@ __global__ void __maxnreg__(192)
     const int NC = ncg * 8;
     float *mbuf = reinterpret_cast<float *>(sm8);  // [ks][NC][kMS8]
     float *mlb = mbuf + ks_n * NC * kMS8;          // [ks][NC][2]
-    float *wts = mlb + ks_n * NC * 2;              // [ks][NC]
-    float *lt = wts + ks_n * NC;                   // [NC]
-    float *mo = lt + NC;                           // [NC]
     if (active) {
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
@@ -439,36 +436,27 @@ __global__ void __maxnreg__(192)
         }
     }
     __syncthreads();
-    if (tid < NC) {
-        float M = -INFINITY;
-        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + tid) * 2]);
-        float L = 0.f;
-        for (int k = 0; k < ks_n; ++k) {
-            const float wk = M == -INFINITY ? 0.f : ex2(mlb[(k * NC + tid) * 2] - M);
-            wts[k * NC + tid] = wk;
-            L += wk * mlb[(k * NC + tid) * 2 + 1];
-        }
-        lt[tid] = L;
-        mo[tid] = M;
-    }
-    __syncthreads();
     const bool single = sd.nsplit == 1;
     float *part_acc = a.ws + sd.ws_off;
     float *part_ml = part_acc + (int64_t)H * sd.nsplit * ncols * kHeadDim;
     const int64_t pidx = ((int64_t)kvh * sd.nsplit + split) * ncols;
     for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads8) {
         const int col = idx / (kHeadDim / 4), d = 4 * (idx - col * (kHeadDim / 4));
+        // the slices' weights of the column (each thread of a column computes them)
+        float M = -INFINITY;
+        for (int k = 0; k < ks_n; ++k) M = fmaxf(M, mlb[(k * NC + col) * 2]);
+        float L = 0.f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         const int sd0 = d + (d >> 5);  // the four dims share one skew
         for (int k = 0; k < ks_n; ++k) {
-            const float wk = wts[k * NC + col];
+            const float wk = M == -INFINITY ? 0.f : ex2(mlb[(k * NC + col) * 2] - M);
+            L += wk * mlb[(k * NC + col) * 2 + 1];
             const float *v = mbuf + (k * NC + col) * kMS8 + sd0;
             O.x += wk * v[0];
             O.y += wk * v[1];
             O.z += wk * v[2];
             O.w += wk * v[3];
         }
-        const float L = lt[col];
         if (single) {
             const float inv = L > 0.f ? 1.f / L : 0.f;
             const int j = col / G;
@@ -480,7 +468,7 @@ __global__ void __maxnreg__(192)
         } else {
             *reinterpret_cast<float4 *>(part_acc + (pidx + col) * kHeadDim + d) = O;
             if (d == 0) {
-                part_ml[(pidx + col) * 2 + 0] = mo[col];
+                part_ml[(pidx + col) * 2 + 0] = M;
                 part_ml[(pidx + col) * 2 + 1] = L;
             }
         }
