@@ -56,7 +56,7 @@ ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3
 # the value the capture was taken with; reported as null otherwise.
 DECODE_TRAFFIC = {"bytes": 40385280,
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "17e46c324ca08d8d25141ecd6766308bac670ebfa56bcd6dcc330e768629e390"}
+                  "sha256": "18967d922d73dac45f2ae5501dcfa4ad0ba5d1c70480fc17f7af53033ef49d42"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
@@ -910,16 +910,25 @@ def main_ours(args):
 
 def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, status, lens_after,
             dev, args):
-    pages = args.page_list
     """Same step through the public calls, inputs from pinned host memory and
     outputs back to it, copies inside the timed region."""
-    S = len(lens_after)
-    h_q = torch.from_numpy(np.stack(q_host).view(np.int16)).pin_memory()
-    kv_rows = torch.stack([torch.stack([k.cpu(), v.cpu()]) for k, v in zip(k_new, v_new)]).pin_memory()
-    ik_rows = torch.stack([i.cpu() for i in ik_new]).pin_memory()
-    d_q = torch.empty(h_q.shape, dtype=torch.int16, device=dev)
-    d_kv = torch.empty(kv_rows.shape, dtype=torch.int16, device=dev)
-    d_ik = torch.empty(ik_rows.shape, dtype=torch.int16, device=dev)
+    pages = args.page_list
+    h_q = torch.from_numpy(np.stack(q_host).view(np.int16))
+    kv_rows = torch.stack([torch.stack([k.cpu(), v.cpu()]) for k, v in zip(k_new, v_new)])
+    ik_rows = torch.stack([i.cpu() for i in ik_new])
+    # the step's inputs, queries then new K/V rows then indexer rows, in one
+    # pinned buffer: one host-to-device copy a graph (every part starts on a
+    # 16-byte boundary)
+    nq, nkv, nik = h_q.numel(), kv_rows.numel(), ik_rows.numel()
+    assert (nq * 2) % 16 == 0 and ((nq + nkv) * 2) % 16 == 0
+    h_in = torch.empty(nq + nkv + nik, dtype=torch.int16).pin_memory()
+    h_in[:nq].copy_(h_q.reshape(-1))
+    h_in[nq:nq + nkv].copy_(kv_rows.reshape(-1))
+    h_in[nq + nkv:].copy_(ik_rows.reshape(-1))
+    d_in = torch.empty(h_in.shape, dtype=torch.int16, device=dev)
+    d_q = d_in[:nq].view(h_q.shape)
+    d_kv = d_in[nq:nq + nkv].view(kv_rows.shape)
+    d_ik = d_in[nq + nkv:].view(ik_rows.shape)
     h_out = torch.empty(h_q.shape, dtype=torch.int16).pin_memory()
     d_out = torch.empty(h_q.shape, dtype=torch.int16, device=dev)
     graphs = {}
@@ -927,9 +936,7 @@ def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, sta
         cf = confs[p]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            d_q.copy_(h_q, non_blocking=True)
-            d_kv.copy_(kv_rows, non_blocking=True)
-            d_ik.copy_(ik_rows, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
             for l in range(N_LAYERS):
                 pkv.decode(lay, step_seqs[p], l, HQ, d_q[l], d_out[l], cf["ws"], status=status,
                            k_new=d_kv[l, 0], v_new=d_kv[l, 1], ik_new=d_ik[l])
@@ -950,7 +957,7 @@ def e2e_arm(torch, pkv, lay, confs, step_seqs, q_host, k_new, v_new, ik_new, sta
         e1.synchronize()
         total += e0.elapsed_time(e1)
     step_bytes = sum(N_LAYERS * layer_bytes(lens_after, confs[p]["pages_used"]) for p in pages)
-    h2d = len(pages) * (h_q.numel() + kv_rows.numel() + ik_rows.numel()) * 2
+    h2d = len(pages) * h_in.numel() * 2
     d2h = len(pages) * h_out.numel() * 2
     return {"value": round(step_bytes / (total / n / 1e3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
