@@ -49,7 +49,8 @@ LENS = [1000, 3000, 6000, 9000]          # cached before the new token
 N_LAYERS, HQ, HKV, D, DI = 13, 16, 2, 256, 128
 PAGES = [16, 48, 128, 256, 512]
 NOMINAL_HBM = 8000.0
-ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3", "allocator"]
+ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3", "page_runs",
+        "allocator"]
 # DRAM bytes (read + write) of one pkv_decode call of the workload (partial +
 # combine kernels), from the ncu capture summarised in
 # profiles/decode_partial_pages256.md, valid while the decode sources hash to
@@ -624,6 +625,55 @@ def row_decode_e4m3(torch, pkv, dev, timer):
             "query_heads_per_s": round(N_LAYERS * len(LENS) * HQ / (ms / 1e3), 1)}
 
 
+def row_page_runs(torch, pkv, dev, timer):
+    """The page-run path against key-by-key copies: the multi-stream decode
+    (13 layer slots, the new token stored by the call) at pages of 16, whose
+    16-row page runs load as 2D TMA tiles, and at pages of 20, whose rows load
+    key by key with cp.async.  Each page size is one CUDA graph."""
+    lens_after = [L + 1 for L in LENS]
+    lay = pkv.layout(N_LAYERS, HKV, D, DI)
+    streams = [synth.make_stream(140 + i, N_LAYERS, L, HKV, D, DI) for i, L in enumerate(lens_after)]
+    new = [[_up(torch, dev, np.concatenate([getattr(st, f)[l][-1:] for st in streams]))
+            for f in ("k", "v", "ik")] for l in range(N_LAYERS)]
+    q = [_up(torch, dev, np.concatenate([synth.queries(160 + l * 4 + i, 1, HQ, D) for i in range(4)]))
+         for l in range(N_LAYERS)]
+    out = [torch.empty_like(x) for x in q]
+    res = {}
+    for ptok in (16, 20):
+        n_pages = sum(synth.pages_for(L, ptok) for L in lens_after) + 8
+        mem, tables, pgs = _paged(torch, pkv, lay, dev, ptok, lens_after, n_pages, 9)
+        for l in range(N_LAYERS):
+            pkv.store(lay, [pkv.seq(g, L, L) for g, L in zip(pgs, LENS)], l,
+                      *(_up(torch, dev, np.concatenate([getattr(st, f)[l][:-1] for st in streams]))
+                        for f in ("k", "v", "ik")))
+        sq = [pkv.seq(g, L, 1) for g, L in zip(pgs, lens_after)]
+        ws = torch.zeros(pkv.decode_ws_size(lay, sq, HQ) // 4 + 64, dtype=torch.float32, device=dev)
+
+        def step():
+            for l in range(N_LAYERS):
+                k_, v_, ik_ = new[l]
+                pkv.decode(lay, sq, l, HQ, q[l], out[l], ws, k_new=k_, v_new=v_, ik_new=ik_)
+
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        ms = timer.ms(g.replay, reps=30)
+        res[ptok] = ms * 1e3 / N_LAYERS
+        del g, mem, tables, pgs, ws
+        torch.cuda.empty_cache()
+    peak, kind = peaks()
+    b = decode_bytes(lens_after)
+    return {"workload": "multi-stream decode, 13 layer slots, new token stored by the call: pages of "
+                        "16 (16-row page runs by TMA) against pages of 20 (rows key by key)",
+            "us_per_layer": {"page_runs_p16": round(res[16], 2), "key_by_key_p20": round(res[20], 2)},
+            "GBps": {"page_runs_p16": round(b / res[16] / 1e3, 1),
+                     "key_by_key_p20": round(b / res[20] / 1e3, 1)},
+            "key_by_key_over_page_runs": round(res[20] / res[16], 4)}
+
+
 def row_allocator(torch, pkv, dev, timer):
     """Host cost of the page pool on the serving-mix arena (792 pages of 256,
     13 layers): a lane opens (a run of state pages claimed from the top, the
@@ -676,7 +726,7 @@ def _gather_all(torch, pkv, lay, seqs, T, dev):
 
 ROW_FNS = {"prefill": row_prefill, "sparse": row_sparse, "mix": row_mix,
            "decode_layer": row_decode_layer, "prompt_cache": row_prompt_cache,
-           "decode_e4m3": row_decode_e4m3, "allocator": row_allocator}
+           "decode_e4m3": row_decode_e4m3, "page_runs": row_page_runs, "allocator": row_allocator}
 
 
 def hot_path_rows(torch, pkv, dev, names, profile=False):
