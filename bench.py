@@ -249,6 +249,102 @@ def oracle_rows(seconds: float, max_rows: int = 1 << 30, part: int = 0, parts: i
     return credited, rows, el
 
 
+def oracle_row_rates(seconds: float):
+    """The oracle as it stands, one thread, on a bounded sample of each other
+    hot-path row's workload, each for about `seconds`: the CPU figure beside
+    the row's GPU figure, in the row's own units."""
+    import oracle as orc
+    orc.build()
+    out = {}
+    shape = orc.Shape(1, HKV, D, DI)
+    # chunked prefill: (query, head) rows of the 512-query chunk at 31,000
+    P0, C = 31000, 512
+    st = synth.make_stream(200, 1, P0 + C, HKV, D, DI)
+    cache = orc.contiguous(shape, P0 + C)
+    orc.put_rows(shape, cache, 0, orc.K, 0, st.k[0])
+    orc.put_rows(shape, cache, 0, orc.V, 0, st.v[0])
+    q = synth.queries(201, C, HQ, D)
+    rng = np.random.default_rng(0)
+    flop, rows, t0 = 0.0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        j, h = int(rng.integers(C)), int(rng.integers(HQ))
+        orc.attend_row(shape, cache, 0, HQ, h, P0 + j, q[j, h])
+        flop += 4.0 * (P0 + j + 1) * D
+        rows += 1
+    el = time.perf_counter() - t0
+    out["prefill"] = {"value": round(flop / el / 1e12, 6), "unit": "TFLOP/s",
+                      "query_heads_per_s": round(rows / el, 1),
+                      "sample": f"{rows} random (query, head) rows of the chunk ({el:.1f} s)"}
+    del cache, st
+    # block-sparse step: pool, scores, top-64 and sparse attention of whole streams of 9,000
+    T = 9000
+    st = synth.make_stream(210, 1, T, HKV, D, DI)
+    cache = orc.contiguous(shape, T)
+    for kind, arr in ((orc.K, st.k[0]), (orc.V, st.v[0]), (orc.IK, st.ik[0])):
+        orc.put_rows(shape, cache, 0, kind, 0, arr)
+    qi = synth.normal_bf16(211, (HQ, DI))
+    qs = synth.queries(212, 1, HQ, D)[0]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        orc.pool(shape, cache, 0, 0, T // 4)
+        sc = orc.scores(shape, cache, 0, HQ, T, qi)
+        ids = orc.topk(sc, 64)
+        orc.sparse_attend(shape, cache, 0, HQ, T, qs, ids)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    out["sparse"] = {"value": round(n / el, 2), "unit": "streams a second",
+                     "us_per_stream": round(el / n * 1e6, 1),
+                     "query_heads_per_s": round(n * HQ / el, 1),
+                     "sample": f"{n} streams of 9,000 positions, 16 heads each ({el:.1f} s)"}
+    del cache, st
+    # e4m3 decode: one query token, 16 heads, over e4m3 rows of 9,001 positions
+    T = 9001
+    shape8 = orc.Shape(1, HKV, D, DI, orc.E4M3)
+    st = synth.make_stream(220, 1, T, HKV, D, DI)
+    cache = orc.contiguous(shape8, -(-T // 4) * 4)
+    orc.put_rows8(shape8, cache, 0, orc.K, 0, st.k[0])
+    orc.put_rows8(shape8, cache, 0, orc.V, 0, st.v[0])
+    q8 = synth.queries(221, 1, HQ, D)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        orc.attend(shape8, cache, 0, HQ, T, q8)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    b8 = T * HKV * 2 * (D + 4) + HQ * D * 2 * 2
+    out["decode_e4m3"] = {"value": round(n * b8 / el / 1e9, 4), "unit": "GB/s",
+                          "query_heads_per_s": round(n * HQ / el, 1),
+                          "sample": f"{n} decodes of one token, 16 heads, 9,001 e4m3 positions "
+                                    f"({el:.1f} s)"}
+    del cache, st
+    # prompt-cache save: a 31,512-position stream in pages of 256 gathered to the contiguous form
+    T = 31512
+    st = synth.make_stream(230, 1, T, HKV, D, DI)
+    ptok = 256
+    npg = synth.pages_for(T, ptok)
+    table = np.ascontiguousarray(synth.shuffled_tables(231, npg, [npg])[0], dtype=np.int32)
+    arena = np.zeros(npg * orc.page_elems(shape, ptok), np.uint16)
+    cache = orc.paged(shape, arena, ptok, table)
+    for kind, arr in ((orc.K, st.k[0]), (orc.V, st.v[0]), (orc.IK, st.ik[0])):
+        orc.put_rows(shape, cache, 0, kind, 0, arr)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        for kind in (orc.K, orc.V, orc.IK):
+            orc.get_rows(shape, cache, 0, kind, 0, T)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    gb = 2 * T * (2 * HKV * D + DI) * 2
+    out["prompt_cache"] = {"value": round(n * gb / el / 1e9, 4), "unit": "GB/s",
+                           "sample": f"{n} gathers of K, V and indexer rows of one layer "
+                                     f"({el:.1f} s)"}
+    return out
+
+
 def _oracle_worker(args):
     seconds, part, parts = args
     return oracle_rows(seconds, part=part, parts=parts)
@@ -934,6 +1030,8 @@ def main_ours(args):
         cpu["all_cores"] = {"value": round(c_all / el_all / 1e9, 4), "unit": "GB/s", "cores": n_all,
                             "sample": f"{r_all} rows, the (stream, head) rows split across "
                                       f"{n_all} processes ({el_all:.1f} s)"}
+        if rows is not None:
+            cpu["rows"] = oracle_row_rates(args.cpu_seconds / 5)
 
     launches = args.steps * sum(N_LAYERS * confs[p]["launches_per_layer"] for p in pages)
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
