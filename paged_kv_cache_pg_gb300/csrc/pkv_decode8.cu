@@ -284,12 +284,17 @@ __global__ void __maxnreg__(192)
             const int j = col / G;
             qr = a.q + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
         }
+        // dims 64 c4 .. 64 c4 + 63 of the row: eight 16-byte loads, two steps each
+        uint4 u[8];
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            uint2 u = make_uint2(0u, 0u);
-            if (qr) u = __ldg(reinterpret_cast<const uint2 *>(qr + 64 * c4 + 4 * kk));
-            qf[kk][0] = h2_bits(__floats2half2_rn(bf16_lo(u.x), bf16_hi(u.x)));
-            qf[kk][1] = h2_bits(__floats2half2_rn(bf16_lo(u.y), bf16_hi(u.y)));
+        for (int i = 0; i < 8; ++i)
+            u[i] = qr ? __ldg(reinterpret_cast<const uint4 *>(qr + 64 * c4) + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qf[2 * i][0] = h2_bits(__floats2half2_rn(bf16_lo(u[i].x), bf16_hi(u[i].x)));
+            qf[2 * i][1] = h2_bits(__floats2half2_rn(bf16_lo(u[i].y), bf16_hi(u[i].y)));
+            qf[2 * i + 1][0] = h2_bits(__floats2half2_rn(bf16_lo(u[i].z), bf16_hi(u[i].z)));
+            qf[2 * i + 1][1] = h2_bits(__floats2half2_rn(bf16_lo(u[i].w), bf16_hi(u[i].w)));
         }
     }
     const int colA = cg * 8 + 2 * c4, colB = colA + 1;
