@@ -361,6 +361,15 @@ int pkv_sparse_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_s
                       int32_t k, void *out, void *ws, size_t ws_bytes, int32_t *dev_status,
                       cudaStream_t stream);
 
+/* ---- diagnostics ------------------------------------------------------------
+ * Every pipeline wait in the kernels (a stage or product barrier) gives up
+ * after about a second, ORs PKV_DEV_TIMEOUT into *dev_status and returns, so
+ * a lost copy ends a launch with an error instead of hanging the GPU.  This
+ * call launches one warp whose wait on a barrier nothing arrives on runs out
+ * the same way (about a second of GPU time).  dev_status: a device int32,
+ * required (EINVAL if NULL). */
+int pkv_diag_wait_runs_out(int32_t *dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -62,7 +62,7 @@ EXPORTS = [
     "pkv_arena_set_event_ops", "pkv_run_pages", "pkv_run_take", "pkv_run_give", "pkv_run_map",
     "pkv_store", "pkv_gather", "pkv_pool", "pkv_decode_ws_size",
     "pkv_decode", "pkv_decode_static", "pkv_block_scores", "pkv_topk", "pkv_sparse_ws_size",
-    "pkv_sparse_decode", "pkv_prefill_ws_size", "pkv_prefill",
+    "pkv_sparse_decode", "pkv_prefill_ws_size", "pkv_prefill", "pkv_diag_wait_runs_out",
 ]
 
 
@@ -107,6 +107,7 @@ def load(path: Optional[str] = None):
         "pkv_topk": [SP, i32, i32, vp, i32, i32, vp, vp],
         "pkv_sparse_ws_size": [LP, SP, i32, i32, i32, ctypes.POINTER(sz)],
         "pkv_sparse_decode": [LP, SP, i32, i32, i32, vp, vp, i32, vp, vp, sz, vp, vp],
+        "pkv_diag_wait_runs_out": [vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -354,3 +355,9 @@ def sparse_decode(lay, seqs, layer, n_q_heads, q, ids, k, out, ws, status=None, 
     _check(load().pkv_sparse_decode(ctypes.byref(lay), arr, n, layer, n_q_heads, _ptr(q),
                                     _ptr(ids), k, _ptr(out), _ptr(ws), ws_bytes, _ptr(status),
                                     _stream(stream)), "pkv_sparse_decode")
+
+
+def diag_wait_runs_out(status, stream=None):
+    """One warp's wait on a barrier nothing arrives on: it gives up after about
+    a second and sets PKV_DEV_TIMEOUT in `status` (a device int32)."""
+    _check(load().pkv_diag_wait_runs_out(_ptr(status), _stream(stream)), "pkv_diag_wait_runs_out")

@@ -149,6 +149,10 @@ def test_decode_refuses_too_many_query_columns(lib):
     assert rc == pkv.EINVAL
 
 
+def test_diag_wait_needs_a_status_word(lib):
+    assert lib.pkv_diag_wait_runs_out(None, None) == pkv.EINVAL   # refused before any launch
+
+
 # ---- arena -------------------------------------------------------------------
 
 @pytest.fixture
