@@ -150,9 +150,9 @@ struct Ctx {
 // tail, new rows, pages not a multiple of 16, selected blocks) goes key by key
 // with 16-byte cp.async through the same swizzle, from one row lookup per key.
 // With a fused store, new rows come from k_new/v_new and are written to the
-// cache here as well.
+// cache here as well; returns whether this warp wrote any.
 template <bool kSparse>
-__device__ __forceinline__ void stage_tile(const Common &c, const DecodeArgs &a,
+__device__ __forceinline__ bool stage_tile(const Common &c, const DecodeArgs &a,
                                            const DecodeMaps &maps, const SeqDev &sd,
                                            const Unit &u, const Ctx &x, int t, int slot,
                                            int lane, uint64_t pol) {
@@ -234,8 +234,10 @@ __device__ __forceinline__ void stage_tile(const Common &c, const DecodeArgs &a,
         __syncwarp();
         if (lane == 0) mbar_arrive(&x.full[slot]);
     }
+    bool wrote = false;
     if (fuse_store) {
         unsigned todo = __ballot_sync(0xffffffffu, fresh && pos >= 0 && !bad);
+        wrote = todo != 0;
         while (todo) {
             const int src = __ffs(todo) - 1;
             todo &= todo - 1;
@@ -260,6 +262,7 @@ __device__ __forceinline__ void stage_tile(const Common &c, const DecodeArgs &a,
             }
         }
     }
+    return wrote;
 }
 
 // Prefetch the cached K and V rows of dense tile t into L2 (one warp).  Tiles
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // holding new positions, the queries and every write wait for it.
     const int my_tiles = active ? (u.ntiles - ks + ks_n - 1) / ks_n : 0;  // tiles ks, ks+ks_n, ...
     bool waited = kSparse;
+    bool wrote = false;  // this warp stored new rows (fused store)
     int issued = 0;
     if (leader) {
         for (; issued < S && issued < my_tiles; ++issued) {
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pdl_wait();
                 waited = true;
             }
-            stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, lane, pol);
+            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, lane, pol);
         }
         if (!kSparse && !waited)
             for (int j = issued; j < my_tiles && j < 2 * S; ++j)
@@ -498,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 fence_proxy_async_smem();  // this slot's reads come before the next tile's writes
-                stage_tile<kSparse>(c, a, maps, sd, u, x, ks + issued * ks_n, slot, lane, pol);
+                wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, ks + issued * ks_n, slot, lane, pol);
                 ++issued;
             }
         }
@@ -511,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&x.full[ks * S + j % S], (j / S) & 1, nullptr);
     }
 
-    if (a.k_new != nullptr) __threadfence();  // stored rows visible before the next kernel starts
+    if (wrote) __threadfence();  // stored rows visible before the next kernel starts
     __syncthreads();
     pdl_trigger();  // every thread has passed its grid-dependency wait
     if (*x.abort_flag) return;
@@ -585,19 +589,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 // A column of a stream with up to 32 splits is one CTA, a thread a dim; past
 // 32 splits it is two CTAs of 128 dims whose threads form two groups of 128
 // (one thread a dim): group 0 sums the first ceil(ns/2) splits, group 1 the
-// rest, and O = O_0 + O_1 (comb_ctas).  Every sum runs in split order.  A
-// thread loads all its splits' values at once (up to 32) while the split
-// maxima load, so one memory round trip covers a column of up to 64 splits.
-// At most 64 registers a thread: a combine CTA then fits on an SM beside a
-// partial CTA of the next call, which can start streaming its keys without
-// waiting for the SM.
+// rest, and O = O_0 + O_1 (comb_ctas).  Every sum of O runs in split order.
+// Each warp finds M and L itself: lane l reads (m, l) of splits l, l + 32,
+// ..., and shuffles reduce them in a fixed order, so every warp gets the same
+// bits without waiting on another warp.  The weights of each batch of 32
+// splits (lane l: split b + l) pass through the warp's own shared row.  A
+// thread issues its first 32 values together with those pairs, so one memory
+// round trip covers a column of up to 64 splits.  At most 64 registers a
+// thread: a combine CTA then fits on an SM beside a partial CTA of the next
+// call, which can start streaming its keys without waiting for the SM.
 template <bool kSparse>
 __global__ void __launch_bounds__(kCombThreads, 4)
     decode_combine(const __grid_constant__ Common c, const DecodeArgs a) {
     constexpr int kBatch = 32;
-    extern __shared__ float comb_smem[];  // w[ns], lsum[ns]
-    __shared__ float sh_l;
     __shared__ float sh_o[kHeadDim / 2];
+    __shared__ float sh_w[kCombThreads / 32][kBatch];  // a warp's weights of one batch
     pdl_wait();
     pdl_trigger();
     const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
@@ -606,52 +612,53 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     const int halves = comb_ctas(ns);
     const int r = (blockIdx.x - sd.comb_off) / halves;  // (unit, column) of the stream
     const int unit = r / sd.ncols, col = r - unit * sd.ncols;
-    float *w = comb_smem, *lsum = comb_smem + ns;
     const int units = kSparse ? c.n_q_heads : c.n_kv_heads;
     const float *part_acc = a.ws + sd.ws_off;
-    const float *part_ml = part_acc + (int64_t)units * ns * sd.ncols * kHeadDim;
+    const float2 *part_ml =
+        reinterpret_cast<const float2 *>(part_acc + (int64_t)units * ns * sd.ncols * kHeadDim);
     const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
     const int64_t stride = (int64_t)sd.ncols * kHeadDim;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float2 *col_ml = part_ml + p0;
+    const int tid = threadIdx.x, lane = tid & 31;
     // two CTAs: 128 dims each, thread t in group t >> 7; one CTA: all 256 dims, one group
     const int grp = halves == 2 ? tid >> 7 : 0, dd = halves == 2 ? tid & 127 : tid;
     const int d = halves == 2 ? (((blockIdx.x - sd.comb_off) & 1) << 7) + dd : dd;
     const int i0 = halves == 2 && grp ? (ns + 1) >> 1 : 0;  // this group's splits
     const int i1 = halves == 2 && !grp ? (ns + 1) >> 1 : ns;
     const float *col_acc = part_acc + p0 * kHeadDim + d;
+    const int warp = tid >> 5;
     float xs[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) xs[j] = i0 + j < i1 ? __ldcg(col_acc + (i0 + j) * stride) : 0.f;
-    for (int i = tid; i < ns; i += kCombThreads) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(part_ml + (p0 + (int64_t)i * sd.ncols) * 2));
-        w[i] = ml.x;
-        lsum[i] = ml.y;
+    const float2 none = make_float2(-INFINITY, 0.f);
+    const float2 ml0 = lane < ns ? __ldcg(col_ml + (int64_t)lane * sd.ncols) : none;
+    const float2 ml1 = lane + 32 < ns ? __ldcg(col_ml + (int64_t)(lane + 32) * sd.ncols) : none;
+    float2 mlb = i0 + lane < i1 ? __ldcg(col_ml + (int64_t)(i0 + lane) * sd.ncols) : none;
+    float M = fmaxf(ml0.x, ml1.x);
+    for (int i = lane + 64; i < ns; i += 32) M = fmaxf(M, __ldcg(col_ml + (int64_t)i * sd.ncols).x);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const bool empty = M == -INFINITY;  // no split saw a key
+    float L = (empty ? 0.f : ex2(ml0.x - M)) * ml0.y + (empty ? 0.f : ex2(ml1.x - M)) * ml1.y;
+    for (int i = lane + 64; i < ns; i += 32) {
+        const float2 v = __ldcg(col_ml + (int64_t)i * sd.ncols);
+        L += (empty ? 0.f : ex2(v.x - M)) * v.y;
     }
-    __syncthreads();
-    if (warp == 0) {
-        float M = -INFINITY;
-        for (int i = lane; i < ns; i += 32) M = fmaxf(M, w[i]);
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float L = 0.f;
-        for (int i = lane; i < ns; i += 32) {
-            const float wi = M == -INFINITY ? 0.f : ex2(w[i] - M);
-            w[i] = wi;
-            L += wi * lsum[i];
-        }
-        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) sh_l = L;
-    }
-    __syncthreads();
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     float O = 0.f;
+    for (int b = i0; b < i1; b += kBatch) {
+        if (b > i0) {
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j)
-        if (i0 + j < i1) O += w[i0 + j] * xs[j];
-    for (int b = i0 + kBatch; b < i1; b += kBatch) {
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) xs[j] = b + j < i1 ? __ldcg(col_acc + (b + j) * stride) : 0.f;
+            for (int j = 0; j < kBatch; ++j) xs[j] = b + j < i1 ? __ldcg(col_acc + (b + j) * stride) : 0.f;
+            mlb = b + lane < i1 ? __ldcg(col_ml + (int64_t)(b + lane) * sd.ncols) : none;
+            __syncwarp();  // the previous batch's weights are read
+        }
+        sh_w[warp][lane] = empty ? 0.f : ex2(mlb.x - M);
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < kBatch; ++j)
-            if (b + j < i1) O += w[b + j] * xs[j];
+            if (b + j < i1) O += sh_w[warp][j] * xs[j];
     }
     if (halves == 2) {
         if (grp == 1) sh_o[dd] = O;
@@ -659,7 +666,6 @@ __global__ void __launch_bounds__(kCombThreads, 4)
         if (grp == 1) return;
         O += sh_o[dd];
     }
-    const float L = sh_l;
     const float o = L > 0.f ? O / L : 0.f;
     Unit u;
     u.unit = unit;
@@ -758,10 +764,8 @@ int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, u
                    float *ws, cudaStream_t stream) {
     if (set_carveout() != PKV_OK) return PKV_ECUDA;
     DecodeArgs a{q, out, ws, nullptr, 0, nullptr, nullptr, nullptr};
-    int max_ns = 1;
-    for (int s = 0; s < c.n_seqs; ++s) max_ns = std::max(max_ns, c.seq[s].nsplit);
-    return launch_status(launch_pdl(decode_combine<false>, plan.total_comb, kCombThreads,
-                                    2 * max_ns * sizeof(float), stream, c, a));
+    return launch_status(
+        launch_pdl(decode_combine<false>, plan.total_comb, kCombThreads, 0, stream, c, a));
 }
 
 int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &maps, bool sparse,
@@ -784,9 +788,7 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;
     if (plan.total_comb > 0) {
-        int max_ns = 1;
-        for (int s = 0; s < cc.n_seqs; ++s) max_ns = std::max(max_ns, cc.seq[s].nsplit);
-        e = launch_pdl(comb, plan.total_comb, kCombThreads, 2 * max_ns * sizeof(float), stream, cc, a);
+        e = launch_pdl(comb, plan.total_comb, kCombThreads, 0, stream, cc, a);
         if (e != cudaSuccess) return PKV_ECUDA;
     }
     return PKV_OK;
