@@ -55,9 +55,9 @@ ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3
 # combine kernels), from the ncu capture summarised in
 # profiles/decode_partial_pages256.md, valid while the decode sources hash to
 # the value the capture was taken with; reported as null otherwise.
-DECODE_TRAFFIC = {"bytes": 40385280,
+DECODE_TRAFFIC = {"bytes": 40364288,
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "18967d922d73dac45f2ae5501dcfa4ad0ba5d1c70480fc17f7af53033ef49d42"}
+                  "sha256": "8cbee4e604f53a7852d94486cce212c5c864747f0f22fb11bf72243f22818041"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
