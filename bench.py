@@ -403,17 +403,23 @@ def bf16_peak():
 
 class FlushTimer:
     """Median CUDA-event time of a call on the current stream, with a buffer
-    twice the L2 written before every timed call (not timed)."""
+    twice the L2 written and then read back before every timed call (not
+    timed): the read writes back the dirty lines the fill left in L2, so that
+    their write-back is not charged to the timed call."""
 
     def __init__(self, torch, dev, profile=False):
         self.torch = torch
         self.buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
         self.profile = profile
 
+    def flush(self):
+        self.buf.zero_()
+        self.sink = self.buf.sum()
+
     def ms(self, fn, reps=20, warm=3):
         t = self.torch
         for _ in range(warm):
-            self.buf.zero_()
+            self.flush()
             fn()
         t.cuda.synchronize()
         e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
@@ -421,7 +427,7 @@ class FlushTimer:
         if self.profile:
             t.cuda.profiler.start()
         for _ in range(reps):
-            self.buf.zero_()
+            self.flush()
             e0.record()
             fn()
             e1.record()

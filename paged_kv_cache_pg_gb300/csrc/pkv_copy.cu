@@ -11,6 +11,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kChunk = 8;  // bf16 elements in a 16-byte chunk
+constexpr int kBatch = 4;  // 16-byte chunks a lane of the store loads before it stores them
 
 // Offset of the page holding `pos`, or -1 for a table entry outside the
 // arena (reported); row is the row inside the page.
@@ -30,44 +31,57 @@ __device__ __forceinline__ int64_t page_or_bad(const SeqDev &s, int32_t pos, int
     return (int64_t)id * s.ps;
 }
 
-// One thread per 16-byte chunk of a new token's rows: 2*H rows of 256
-// (K then V) and, with indexer keys, one row of 128.
+// A warp stores one new token at a time: its 2*H rows of 256 (K then V)
+// and, with indexer keys, its row of 128.  The stream, page and row are found
+// once per token; lane l copies the token's 16-byte chunks l, l + 32, ...,
+// up to kBatch of them loaded before any is stored.
 __global__ void __launch_bounds__(kThreads) store_kernel(const __grid_constant__ Common c,
-                                                         int64_t total_chunks,
+                                                         int32_t total_tokens,
                                                          const uint16_t *__restrict__ k_new,
                                                          const uint16_t *__restrict__ v_new,
                                                          const uint16_t *__restrict__ ik_new) {
     pdl_wait();
     const int H = c.n_kv_heads;
-    const int row_chunks = kHeadDim / kChunk;  // 32
-    const int ik_chunks = c.idx_dim / kChunk;  // 16 or 0
-    const int per_tok = 2 * H * row_chunks + ik_chunks;
-    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total_chunks;
-         i += (int64_t)gridDim.x * kThreads) {
-        const int32_t tok = static_cast<int32_t>(i / per_tok);
-        const int32_t r = static_cast<int32_t>(i % per_tok);
+    constexpr int row_chunks = kHeadDim / kChunk;  // 32
+    const int kv_chunks = 2 * H * row_chunks;
+    const int per_tok = kv_chunks + c.idx_dim / kChunk;
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * (kThreads / 32);
+    for (int tok = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); tok < total_tokens;
+         tok += nwarps) {
         const int s = find_seq(c.n_seqs, tok, [&](int t) { return c.seq[t].tok_off; });
         const SeqDev &sd = c.seq[s];
         const int32_t pos = sd.len - sd.n_new + (tok - sd.tok_off);
         int32_t row;
-        const int64_t page = page_or_bad(sd, pos, &row, c.status);
+        const int64_t page = page_or_bad(sd, pos, &row, lane == 0 ? c.status : nullptr);
         if (page < 0) continue;
-        const uint16_t *src;
-        int64_t dst;
-        if (r < 2 * H * row_chunks) {
-            const int kind = r / (H * row_chunks);  // 0 = K, 1 = V
-            const int head = (r / row_chunks) % H;
-            const int ch = r % row_chunks;
-            src = (kind ? v_new : k_new) + ((int64_t)tok * H + head) * kHeadDim + ch * kChunk;
-            dst = page + (kind ? off_v(H, sd.ptok, head, row) : off_k(sd.ptok, head, row)) +
-                  ch * kChunk;
-        } else {
-            const int ch = r - 2 * H * row_chunks;
-            src = ik_new + (int64_t)tok * c.idx_dim + ch * kChunk;
-            dst = page + off_ik(H, c.idx_dim, sd.ptok, row) + ch * kChunk;
+        uint16_t *base = const_cast<uint16_t *>(sd.layer_base) + page;
+        for (int r0 = 0; r0 < per_tok; r0 += 32 * kBatch) {
+            uint4 val[kBatch];
+            int64_t dst[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int r = r0 + 32 * b + lane;
+                dst[b] = -1;
+                if (r >= per_tok) continue;
+                const uint16_t *src;
+                if (r < kv_chunks) {
+                    const int kh = r / row_chunks, ch = r % row_chunks;  // kh: K heads, then V heads
+                    const int kind = kh >= H, head = kh - kind * H;
+                    src = (kind ? v_new : k_new) + ((int64_t)tok * H + head) * kHeadDim + ch * kChunk;
+                    dst[b] = (kind ? off_v(H, sd.ptok, head, row) : off_k(sd.ptok, head, row)) +
+                             ch * kChunk;
+                } else {
+                    const int ch = r - kv_chunks;
+                    src = ik_new + (int64_t)tok * c.idx_dim + ch * kChunk;
+                    dst[b] = off_ik(H, c.idx_dim, sd.ptok, row) + ch * kChunk;
+                }
+                val[b] = __ldg(reinterpret_cast<const uint4 *>(src));
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b)
+                if (dst[b] >= 0) *reinterpret_cast<uint4 *>(base + dst[b]) = val[b];
         }
-        uint16_t *base = const_cast<uint16_t *>(sd.layer_base);
-        *reinterpret_cast<uint4 *>(base + dst) = __ldg(reinterpret_cast<const uint4 *>(src));
     }
     pdl_trigger_after_writes();  // the next decode may read these rows early
 }
@@ -233,10 +247,9 @@ unsigned grid_for(int64_t work) {
 
 int launch_store(const Common &c, int32_t total_tokens, const uint16_t *k_new,
                  const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream) {
-    const int64_t per_tok = 2 * c.n_kv_heads * (kHeadDim / kChunk) + c.idx_dim / kChunk;
-    const int64_t total = per_tok * total_tokens;
-    return launch_status(launch_pdl(store_kernel, grid_for(total), kThreads, 0, stream, c, total,
-                                    k_new, v_new, ik_new));
+    // a warp a token
+    return launch_status(launch_pdl(store_kernel, grid_for((int64_t)total_tokens * 32), kThreads,
+                                    0, stream, c, total_tokens, k_new, v_new, ik_new));
 }
 
 int launch_gather(const Common &c, int32_t kind, int64_t total_rows, uint16_t *out,
