@@ -11,7 +11,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kChunk = 8;  // bf16 elements in a 16-byte chunk
-constexpr int kBatch = 4;  // 16-byte chunks a lane of the store loads before it stores them
+constexpr int kBatch = 4;  // 16-byte chunks a lane loads before it stores them
 
 // Offset of the page holding `pos`, or -1 for a table entry outside the
 // arena (reported); row is the row inside the page.
@@ -86,39 +86,58 @@ __global__ void __launch_bounds__(kThreads) store_kernel(const __grid_constant__
     pdl_trigger_after_writes();  // the next decode may read these rows early
 }
 
-// One thread per 16-byte chunk of an output row.  work_off holds each
-// stream's first output row.
+// Gather of one kind into packed rows; work_off holds each stream's first
+// output row.  K or V (kKV): a warp per output row (a position's rows of every
+// head, 32 chunks of 16 bytes a head), lane l taking chunk l of each head and
+// loading up to kBatch heads before it stores them.  Indexer or pooled rows
+// (128 dims, 16 chunks): a half-warp per row.  The stream, page and row are
+// found once per row; rows behind a bad table entry come out as zeros.
+template <bool kKV>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ Common c,
-                                                          int32_t kind, int64_t total_chunks,
+                                                          int32_t kind, int32_t total_rows,
                                                           uint16_t *__restrict__ out) {
     pdl_wait();
     pdl_trigger();
+    constexpr int row_chunks = (kKV ? kHeadDim : kIdxDim) / kChunk;  // 32 or 16
+    constexpr int rows_per_warp = 32 / row_chunks;                     // 1 or 2
     const int H = c.n_kv_heads;
-    const bool kv = kind == PKV_K || kind == PKV_V;
-    const int row_chunks = (kv ? kHeadDim : c.idx_dim) / kChunk;
-    const int per_row = (kv ? H : 1) * row_chunks;  // chunks of one output row
-    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total_chunks;
-         i += (int64_t)gridDim.x * kThreads) {
-        const int32_t orow = static_cast<int32_t>(i / per_row);
-        const int32_t r = static_cast<int32_t>(i % per_row);
+    const int lane = threadIdx.x & 31, sub = lane / row_chunks, ch = lane % row_chunks;
+    const int nwarps = gridDim.x * (kThreads / 32);
+    for (int w = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); w * rows_per_warp < total_rows;
+         w += nwarps) {
+        const int orow = w * rows_per_warp + sub;
+        if (orow >= total_rows) continue;
         const int s = find_seq(c.n_seqs, orow, [&](int t) { return c.seq[t].work_off; });
         const SeqDev &sd = c.seq[s];
         const int32_t idx = orow - sd.work_off;  // position, or block for PKV_P
         const int32_t pos = kind == PKV_P ? 4 * idx : idx;
         int32_t row;
-        int64_t page = page_or_bad(sd, pos, &row, c.status);
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (page >= 0) {
-            int64_t src;
-            const int ch = r % row_chunks;
-            if (kind == PKV_K) src = off_k(sd.ptok, r / row_chunks, row);
-            else if (kind == PKV_V) src = off_v(H, sd.ptok, r / row_chunks, row);
-            else if (kind == PKV_IK) src = off_ik_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row);
-            else src = off_p_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row / 4);
-            val = *reinterpret_cast<const uint4 *>(sd.layer_base + page + src + ch * kChunk);
+        const int64_t page = page_or_bad(sd, pos, &row, ch == 0 ? c.status : nullptr);
+        const uint16_t *lb = sd.layer_base + page;
+        if (kKV) {
+            uint16_t *dst = out + ((int64_t)orow * H * row_chunks + ch) * kChunk;
+            const uint16_t *src = lb + (kind == PKV_V ? off_v(H, sd.ptok, 0, row) : off_k(sd.ptok, 0, row)) +
+                                  ch * kChunk;
+            const int64_t head_step = (int64_t)sd.ptok * kHeadDim;  // the next head's row
+            for (int h0 = 0; h0 < H; h0 += kBatch) {
+                uint4 val[kBatch];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b)
+                    val[b] = page >= 0 && h0 + b < H
+                                 ? *reinterpret_cast<const uint4 *>(src + (h0 + b) * head_step)
+                                 : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b)
+                    if (h0 + b < H)
+                        *reinterpret_cast<uint4 *>(dst + (int64_t)(h0 + b) * row_chunks * kChunk) = val[b];
+            }
+        } else {
+            const int64_t off = kind == PKV_IK ? off_ik_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row)
+                                               : off_p_f(c.kv_fp8, H, c.idx_dim, sd.ptok, row / 4);
+            const uint4 val = page >= 0 ? *reinterpret_cast<const uint4 *>(lb + off + ch * kChunk)
+                                        : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(out + ((int64_t)orow * row_chunks + ch) * kChunk) = val;
         }
-        *reinterpret_cast<uint4 *>(out + (int64_t)orow * per_row * kChunk + (int64_t)r * kChunk) =
-            val;
     }
 }
 
@@ -129,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const __grid_constant__ 
     pdl_wait();
     pdl_trigger();
     const int H = c.n_kv_heads;
-    const int per_block = c.idx_dim / kChunk;  // 16
+    constexpr int per_block = kIdxDim / kChunk;  // 16 (idx_dim is 128 when there are indexer rows)
     for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total_chunks;
          i += (int64_t)gridDim.x * kThreads) {
         const int32_t item = static_cast<int32_t>(i / per_block);
@@ -254,11 +273,13 @@ int launch_store(const Common &c, int32_t total_tokens, const uint16_t *k_new,
 
 int launch_gather(const Common &c, int32_t kind, int64_t total_rows, uint16_t *out,
                   cudaStream_t stream) {
-    const bool kv = kind == PKV_K || kind == PKV_V;
-    const int64_t per_row = (kv ? c.n_kv_heads : 1) * ((kv ? kHeadDim : c.idx_dim) / kChunk);
-    const int64_t total = per_row * total_rows;
-    return launch_status(
-        launch_pdl(gather_kernel, grid_for(total), kThreads, 0, stream, c, kind, total, out));
+    if (total_rows > INT32_MAX - 64) return PKV_EINVAL;  // int32 row indices
+    const int rows = static_cast<int32_t>(total_rows);
+    if (kind == PKV_K || kind == PKV_V)  // a warp a row
+        return launch_status(launch_pdl(gather_kernel<true>, grid_for(total_rows * 32), kThreads,
+                                        0, stream, c, kind, rows, out));
+    return launch_status(launch_pdl(gather_kernel<false>, grid_for(total_rows * 16), kThreads, 0,
+                                    stream, c, kind, rows, out));  // a half-warp a row
 }
 
 int launch_store8(const Common &c, int32_t total_tokens, const uint16_t *k_new,
