@@ -223,36 +223,48 @@ __global__ void __launch_bounds__(kThreads) store8_kernel(const __grid_constant_
     pdl_trigger_after_writes();  // the next decode may read these rows early
 }
 
-// e4m3 gather: codes (16 bytes a thread, [rows][H][256] out) or scales (a
-// float a thread, [rows][H] out) of positions 0 .. len-1 through the table.
+// e4m3 gather: codes ([rows][H][256] bytes out) or scales ([rows][H] float32
+// out) of positions 0 .. len-1 through the table.  A warp per position: the
+// stream, page and row are found once; for codes lane l takes 16-byte chunk
+// l & 15 of heads l >> 4, (l >> 4) + 2, ...; for scales lane l takes head l.
 __global__ void __launch_bounds__(kThreads) gather8_kernel(const __grid_constant__ Common c,
-                                                           int32_t kind, int64_t total,
+                                                           int32_t kind, int32_t total_rows,
                                                            uint8_t *__restrict__ out) {
     pdl_wait();
     pdl_trigger();
     const int H = c.n_kv_heads;
     const bool codes = kind == PKV_K || kind == PKV_V;
     const bool v = kind == PKV_V || kind == PKV_VS;
-    const int per_row = codes ? H * (kHeadDim / 16) : H;  // items of one position
-    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * kThreads) {
-        const int32_t orow = static_cast<int32_t>(i / per_row);
-        const int32_t r = static_cast<int32_t>(i % per_row);
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * (kThreads / 32);
+    for (int orow = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); orow < total_rows;
+         orow += nwarps) {
         const int s = find_seq(c.n_seqs, orow, [&](int t) { return c.seq[t].work_off; });
         const SeqDev &sd = c.seq[s];
         int32_t row;
-        const int64_t page = page_or_bad(sd, orow - sd.work_off, &row, c.status);
+        const int64_t page = page_or_bad(sd, orow - sd.work_off, &row, lane == 0 ? c.status : nullptr);
         const uint8_t *lb = reinterpret_cast<const uint8_t *>(sd.layer_base) + 2 * page;
         if (codes) {
-            const int head = r / (kHeadDim / 16), ch = r % (kHeadDim / 16);
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (page >= 0)
-                val = *reinterpret_cast<const uint4 *>(lb + off8_code(v, H, sd.ptok, head, row) + 16 * ch);
-            *reinterpret_cast<uint4 *>(out + i * 16) = val;
+            const int ch = lane & 15;
+            uint8_t *dst = out + (int64_t)orow * H * kHeadDim + 16 * ch;
+            for (int h0 = lane >> 4; h0 < H; h0 += 2 * kBatch) {
+                uint4 val[kBatch];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int head = h0 + 2 * b;
+                    val[b] = page >= 0 && head < H
+                                 ? *reinterpret_cast<const uint4 *>(lb + off8_code(v, H, sd.ptok, head, row) + 16 * ch)
+                                 : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b)
+                    if (h0 + 2 * b < H)
+                        *reinterpret_cast<uint4 *>(dst + (int64_t)(h0 + 2 * b) * kHeadDim) = val[b];
+            }
         } else {
-            float val = 0.f;
-            if (page >= 0) val = *reinterpret_cast<const float *>(lb + off8_scale(v, H, sd.ptok, r, row));
-            reinterpret_cast<float *>(out)[i] = val;
+            for (int head = lane; head < H; head += 32)
+                reinterpret_cast<float *>(out)[(int64_t)orow * H + head] =
+                    page >= 0 ? *reinterpret_cast<const float *>(lb + off8_scale(v, H, sd.ptok, head, row)) : 0.f;
         }
     }
 }
@@ -291,10 +303,10 @@ int launch_store8(const Common &c, int32_t total_tokens, const uint16_t *k_new,
 
 int launch_gather8(const Common &c, int32_t kind, int64_t total_rows, void *out,
                    cudaStream_t stream) {
-    const bool codes = kind == PKV_K || kind == PKV_V;
-    const int64_t total = total_rows * c.n_kv_heads * (codes ? kHeadDim / 16 : 1);
-    return launch_status(launch_pdl(gather8_kernel, grid_for(total), kThreads, 0, stream, c, kind,
-                                    total, static_cast<uint8_t *>(out)));
+    if (total_rows > INT32_MAX - 64) return PKV_EINVAL;  // int32 row indices
+    return launch_status(launch_pdl(gather8_kernel, grid_for(total_rows * 32), kThreads, 0, stream,
+                                    c, kind, static_cast<int32_t>(total_rows),
+                                    static_cast<uint8_t *>(out)));  // a warp a position
 }
 
 int launch_pool(const Common &c, int32_t total_blocks, cudaStream_t stream) {
