@@ -3,7 +3,8 @@
 // Scores: each (head, block) score is the float32 chain
 // acc = fmaf(qi[d], P[b][d], acc), d = 0 .. Di-1, run by one thread (the
 // order is part of the result: a top-k decision downstream must see the same
-// bits on any cache layout); a thread runs four such chains side by side.
+// bits on any cache layout); a thread runs two such chains side by side, and
+// a CTA takes 32 blocks, so a stream of 2,250 blocks spreads over 71 CTAs.
 // Pooled rows are looked up once per block (pg_at on its first position) and
 // staged in shared memory with 16-byte loads.
 //
@@ -19,7 +20,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kScoreBlocks = 64;   // blocks a CTA
+constexpr int kScoreBlocks = 32;   // blocks a CTA: a lane each
 constexpr int kScoreThreads = 256;
 constexpr int kPStride = kIdxDim + 1;  // float stride of a staged pooled row
 constexpr int kMaxQHeads = 64;
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(kScoreThreads)
     }
     __syncthreads();
     // the 64 pooled rows, 16 bytes a load and every load in flight at once
-    constexpr int kLoads = kScoreBlocks * (kIdxDim / 8) / kScoreThreads;  // 4
+    constexpr int kLoads = kScoreBlocks * (kIdxDim / 8) / kScoreThreads;  // 2
     uint4 w[kLoads];
 #pragma unroll
     for (int it = 0; it < kLoads; ++it) {
@@ -82,30 +83,24 @@ __global__ void __launch_bounds__(kScoreThreads)
     }
     __syncthreads();
     const int lane = tid & 31, warp = tid >> 5;
-    // a warp takes heads h and h + 8, each lane blocks lane and lane + 32 of
-    // the tile: four chains side by side, each still summed in d order
-    const float *pa = ps + lane * kPStride, *pb = ps + (lane + 32) * kPStride;
+    // a warp takes heads h and h + 8, each lane block lane of the tile: two
+    // chains side by side, each still summed in d order
+    const float *pa = ps + lane * kPStride;
     for (int h = warp; h < Hq; h += 2 * (kScoreThreads / 32)) {
         const int h2 = h + kScoreThreads / 32;
         const bool two = h2 < Hq;
         const float *qa = qs + h * Di, *qb = qs + (two ? h2 : h) * Di;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll 8
         for (int d = 0; d < kIdxDim; ++d) {
-            const float x = qa[d], y = qb[d], u = pa[d], v = pb[d];
-            a0 = __fmaf_rn(x, u, a0);
-            a1 = __fmaf_rn(x, v, a1);
-            a2 = __fmaf_rn(y, u, a2);
-            a3 = __fmaf_rn(y, v, a3);
+            const float u = pa[d];
+            a0 = __fmaf_rn(qa[d], u, a0);
+            a1 = __fmaf_rn(qb[d], u, a1);
         }
-        const int ba = b0 + lane, bb = ba + 32;
-        float *row_a = scores + ((int64_t)s * Hq + h) * ld;
-        if (ba < ld) row_a[ba] = ba < nb ? a0 : -INFINITY;
-        if (bb < ld) row_a[bb] = bb < nb ? a1 : -INFINITY;
-        if (two) {
-            float *row_b = scores + ((int64_t)s * Hq + h2) * ld;
-            if (ba < ld) row_b[ba] = ba < nb ? a2 : -INFINITY;
-            if (bb < ld) row_b[bb] = bb < nb ? a3 : -INFINITY;
+        const int ba = b0 + lane;
+        if (ba < ld) {
+            scores[((int64_t)s * Hq + h) * ld + ba] = ba < nb ? a0 : -INFINITY;
+            if (two) scores[((int64_t)s * Hq + h2) * ld + ba] = ba < nb ? a1 : -INFINITY;
         }
     }
 }
