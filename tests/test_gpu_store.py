@@ -57,6 +57,28 @@ def test_gather_through_tables_gives_contiguous_bytes(ptok):
             assert np.array_equal(host_u16(out), want)
 
 
+@pytest.mark.parametrize("hkv,ptok", [(3, 16), (8, 48), (8, None)])
+def test_store_and_gather_with_many_kv_heads(hkv, ptok):
+    # 3 and 8 KV heads: a store lane takes more than one batch of chunks
+    # (2*H*32 + 16 chunks a token) and a gather lane more than one batch of
+    # heads; bytes must still equal the oracle's placement and read back
+    t = torch()
+    lay = pkv.layout(1, hkv, 256, 128)
+    streams = _streams([333, 1029], n_layers=1, hkv=hkv, seed=40 + hkv)
+    pl = place(lay, streams, ptok, seed=hkv)
+    for i in range(len(pl.buffers)):
+        assert np.array_equal(host_u16(pl.body(i)), pl.oarenas[i])
+    assert pl.guards_intact()
+    seqs = pl.seqs()
+    total = sum(s.length for s in streams)
+    for kind, attr, shape in [(pkv.K, "k", (hkv, 256)), (pkv.V, "v", (hkv, 256)),
+                              (pkv.IK, "ik", (128,))]:
+        out = t.empty((total,) + shape, dtype=t.int16, device="cuda")
+        pkv.gather(lay, seqs, 0, kind, out)
+        want = np.concatenate([getattr(s, attr)[0] for s in streams])
+        assert np.array_equal(host_u16(out), want)
+
+
 def test_reversed_table_single_stream_matches_contiguous():
     lay = pkv.layout(1, 1, 256, 128)
     s = _streams([64], n_layers=1, hkv=1)
