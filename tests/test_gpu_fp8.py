@@ -47,22 +47,25 @@ def test_e4m3_store_bytes_equal_oracle(ptok):
     assert pl.guards_intact()
 
 
-def test_e4m3_gather_codes_and_scales_equal_oracle():
+@pytest.mark.parametrize("hkv", [2, 3, 8])
+def test_e4m3_gather_codes_and_scales_equal_oracle(hkv):
+    # 3 and 8 KV heads: a gather lane takes several heads (16 lanes a head's
+    # 256 code bytes, heads two apart)
     t = torch()
-    lay = _lay()
+    lay = _lay(hkv=hkv)
     lens = [300, 77]
-    streams = _streams(lens, seed=2100)
+    streams = _streams(lens, hkv=hkv, seed=2100 + hkv)
     pl = place(lay, streams, 48, seed=4)
     seqs = pl.seqs(lens, [0, 0])
     for layer in range(2):
         for kind in (pkv.K, pkv.V):
-            out = t.empty((sum(lens), 2, 256), dtype=t.uint8, device="cuda")
+            out = t.empty((sum(lens), hkv, 256), dtype=t.uint8, device="cuda")
             pkv.gather(lay, seqs, layer, kind, out)
             want = np.concatenate([orc.get_rows8(pl.shape, oc, layer, kind, 0, T)
                                    for oc, T in zip(pl.ocaches, lens)])
             assert np.array_equal(out.cpu().numpy(), want)
         for kind in (pkv.KS, pkv.VS):
-            out = t.empty((sum(lens), 2), dtype=t.float32, device="cuda")
+            out = t.empty((sum(lens), hkv), dtype=t.float32, device="cuda")
             pkv.gather(lay, seqs, layer, kind, out)
             want = np.concatenate([orc.get_rows8(pl.shape, oc, layer, kind, 0, T)
                                    for oc, T in zip(pl.ocaches, lens)])
