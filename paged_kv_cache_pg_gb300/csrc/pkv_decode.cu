@@ -745,19 +745,24 @@ int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan) {
 // Every kernel of a decode call asks for the largest shared-memory carveout:
 // an SM configured for a small one (as a kernel using little shared memory
 // would leave it) cannot take a partial CTA of the next call until it drains.
+// The partial kernels' dynamic shared memory is set in the same pass.
 static int set_carveout() {
-    static bool done = false;
-    if (done) return PKV_OK;
-    const void *fns[] = {reinterpret_cast<const void *>(decode_combine<false>),
-                         reinterpret_cast<const void *>(decode_combine<true>),
-                         reinterpret_cast<const void *>(decode_partial<false>),
-                         reinterpret_cast<const void *>(decode_partial<true>)};
-    for (const void *f : fns)
-        if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-            return PKV_ECUDA;
-    done = true;
-    return PKV_OK;
+    static std::atomic<uint64_t> done{0};
+    return once_per_device(done, [] {
+        const void *fns[] = {reinterpret_cast<const void *>(decode_combine<false>),
+                             reinterpret_cast<const void *>(decode_combine<true>),
+                             reinterpret_cast<const void *>(decode_partial<false>),
+                             reinterpret_cast<const void *>(decode_partial<true>)};
+        for (const void *f : fns)
+            if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                return PKV_ECUDA;
+        for (int i = 2; i < 4; ++i)
+            if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytes)) != cudaSuccess)
+                return PKV_ECUDA;
+        return PKV_OK;
+    });
 }
 
 int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, uint16_t *out,
@@ -778,13 +783,6 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     auto part = sparse ? decode_partial<true> : decode_partial<false>;
     auto comb = sparse ? decode_combine<true> : decode_combine<false>;
     if (set_carveout() != PKV_OK) return PKV_ECUDA;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[sparse]) {
-        if (cudaFuncSetAttribute(part, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
-            return PKV_ECUDA;
-        attr_set[sparse] = true;
-    }
     cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;
     if (plan.total_comb > 0) {

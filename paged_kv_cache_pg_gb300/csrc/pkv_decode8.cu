@@ -485,15 +485,16 @@ __global__ void __maxnreg__(192)
 int launch_decode8(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
                    const uint16_t *q, uint16_t *out, float *ws, const uint16_t *k_new,
                    const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(decode8_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmem8)) != cudaSuccess ||
-            cudaFuncSetAttribute(decode8_partial, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-            return PKV_ECUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (once_per_device(attr_done, [] {
+            if (cudaFuncSetAttribute(decode8_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmem8)) != cudaSuccess)
+                return PKV_ECUDA;
+            return cuda_rc(cudaFuncSetAttribute(decode8_partial,
+                                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                cudaSharedmemCarveoutMaxShared));
+        }) != PKV_OK)
+        return PKV_ECUDA;
     Decode8Args a{q, out, ws, k_new, v_new, ik_new};
     cudaError_t e =
         launch_pdl(decode8_partial, plan.total_items, kThreads8, kSmem8, stream, c, maps, a);

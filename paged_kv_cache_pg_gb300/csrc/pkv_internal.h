@@ -2,6 +2,7 @@
 // Nothing here is part of the ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -121,6 +122,22 @@ __host__ __device__ inline int64_t off8_scale(bool v, int32_t h_kv, int32_t ptok
     return 2 * (int64_t)h_kv * ptok * kHeadDim + (v ? 4 * (int64_t)h_kv * ptok : 0) +
            4 * ((int64_t)head * ptok + row);
 }
+
+// Runs set() on the current device until it succeeds there once: a kernel's
+// attributes belong to each device's context, so a process that uses several
+// GPUs sets them on each.  Two threads may both run set() the first time
+// (it only sets attributes).  Returns set()'s code, or PKV_ECUDA.
+template <typename F>
+inline int once_per_device(std::atomic<uint64_t> &done, F set) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ECUDA;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return PKV_OK;
+    const int rc = set();
+    if (rc == PKV_OK) done.fetch_or(bit, std::memory_order_release);
+    return rc;
+}
+inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ECUDA; }
 
 // Host helpers (pkv_host.cu).
 int validate_layout(const pkv_layout *layout);

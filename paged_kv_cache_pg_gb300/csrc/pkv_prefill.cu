@@ -561,13 +561,13 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
 
 int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
                    const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(prefill_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kPSmem)) != cudaSuccess)
-            return PKV_ECUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (once_per_device(attr_done, [] {
+            return cuda_rc(cudaFuncSetAttribute(prefill_partial,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(kPSmem)));
+        }) != PKV_OK)
+        return PKV_ECUDA;
     PrefillArgs a{q, out, ws};
     cudaError_t e = launch_pdl(prefill_partial, plan.total_items, kPThreads, kPSmem, stream, c, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;

@@ -244,14 +244,13 @@ int launch_scores(const Common &c, float *scores, int32_t ld, const uint16_t *qi
     (void)max_nb;
     const int tiles = (ld + kScoreBlocks - 1) / kScoreBlocks;
     const size_t dyn = static_cast<size_t>(c.n_q_heads) * c.idx_dim * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxQHeads * kIdxDim * static_cast<int>(sizeof(float))) !=
-            cudaSuccess)
-            return PKV_ECUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (once_per_device(attr_done, [] {
+            return cuda_rc(cudaFuncSetAttribute(
+                scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                kMaxQHeads * kIdxDim * static_cast<int>(sizeof(float))));
+        }) != PKV_OK)
+        return PKV_ECUDA;
     return launch_status(launch_pdl(scores_kernel, c.n_seqs * tiles, kScoreThreads, dyn, stream,
                                     c, qi, scores, ld, tiles));
 }
@@ -262,13 +261,13 @@ int launch_topk(const Common &c, const float *scores, int32_t ld, int32_t k, int
     for (int s = 0; s < c.n_seqs; ++s) max_nb = std::max(max_nb, c.seq[s].len / 4);
     const bool in_smem = max_nb <= kTopSmemKeys;
     const size_t dyn = in_smem ? static_cast<size_t>(max_nb) * 4 : 0;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kTopSmemKeys * 4) != cudaSuccess)
-            return PKV_ECUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (once_per_device(attr_done, [] {
+            return cuda_rc(cudaFuncSetAttribute(topk_kernel,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                kTopSmemKeys * 4));
+        }) != PKV_OK)
+        return PKV_ECUDA;
     return launch_status(launch_pdl(topk_kernel, c.n_seqs * c.n_q_heads, kTopThreads, dyn, stream,
                                     c, scores, ld, k, ids, static_cast<int32_t>(in_smem)));
 }
