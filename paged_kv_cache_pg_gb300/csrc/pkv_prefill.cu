@@ -522,6 +522,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 // Work items: (KV head, M-tile, split) per stream, splits fastest.  A stream
 // is split only as far as filling the SMs needs, from its own shape alone.
+// Split model of plan_prefill, in hundredths of a microsecond.
+constexpr int64_t kTileCost = 126;   // a 32-key tile of one 128-row M-tile
+constexpr int64_t kCtaCost = 1200;   // a CTA's fixed cost
+constexpr int64_t kPartialCost = 4;  // a (unit, split) partial written and read back
+constexpr int kMaxPrefillSplits = 64;
+
 int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
     int32_t items = 0, comb = 0;
     int64_t floats = 0;
@@ -538,8 +544,32 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
             continue;
         }
         const int mtiles = (d.ncols + kM - 1) / kM;
-        int ns = std::max(1, nsm / (H * mtiles));
-        ns = std::min(ns, std::max(1, d.len / (4 * kN)));
+        // Splits.  A stream whose (KV head, M-tile) units fill the SMs by
+        // themselves is not split.  Otherwise the count with the least
+        // modelled time for this stream's grid on nsm SMs: waves x (tiles a
+        // CTA x a tile's time + a CTA's fixed cost) + the split partials'
+        // round trip through HBM.  The costs are this kernel's on GB300:
+        // about 1.26 us a 32-key tile of 128 rows, 12 us a CTA (Q load, TMEM,
+        // pipeline fill, epilogue) and 0.04 us a (unit, split) partial of
+        // 128 rows written and read back.  For 512 queries on 31,000 keys it
+        // picks 7 splits, 448 CTAs in three nearly full waves; 2 splits
+        // would give one wave of 128 CTAs with 24 SMs idle.  Only the
+        // stream's own length and rows and the SM count enter, so paged and
+        // contiguous caches get the same splits.
+        const int64_t units = (int64_t)H * mtiles, tiles = (d.len + kN - 1) / kN;
+        const int max_ns =
+            units >= nsm ? 1 : std::max(1, std::min(kMaxPrefillSplits, d.len / (4 * kN)));
+        int ns = 1;
+        int64_t best = INT64_MAX;
+        for (int n = 1; n <= max_ns; ++n) {
+            const int64_t waves = (units * n + nsm - 1) / nsm;
+            const int64_t cost = waves * (((tiles + n - 1) / n) * kTileCost + kCtaCost) +
+                                 (n > 1 ? n * units * kPartialCost : 0);
+            if (cost < best) {
+                best = cost;
+                ns = n;
+            }
+        }
         int sl = (d.len + ns - 1) / ns;
         sl = (sl + kN - 1) / kN * kN;
         ns = (d.len + sl - 1) / sl;
