@@ -145,10 +145,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const SeqDev &sd = c.seq[s];
     const int H = c.n_kv_heads, G = c.group;
     const int mtiles = (sd.ncols + kM - 1) / kM;
+    // consecutive CTAs share a (KV head, split): the M-tiles that read the
+    // same key range run in the same wave and find its tiles in L2
     const int item = blockIdx.x - sd.work_off;
     const int kvh = item / (mtiles * sd.nsplit);
-    const int mt = (item / sd.nsplit) % mtiles;
-    const int split = item % sd.nsplit;
+    const int split = (item / mtiles) % sd.nsplit;
+    const int mt = item % mtiles;
     const int col0 = mt * kM;
     const int rows = min(kM, sd.ncols - col0);
     const int qbase = sd.len - sd.n_new;
