@@ -59,7 +59,8 @@ constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(2
 constexpr size_t kOffPos = (size_t)kSlots * kStageBytes;
 constexpr size_t kOffPage = kOffPos + kSlots * kTile * 4;
 constexpr size_t kOffBar = kOffPage + ((kMaxPages + 1) & ~1) * 8;
-constexpr size_t kSmemBytes = 1024 + kOffBar + 2 * kSlots * 8 + 16;  // + alignment slack
+constexpr size_t kOffUses = kOffBar + 2 * kSlots * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + kOffUses + kSlots * 4;  // + alignment slack
 static_assert(kMaxPages >= kMaxSparseBlocks, "the page list also holds block rows");
 static_assert(kSlots % (kWarps / 2) == 0, "every key slice gets the same number of slots");
 static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * 2 * 4 <= kSlots * kStageBytes,
@@ -140,6 +141,7 @@ struct Ctx {
     uint64_t *full;      // [slot]
     uint64_t *empty;     // [slot]
     volatile int *abort_flag;
+    int32_t *uses;       // [slot]: copies staged into it
     int first_page;      // dense: page of the split's first key
     int64_t fallback;    // sparse: a row surely written (position 0)
 };
@@ -297,7 +299,10 @@ __device__ __forceinline__ void prefetch_tile(const Common &c, const SeqDev &sd,
     }
 }
 
-template <bool kSparse>
+// kSpread: built for calls with a stream of more than 16 query columns a
+// unit (one key slice a CTA), whose tiles the column groups' lead warps stage
+// in turn; the instantiation without it keeps the leader-only staging code.
+template <bool kSparse, bool kSpread>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
                    const DecodeArgs a) {
@@ -311,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
     x.empty = x.full + kSlots;
     x.abort_flag = reinterpret_cast<volatile int *>(x.empty + kSlots);
+    x.uses = reinterpret_cast<int32_t *>(smem + kOffUses);
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int dh = (tid >> 5) & 1;              // which half of the 256 dims this warp sums
@@ -323,13 +329,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = kSlots / ks_n;                // slots of one key slice
     const int cg = warp % ncg, ks = warp / ncg;
     const bool active = ks < ks_n;
-    const bool leader = active && cg == 0 && dh == 0;  // stages the slice's tiles
+    // Who stages a slice's tiles: its leader.  When the CTA has a single
+    // slice (many query columns), the lead warps of the column groups take
+    // its tiles in turn (tile j by column group j mod ncg), so that one
+    // warp's copy issue does not set the pace of all eight.
+    const bool leader = active && cg == 0 && dh == 0;
+    const bool spread = kSpread && ks_n == 1;
+    auto spread_stager = [&](int j) { return active && dh == 0 && j % ncg == cg; };
     const int qbase = sd.len - sd.n_new;
 
     if (tid == 0) {
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&x.full[i], 1);
             mbar_init(&x.empty[i], 2 * ncg);
+            x.uses[i] = 0;
         }
         *x.abort_flag = 0;
         fence_mbar_init();
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool waited = kSparse;
     bool wrote = false;  // this warp stored new rows (fused store)
     int issued = 0;
-    if (leader) {
+    if (leader && !spread) {
         for (; issued < S && issued < my_tiles; ++issued) {
             const int t = ks + issued * ks_n;
             if (!waited && u.key0 + t * kTile + kTile > qbase) {
@@ -406,6 +419,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!kSparse && !waited)
             for (int j = issued; j < my_tiles && j < 2 * S; ++j)
                 prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
+    }
+    if (spread) {
+        for (int j = 0; j < S && j < my_tiles; ++j) {
+            if (!spread_stager(j)) continue;
+            const int t = ks + j * ks_n;
+            if (!waited && u.key0 + t * kTile + kTile > qbase) {
+                pdl_wait();
+                waited = true;
+            }
+            if (lane == 0) x.uses[ks * S + j] += 1;
+            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + j, lane, pol);
+        }
+        if (!kSparse && !waited)
+            for (int j = S; j < my_tiles && j < 2 * S; ++j)
+                if (spread_stager(j)) prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
     }
     if (!waited) pdl_wait();
 
@@ -493,23 +521,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16(acc[i], y0, y1, y2, y3, pb0, pb1);
                 mma_bf16(acc[i], y0, y1, y2, y3, pc0, pc1);
             }
-            // release the slot; its leader refills it with the slice's tile j + S
+            // release the slot; the slice's leader (or the stager of tile
+            // j + S when staging is spread) refills it with tile j + S
             __syncwarp();
             if (lane == 0) mbar_arrive(&x.empty[slot]);
-            if (leader && issued < my_tiles) {
+            if (!spread ? leader && issued < my_tiles : j + S < my_tiles && spread_stager(j + S)) {
                 if (!mbar_wait(&x.empty[slot], (j / S) & 1, c.status)) {
                     *x.abort_flag = 1;
                     break;
                 }
                 fence_proxy_async_smem();  // this slot's reads come before the next tile's writes
-                wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, ks + issued * ks_n, slot, lane, pol);
+                if (spread && lane == 0) x.uses[slot] += 1;
+                wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, ks + (j + S) * ks_n, slot, lane, pol);
                 ++issued;
             }
         }
         l0 = warp_sum_lanes(l0);
         l1 = warp_sum_lanes(l1);
     }
-    if (leader && *x.abort_flag) {
+    if (leader && !spread && *x.abort_flag) {
         // let every copy this slice issued land before the CTA's memory is released
         for (int j = issued > S ? issued - S : 0; j < issued; ++j)
             mbar_wait(&x.full[ks * S + j % S], (j / S) & 1, nullptr);
@@ -518,7 +548,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (wrote) __threadfence();  // stored rows visible before the next kernel starts
     __syncthreads();
     pdl_trigger();  // every thread has passed its grid-dependency wait
-    if (*x.abort_flag) return;
+    if (*x.abort_flag) {
+        // spread staging: a slot is refilled only once its previous tile was
+        // consumed, so at most its last copy can be in flight; let it land
+        if (spread && tid < kSlots && x.uses[tid] > 0)
+            mbar_wait(&x.full[tid], (x.uses[tid] - 1) & 1, nullptr);
+        return;
+    }
 
     // ---- merge the key slices (ks = 0, 1, ...) in order, inside the CTA ----
     const int NC = ncg * 8;
@@ -751,13 +787,14 @@ static int set_carveout() {
     return once_per_device(done, [] {
         const void *fns[] = {reinterpret_cast<const void *>(decode_combine<false>),
                              reinterpret_cast<const void *>(decode_combine<true>),
-                             reinterpret_cast<const void *>(decode_partial<false>),
-                             reinterpret_cast<const void *>(decode_partial<true>)};
+                             reinterpret_cast<const void *>(decode_partial<false, false>),
+                             reinterpret_cast<const void *>(decode_partial<false, true>),
+                             reinterpret_cast<const void *>(decode_partial<true, false>)};
         for (const void *f : fns)
             if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                 return PKV_ECUDA;
-        for (int i = 2; i < 4; ++i)
+        for (int i = 2; i < 5; ++i)
             if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes)) != cudaSuccess)
                 return PKV_ECUDA;
@@ -780,7 +817,11 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     DecodeArgs a{q, out, ws, ids, k, k_new, v_new, ik_new};
     // streams with no queries own no CTAs: give them an empty range
     Common cc = c;
-    auto part = sparse ? decode_partial<true> : decode_partial<false>;
+    // a stream with more than 16 query columns a unit has one key slice a CTA
+    bool wide = false;
+    for (int s = 0; s < c.n_seqs; ++s) wide |= c.seq[s].ncols > 16;
+    auto part = sparse ? decode_partial<true, false>
+                       : (wide ? decode_partial<false, true> : decode_partial<false, false>);
     auto comb = sparse ? decode_combine<true> : decode_combine<false>;
     if (set_carveout() != PKV_OK) return PKV_ECUDA;
     cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, maps, a);
