@@ -8,11 +8,14 @@
 // Pooled rows are looked up once per block (pg_at on its first position) and
 // staged in shared memory with 16-byte loads.
 //
-// Top-k: one CTA per (stream, head) finds the k-th largest score by an 8-bit
-// radix select on order-preserving keys (held in shared memory when the row
-// fits; each pass's digit found by one warp in parallel), then writes the
-// selected block ids in ascending order with an ordered compaction; an exact
-// tie at the threshold goes to the lower ids.
+// Top-k: one CTA per (stream, head) finds the k-th largest score on
+// order-preserving keys (held in shared memory when the row fits): one
+// histogram of the keys' top 11 bits locates the bin holding it, and when
+// that bin holds at most 512 keys the k-th largest is found by ranking them
+// directly; otherwise an 8-bit radix select over all 32 bits (each pass's
+// digit found by one warp in parallel).  The selected block ids are written
+// in ascending order by an ordered compaction; an exact tie at the threshold
+// goes to the lower ids.
 #include <algorithm>
 
 #include "pkv_dev.cuh"
@@ -107,6 +110,9 @@ __global__ void __launch_bounds__(kScoreThreads)
 
 constexpr int kTopThreads = 256;
 constexpr int kTopSmemKeys = 12288;  // order keys of a row held in shared memory (48 KB)
+constexpr int kTopBins = 2048;       // the first histogram: the keys' top 11 bits
+constexpr int kTopCand = 512;        // keys of the threshold bin ranked directly
+static_assert(kTopBins % kTopThreads == 0, "a thread sums whole groups of bins");
 
 __device__ __forceinline__ uint32_t order_key(float x) {
     uint32_t u = __float_as_uint(x);
@@ -146,9 +152,11 @@ __global__ void __launch_bounds__(kTopThreads)
     topk_kernel(const __grid_constant__ Common c, const float *__restrict__ scores, int32_t ld,
                 int32_t k, int32_t *__restrict__ ids, int32_t keys_in_smem) {
     __shared__ int hist[256];
+    __shared__ int hist11[kTopBins];      // counts of the keys' top 11 bits
+    __shared__ uint32_t cand[kTopCand];   // keys of the threshold bin
     __shared__ int warp_tot[kTopThreads / 32];
     __shared__ uint32_t sh_prefix;
-    __shared__ int sh_need;
+    __shared__ int sh_need, sh_m, sh_cnt;
     extern __shared__ uint32_t skeys[];  // the row's order keys, when it fits
     pdl_wait();
     pdl_trigger();
@@ -164,10 +172,73 @@ __global__ void __launch_bounds__(kTopThreads)
     __syncthreads();
     auto key_of = [&](int b) -> uint32_t { return in_smem ? skeys[b] : order_key(row[b]); };
 
-    // radix select: the key T with count(key > T) < kk <= count(key >= T)
+    // The threshold key T with count(key > T) < kk <= count(key >= T), and
+    // `need`, the number of keys equal to T to take.  First the top 11 bits:
+    // one histogram and a block-wide suffix count find the bin holding T;
+    // when that bin holds at most kTopCand keys, T is the one of them with
+    // the right rank among them.  Otherwise an 8-bit radix select over all
+    // 32 bits finds it.
     uint32_t prefix = 0, mask = 0;
     int need = kk;  // selected elements still to find inside the current prefix
+    bool found = false;
     if (kk > 0) {
+        for (int i = tid; i < kTopBins; i += kTopThreads) hist11[i] = 0;
+        if (tid == 0) sh_cnt = 0;
+        __syncthreads();
+        for (int b = tid; b < nb; b += kTopThreads) atomicAdd(&hist11[key_of(b) >> 21], 1);
+        __syncthreads();
+        // thread t: bins 2047 - 8t down to 2040 - 8t (descending keys)
+        constexpr int per = kTopBins / kTopThreads;
+        int own = 0;
+#pragma unroll
+        for (int i = 0; i < per; ++i) own += hist11[kTopBins - 1 - (per * tid + i)];
+        int above;  // keys in higher bins
+        block_exclusive_scan(own, &above, warp_tot);
+        if (above < need && need <= above + own) {  // the threshold bin is one of this thread's
+            int acc = above;
+            for (int i = 0; i < per; ++i) {
+                const int bin = kTopBins - 1 - (per * tid + i);
+                if (acc + hist11[bin] >= need) {
+                    sh_prefix = static_cast<uint32_t>(bin);
+                    sh_need = need - acc;
+                    sh_m = hist11[bin];
+                    break;
+                }
+                acc += hist11[bin];
+            }
+        }
+        __syncthreads();
+        const uint32_t bin = sh_prefix;
+        const int need1 = sh_need, m = sh_m;
+        if (m <= kTopCand) {
+            for (int b = tid; b < nb; b += kTopThreads) {
+                const uint32_t key = key_of(b);
+                if ((key >> 21) == bin) cand[atomicAdd(&sh_cnt, 1)] = key;
+            }
+            __syncthreads();
+            // T: the candidate with fewer than need1 larger candidates and at
+            // least need1 at or above it (equal keys write the same values)
+            for (int i = tid; i < m; i += kTopThreads) {
+                const uint32_t x = cand[i];
+                int gt = 0, ge = 0;
+                for (int j = 0; j < m; ++j) {
+                    const uint32_t y = cand[j];
+                    gt += y > x;
+                    ge += y >= x;
+                }
+                if (gt < need1 && need1 <= ge) {
+                    sh_prefix = x;
+                    sh_need = need1 - gt;
+                }
+            }
+            __syncthreads();
+            prefix = sh_prefix;
+            need = sh_need;
+            found = true;
+        }
+        __syncthreads();  // every thread has read sh_prefix and sh_need
+    }
+    if (kk > 0 && !found) {
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += kTopThreads) hist[i] = 0;
             __syncthreads();

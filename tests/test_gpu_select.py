@@ -77,6 +77,11 @@ def test_topk_ids_bit_identical_to_oracle(k):
     sc[1] = np.round(sc[1] * 2)            # heavy exact ties
     sc[4, 0, :] = 0.0                      # all equal
     sc[4, 1, ::2] = -0.0                   # signed zeros tie with +0
+    # more than 512 keys in the threshold's top-11-bit bin: the kernel's
+    # radix path instead of ranking the bin's keys directly
+    sc[0, 1, :] = 1.0                      # 2,250 equal keys
+    sc[0, 2, :] = 1.0
+    sc[0, 2, rng.choice(2250, 30, replace=False)] = 5.0   # 30 above, the rest tie at 1.0
     got = _topk(sc, lens, hq, k)
     for i, T in enumerate(lens):
         want = orc.topk(sc[i], k, nb=T // 4)
