@@ -710,6 +710,91 @@ __global__ void __launch_bounds__(kCombThreads, 4)
 }
 static_assert(kCombThreads == kHeadDim, "a thread a dim (one group), or two groups of half the dims");
 
+// The same merge for calls with many query columns and few splits (a prefill
+// chunk: thousands of columns, a few splits each), where a CTA a column
+// would spend its time being scheduled: a warp a (unit, column), eight
+// columns a CTA, lane l summing dims 8l .. 8l+7.  Lane i holds split i's
+// (m, l) (and i + 32's), so M and L reduce by shuffles as in decode_combine,
+// and O sums the splits in order, loading eight splits' values at a time.
+// comb_off counts these CTAs (set by launch_combine).
+__global__ void __launch_bounds__(kCombThreads)
+    combine_cols(const __grid_constant__ Common c, const DecodeArgs a) {
+    constexpr int kB = 8;  // splits loaded at a time
+    pdl_wait();
+    pdl_trigger();
+    const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
+    const SeqDev &sd = c.seq[s];
+    const int ns = sd.nsplit;
+    const int lane = threadIdx.x & 31;
+    const int r = (blockIdx.x - sd.comb_off) * (kCombThreads / 32) + (threadIdx.x >> 5);
+    if (r >= c.n_kv_heads * sd.ncols) return;  // past the stream's last column
+    const int unit = r / sd.ncols, col = r - unit * sd.ncols;
+    const float *part_acc = a.ws + sd.ws_off;
+    const float2 *col_ml =
+        reinterpret_cast<const float2 *>(part_acc + (int64_t)c.n_kv_heads * ns * sd.ncols * kHeadDim) +
+        (int64_t)unit * ns * sd.ncols + col;
+    const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
+    const float *col_acc = part_acc + p0 * kHeadDim + 8 * lane;
+    const int64_t stride = (int64_t)sd.ncols * kHeadDim;
+    const float2 none = make_float2(-INFINITY, 0.f);
+    const float2 ml0 = lane < ns ? __ldcg(col_ml + (int64_t)lane * sd.ncols) : none;
+    const float2 ml1 = lane + 32 < ns ? __ldcg(col_ml + (int64_t)(lane + 32) * sd.ncols) : none;
+    float M = fmaxf(ml0.x, ml1.x);
+    for (int i = lane + 64; i < ns; i += 32) M = fmaxf(M, __ldcg(col_ml + (int64_t)i * sd.ncols).x);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const bool empty = M == -INFINITY;
+    const float w0 = empty ? 0.f : ex2(ml0.x - M), w1 = empty ? 0.f : ex2(ml1.x - M);
+    float L = w0 * ml0.y + w1 * ml1.y;
+    for (int i = lane + 64; i < ns; i += 32) {
+        const float2 v = __ldcg(col_ml + (int64_t)i * sd.ncols);
+        L += (empty ? 0.f : ex2(v.x - M)) * v.y;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    float O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int b = 0; b < ns; b += kB) {
+        float4 v[kB][2];
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+            if (b + j < ns) {
+                v[j][0] = __ldcg(reinterpret_cast<const float4 *>(col_acc + (b + j) * stride));
+                v[j][1] = __ldcg(reinterpret_cast<const float4 *>(col_acc + (b + j) * stride) + 1);
+            }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int i = b + j;
+            if (i >= ns) break;
+            float w;
+            if (i < 64) w = __shfl_sync(0xffffffffu, i < 32 ? w0 : w1, i & 31);
+            else w = empty ? 0.f : ex2(__ldcg(col_ml + (int64_t)i * sd.ncols).x - M);
+            O[0] += w * v[j][0].x;
+            O[1] += w * v[j][0].y;
+            O[2] += w * v[j][0].z;
+            O[3] += w * v[j][0].w;
+            O[4] += w * v[j][1].x;
+            O[5] += w * v[j][1].y;
+            O[6] += w * v[j][1].z;
+            O[7] += w * v[j][1].w;
+        }
+    }
+    // o = O / L as in decode_combine, so both give the same bits for up to
+    // 32 splits (the same sums in the same order)
+    const bool any = L > 0.f;
+    const float lz = any ? L : 1.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) O[k] = any ? O[k] / lz : 0.f;
+    uint4 pk;
+    pk.x = pack_bf16(O[0], O[1]);
+    pk.y = pack_bf16(O[2], O[3]);
+    pk.z = pack_bf16(O[4], O[5]);
+    pk.w = pack_bf16(O[6], O[7]);
+    Unit u;
+    u.unit = unit;
+    u.kvh = unit;
+    *reinterpret_cast<uint4 *>(a.out + q_row<false>(c, sd, u, col) * kHeadDim + 8 * lane) = pk;
+}
+
 }  // namespace
 
 // ---- fixed scratch for pkv_decode_static -------------------------------------
@@ -806,6 +891,26 @@ int launch_combine(const Common &c, const DecodePlan &plan, const uint16_t *q, u
                    float *ws, cudaStream_t stream) {
     if (set_carveout() != PKV_OK) return PKV_ECUDA;
     DecodeArgs a{q, out, ws, nullptr, 0, nullptr, nullptr, nullptr};
+    // many split columns with few splits each (a prefill chunk): a warp a column
+    int nsm = 0;
+    if (sm_count(&nsm) != PKV_OK) return PKV_ECUDA;
+    int64_t cols = 0;
+    int max_ns = 0;
+    for (int s = 0; s < c.n_seqs; ++s)
+        if (c.seq[s].nsplit > 1) {
+            cols += (int64_t)c.n_kv_heads * c.seq[s].ncols;
+            max_ns = std::max(max_ns, c.seq[s].nsplit);
+        }
+    if (cols >= 8 * (int64_t)nsm && max_ns <= 64) {
+        Common cc = c;
+        int32_t ctas = 0;
+        for (int s = 0; s < cc.n_seqs; ++s) {
+            cc.seq[s].comb_off = ctas;
+            if (cc.seq[s].nsplit > 1)
+                ctas += (c.n_kv_heads * cc.seq[s].ncols + kCombThreads / 32 - 1) / (kCombThreads / 32);
+        }
+        return launch_status(launch_pdl(combine_cols, ctas, kCombThreads, 0, stream, cc, a));
+    }
     return launch_status(
         launch_pdl(decode_combine<false>, plan.total_comb, kCombThreads, 0, stream, c, a));
 }
