@@ -546,21 +546,21 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
             continue;
         }
         const int mtiles = (d.ncols + kM - 1) / kM;
-        // Splits.  A stream whose (KV head, M-tile) units fill the SMs by
-        // themselves is not split.  Otherwise the count with the least
-        // modelled time for this stream's grid on nsm SMs: waves x (tiles a
-        // CTA x a tile's time + a CTA's fixed cost) + the split partials'
-        // round trip through HBM.  The costs are this kernel's on GB300:
-        // about 1.26 us a 32-key tile of 128 rows, 12 us a CTA (Q load, TMEM,
-        // pipeline fill, epilogue) and 0.04 us a (unit, split) partial of
-        // 128 rows written and read back.  For 512 queries on 31,000 keys it
-        // picks 7 splits, 448 CTAs in three nearly full waves; 2 splits
-        // would give one wave of 128 CTAs with 24 SMs idle.  Only the
-        // stream's own length and rows and the SM count enter, so paged and
-        // contiguous caches get the same splits.
+        // Splits: the count with the least modelled time for this stream's
+        // grid on nsm SMs, waves x (tiles a CTA x a tile's time + a CTA's
+        // fixed cost) + the split partials' round trip through HBM.  The
+        // costs are this kernel's on GB300: about 1.26 us a 32-key tile of
+        // 128 rows, 12 us a CTA (Q load, TMEM, pipeline fill, epilogue) and
+        // 0.04 us a (unit, split) partial of 128 rows written and read back.
+        // For 512 queries on 31,000 keys it picks 7 splits, 448 CTAs in
+        // three nearly full waves (2 splits would give one wave of 128 CTAs
+        // with 24 SMs idle).  For 2,048 queries at 16,384 (256 units) it
+        // picks 4 splits, 7 nearly full waves, against 2 waves unsplit, the
+        // second two-thirds full.  Only the stream's own length and rows and
+        // the SM count enter, so paged and contiguous caches get the same
+        // splits.
         const int64_t units = (int64_t)H * mtiles, tiles = (d.len + kN - 1) / kN;
-        const int max_ns =
-            units >= nsm ? 1 : std::max(1, std::min(kMaxPrefillSplits, d.len / (4 * kN)));
+        const int max_ns = std::max(1, std::min(kMaxPrefillSplits, d.len / (4 * kN)));
         int ns = 1;
         int64_t best = INT64_MAX;
         for (int n = 1; n <= max_ns; ++n) {
