@@ -55,9 +55,9 @@ ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3
 # combine kernels), from the ncu capture summarised in
 # profiles/decode_partial_pages256.md, valid while the decode sources hash to
 # the value the capture was taken with; reported as null otherwise.
-DECODE_TRAFFIC = {"bytes": 40375040,
+DECODE_TRAFFIC = {"bytes": 40377600,
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "12d416d44711e705d89957330b8fafe06166b34e919c40824029b8f4258b0159"}
+                  "sha256": "7f6bf841c747d0e9920ea9a204187cf0254253d8d054efb0452d397f26966350"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
