@@ -144,6 +144,7 @@ __global__ void __maxnreg__(192)
     // scales, all completing on the slot's barrier.  With a fused store, the
     // rows of new positions are quantized here from k_new / v_new (the same
     // rule as pkv_store), written to the cache and to the stage directly.
+    bool wrote = false;  // this warp stored new rows (fused store)
     auto issue = [&](int t) {
         const int kt = key0 + (ks + t * ks_n) * kT8;
         const int slot = warp * kDepth8 + t % kDepth8;
@@ -201,6 +202,7 @@ __global__ void __maxnreg__(192)
                 todo &= todo - 1;
                 const int p = kt + rr;                           // its position
                 const bool write = !__shfl_sync(0xffffffffu, bad, rr);
+                wrote |= write;
                 const int64_t tr = (int64_t)sd.tok_off + (p - qbase);  // its packed input row
                 const int64_t pg_rr = shfl64(pg, rr);
                 const int row_rr = __shfl_sync(0xffffffffu, row, rr);
@@ -418,7 +420,7 @@ __global__ void __maxnreg__(192)
     }
 
     // ---- merge the key slices of each column group in a fixed order ----
-    if (fuse) __threadfence();  // stored rows visible before the next kernel starts
+    if (wrote) __threadfence();  // stored rows visible before the next kernel starts
     __syncthreads();
     if (fuse) pdl_trigger();
     const int NC = ncg * 8;
