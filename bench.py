@@ -57,7 +57,7 @@ ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3
 # the value the capture was taken with; reported as null otherwise.
 DECODE_TRAFFIC = {"bytes": 40377600,
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "7f6bf841c747d0e9920ea9a204187cf0254253d8d054efb0452d397f26966350"}
+                  "sha256": "81831ab304103b23ab0169048dd70500ad2d917bfcf337f357f7bb7e196b9d20"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 

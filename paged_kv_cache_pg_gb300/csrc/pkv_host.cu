@@ -27,17 +27,17 @@ int validate_layout(const pkv_layout *L) {
 
 
 int sm_count(int *out) {
-    static int cached[64];
+    static std::atomic<int> cached[64];  // per device, 0 until first asked
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ECUDA;
     if (dev < 0 || dev >= 64) return PKV_ECUDA;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return PKV_ECUDA;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    *out = cached[dev];
+    *out = n;
     return PKV_OK;
 }
 
