@@ -57,7 +57,7 @@ ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3
 # the value the capture was taken with; reported as null otherwise.
 DECODE_TRAFFIC = {"bytes": 40377600,
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "81831ab304103b23ab0169048dd70500ad2d917bfcf337f357f7bb7e196b9d20"}
+                  "sha256": "8b99ba9ebaa47951c66e0daa5c89d355954015e72ad200eea5aa5ed84af227bb"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 

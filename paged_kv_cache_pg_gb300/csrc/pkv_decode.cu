@@ -9,16 +9,20 @@
 // key slices; each slice is a pair of warps per column group of 8 query
 // columns (both compute S for the tile, each accumulates O for half of the
 // 256 dims).  A slice's lead warp stages its tiles into the slice's share of
-// the CTA's twelve 16 KB stage slots: it looks each key's row up once per
-// tile (#1169: key_at once per key per tile, beside the key ids; kept here as
-// the split's page offsets in shared memory and the row addresses in the
-// lanes) and copies a whole 16-row page run by 2D TMA, or key by key with
-// cp.async.  Cached rows stream before the grid-dependency wait; tiles past
-// the slots are prefetched into L2.  The warps compute S^T = K Q^T and
-// O^T += V^T P^T with warp MMAs (bf16 in, float32 accumulate), keep an online
-// softmax per query column, and merge their key slices in a fixed order.
-// Splits have a fixed length set by the stream's key count and the SM count,
-// so paged and contiguous caches give the same bits.
+// the CTA's twelve 16 KB stage slots (with one slice a CTA, more than 16
+// query columns a unit, the column groups' lead warps take its tiles in
+// turn): it looks each key's row up once per tile (#1169: key_at once per key
+// per tile, beside the key ids; kept here as the split's page offsets in
+// shared memory and the row addresses in the lanes) and copies a whole
+// 16-row page run by 2D TMA, or key by key with cp.async.  Cached rows stream
+// before the grid-dependency wait; tiles past the slots are prefetched into
+// L2.  The warps compute S^T = K Q^T and O^T += V^T P^T with warp MMAs (bf16
+// in, float32 accumulate), keep an online softmax per query column, and merge
+// their key slices in a fixed order.  Splits have a fixed length set by the
+// stream's key count and the SM count, so paged and contiguous caches give
+// the same bits.  A second kernel merges the splits: a CTA a query column
+// (decode_combine), or, for calls with thousands of columns and few splits
+// (a prefill chunk), a warp a column (combine_cols).
 #include <algorithm>
 #include <cfloat>
 #include <mutex>
