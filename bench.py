@@ -401,6 +401,9 @@ def bf16_peak():
         return 1900.0, "fallback"
 
 
+GRAPH_TIMING = "the row's calls captured once in a CUDA graph, each timed repetition a replay, L2 flushed before it"
+
+
 class FlushTimer:
     """Median CUDA-event time of a call on the current stream, with a buffer
     twice the L2 written and then read back before every timed call (not
@@ -416,12 +419,23 @@ class FlushTimer:
         self.buf.zero_()
         self.sink = self.buf.sum()
 
-    def ms(self, fn, reps=20, warm=3):
+    def ms(self, fn, reps=20, warm=3, graph=False):
+        """With `graph`, the calls of `fn` are captured once into a CUDA graph
+        and each timed repetition replays it (as a serving loop would), so the
+        host's time to issue the calls stays out of the timed region."""
         t = self.torch
         for _ in range(warm):
             self.flush()
             fn()
         t.cuda.synchronize()
+        run = fn
+        if graph:
+            g = t.cuda.CUDAGraph()
+            with t.cuda.graph(g):
+                fn()
+            g.replay()
+            t.cuda.synchronize()
+            run = g.replay
         e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
         out = []
         if self.profile:
@@ -429,7 +443,7 @@ class FlushTimer:
         for _ in range(reps):
             self.flush()
             e0.record()
-            fn()
+            run()
             e1.record()
             e1.synchronize()
             out.append(e0.elapsed_time(e1))
@@ -488,14 +502,15 @@ def row_prefill(torch, pkv, dev, timer):
     def step():
         store(), pool(), attend()
 
-    t = {"store": timer.ms(store), "pool": timer.ms(pool), "prefill": timer.ms(attend),
-         "step": timer.ms(step)}
+    t = {"store": timer.ms(store, graph=True), "pool": timer.ms(pool, graph=True),
+         "prefill": timer.ms(attend, graph=True), "step": timer.ms(step, graph=True)}
     if int(status.item()) != 0:
         raise RuntimeError(f"prefill row: device status {int(status.item())}")
     flop = 4.0 * sum(P0 + j + 1 for j in range(C)) * HQ * D
     peak, kind = bf16_peak()
     tf = flop / (t["prefill"] / 1e3) / 1e12
-    return {"workload": "chunked prefill: 512 queries on 31,000 cached positions, pages of 256, "
+    return {"timing": GRAPH_TIMING,
+            "workload": "chunked prefill: 512 queries on 31,000 cached positions, pages of 256, "
                         "16/2 heads", "us": {k: round(v * 1e3, 2) for k, v in t.items()},
             "flop": flop, "TFLOPs": round(tf, 1),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
@@ -534,8 +549,9 @@ def row_sparse(torch, pkv, dev, timer):
     def step():
         sc(), tk(), att()
 
-    t = {"block_scores": timer.ms(sc), "topk": timer.ms(tk), "sparse_decode": timer.ms(att),
-         "step": timer.ms(step)}
+    t = {"block_scores": timer.ms(sc, graph=True), "topk": timer.ms(tk, graph=True),
+         "sparse_decode": timer.ms(att, graph=True), "step": timer.ms(step, graph=True)}
+    step_direct = timer.ms(step)
     if int(status.item()) != 0:
         raise RuntimeError(f"sparse row: device status {int(status.item())}")
     # algorithmic bytes: pooled rows, scores written and read back, the selected
@@ -546,9 +562,11 @@ def row_sparse(torch, pkv, dev, timer):
     peak, kind = peaks()
     gbs = (b_scores + b_topk + b_att) / (t["step"] / 1e3) / 1e9
     att_gbs = b_att / (t["sparse_decode"] / 1e3) / 1e9
-    return {"workload": "block-sparse decode: 2 streams of 9,000, pages of 128, top-64 blocks",
+    return {"timing": GRAPH_TIMING,
+            "workload": "block-sparse decode: 2 streams of 9,000, pages of 128, top-64 blocks",
             "us": {k: round(v * 1e3, 2) for k, v in t.items()},
             "bytes": {"block_scores": b_scores, "topk": b_topk, "sparse_decode": b_att},
+            "step_us_direct_calls": round(step_direct * 1e3, 2),
             "GBps_step": round(gbs, 1), "GBps_sparse_decode": round(att_gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "peak_kind": kind},
@@ -593,14 +611,16 @@ def row_mix(torch, pkv, dev, timer):
     def step():
         dec(), pre()
 
-    t = {"draft_window_decode": timer.ms(dec), "prefill_lane": timer.ms(pre), "step": timer.ms(step)}
+    t = {"draft_window_decode": timer.ms(dec, graph=True), "prefill_lane": timer.ms(pre, graph=True),
+         "step": timer.ms(step, graph=True)}
     if int(status.item()) != 0:
         raise RuntimeError(f"mix row: device status {int(status.item())}")
     dec_bytes = sum(totals[:3]) * HKV * D * 2 * 2 + 2 * 3 * W * HQ * D * 2
     flop = 4.0 * sum(P0 + j + 1 for j in range(C)) * HQ * D
     peak, kind = peaks()
     dgbs = dec_bytes / (t["draft_window_decode"] / 1e3) / 1e9
-    return {"workload": "serving mix: 792 x 256 arena; 3 streams {9000, 24000, 40956} with 4-query "
+    return {"timing": GRAPH_TIMING,
+            "workload": "serving mix: 792 x 256 arena; 3 streams {9000, 24000, 40956} with 4-query "
                         "draft windows; 1 stream with a 2048-query chunk at 16,384",
             "us": {k: round(v * 1e3, 2) for k, v in t.items()},
             "draft_window_GBps": round(dgbs, 1), "draft_window_frac": round(dgbs / peak, 4),
@@ -627,10 +647,11 @@ def row_decode_layer(torch, pkv, dev, timer):
     def dec():
         pkv.decode(lay, sq, 0, HQ, q, out, ws, k_new=kn, v_new=vn, ik_new=ikn)
 
-    ms = timer.ms(dec, reps=50)
+    ms = timer.ms(dec, reps=50, graph=True)
     peak, kind = peaks()
     gbs = decode_bytes(lens_after) / (ms / 1e3) / 1e9
-    return {"workload": "one layer of the multi-stream decode at pages of 256, L2 flushed "
+    return {"timing": GRAPH_TIMING,
+            "workload": "one layer of the multi-stream decode at pages of 256, L2 flushed "
                         "before every call", "us": round(ms * 1e3, 2), "GBps": round(gbs, 1),
             "frac": round(gbs / peak, 4), "peak_kind": kind}
 
@@ -663,7 +684,7 @@ def row_prompt_cache(torch, pkv, dev, timer):
         pkv.store(lay, dst, 0, k, v, ik)
         pkv.pool(lay, dst, 0)
 
-    t = {"save": timer.ms(save), "restore": timer.ms(restore)}
+    t = {"save": timer.ms(save, graph=True), "restore": timer.ms(restore, graph=True)}
     torch.cuda.synchronize()
     same = all(torch.equal(a, b) for a, b in zip(_gather_all(torch, pkv, lay, dst, T, dev), (k, v, ik, pooled)))
     row = T * (2 * HKV * D + DI) * 2 + (T // 4) * DI * 2   # bytes of one copy of the stream
@@ -672,7 +693,8 @@ def row_prompt_cache(torch, pkv, dev, timer):
     peak, kind = peaks()
     g_save = b_save / (t["save"] / 1e3) / 1e9
     g_restore = b_restore / (t["restore"] / 1e3) / 1e9
-    return {"workload": "prompt-cache save/restore: 1 stream of 31,512 positions, pages of 256, "
+    return {"timing": GRAPH_TIMING,
+            "workload": "prompt-cache save/restore: 1 stream of 31,512 positions, pages of 256, "
                         "one layer (K, V, indexer, pooled rows)",
             "us": {k_: round(v_ * 1e3, 2) for k_, v_ in t.items()},
             "GBps": {"save": round(g_save, 1), "restore": round(g_restore, 1)},

@@ -88,6 +88,22 @@ def test_topk_ids_bit_identical_to_oracle(k):
         assert np.array_equal(got[i], want), (i, T)
 
 
+@pytest.mark.parametrize("m", [63, 64, 65])
+def test_topk_threshold_bin_of_63_64_65_keys(m):
+    """m keys in [3, 3.5), one top-11-bit bin, above every other key: a
+    threshold inside that bin takes the one-warp sort up to 64 keys and the
+    direct ranking past it."""
+    rng = np.random.default_rng(900 + m)
+    sc = rng.uniform(-1.9, 1.9, (1, 2, 2250)).astype(np.float32)
+    for h in range(2):
+        pos = rng.choice(2250, m, replace=False)
+        sc[0, h, pos] = rng.uniform(3.01, 3.49, m).astype(np.float32)
+    sc[0, 1, pos[: m // 2]] = 3.25  # exact ties inside the bin
+    for k in (1, 10, m - 1, m):
+        got = _topk(sc, [9000], 2, k)
+        assert np.array_equal(got[0], orc.topk(sc[0], k, nb=2250)), k
+
+
 def test_sparse_config_scores_topk_and_attention():
     t = torch()
     lens = [9000, 9000]
