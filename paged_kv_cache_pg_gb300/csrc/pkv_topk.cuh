@@ -1,5 +1,5 @@
-// Block-wide top-k selection of one row of block scores, for any block of
-// 256 threads and shared memory the caller provides.
+// Block-wide top-k selection of one row of block scores, for a block of
+// kTopThreads threads and shared memory the caller provides.
 //
 // The k-th largest order key T is found first (one histogram of the keys'
 // top 11 bits locates the bin holding it; when that bin holds at most 64 keys
@@ -13,7 +13,11 @@
 
 namespace pkv {
 
-constexpr int kTopThreads = 256;
+#ifndef PKV_TOPK_THREADS
+#define PKV_TOPK_THREADS 512
+#endif
+constexpr int kTopThreads = PKV_TOPK_THREADS;
+static_assert(kTopThreads % 32 == 0 && kTopThreads <= 1024, "whole warps, at most 32 of them");
 constexpr int kTopBins = 2048;       // the first histogram: the keys' top 11 bits
 constexpr int kTopCand = 512;        // keys of the threshold bin ranked directly
 static_assert(kTopBins % kTopThreads == 0, "a thread sums whole groups of bins");
@@ -87,7 +91,7 @@ __device__ __forceinline__ void block_exclusive_scan2(int v0, int v1, int *excl0
     *excl1 = before.y + x1 - v1;
 }
 
-// The shared memory one selection works in (any 256-thread block).
+// The shared memory one selection works in.
 struct TopkSmem {
     int *hist;         // [256]
     int *hist11;       // [kTopBins]
