@@ -22,15 +22,23 @@ namespace {
 
 constexpr int kScoreBlocks = 32;   // blocks a CTA: a lane each
 constexpr int kScoreThreads = 256;
-constexpr int kPStride = kIdxDim + 1;  // float stride of a staged pooled row
+// float stride of a staged pooled row: 16-byte rows whose lanes' 16-byte
+// loads spread over the banks (528 B apart)
+constexpr int kPStride = kIdxDim + 4;
 constexpr int kMaxQHeads = 64;
 
-__global__ void __launch_bounds__(kScoreThreads)
+// Four bf16 values (two packed words, low half first) as floats: exact.
+__device__ __forceinline__ float4 bf16x4_to_float4(uint32_t u0, uint32_t u1) {
+    return make_float4(__uint_as_float(u0 << 16), __uint_as_float(u0 & 0xffff0000u),
+                       __uint_as_float(u1 << 16), __uint_as_float(u1 & 0xffff0000u));
+}
+
+__global__ void __launch_bounds__(kScoreThreads, 1)
     scores_kernel(const __grid_constant__ Common c, const uint16_t *__restrict__ qi,
                   float *__restrict__ scores, int32_t ld, int32_t tiles_per_seq) {
-    __shared__ float ps[kScoreBlocks * kPStride];
+    __shared__ __align__(16) float ps[kScoreBlocks * kPStride];
     __shared__ int64_t prow[kScoreBlocks];  // each block's pooled row (-1 past the end)
-    extern __shared__ float qs[];  // [n_q_heads][Di]
+    extern __shared__ float4 qs4[];  // [n_q_heads][Di / 4]
     pdl_wait();
     pdl_trigger();
     const int s = blockIdx.x / tiles_per_seq;
@@ -55,10 +63,8 @@ __global__ void __launch_bounds__(kScoreThreads)
         const uint4 *src = reinterpret_cast<const uint4 *>(qi + (int64_t)sd.tok_off * Hq * Di);
         for (int i = tid; i < Hq * Di / 8; i += kScoreThreads) {
             const uint4 w = __ldg(src + i);
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                qs[8 * i + e] = __uint_as_float((e & 1) ? (u[e / 2] & 0xffff0000u) : (u[e / 2] << 16));
+            qs4[2 * i] = bf16x4_to_float4(w.x, w.y);
+            qs4[2 * i + 1] = bf16x4_to_float4(w.z, w.w);
         }
     }
     __syncthreads();
@@ -75,27 +81,32 @@ __global__ void __launch_bounds__(kScoreThreads)
 #pragma unroll
     for (int it = 0; it < kLoads; ++it) {
         const int i = tid + it * kScoreThreads, bl = i >> 4, c16 = i & 15;
-        const uint32_t u[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            ps[bl * kPStride + 8 * c16 + e] =
-                __uint_as_float((e & 1) ? (u[e / 2] & 0xffff0000u) : (u[e / 2] << 16));
+        float4 *dst = reinterpret_cast<float4 *>(ps + bl * kPStride + 8 * c16);
+        dst[0] = bf16x4_to_float4(w[it].x, w[it].y);
+        dst[1] = bf16x4_to_float4(w[it].z, w[it].w);
     }
     __syncthreads();
     const int lane = tid & 31, warp = tid >> 5;
     // a warp takes heads h and h + 8, each lane block lane of the tile: two
     // chains side by side, each still summed in d order
-    const float *pa = ps + lane * kPStride;
+    // (four dims a shared-memory load, each chain still taken in d order)
+    const float4 *pa = reinterpret_cast<const float4 *>(ps + lane * kPStride);
     for (int h = warp; h < Hq; h += 2 * (kScoreThreads / 32)) {
         const int h2 = h + kScoreThreads / 32;
         const bool two = h2 < Hq;
-        const float *qa = qs + h * Di, *qb = qs + (two ? h2 : h) * Di;
+        const float4 *qa = qs4 + h * (kIdxDim / 4), *qb = qs4 + (two ? h2 : h) * (kIdxDim / 4);
         float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-        for (int d = 0; d < kIdxDim; ++d) {
-            const float u = pa[d];
-            a0 = __fmaf_rn(qa[d], u, a0);
-            a1 = __fmaf_rn(qb[d], u, a1);
+#pragma unroll 4
+        for (int d4 = 0; d4 < kIdxDim / 4; ++d4) {
+            const float4 u = pa[d4], x = qa[d4], y = qb[d4];
+            a0 = __fmaf_rn(x.x, u.x, a0);
+            a1 = __fmaf_rn(y.x, u.x, a1);
+            a0 = __fmaf_rn(x.y, u.y, a0);
+            a1 = __fmaf_rn(y.y, u.y, a1);
+            a0 = __fmaf_rn(x.z, u.z, a0);
+            a1 = __fmaf_rn(y.z, u.z, a1);
+            a0 = __fmaf_rn(x.w, u.w, a0);
+            a1 = __fmaf_rn(y.w, u.w, a1);
         }
         const int ba = b0 + lane;
         if (ba < ld) {
