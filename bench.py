@@ -52,10 +52,10 @@ NOMINAL_HBM = 8000.0
 ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3", "page_runs",
         "allocator"]
 # DRAM bytes (read + write) of one pkv_decode call of the workload (partial +
-# combine kernels), from the ncu capture summarised in
-# profiles/decode_partial_pages256.md, valid while the decode sources hash to
-# the value the capture was taken with; reported as null otherwise.
-DECODE_TRAFFIC = {"bytes": 40377600,
+# combine kernels), from one ncu capture of the decode kernels (summary under
+# profiles/), valid while the decode sources hash to the value the capture
+# was taken with; reported as null, with the capture date, otherwise.
+DECODE_TRAFFIC = {"bytes": 40377600, "captured": "2026-12-02",
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
                   "sha256": "8b99ba9ebaa47951c66e0daa5c89d355954015e72ad200eea5aa5ed84af227bb"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
@@ -1041,6 +1041,8 @@ def main_ours(args):
     achieved = decode_bytes(lens_after) / dur / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": decode_traffic(),
+            "traffic_captured": DECODE_TRAFFIC["captured"],
+            "traffic_valid": decode_traffic() is not None,
             "algorithmic_bytes": decode_bytes(lens_after),
             "kernel": "pkv_decode (split-KV partial with fused store + combine), one layer, 4 streams",
             "avg_launch_us": round(dur * 1e6, 3), "peak_kind": peak_kind,

@@ -322,7 +322,10 @@ int pkv_prefill(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, i
  * the process exits) instead of a workspace.  The call allocates nothing.
  * EINVAL if the batch needs more than 4 MiB of partials (pkv_decode_ws_size
  * tells).  The first call on a device looks the array's address up on that
- * device, so make it before capturing a stream into a graph.  All calls share
+ * device, so make it before capturing a stream into a graph.  The address is
+ * kept for the life of the process: after cudaDeviceReset on a device the
+ * kept address is stale, so the call must not be used on that device again
+ * in the same process.  All calls share
  * the one array: calls that may run at the same time on the GPU (different
  * streams, or graphs launched concurrently) race on it; issue them in order.
  * Nothing in the array needs to start at zero. */

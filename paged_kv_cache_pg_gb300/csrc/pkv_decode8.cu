@@ -15,11 +15,16 @@
 // be a NaN pattern).  Per tile a warp computes S^T = K Q^T and
 // O^T += V^T P^T with mma.sync in f16 (an e4m3 code widens to f16 exactly;
 // the queries are converted once), applies the K scale to S in float32,
-// and keeps an online softmax per query column.  The V scale is folded into
-// P relative to the largest V scale the warp has seen (R, rescaled like the
-// running max), so P' = P x scale_v / R stays in [0, 1] where f16 is
-// precise, and P' is split into f16 hi + lo parts; O is multiplied by R at
-// the end.  Dims are permuted inside the MMAs so
+// and keeps an online softmax per query column.  The V scale s = 2^E x mant
+// (mant in [1, 2)) is folded into each key's weight: the sum of weights L
+// keeps the logit's running maximum m, while O keeps a running maximum u of
+// logit + E of its own, so the weight of the key that carries most of O is
+// near 1 and every weight 2^(x + E - u) x mant lies in [0, 2), where f16 is
+// precise whatever the spread of the row scales (a reference on the scales
+// alone lets the weight of a large-scale key with a small softmax weight
+// fall into f16's subnormals).  The weights are split into f16 hi + lo
+// parts; O is brought back to m's reference once, at the end.  Dims are
+// permuted inside the MMAs so
 // every operand fragment comes from contiguous 16-byte shared-memory loads:
 // in S thread group c (lane & 3) sums dims 64c .. 64c+63; in O^T row g of
 // M-tile m is dim 32g + 2m and row g+8 is dim 32g + 2m + 1.
@@ -95,6 +100,16 @@ __device__ __forceinline__ float max_over_g(float v) {  // lanes sharing lane & 
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
     return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+
+// s = 2^e x mant with mant in [1, 2); a zero or subnormal scale (a row of
+// values below 2^-126 x 448) gives e = -inf, so its weight is 0.
+__device__ __forceinline__ void pow2_split(float s, float &e, float &mant) {
+    const uint32_t b = __float_as_uint(s);
+    const int ex = static_cast<int>((b >> 23) & 0xffu);
+    const bool normal = ex != 0 && ex != 0xff;
+    e = normal ? static_cast<float>(ex - 127) : -INFINITY;
+    mant = normal ? __uint_as_float((b & 0x007fffffu) | 0x3f800000u) : 0.f;
 }
 
 __device__ __forceinline__ float sum_over_g(float v) {
@@ -307,7 +322,7 @@ __global__ void __maxnreg__(192)
 #pragma unroll
     for (int m = 0; m < 16; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-    float R = 0.f;  // the largest V scale of the tiles so far
+    float uA = -INFINITY, uB = -INFINITY;  // running max of logit + V-scale exponent (O's reference)
 
     for (int t = 0; t < my_tiles; ++t) {
         const int slot = warp * kDepth8 + t % kDepth8;
@@ -357,25 +372,27 @@ __global__ void __maxnreg__(192)
         lB = lB * alB + sum_over_g(p[1] + p[3]);
         mA = nA;
         mB = nB;
-        // the tile's largest V scale (lanes 0 .. 15 hold the 16 keys' scales)
-        float smax = lane < 16 ? scl[16 + lane] : 0.f;
-#pragma unroll
-        for (int o = 8; o; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
-        smax = __shfl_sync(0xffffffffu, smax, 0);
-        const float Rn = fmaxf(R, smax);
-        const float rho = Rn > 0.f ? R / Rn : 0.f;  // O was accumulated relative to R
-        R = Rn;
-        const float invR = R > 0.f ? 1.f / R : 0.f;
+        // ---- weights of O: 2^(x + E - u) x mant for the V scale 2^E x mant ----
+        float ea, ma, eb, mb;
+        pow2_split(scl[16 + g], ea, ma);
+        pow2_split(scl[16 + g + 8], eb, mb);
+        const float y0 = x[0] + ea, y1 = x[1] + ea, y2 = x[2] + eb, y3 = x[3] + eb;
+        const float nuA = fmaxf(uA, max_over_g(fmaxf(y0, y2)));
+        const float nuB = fmaxf(uB, max_over_g(fmaxf(y1, y3)));
+        const float vA = nuA == -INFINITY ? 0.f : nuA, vB = nuB == -INFINITY ? 0.f : nuB;
+        const float beA = ex2(uA - vA), beB = ex2(uB - vB);  // 0 while nothing was accumulated
+        uA = nuA;
+        uB = nuB;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
-            acc[m][0] *= alA * rho;
-            acc[m][1] *= alB * rho;
-            acc[m][2] *= alA * rho;
-            acc[m][3] *= alB * rho;
+            acc[m][0] *= beA;
+            acc[m][1] *= beB;
+            acc[m][2] *= beA;
+            acc[m][3] *= beB;
         }
-        // ---- P' = P x V scale / R, f16 hi + lo, to the B-operand layout ----
-        const float sva = scl[16 + g] * invR, svb = scl[16 + g + 8] * invR;
-        const float q0 = p[0] * sva, q1 = p[1] * sva, q2 = p[2] * svb, q3 = p[3] * svb;
+        // ---- the weights as f16 hi + lo, to the B-operand layout ----
+        const float q0 = ex2(y0 - vA) * ma, q1 = ex2(y1 - vB) * ma;
+        const float q2 = ex2(y2 - vA) * mb, q3 = ex2(y3 - vB) * mb;
         const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
         const __half2 l01 = __floats2half2_rn(q0 - __low2float(h01), q1 - __high2float(h01));
         const __half2 l23 = __floats2half2_rn(q2 - __low2float(h23), q3 - __high2float(h23));
@@ -427,13 +444,16 @@ __global__ void __maxnreg__(192)
     float *mbuf = reinterpret_cast<float *>(sm8);  // [ks][NC][kMS8]
     float *mlb = mbuf + ks_n * NC * kMS8;          // [ks][NC][2]
     if (active) {
+        // O from its own reference u back to the logits' m: 2^(u - m)
+        const float fA = uA == -INFINITY ? 0.f : ex2(uA - mA);
+        const float fB = uB == -INFINITY ? 0.f : ex2(uB - mB);
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
             const int d0 = 33 * g + 2 * m;  // dim 32 g + 2 m, skewed by g
-            mbuf[(ks * NC + colA) * kMS8 + d0] = acc[m][0] * R;
-            mbuf[(ks * NC + colB) * kMS8 + d0] = acc[m][1] * R;
-            mbuf[(ks * NC + colA) * kMS8 + d0 + 1] = acc[m][2] * R;
-            mbuf[(ks * NC + colB) * kMS8 + d0 + 1] = acc[m][3] * R;
+            mbuf[(ks * NC + colA) * kMS8 + d0] = acc[m][0] * fA;
+            mbuf[(ks * NC + colB) * kMS8 + d0] = acc[m][1] * fB;
+            mbuf[(ks * NC + colA) * kMS8 + d0 + 1] = acc[m][2] * fA;
+            mbuf[(ks * NC + colB) * kMS8 + d0 + 1] = acc[m][3] * fB;
         }
         if (g == 0) {
             mlb[(ks * NC + colA) * 2 + 0] = mA;

@@ -25,6 +25,21 @@ def normal_bf16(seed: int, shape: Sequence[int]) -> np.ndarray:
     return (x.view(np.uint32) >> 16).astype(np.uint16)
 
 
+def scale_pow2(bits: np.ndarray, e) -> np.ndarray:
+    """bf16 bit patterns times 2**e, exactly: a power of two moves the
+    exponent only.  `e` is an int or an integer array broadcastable to `bits`.
+    Raises if a nonzero result would leave the normal bf16 range."""
+    x = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    y = (x * np.exp2(np.asarray(e, np.float64))).astype(np.float32)
+    a = np.abs(y)
+    if not np.all((a == 0) | ((a >= 2.0 ** -126) & (a < 2.0 ** 127))):
+        raise ValueError("scaled value outside the normal bf16 range")
+    u = y.view(np.uint32)
+    if np.any(u & 0xFFFF):
+        raise ValueError("scaling was not exact")
+    return (u >> 16).astype(np.uint16)
+
+
 def pages_for(length: int, ptok: int) -> int:
     """Pages a stream of `length` positions occupies."""
     return -(-length // ptok)

@@ -39,18 +39,35 @@ def bound(ref: np.ndarray) -> np.ndarray:
     return ATOL + RTOL * np.abs(ref) + half_ulp_bf16(ref)
 
 
+# Totals over every within_tol call of the session: elements checked,
+# elements inside the bound only thanks to its half-ulp term, and the worst
+# error of a passing check as a fraction of its bound (printed in the pytest
+# summary by conftest.py).
+TOL_STATS = {"calls": 0, "checked": 0, "needed_half_ulp": 0, "worst_frac_of_bound": 0.0}
+
+
 def within_tol(gpu_bf16_bits: np.ndarray, ref: np.ndarray):
     """|gpu - ref| <= bound(ref) elementwise.
 
     Returns (ok, report); the report names the worst element, its index,
-    the GPU value and the oracle value, and how many elements fail."""
+    the GPU value and the oracle value, how many elements fail, and how
+    many pass only through the half-ulp term of the bound."""
     g = (gpu_bf16_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     g = g.reshape(ref.shape)
-    err = np.abs(g - ref) - bound(ref)
+    diff = np.abs(g - ref)
+    err = diff - bound(ref)
     ok = bool((err <= 0).all() and np.isfinite(g).all())
+    half = int(((diff > ATOL + RTOL * np.abs(ref)) & (err <= 0)).sum())
+    frac = float(np.nanmax(np.where(np.isfinite(diff), diff / bound(ref), np.inf))) if ref.size else 0.0
+    TOL_STATS["calls"] += 1
+    TOL_STATS["checked"] += int(ref.size)
+    TOL_STATS["needed_half_ulp"] += half
+    if ok:   # red controls, which must fail, do not count
+        TOL_STATS["worst_frac_of_bound"] = max(TOL_STATS["worst_frac_of_bound"], frac)
     i = np.unravel_index(int(np.nanargmax(np.where(np.isfinite(err), err, np.inf))), ref.shape)
     report = (f"worst excess {float(err[i]):.3g} at {tuple(int(x) for x in i)}: gpu {g[i]!r} "
               f"oracle {ref[i]!r}; {int((err > 0).sum())} of {err.size} outside; "
+              f"{half} inside only through the half-ulp term; "
               f"non-finite {int((~np.isfinite(g)).sum())}")
     return ok, report
 

@@ -1,0 +1,269 @@
+"""GPU parity on inputs that reach every numeric branch of the kernels.
+
+The other parity tests draw queries and keys from N(0, 1): with D = 256 and
+the 1/16 scale their logits are about N(0, 1), so a row's softmax stays
+flat, its running maximum barely moves after the first tile, and every row's
+magnitude is near 1.  The contract still holds every attention row within
+the float64 bound over all inputs (#1169 Receipt: "attention rows within a
+float64 bound"), so here the inputs are shaped to reach what those draws do
+not:
+
+- queries scaled by 8 and 16 (exact powers of two): logits of standard
+  deviation 8 and 16, a few keys carry each row's softmax and the running
+  maximum of a row keeps jumping from tile to tile;
+- a key planted late in the context along one head's query, its logit far
+  above every earlier one, after many tiles of keys;
+- value rows scaled by 2^e with e spread over [-20, 20] across positions
+  (and key rows over [-4, 4]), in the bf16 and the e4m3 layouts (the e4m3
+  decode folds each row's value scale into its softmax weight);
+- a prefill chunk whose every row is checked and which takes several
+  splits, several 128-row M-tiles and the column-per-warp combine.
+
+For the prefill the lazy rescale of O (corrected only when a row's running
+maximum grows by more than 2^8) is shown to fire: the test computes the
+rows' logits from the inputs and asserts that some row's maximum past the
+first 32-key tile of its split exceeds that tile's maximum by more than 8 in
+log2 units, for the split lengths the call can have taken.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+from paged_kv_cache_pg_gb300 import pkv, synth
+
+from gpu_setup import decode, dev_u16, host_u16, oracle_decode, place, torch, within_tol
+
+pytestmark = pytest.mark.gpu
+
+LOG2E = 1.4426950408889634
+TILE = 32          # keys a prefill S tile
+RESCALE = 8.0      # log2 units of growth before the prefill rescales O
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_pg_gb300 import build
+    build.build()
+    pkv.load()
+
+
+def _f(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _planted(stream, layer, pos, kvh, row_bits):
+    """The stream with key `pos` of KV head `kvh` replaced by row_bits."""
+    k = stream.k.copy()
+    k[layer, pos, kvh] = row_bits
+    return synth.Stream(stream.length, k, stream.v, stream.ik)
+
+
+def _spread(stream, seed, k_range=4, v_range=20):
+    """Key rows times 2^[-k_range, k_range] and value rows times
+    2^[-v_range, v_range], drawn per (layer, position, head)."""
+    rng = np.random.default_rng(seed)
+    shp = stream.k.shape[:3] + (1,)
+    ek = rng.integers(-k_range, k_range + 1, shp)
+    ev = rng.integers(-v_range, v_range + 1, shp)
+    return synth.Stream(stream.length, synth.scale_pow2(stream.k, ek),
+                        synth.scale_pow2(stream.v, ev), stream.ik)
+
+
+def _logits_log2(stream, layer, q, qbase, group):
+    """logits[j, h, key] in log2 units for query j (position qbase + j) and
+    head h, -inf past the causal limit: only to state which rows make the
+    prefill rescale; the parity reference is the oracle."""
+    n, hq, _ = q.shape
+    qf = _f(q)
+    out = np.full((n, hq, stream.length), -np.inf)
+    for h in range(hq):
+        kf = _f(stream.k[layer, :, h // group])          # [T][D]
+        s = qf[:, h, :] @ kf.T / 16.0 * LOG2E            # [n][T]
+        for j in range(n):
+            out[j, h, :qbase + j + 1] = s[j, :qbase + j + 1]
+    return out
+
+
+def _rescale_rows(lg, split_len):
+    """Rows whose running maximum grows by more than RESCALE over the first
+    tile of some split of `split_len` keys."""
+    n, hq, T = lg.shape
+    fires = 0
+    for k0 in range(0, T, split_len):
+        k1 = min(T, k0 + split_len)
+        first = lg[:, :, k0:min(k1, k0 + TILE)].max(axis=2)
+        later = lg[:, :, k0 + TILE:k1].max(axis=2) if k1 > k0 + TILE else np.full((n, hq), -np.inf)
+        ok = np.isfinite(first) & (later > first + RESCALE + 0.5)
+        fires += int(ok.sum())
+    return fires
+
+
+def _prefill(pl, lens, n_new, layer, hq, q_list):
+    t = torch()
+    seqs = pl.seqs(lens, n_new)
+    q = dev_u16(np.concatenate(q_list))
+    out = t.zeros_like(q)
+    ws_bytes = pkv.prefill_ws_size(pl.lay, seqs, hq)
+    ws = t.zeros(max(64, ws_bytes // 4 + 64), dtype=t.float32, device="cuda")
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    pkv.prefill(pl.lay, seqs, layer, hq, q, out, ws, status=status)
+    t.cuda.synchronize()
+    assert int(status.item()) == 0
+    return host_u16(out), ws_bytes
+
+
+# ---- prefill: the lazy rescale of O ---------------------------------------------
+
+@pytest.mark.parametrize("qscale", [3, 4])          # queries x 8, x 16
+@pytest.mark.parametrize("ptok", [16, 48, None])
+def test_prefill_lazy_rescale_fires_and_matches_oracle(qscale, ptok):
+    lay = pkv.layout(1, 2, 256, 128)
+    lens, n_new = [200, 77], [60, 77]   # one split each (fewer than 256 keys)
+    base = [synth.make_stream(4000 + i, 1, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q = [synth.scale_pow2(synth.queries(4100 + i, n, 16, 256), qscale)
+         for i, n in enumerate(n_new)]
+    # a key at position 150 along query 40 (position 180) of head 3, unscaled
+    streams = [_planted(base[0], 0, 150, 0, synth.queries(4100, n_new[0], 16, 256)[40, 3]),
+               base[1]]
+    fires = sum(_rescale_rows(_logits_log2(s, 0, qq, T - n, 8), 1 << 30)
+                for s, qq, T, n in zip(streams, q, lens, n_new))
+    assert fires > 0, "no row's running max grows past the rescale threshold"
+    pl = place(lay, streams, ptok, seed=11) if ptok else place(lay, streams, None)
+    got, ws_bytes = _prefill(pl, lens, n_new, 0, 16, q)
+    assert ws_bytes == 0                  # one split: the premise above holds for it
+    ok, report = within_tol(got, oracle_decode(pl, 0, 16, q))
+    assert ok, report
+    if ptok:
+        cont = place(lay, streams, None)
+        assert np.array_equal(_prefill(cont, lens, n_new, 0, 16, q)[0], got)
+
+
+@pytest.mark.parametrize("qscale", [0, 3])
+def test_prefill_mid_chunk_every_row_several_splits_and_mtiles(qscale):
+    # 2,048 cached positions + a 256-query chunk, pages of 48: 16 M-tiles of
+    # 128 rows a KV head, several splits (so split partials, merged by the
+    # column-per-warp combine: 4,096 split columns), every row checked
+    lay = pkv.layout(1, 2, 256, 128)
+    P0, C = 2048, 256
+    T = P0 + C
+    s = synth.make_stream(4200 + qscale, 1, T, 2, 256, 128)
+    q = synth.scale_pow2(synth.queries(4300 + qscale, C, 16, 256), qscale)
+    pl = place(lay, [s], 48, seed=12)
+    got, ws_bytes = _prefill(pl, [T], [C], 0, 16, [q])
+    # partials of several splits: 2 heads x ns x 2,048 columns x (256 + 2) floats
+    ns = ws_bytes // 4 // (2 * C * 8 * 258)
+    assert ns >= 2, ws_bytes
+    ok, report = within_tol(got, oracle_decode(pl, 0, 16, [q]))
+    assert ok, report
+    cont = place(lay, [s], None)
+    assert np.array_equal(_prefill(cont, [T], [C], 0, 16, [q])[0], got)
+    if qscale:
+        # the split lengths the plan can have used for ns splits
+        lens_ok = {-(-(-(-T // n)) // TILE) * TILE for n in range(1, 65)}
+        lens_ok = [sl for sl in lens_ok if -(-T // sl) == ns]
+        lg = _logits_log2(s, 0, q, P0, 8)
+        for sl in lens_ok:
+            assert _rescale_rows(lg, sl) > 0, sl
+
+
+# ---- decode: peaked softmax, a late jump of the running max ----------------------
+
+@pytest.mark.parametrize("qscale", [0, 3, 4])
+def test_decode_peaked_softmax_and_late_key(qscale):
+    lay = pkv.layout(1, 2, 256, 128)
+    lens = [1001, 3001, 6001, 9001]
+    base = [synth.make_stream(4400 + i, 1, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q0 = [synth.queries(4500 + i, 1, 16, 256) for i in range(4)]
+    q = [synth.scale_pow2(x, qscale) for x in q0]
+    # stream i: a key 3 positions before its query, along head 5's query
+    # (KV head 0), so that row's maximum jumps in the last tile of the last split
+    streams = [_planted(b, 0, T - 3, 0, x[0, 5]) for b, T, x in zip(base, lens, q0)]
+    cont = place(lay, streams, None)
+    got = decode(cont, 0, 16, q)
+    ok, report = within_tol(got, oracle_decode(cont, 0, 16, q))
+    assert ok, report
+    pl = place(lay, streams, 16, seed=13)
+    assert np.array_equal(decode(pl, 0, 16, q), got)
+
+
+@pytest.mark.parametrize("qscale", [3, 4])
+def test_draft_windows_peaked(qscale):
+    lay = pkv.layout(1, 2, 256, 128)
+    lens = [2004, 704, 97, 4]
+    streams = [synth.make_stream(4600 + i, 1, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q = [synth.scale_pow2(synth.queries(4700 + i, 4, 16, 256), qscale) for i in range(4)]
+    cont = place(lay, streams, None)
+    got = decode(cont, 0, 16, q)
+    ok, report = within_tol(got, oracle_decode(cont, 0, 16, q))
+    assert ok, report
+    pl = place(lay, streams, 48, seed=14)
+    assert np.array_equal(decode(pl, 0, 16, q), got)
+
+
+def test_decode_value_rows_spread_over_2_pow_40():
+    lay = pkv.layout(1, 2, 256, 128)
+    lens = [3001, 513]
+    streams = [_spread(synth.make_stream(4800 + i, 1, T, 2, 256, 128), 4810 + i)
+               for i, T in enumerate(lens)]
+    for qscale in (0, 3):
+        q = [synth.scale_pow2(synth.queries(4900 + i, 1, 16, 256), qscale) for i in range(2)]
+        pl = place(lay, streams, 48, seed=15)
+        got = decode(pl, 0, 16, q)
+        ok, report = within_tol(got, oracle_decode(pl, 0, 16, q))
+        assert ok, (qscale, report)
+
+
+# ---- block-sparse decode ---------------------------------------------------------
+
+@pytest.mark.parametrize("qscale", [3, 4])
+def test_sparse_decode_peaked(qscale):
+    t = torch()
+    lens = [9000, 2000]
+    hq, k = 16, 64
+    lay = pkv.layout(1, 2, 256, 128)
+    streams = [synth.make_stream(5000 + i, 1, T, 2, 256, 128) for i, T in enumerate(lens)]
+    pl = place(lay, streams, 128, seed=16)
+    rng = np.random.default_rng(5100 + qscale)
+    ids = np.stack([np.stack([np.sort(rng.choice(T // 4, k, replace=False)) for _ in range(hq)])
+                    for T in lens]).astype(np.int32)
+    q = [synth.scale_pow2(synth.queries(5200 + i, 1, hq, 256), qscale) for i in range(2)]
+    seqs = pl.seqs(lens, [1, 1])
+    dq = dev_u16(np.concatenate(q))
+    out = t.zeros_like(dq)
+    ws = t.zeros(pkv.sparse_ws_size(lay, seqs, hq, k) // 4 + 64, dtype=t.float32, device="cuda")
+    pkv.sparse_decode(lay, seqs, 0, hq, dq, t.from_numpy(ids).cuda(), k, out, ws)
+    t.cuda.synchronize()
+    got = host_u16(out).reshape(2, hq, 256)
+    for i, T in enumerate(lens):
+        want = orc.sparse_attend(pl.shape, pl.ocaches[i], 0, hq, T, q[i][0], ids[i])
+        ok, report = within_tol(got[i], want)
+        assert ok, (i, report)
+
+
+# ---- e4m3: value scales folded into the softmax weights ---------------------------
+
+@pytest.mark.parametrize("qscale", [0, 3])
+def test_e4m3_decode_row_scales_spread(qscale):
+    lay = pkv.layout(1, 2, 256, 128, pkv.KV_E4M3)
+    lens = [3001, 1001, 40]
+    streams = [_spread(synth.make_stream(5300 + i, 1, T, 2, 256, 128), 5310 + i)
+               for i, T in enumerate(lens)]
+    q = [synth.scale_pow2(synth.queries(5400 + i, 1, 16, 256), qscale) for i in range(3)]
+    pl = place(lay, streams, 48, seed=17)
+    got = decode(pl, 0, 16, q)
+    ok, report = within_tol(got, oracle_decode(pl, 0, 16, q))
+    assert ok, report
+    cont = place(lay, streams, None)
+    assert np.array_equal(decode(cont, 0, 16, q), got)
+
+
+@pytest.mark.parametrize("qscale", [3, 4])
+def test_e4m3_decode_peaked_windows(qscale):
+    lay = pkv.layout(1, 2, 256, 128, pkv.KV_E4M3)
+    lens = [2004, 97]
+    streams = [synth.make_stream(5500 + i, 1, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q = [synth.scale_pow2(synth.queries(5600 + i, 4, 16, 256), qscale) for i in range(2)]
+    pl = place(lay, streams, 16, seed=18)
+    got = decode(pl, 0, 16, q)
+    ok, report = within_tol(got, oracle_decode(pl, 0, 16, q))
+    assert ok, report

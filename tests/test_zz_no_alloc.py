@@ -8,17 +8,19 @@ as pkv_decode minus the workspace, and keeps its split partials in a fixed
 array inside the library.
 
 This test calls it through the C ABI twice in a row, with different queries
-and layers (so a stale partial left in the shared array would show), and
-compares each output with pkv_decode's on the same inputs, within the bound
-the other parity tests use.  A batch whose partials would not fit the fixed
-array must be refused.  The file is named to run last.
+and layers (so a stale partial left in the shared array would show).  Both
+entry points run the same kernels with the same split plan, so each output
+must equal pkv_decode's on the same inputs bit for bit; each is also checked
+against the oracle within the bound the other parity tests use.  A batch
+whose partials would not fit the fixed array must be refused.  The file is
+named to run last.
 """
 import numpy as np
 import pytest
 
 from paged_kv_cache_pg_gb300 import pkv, synth
 
-from gpu_setup import dev_u16, host_u16, place, torch, within_tol
+from gpu_setup import dev_u16, host_u16, oracle_decode, place, torch, within_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -40,15 +42,15 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
     ws = t.zeros(pkv.decode_ws_size(lay, seqs, 16) // 4 + 64, dtype=t.float32, device="cuda")
     assert pkv.decode_ws_size(lay, seqs, 16) <= pkv.STATIC_SCRATCH_BYTES
     for call, layer in enumerate((1, 0)):
-        q = dev_u16(np.concatenate([synth.queries(800 + 10 * call + i, 1, 16, 256)
-                                    for i in range(4)]))
+        q_list = [synth.queries(800 + 10 * call + i, 1, 16, 256) for i in range(4)]
+        q = dev_u16(np.concatenate(q_list))
         want = t.zeros_like(q)
         got = t.zeros_like(q)
         pkv.decode(lay, seqs, layer, 16, q, want, ws)
         pkv.decode_static(lay, seqs, layer, 16, q, got)
         t.cuda.synchronize()
-        ref = (host_u16(want).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-        ok, report = within_tol(host_u16(got), ref)
+        assert np.array_equal(host_u16(got), host_u16(want)), f"call {call}: outputs differ"
+        ok, report = within_tol(host_u16(got), oracle_decode(pl, layer, 16, q_list, lens))
         assert ok, f"call {call}: {report}"
 
 
