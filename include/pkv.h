@@ -28,14 +28,17 @@
  *   - Kernels launch with programmatic dependent launch: a call's kernels
  *     may start while the kernel before them on the stream is still running,
  *     and wait for it before touching anything it may write.  Two things are
- *     read before that wait: page tables and the rows of cached positions
- *     (below len - n_new) of pkv_decode / pkv_decode_static.  So those must
- *     not be written by the kernel immediately before on the stream, unless
- *     that kernel is one of this library's stores (pkv_store, or pkv_decode
- *     with k_new), which make their rows visible before letting the next
- *     kernel start.  Rows, tables and inputs written earlier on the stream,
- *     or by a copy or a kernel launched without programmatic dependent
- *     launch, need nothing.
+ *     read before that wait: page tables, and the rows of cached positions
+ *     more than 32 below a stream's new tokens (below len - n_new - 32) in
+ *     pkv_decode / pkv_decode_static with a bf16 layout.  So those must not
+ *     be written by the kernel immediately before on the stream, unless that
+ *     kernel is pkv_store, which makes its rows visible before letting the
+ *     next kernel start.  A pkv_decode with k_new writes only its own new
+ *     rows (at most 32 a stream), which for a stream decoding in order lie
+ *     within the 32 positions below the next call's new tokens, so decode
+ *     calls of the same stream and layer may follow each other directly.
+ *     Rows, tables and inputs written earlier on the stream, or by a copy or
+ *     a kernel launched without programmatic dependent launch, need nothing.
  *   - A multi-stream launch takes one pkv_seq per stream, each with its own
  *     page table (PR #2244 "the grouped draft head's lanes carry their page
  *     table": a grouped launch built without each stream's table read and
@@ -276,12 +279,11 @@ int pkv_pool(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int3
  * the cache (as pkv_store would; quantized by the same rule for an e4m3
  * layout) and reads them from those inputs; with them NULL the new rows must
  * already be in the cache.
- * Ordering: the call may read cached rows (positions below len - n_new)
- * before the kernel queued just before it on the stream has finished, so that
- * kernel must not write them unless it is a store of this library (pkv_store,
- * or a pkv_decode with k_new), which makes its rows visible before the next
- * kernel may start; q, k_new, v_new, ik_new, ws and out are only touched
- * after it finishes.
+ * Ordering: the call may read cached rows more than 32 positions below the
+ * new tokens (positions below len - n_new - 32) before the kernel queued
+ * just before it on the stream has finished, so that kernel must not write
+ * them unless it is pkv_store (see the conventions above); q, k_new, v_new,
+ * ik_new, ws, out and the rows above are only touched after it finishes.
  * The split partials go to ws and a second kernel combines them, splits in
  * ascending order.  ws: device, >= pkv_decode_ws_size bytes (0 when no
  * stream needs more than one split), 256-byte aligned, no initialization;

@@ -54,6 +54,11 @@ constexpr int kMinSplitDense = PKV_DECODE_MIN_SPLIT;    // keys
 constexpr int kMinSplitSparse = PKV_SPARSE_MIN_SPLIT;
 constexpr int kMaxSplitLen = 1024;           // keys of one split (bounds the page list)
 constexpr int kMaxSplits = 2048;
+// Rows read before the grid-dependency wait lie at least this many positions
+// below a stream's new tokens: a decode of the same stream queued just before
+// (its fused store writes at most 32 rows, right below this call's new
+// tokens) may still be writing the rows above.
+constexpr int kFreshGuard = 32;
 constexpr int kCombThreads = 256;
 constexpr int kMaxPages = kMaxSplitLen / 4 + 2;  // pages one split can touch
 constexpr int kMaxSparseBlocks = kMaxSplitLen / 4;
@@ -155,13 +160,15 @@ struct Ctx {
 // copy per 64-dim chunk (8 per tile, K and V); any other tile (the ragged
 // tail, new rows, pages not a multiple of 16, selected blocks) goes key by key
 // with 16-byte cp.async through the same swizzle, from one row lookup per key.
-// With a fused store, new rows come from k_new/v_new and are written to the
-// cache here as well; returns whether this warp wrote any.
+// With a fused store, new rows come from k_new/v_new, and are written to the
+// cache here as well when `write_rows` (the caller stored them otherwise);
+// returns whether this warp wrote any.  The copies complete on `bar`.
 template <bool kSparse>
 __device__ __forceinline__ bool stage_tile(const Common &c, const DecodeArgs &a,
                                            const DecodeMaps &maps, const SeqDev &sd,
                                            const Unit &u, const Ctx &x, int t, int slot,
-                                           int lane, uint64_t pol) {
+                                           uint64_t *bar, int lane, uint64_t pol,
+                                           bool write_rows = true) {
     const int H = c.n_kv_heads;
     const int qbase = sd.len - sd.n_new;
     const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;  // V row - K row
@@ -209,11 +216,11 @@ __device__ __forceinline__ bool stage_tile(const Common &c, const DecodeArgs &a,
         if (lane == 0) {
             const int y = static_cast<int>(sd.layer_row + krow / kHeadDim);  // row-aligned
             const int yv = y + static_cast<int>(v_gap / kHeadDim);
-            mbar_arrive_expect_tx(&x.full[slot], kTile * 2 * 512);
+            mbar_arrive_expect_tx(bar, kTile * 2 * 512);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                tma_load_2d(kst + j * kPlane, map, 64 * j, y, &x.full[slot], pol);
-                tma_load_2d(vst + j * kPlane, map, 64 * j, yv, &x.full[slot], pol);
+                tma_load_2d(kst + j * kPlane, map, 64 * j, y, bar, pol);
+                tma_load_2d(vst + j * kPlane, map, 64 * j, yv, bar, pol);
             }
         }
     } else {
@@ -236,12 +243,12 @@ __device__ __forceinline__ bool stage_tile(const Common &c, const DecodeArgs &a,
             cp_async16(kst + swz(r, lane), kr + lane * 8, pol);
             cp_async16(vst + swz(r, lane), vr + lane * 8, pol);
         }
-        cp_async_mbar_arrive(&x.full[slot]);
+        cp_async_mbar_arrive(bar);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&x.full[slot]);
+        if (lane == 0) mbar_arrive(bar);
     }
     bool wrote = false;
-    if (fuse_store) {
+    if (fuse_store && write_rows) {
         unsigned todo = __ballot_sync(0xffffffffu, fresh && pos >= 0 && !bad);
         wrote = todo != 0;
         while (todo) {
@@ -402,11 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
+    // dense: nothing this CTA writes is read by the next kernel before its own
+    // wait (a decode reads no row within kFreshGuard of its new tokens early)
+    if (!kSparse && tid == 0) pdl_trigger();
 
     const uint64_t pol = policy_evict_first();
-    // Rows of cached positions do not depend on the previous kernel on the
-    // stream: the first tiles stream before the grid-dependency wait.  Tiles
-    // holding new positions, the queries and every write wait for it.
+    // Rows of cached positions more than kFreshGuard below the new tokens do
+    // not depend on the previous kernel on the stream: the first tiles stream
+    // before the grid-dependency wait (the call's prefetch kernel has asked L2
+    // for the rest).  Other tiles, the queries and every write wait for it.
+    const int early_end = qbase - kFreshGuard;
     const int my_tiles = active ? (u.ntiles - ks + ks_n - 1) / ks_n : 0;  // tiles ks, ks+ks_n, ...
     bool waited = kSparse;
     bool wrote = false;  // this warp stored new rows (fused store)
@@ -414,30 +426,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (leader && !spread) {
         for (; issued < S && issued < my_tiles; ++issued) {
             const int t = ks + issued * ks_n;
-            if (!waited && u.key0 + t * kTile + kTile > qbase) {
+            if (!waited && u.key0 + t * kTile + kTile > early_end) {
                 pdl_wait();
                 waited = true;
             }
-            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, lane, pol);
+            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, &x.full[ks * S + issued], lane, pol);
         }
         if (!kSparse && !waited)
             for (int j = issued; j < my_tiles && j < 2 * S; ++j)
-                prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
+                if (u.key0 + (ks + j * ks_n) * kTile + kTile <= early_end)
+                    prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
     }
     if (spread) {
         for (int j = 0; j < S && j < my_tiles; ++j) {
             if (!spread_stager(j)) continue;
             const int t = ks + j * ks_n;
-            if (!waited && u.key0 + t * kTile + kTile > qbase) {
+            if (!waited && u.key0 + t * kTile + kTile > early_end) {
                 pdl_wait();
                 waited = true;
             }
             if (lane == 0) x.uses[ks * S + j] += 1;
-            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + j, lane, pol);
+            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + j, &x.full[ks * S + j], lane, pol);
         }
         if (!kSparse && !waited)
             for (int j = S; j < my_tiles && j < 2 * S; ++j)
-                if (spread_stager(j)) prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
+                if (spread_stager(j) && u.key0 + (ks + j * ks_n) * kTile + kTile <= early_end)
+                    prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
     }
     if (!waited) pdl_wait();
 
@@ -536,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();  // this slot's reads come before the next tile's writes
                 if (spread && lane == 0) x.uses[slot] += 1;
-                wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, ks + (j + S) * ks_n, slot, lane, pol);
+                wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, ks + (j + S) * ks_n, slot, &x.full[slot], lane, pol);
                 ++issued;
             }
         }
@@ -549,9 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&x.full[ks * S + j % S], (j / S) & 1, nullptr);
     }
 
-    if (wrote) __threadfence();  // stored rows visible before the next kernel starts
     __syncthreads();
-    pdl_trigger();  // every thread has passed its grid-dependency wait
+    if (kSparse) pdl_trigger();  // every thread has passed its grid-dependency wait
     if (*x.abort_flag) {
         // spread staging: a slot is refilled only once its previous tile was
         // consumed, so at most its last copy can be in flight; let it land
@@ -644,8 +657,10 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     constexpr int kBatch = 32;
     __shared__ float sh_o[kHeadDim / 2];
     __shared__ float sh_w[kCombThreads / 32][kBatch];  // a warp's weights of one batch
-    pdl_wait();
+    // the next kernel may start now: it waits for this grid before reading
+    // anything this grid writes, and its CTAs stream their cached rows meanwhile
     pdl_trigger();
+    pdl_wait();
     const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
     const SeqDev &sd = c.seq[s];
     const int ns = sd.nsplit;
@@ -876,6 +891,7 @@ static int set_carveout() {
     return once_per_device(done, [] {
         const void *fns[] = {reinterpret_cast<const void *>(decode_combine<false>),
                              reinterpret_cast<const void *>(decode_combine<true>),
+                             reinterpret_cast<const void *>(combine_cols),
                              reinterpret_cast<const void *>(decode_partial<false, false>),
                              reinterpret_cast<const void *>(decode_partial<false, true>),
                              reinterpret_cast<const void *>(decode_partial<true, false>)};
@@ -883,7 +899,7 @@ static int set_carveout() {
             if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                 return PKV_ECUDA;
-        for (int i = 2; i < 5; ++i)
+        for (int i = 3; i < 6; ++i)
             if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes)) != cudaSuccess)
                 return PKV_ECUDA;

@@ -226,6 +226,48 @@ def test_fused_store_decode_equals_store_then_decode(ptok):
 
 
 @pytest.mark.parametrize("ptok", [16, 256, None])
+def test_token_by_token_decode_of_one_stream_and_layer(ptok):
+    # Decoding in order: each call stores its token (fused) and attends it, the
+    # calls queued back to back on one stream with nothing between them, so
+    # each call's early reads of cached rows overlap the previous call's
+    # store of the row just below its own token.  Every step's output is
+    # checked against the oracle, and the cache ends as the oracle's placement.
+    from gpu_setup import CANARY
+    t = torch()
+    lay = pkv.layout(1, 2, 256, 128)
+    T0, steps, layer = 3000, 48, 0
+    full = _streams([T0 + steps], 1, 2, seed=960)
+    pl = place(lay, full, ptok, seed=8)
+    canary = int(np.array([CANARY], np.uint16).view(np.int16)[0])
+    body = pl.body(0)
+    tab = pl.tables[0] if ptok else None
+    for p in range(T0, T0 + steps):
+        for kind, heads, width in ((pkv.K, 2, 256), (pkv.V, 2, 256), (pkv.IK, 1, 128)):
+            for h in range(heads):
+                off = pkv.pg_row(lay, pl.pgs[0], tab, layer, kind, h, p)
+                body[off:off + width] = canary
+    s = full[0]
+    qs = [synth.queries(970 + j, 1, 16, 256) for j in range(steps)]
+    outs = []
+    ws = t.zeros(pkv.decode_ws_size(lay, pl.seqs([T0 + steps], [1]), 16) // 4 + 64,
+                 dtype=t.float32, device="cuda")
+    ins = [(dev_u16(s.k[layer][p:p + 1]), dev_u16(s.v[layer][p:p + 1]), dev_u16(s.ik[layer][p:p + 1]),
+            dev_u16(qs[p - T0])) for p in range(T0, T0 + steps)]
+    t.cuda.synchronize()
+    for j, (kn, vn, ikn, dq) in enumerate(ins):
+        out = t.zeros_like(dq)
+        pkv.decode(lay, pl.seqs([T0 + j + 1], [1]), layer, 16, dq, out, ws, k_new=kn, v_new=vn,
+                   ik_new=ikn)
+        outs.append(out)
+    t.cuda.synchronize()
+    assert np.array_equal(host_u16(pl.body(0)), pl.oarenas[0])
+    for j in range(steps):
+        ref = oracle_decode(pl, layer, 16, [qs[j]], lens=[T0 + j + 1])
+        ok, worst = within_tol(host_u16(outs[j]), ref)
+        assert ok, (j, worst)
+
+
+@pytest.mark.parametrize("ptok", [16, 256, None])
 def test_decode_right_after_a_store_of_its_cached_rows(ptok):
     # A store of every row of the streams and a decode that reads those rows
     # as cached positions, back to back on one stream: the decode stages
