@@ -374,6 +374,14 @@ int pkv_sparse_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_s
  * the same way (about a second of GPU time).  dev_status: a device int32,
  * required (EINVAL if NULL). */
 int pkv_diag_wait_runs_out(int32_t *dev_status, cudaStream_t stream);
+/* The same inside one CTA shaped like the decode's partial CTA (eight warps
+ * in four key slices of two, twelve stage slots with full and empty
+ * barriers): the lead warp of slice `withheld_slice` (0..3) never arrives for
+ * its second tile, both warps of that slice run out of time and raise the
+ * CTA's abort flag, the other slices finish, and the whole CTA meets at its
+ * barrier and returns with PKV_DEV_TIMEOUT set (about a second).  EINVAL if
+ * dev_status is NULL or the slice is out of range. */
+int pkv_diag_cta_wait_runs_out(int32_t *dev_status, int32_t withheld_slice, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -63,6 +63,7 @@ EXPORTS = [
     "pkv_store", "pkv_gather", "pkv_pool", "pkv_decode_ws_size",
     "pkv_decode", "pkv_decode_static", "pkv_block_scores", "pkv_topk", "pkv_sparse_ws_size",
     "pkv_sparse_decode", "pkv_prefill_ws_size", "pkv_prefill", "pkv_diag_wait_runs_out",
+    "pkv_diag_cta_wait_runs_out",
 ]
 
 
@@ -108,6 +109,7 @@ def load(path: Optional[str] = None):
         "pkv_sparse_ws_size": [LP, SP, i32, i32, i32, ctypes.POINTER(sz)],
         "pkv_sparse_decode": [LP, SP, i32, i32, i32, vp, vp, i32, vp, vp, sz, vp, vp],
         "pkv_diag_wait_runs_out": [vp, vp],
+        "pkv_diag_cta_wait_runs_out": [vp, i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -361,3 +363,12 @@ def diag_wait_runs_out(status, stream=None):
     """One warp's wait on a barrier nothing arrives on: it gives up after about
     a second and sets PKV_DEV_TIMEOUT in `status` (a device int32)."""
     _check(load().pkv_diag_wait_runs_out(_ptr(status), _stream(stream)), "pkv_diag_wait_runs_out")
+
+
+def diag_cta_wait_runs_out(status, withheld_slice=2, stream=None):
+    """A decode-shaped CTA (eight warps, four key slices, twelve stage slots)
+    in which one slice's stage never lands: that slice's waits give up after
+    about a second, the CTA returns as a whole and PKV_DEV_TIMEOUT is set in
+    `status` (a device int32)."""
+    _check(load().pkv_diag_cta_wait_runs_out(_ptr(status), withheld_slice, _stream(stream)),
+           "pkv_diag_cta_wait_runs_out")
