@@ -138,9 +138,6 @@ __device__ __forceinline__ int64_t q_row(const Common &c, const SeqDev &sd, cons
     return ((int64_t)sd.tok_off + j) * c.n_q_heads + u.kvh * c.group + (col - j * c.group);
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // The state one CTA shares between its warps.
 struct Ctx {

@@ -92,9 +92,6 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
                  : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 __device__ __forceinline__ float max_over_g(float v) {  // lanes sharing lane & 3
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));

@@ -107,6 +107,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     }
 }
 
+// Orders this thread's earlier shared-memory accesses before later
+// async-proxy (bulk copy, TMA) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // One bulk async copy global -> shared, completing on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).  Streamed rows are read once: evict first.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
