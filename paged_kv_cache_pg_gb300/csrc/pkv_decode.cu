@@ -9,20 +9,22 @@
 // key slices; each slice is a pair of warps per column group of 8 query
 // columns (both compute S for the tile, each accumulates O for half of the
 // 256 dims).  A slice's lead warp stages its tiles into the slice's share of
-// the CTA's twelve 16 KB stage slots (with one slice a CTA, more than 16
-// query columns a unit, the column groups' lead warps take its tiles in
-// turn): it looks each key's row up once per tile (#1169: key_at once per key
-// per tile, beside the key ids; kept here as the split's page offsets in
-// shared memory and the row addresses in the lanes) and copies a whole
-// 16-row page run by 2D TMA, or key by key with cp.async.  Cached rows stream
-// before the grid-dependency wait; tiles past the slots are prefetched into
-// L2.  The warps compute S^T = K Q^T and O^T += V^T P^T with warp MMAs (bf16
-// in, float32 accumulate), keep an online softmax per query column, and merge
-// their key slices in a fixed order.  Splits have a fixed length set by the
-// stream's key count and the SM count, so paged and contiguous caches give
-// the same bits.  A second kernel merges the splits: a CTA a query column
+// the CTA's twelve 16 KB stage slots: it looks each key's row up once per
+// tile (#1169: key_at once per key per tile, beside the key ids; kept here as
+// the split's page offsets in shared memory and the row addresses in the
+// lanes) and copies a whole 16-row page run by 2D TMA, or key by key with
+// cp.async.  Cached rows more than 32 positions below the new tokens stream
+// before the grid-dependency wait, and every dense CTA lets the next kernel
+// start at entry; tiles past the slots are prefetched into L2.  The warps
+// compute S^T = K Q^T and O^T += V^T P^T with warp MMAs (bf16 in, float32
+// accumulate), keep an online softmax per query column, and merge their key
+// slices in a fixed order.  Splits have a fixed length set by the stream's
+// key count and the SM count, so paged and contiguous caches give the same
+// bits.  A second kernel merges the splits: a CTA a query column
 // (decode_combine), or, for calls with thousands of columns and few splits
-// (a prefill chunk), a warp a column (combine_cols).
+// (a prefill chunk), a warp a column (combine_cols).  Units of more than 16
+// query columns (draft windows) are routed to the tensor-core chunk kernel
+// by the host and never reach these kernels.
 #include <algorithm>
 #include <cfloat>
 #include <mutex>
@@ -68,8 +70,7 @@ constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(2
 constexpr size_t kOffPos = (size_t)kSlots * kStageBytes;
 constexpr size_t kOffPage = kOffPos + kSlots * kTile * 4;
 constexpr size_t kOffBar = kOffPage + ((kMaxPages + 1) & ~1) * 8;
-constexpr size_t kOffUses = kOffBar + 2 * kSlots * 8 + 16;
-constexpr size_t kSmemBytes = 1024 + kOffUses + kSlots * 4;  // + alignment slack
+constexpr size_t kSmemBytes = 1024 + kOffBar + 2 * kSlots * 8 + 16;  // + alignment slack
 static_assert(kMaxPages >= kMaxSparseBlocks, "the page list also holds block rows");
 static_assert(kSlots % (kWarps / 2) == 0, "every key slice gets the same number of slots");
 static_assert(kMaxCols * kMergeStride * 4 + kMaxCols * 2 * 4 <= kSlots * kStageBytes,
@@ -147,7 +148,6 @@ struct Ctx {
     uint64_t *full;      // [slot]
     uint64_t *empty;     // [slot]
     volatile int *abort_flag;
-    int32_t *uses;       // [slot]: copies staged into it
     int first_page;      // dense: page of the split's first key
     int64_t fallback;    // sparse: a row surely written (position 0)
 };
@@ -157,15 +157,13 @@ struct Ctx {
 // copy per 64-dim chunk (8 per tile, K and V); any other tile (the ragged
 // tail, new rows, pages not a multiple of 16, selected blocks) goes key by key
 // with 16-byte cp.async through the same swizzle, from one row lookup per key.
-// With a fused store, new rows come from k_new/v_new, and are written to the
-// cache here as well when `write_rows` (the caller stored them otherwise);
-// returns whether this warp wrote any.  The copies complete on `bar`.
+// With a fused store, new rows come from k_new/v_new and are written to the
+// cache here as well.  The copies complete on `bar`.
 template <bool kSparse>
-__device__ __forceinline__ bool stage_tile(const Common &c, const DecodeArgs &a,
+__device__ __forceinline__ void stage_tile(const Common &c, const DecodeArgs &a,
                                            const DecodeMaps &maps, const SeqDev &sd,
                                            const Unit &u, const Ctx &x, int t, int slot,
-                                           uint64_t *bar, int lane, uint64_t pol,
-                                           bool write_rows = true) {
+                                           uint64_t *bar, int lane, uint64_t pol) {
     const int H = c.n_kv_heads;
     const int qbase = sd.len - sd.n_new;
     const int64_t v_gap = (int64_t)H * sd.ptok * kHeadDim;  // V row - K row
@@ -244,10 +242,8 @@ __device__ __forceinline__ bool stage_tile(const Common &c, const DecodeArgs &a,
         __syncwarp();
         if (lane == 0) mbar_arrive(bar);
     }
-    bool wrote = false;
-    if (fuse_store && write_rows) {
+    if (fuse_store) {
         unsigned todo = __ballot_sync(0xffffffffu, fresh && pos >= 0 && !bad);
-        wrote = todo != 0;
         while (todo) {
             const int src = __ffs(todo) - 1;
             todo &= todo - 1;
@@ -272,7 +268,6 @@ __device__ __forceinline__ bool stage_tile(const Common &c, const DecodeArgs &a,
             }
         }
     }
-    return wrote;
 }
 
 // Prefetch the cached K and V rows of dense tile t into L2 (one warp).  Tiles
@@ -307,10 +302,7 @@ __device__ __forceinline__ void prefetch_tile(const Common &c, const SeqDev &sd,
     }
 }
 
-// kSpread: built for calls with a stream of more than 16 query columns a
-// unit (one key slice a CTA), whose tiles the column groups' lead warps stage
-// in turn; the instantiation without it keeps the leader-only staging code.
-template <bool kSparse, bool kSpread>
+template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
                    const DecodeArgs a) {
@@ -324,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
     x.empty = x.full + kSlots;
     x.abort_flag = reinterpret_cast<volatile int *>(x.empty + kSlots);
-    x.uses = reinterpret_cast<int32_t *>(smem + kOffUses);
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int dh = (tid >> 5) & 1;              // which half of the 256 dims this warp sums
@@ -337,20 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = kSlots / ks_n;                // slots of one key slice
     const int cg = warp % ncg, ks = warp / ncg;
     const bool active = ks < ks_n;
-    // Who stages a slice's tiles: its leader.  When the CTA has a single
-    // slice (many query columns), the lead warps of the column groups take
-    // its tiles in turn (tile j by column group j mod ncg), so that one
-    // warp's copy issue does not set the pace of all eight.
-    const bool leader = active && cg == 0 && dh == 0;
-    const bool spread = kSpread && ks_n == 1;
-    auto spread_stager = [&](int j) { return active && dh == 0 && j % ncg == cg; };
+    const bool leader = active && cg == 0 && dh == 0;  // stages its slice's tiles
     const int qbase = sd.len - sd.n_new;
 
     if (tid == 0) {
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&x.full[i], 1);
             mbar_init(&x.empty[i], 2 * ncg);
-            x.uses[i] = 0;
         }
         *x.abort_flag = 0;
         fence_mbar_init();
@@ -418,36 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int early_end = qbase - kFreshGuard;
     const int my_tiles = active ? (u.ntiles - ks + ks_n - 1) / ks_n : 0;  // tiles ks, ks+ks_n, ...
     bool waited = kSparse;
-    bool wrote = false;  // this warp stored new rows (fused store)
     int issued = 0;
-    if (leader && !spread) {
+    if (leader) {
         for (; issued < S && issued < my_tiles; ++issued) {
             const int t = ks + issued * ks_n;
             if (!waited && u.key0 + t * kTile + kTile > early_end) {
                 pdl_wait();
                 waited = true;
             }
-            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, &x.full[ks * S + issued], lane, pol);
+            stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + issued, &x.full[ks * S + issued], lane, pol);
         }
         if (!kSparse && !waited)
             for (int j = issued; j < my_tiles && j < 2 * S; ++j)
                 if (u.key0 + (ks + j * ks_n) * kTile + kTile <= early_end)
-                    prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
-    }
-    if (spread) {
-        for (int j = 0; j < S && j < my_tiles; ++j) {
-            if (!spread_stager(j)) continue;
-            const int t = ks + j * ks_n;
-            if (!waited && u.key0 + t * kTile + kTile > early_end) {
-                pdl_wait();
-                waited = true;
-            }
-            if (lane == 0) x.uses[ks * S + j] += 1;
-            wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, t, ks * S + j, &x.full[ks * S + j], lane, pol);
-        }
-        if (!kSparse && !waited)
-            for (int j = S; j < my_tiles && j < 2 * S; ++j)
-                if (spread_stager(j) && u.key0 + (ks + j * ks_n) * kTile + kTile <= early_end)
                     prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
     }
     if (!waited) pdl_wait();
@@ -536,25 +503,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16(acc[i], y0, y1, y2, y3, pb0, pb1);
                 mma_bf16(acc[i], y0, y1, y2, y3, pc0, pc1);
             }
-            // release the slot; the slice's leader (or the stager of tile
-            // j + S when staging is spread) refills it with tile j + S
+            // release the slot; the slice's leader refills it with tile j + S
             __syncwarp();
             if (lane == 0) mbar_arrive(&x.empty[slot]);
-            if (!spread ? leader && issued < my_tiles : j + S < my_tiles && spread_stager(j + S)) {
+            if (leader && issued < my_tiles) {
                 if (!mbar_wait(&x.empty[slot], (j / S) & 1, c.status)) {
                     *x.abort_flag = 1;
                     break;
                 }
                 fence_proxy_async_smem();  // this slot's reads come before the next tile's writes
-                if (spread && lane == 0) x.uses[slot] += 1;
-                wrote |= stage_tile<kSparse>(c, a, maps, sd, u, x, ks + (j + S) * ks_n, slot, &x.full[slot], lane, pol);
+                stage_tile<kSparse>(c, a, maps, sd, u, x, ks + (j + S) * ks_n, slot, &x.full[slot], lane, pol);
                 ++issued;
             }
         }
         l0 = warp_sum_lanes(l0);
         l1 = warp_sum_lanes(l1);
     }
-    if (leader && !spread && *x.abort_flag) {
+    if (leader && *x.abort_flag) {
         // let every copy this slice issued land before the CTA's memory is released
         for (int j = issued > S ? issued - S : 0; j < issued; ++j)
             mbar_wait(&x.full[ks * S + j % S], (j / S) & 1, nullptr);
@@ -562,13 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __syncthreads();
     if (kSparse) pdl_trigger();  // every thread has passed its grid-dependency wait
-    if (*x.abort_flag) {
-        // spread staging: a slot is refilled only once its previous tile was
-        // consumed, so at most its last copy can be in flight; let it land
-        if (spread && tid < kSlots && x.uses[tid] > 0)
-            mbar_wait(&x.full[tid], (x.uses[tid] - 1) & 1, nullptr);
-        return;
-    }
+    if (*x.abort_flag) return;
 
     // ---- merge the key slices (ks = 0, 1, ...) in order, inside the CTA ----
     const int NC = ncg * 8;
@@ -889,14 +848,13 @@ static int set_carveout() {
         const void *fns[] = {reinterpret_cast<const void *>(decode_combine<false>),
                              reinterpret_cast<const void *>(decode_combine<true>),
                              reinterpret_cast<const void *>(combine_cols),
-                             reinterpret_cast<const void *>(decode_partial<false, false>),
-                             reinterpret_cast<const void *>(decode_partial<false, true>),
-                             reinterpret_cast<const void *>(decode_partial<true, false>)};
+                             reinterpret_cast<const void *>(decode_partial<false>),
+                             reinterpret_cast<const void *>(decode_partial<true>)};
         for (const void *f : fns)
             if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                 return PKV_ECUDA;
-        for (int i = 3; i < 6; ++i)
+        for (int i = 3; i < 5; ++i)
             if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes)) != cudaSuccess)
                 return PKV_ECUDA;
@@ -939,11 +897,10 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
     DecodeArgs a{q, out, ws, ids, k, k_new, v_new, ik_new};
     // streams with no queries own no CTAs: give them an empty range
     Common cc = c;
-    // a stream with more than 16 query columns a unit has one key slice a CTA
-    bool wide = false;
-    for (int s = 0; s < c.n_seqs; ++s) wide |= c.seq[s].ncols > 16;
-    auto part = sparse ? decode_partial<true, false>
-                       : (wide ? decode_partial<false, true> : decode_partial<false, false>);
+    // units of more than 16 query columns take the tensor-core route instead
+    for (int s = 0; s < c.n_seqs; ++s)
+        if (c.seq[s].ncols > 16) return PKV_EINVAL;
+    auto part = sparse ? decode_partial<true> : decode_partial<false>;
     auto comb = sparse ? decode_combine<true> : decode_combine<false>;
     if (set_carveout() != PKV_OK) return PKV_ECUDA;
     cudaError_t e = launch_pdl(part, plan.total_items, kThreads, kSmemBytes, stream, cc, maps, a);

@@ -318,9 +318,21 @@ extern "C" int pkv_pool(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs
     return launch_pool(c, blocks, stream);
 }
 
+// Dense bf16 decode calls with a unit of more than 16 query columns (a
+// stream's draft window: 4 queries x 8 heads) run on the tensor-core chunk
+// kernel: the MMA work per key is large enough there that tcgen05 beats the
+// warp-MMA decode (the window's new rows are stored first when the call
+// brings them).
+static bool tensor_route(const Common &c, bool sparse) {
+    if (sparse || c.kv_fp8) return false;
+    for (int s = 0; s < c.n_seqs; ++s)
+        if (c.seq[s].n_new * c.group > 16) return true;
+    return false;
+}
+
 static int decode_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
                          int32_t layer, int32_t n_q_heads, bool sparse, int32_t k,
-                         int32_t *dev_status, Common *c, DecodePlan *plan) {
+                         int32_t *dev_status, Common *c, DecodePlan *plan, bool *tensor = nullptr) {
     int rc = fill_common(L, seqs, n_seqs, layer, n_q_heads, dev_status, c);
     if (rc) return rc;
     if (sparse) {
@@ -334,7 +346,29 @@ static int decode_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seq
     int nsm = 0;
     rc = sm_count(&nsm);
     if (rc) return rc;
-    return plan_decode(*c, sparse, k, nsm, plan);
+    const bool route = tensor_route(*c, sparse);
+    if (tensor) *tensor = route;
+    return route ? plan_prefill(*c, nsm, plan) : plan_decode(*c, sparse, k, nsm, plan);
+}
+
+// The tensor-core route of a dense decode call: the new rows (when given)
+// are stored, then the chunk kernel attends them (its split partials merged
+// by the decode combine).
+static int launch_tensor_route(const pkv_layout *L, const pkv_seq *seqs, const Common &c,
+                               const DecodePlan &plan, const void *q, const void *k_new,
+                               const void *v_new, const void *ik_new, void *out, float *ws,
+                               cudaStream_t stream) {
+    if (k_new) {
+        const int rc = launch_store(c, total_new(c), static_cast<const uint16_t *>(k_new),
+                                    static_cast<const uint16_t *>(v_new),
+                                    static_cast<const uint16_t *>(ik_new), stream);
+        if (rc) return rc;
+    }
+    DecodeMaps maps;
+    Common cc = c;
+    plan_maps(cc, L, seqs, maps);
+    return launch_prefill(cc, plan, maps, static_cast<const uint16_t *>(q),
+                          static_cast<uint16_t *>(out), ws, stream);
 }
 
 extern "C" int pkv_decode_ws_size(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
@@ -354,7 +388,8 @@ extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
                           int32_t *dev_status, cudaStream_t stream) {
     Common c;
     DecodePlan plan;
-    int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, false, 0, dev_status, &c, &plan);
+    bool tensor = false;
+    int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, false, 0, dev_status, &c, &plan, &tensor);
     if (rc) return rc;
     if (plan.total_items == 0) return PKV_OK;
     if (!q || !out || !aligned16(q) || !aligned16(out)) return PKV_EINVAL;
@@ -366,6 +401,9 @@ extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
     if (plan.ws_bytes > 0 &&
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
+    if (tensor)
+        return launch_tensor_route(L, seqs, c, plan, q, k_new, v_new, L->idx_dim ? ik_new : nullptr,
+                                   out, static_cast<float *>(ws), stream);
     DecodeMaps maps;  // copied into the launch's parameters
     plan_maps(c, L, seqs, maps);
     if (c.kv_fp8)
@@ -386,7 +424,8 @@ extern "C" int pkv_decode_static(const pkv_layout *L, const pkv_seq *seqs, int32
                                  void *out, int32_t *dev_status, cudaStream_t stream) {
     Common c;
     DecodePlan plan;
-    int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, false, 0, dev_status, &c, &plan);
+    bool tensor = false;
+    int rc = decode_common(L, seqs, n_seqs, layer, n_q_heads, false, 0, dev_status, &c, &plan, &tensor);
     if (rc) return rc;
     if (plan.ws_bytes > kStaticScratchBytes) return PKV_EINVAL;  // over the fixed scratch
     if (plan.total_items == 0) return PKV_OK;
@@ -399,6 +438,9 @@ extern "C" int pkv_decode_static(const pkv_layout *L, const pkv_seq *seqs, int32
     void *scratch = nullptr;
     rc = static_scratch(&scratch);
     if (rc) return rc;
+    if (tensor)
+        return launch_tensor_route(L, seqs, c, plan, q, k_new, v_new, L->idx_dim ? ik_new : nullptr,
+                                   out, static_cast<float *>(scratch), stream);
     DecodeMaps maps;
     plan_maps(c, L, seqs, maps);
     if (c.kv_fp8)
