@@ -30,7 +30,7 @@
  *     and wait for it before touching anything it may write.  Two things are
  *     read before that wait: page tables, and the rows of cached positions
  *     more than 32 below a stream's new tokens (below len - n_new - 32) in
- *     pkv_decode / pkv_decode_static with a bf16 layout.  So those must not
+ *     pkv_decode / pkv_decode_static.  So those must not
  *     be written by the kernel immediately before on the stream, unless that
  *     kernel is pkv_store, which makes its rows visible before letting the
  *     next kernel start.  A pkv_decode with k_new writes only its own new

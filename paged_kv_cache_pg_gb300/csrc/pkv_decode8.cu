@@ -156,7 +156,6 @@ __global__ void __maxnreg__(192)
     // scales, all completing on the slot's barrier.  With a fused store, the
     // rows of new positions are quantized here from k_new / v_new (the same
     // rule as pkv_store), written to the cache and to the stage directly.
-    bool wrote = false;  // this warp stored new rows (fused store)
     auto issue = [&](int t) {
         const int kt = key0 + (ks + t * ks_n) * kT8;
         const int slot = warp * kDepth8 + t % kDepth8;
@@ -214,7 +213,6 @@ __global__ void __maxnreg__(192)
                 todo &= todo - 1;
                 const int p = kt + rr;                           // its position
                 const bool write = !__shfl_sync(0xffffffffu, bad, rr);
-                wrote |= write;
                 const int64_t tr = (int64_t)sd.tok_off + (p - qbase);  // its packed input row
                 const int64_t pg_rr = shfl64(pg, rr);
                 const int row_rr = __shfl_sync(0xffffffffu, row, rr);
@@ -276,17 +274,21 @@ __global__ void __maxnreg__(192)
         }
     };
 
-    // rows of cached positions stream before the grid-dependency wait; a tile
-    // holding a new position (stored by the previous kernel) waits for it
+    // nothing this CTA writes is read by the next kernel before its own wait
+    // (a decode reads no row within 32 positions of its new tokens early)
+    if (tid == 0) pdl_trigger();
+    // rows of cached positions more than 32 below the new tokens stream
+    // before the grid-dependency wait; later tiles (a decode of the same
+    // stream queued just before may still be storing the rows right below
+    // the new tokens) wait for it
     int issued = 0;
     for (; issued < kDepth8 && issued < my_tiles; ++issued) {
         const int kt = key0 + (ks + issued * ks_n) * kT8;
-        if (kt + kT8 > qbase) break;
+        if (kt + kT8 > qbase - 32) break;
         issue(issued);
     }
     pdl_wait();
     __syncthreads();
-    if (!fuse) pdl_trigger();  // with a fused store: once the new rows are written
     for (; issued < kDepth8 && issued < my_tiles; ++issued) issue(issued);
 
     // the queries of this thread's B-operand column, in the permuted dim order
@@ -434,9 +436,7 @@ __global__ void __maxnreg__(192)
     }
 
     // ---- merge the key slices of each column group in a fixed order ----
-    if (wrote) __threadfence();  // stored rows visible before the next kernel starts
     __syncthreads();
-    if (fuse) pdl_trigger();
     const int NC = ncg * 8;
     float *mbuf = reinterpret_cast<float *>(sm8);  // [ks][NC][kMS8]
     float *mlb = mbuf + ks_n * NC * kMS8;          // [ks][NC][2]
