@@ -55,9 +55,9 @@ ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3
 # combine kernels), from one ncu capture of the decode kernels (summary under
 # profiles/), valid while the decode sources hash to the value the capture
 # was taken with; reported as null, with the capture date, otherwise.
-DECODE_TRAFFIC = {"bytes": 40373504, "captured": "2026-12-02",
+DECODE_TRAFFIC = {"bytes": 40377856, "captured": "2026-12-02",
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "a7a3b6d4fd9efda0322904d3ae8afa8b9135bd214244309b1f59e14b985b4930"}
+                  "sha256": "e4563fc5c8b501f351335dac9daa7b2a0307fcd61ada212f0b9dd8a9c55e96b6"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
@@ -474,13 +474,18 @@ def _place(torch, pkv, lay, dev, pg, stream, upto):
     pkv.pool(lay, sq, 0)
 
 
-def row_prefill(torch, pkv, dev, timer):
-    """512-query chunk on 31,000 cached positions, pages of 256: the chunk's
-    store, its pooled blocks, then the tensor-core attention."""
-    P0, C = 31000, 512
+PREFILL_P0, PREFILL_C = 31000, 512
+
+
+def _prefill_chunk(torch, pkv, dev, ptok):
+    """The 512-query chunk on 31,000 cached positions in an arena of
+    `ptok`-position pages: (store, pool, attend, status, buffers), each call
+    on the current stream; the caller holds `buffers` (the arena and its
+    table) while it calls them."""
+    P0, C = PREFILL_P0, PREFILL_C
     T = P0 + C
     lay = pkv.layout(1, HKV, D, DI)
-    mem, tables, pgs = _paged(torch, pkv, lay, dev, 256, [T], synth.pages_for(T, 256) + 4, 4)
+    mem, tables, pgs = _paged(torch, pkv, lay, dev, ptok, [T], synth.pages_for(T, ptok) + 4, 4)
     s = synth.make_stream(40, 1, T, HKV, D, DI)
     _place(torch, pkv, lay, dev, pgs[0], s, P0)
     kc, vc, ic = (_up(torch, dev, x[0][P0:]) for x in (s.k, s.v, s.ik))
@@ -498,6 +503,15 @@ def row_prefill(torch, pkv, dev, timer):
 
     def attend():
         pkv.prefill(lay, sq, 0, HQ, q, out, ws, status=status)
+
+    return store, pool, attend, status, (mem, tables)
+
+
+def row_prefill(torch, pkv, dev, timer):
+    """512-query chunk on 31,000 cached positions, pages of 256: the chunk's
+    store, its pooled blocks, then the tensor-core attention."""
+    P0, C = PREFILL_P0, PREFILL_C
+    store, pool, attend, status, buffers = _prefill_chunk(torch, pkv, dev, 256)
 
     def step():
         store(), pool(), attend()
@@ -788,14 +802,28 @@ def row_page_runs(torch, pkv, dev, timer):
         res[ptok] = ms * 1e3 / N_LAYERS
         del g, mem, tables, pgs, ws
         torch.cuda.empty_cache()
+    # the chunked prefill, whose one producer warp a K or V ring issues a
+    # tile's copies: 8 TMA boxes a 32-key tile of 16-row runs, or 32
+    # cp.async a lane key by key
+    pre = {}
+    for ptok in (16, 20):
+        store, pool, attend, status, buffers = _prefill_chunk(torch, pkv, dev, ptok)
+        pre[ptok] = timer.ms(attend, graph=True) * 1e3
+        if int(status.item()) != 0:
+            raise RuntimeError(f"page-run row: device status {int(status.item())}")
+        del store, pool, attend, status, buffers
+        torch.cuda.empty_cache()
     peak, kind = peaks()
     b = decode_bytes(lens_after)
-    return {"workload": "multi-stream decode, 13 layer slots, new token stored by the call: pages of "
-                        "16 (16-row page runs by TMA) against pages of 20 (rows key by key)",
+    return {"workload": "multi-stream decode, 13 layer slots, new token stored by the call, and the "
+                        "512-query prefill chunk on 31,000 positions: pages of 16 (16-row page runs "
+                        "by TMA) against pages of 20 (rows key by key)",
             "us_per_layer": {"page_runs_p16": round(res[16], 2), "key_by_key_p20": round(res[20], 2)},
             "GBps": {"page_runs_p16": round(b / res[16] / 1e3, 1),
                      "key_by_key_p20": round(b / res[20] / 1e3, 1)},
-            "key_by_key_over_page_runs": round(res[20] / res[16], 4)}
+            "key_by_key_over_page_runs": round(res[20] / res[16], 4),
+            "prefill_us": {"page_runs_p16": round(pre[16], 2), "key_by_key_p20": round(pre[20], 2)},
+            "prefill_key_by_key_over_page_runs": round(pre[20] / pre[16], 4)}
 
 
 def row_allocator(torch, pkv, dev, timer):
