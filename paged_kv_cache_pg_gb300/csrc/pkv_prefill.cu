@@ -141,9 +141,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].work_off; });
-    const SeqDev &sd = c.seq[s];
     const int H = c.n_kv_heads, G = c.group;
+    // the stream whose block of work items holds this CTA (the blocks are
+    // laid out longest CTA first, not in stream order)
+    int s = 0;
+    for (int t = 0; t < c.n_seqs; ++t) {
+        const SeqDev &st = c.seq[t];
+        const int items = H * ((st.ncols + kM - 1) / kM) * st.nsplit;
+        if (st.ncols > 0 && (int)blockIdx.x >= st.work_off && (int)blockIdx.x < st.work_off + items) s = t;
+    }
+    const SeqDev &sd = c.seq[s];
     const int mtiles = (sd.ncols + kM - 1) / kM;
     // consecutive CTAs share a (KV head, split): the M-tiles that read the
     // same key range run in the same wave and find its tiles in L2
@@ -536,7 +543,7 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
     const int H = c.n_kv_heads;
     for (int s = 0; s < c.n_seqs; ++s) {
         SeqDev &d = c.seq[s];
-        d.work_off = items;
+        d.work_off = 0;
         d.comb_off = comb;
         d.ws_off = floats;
         d.ncols = d.n_new * c.group;
@@ -578,12 +585,27 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         if (ns > 2048) return PKV_EINVAL;
         d.nsplit = ns;
         d.split_len = sl;
-        items += H * mtiles * ns;
         if (ns > 1) {
             comb += H * d.ncols * comb_ctas(ns);
             floats += (int64_t)H * ns * d.ncols * (kHeadDim + 2);
             floats = (floats + 63) / 64 * 64;
         }
+    }
+    // Work-item blocks in the grid, longest CTA first (most key tiles a
+    // split, ties in stream order): the SMs that take the long CTAs first are
+    // refilled with short ones, instead of a long stream's CTAs starting last
+    // and running alone at the end.  Only the launch order changes: each
+    // stream's splits, and so its results, stay its own.
+    int order[PKV_MAX_SEQS];
+    for (int s = 0; s < c.n_seqs; ++s) order[s] = s;
+    std::stable_sort(order, order + c.n_seqs, [&](int x, int y) {
+        return c.seq[x].split_len > c.seq[y].split_len;
+    });
+    for (int k = 0; k < c.n_seqs; ++k) {
+        SeqDev &d = c.seq[order[k]];
+        if (d.ncols == 0) continue;
+        d.work_off = items;
+        items += H * ((d.ncols + kM - 1) / kM) * d.nsplit;
     }
     plan->total_items = items;
     plan->total_comb = comb;
