@@ -108,6 +108,24 @@ def test_draft_window_causal_decode(nq, hq, hkv):
     assert np.array_equal(decode(pl, 0, hq, q), a)
 
 
+def test_draft_windows_alone_equal_windows_in_batch():
+    # Windows of 4 queries x 8 heads (32 columns a unit) run on the tensor
+    # cores, with the work items of the longest splits launched first across
+    # streams: a stream's output must not depend on the streams beside it.
+    lay = pkv.layout(1, 2, 256, 128)
+    lens = [900 + 4, 5000 + 4, 2600 + 4]
+    streams = _streams(lens, 1, 2, seed=700)
+    q = [synth.queries(710 + i, 4, 16, 256) for i in range(3)]
+    pl = place(lay, streams, 48, seed=7)
+    both = decode(pl, 0, 16, q)
+    ok, worst = within_tol(both, oracle_decode(place(lay, streams, None), 0, 16, q))
+    assert ok, worst
+    rows = np.split(both, 3)
+    for i in range(3):
+        sub = place(lay, [streams[i]], 48, seed=720 + i)
+        assert np.array_equal(decode(sub, 0, 16, [q[i]]), rows[i])
+
+
 @pytest.mark.parametrize("length", [1, 2, 15, 16, 17, 127, 128, 129, 4095, 40960])
 def test_ragged_lengths(length):
     lay = pkv.layout(1, 2, 256, 0)
