@@ -453,9 +453,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // key r's row from lane r's lookup; keys past the split repeat its last row
 #pragma unroll 8
                 for (int rr = 0; rr < kN; ++rr)
-                    cp_async16(dst + swz128(kRegionKV, rr, lane), sd.layer_base + shfl64(krow, rr) + lane * 8,
-                               pol);
-                cp_async_mbar_arrive(&full[b]);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                     smem_u32(dst + swz128(kRegionKV, rr, lane))),
+                                 "l"(sd.layer_base + shfl64(krow, rr) + lane * 8)
+                                 : "memory");
+                // these are generic-proxy writes and the tensor cores read the
+                // tile through the async proxy: each lane waits for its own
+                // copies and fences the proxies before the warp's one arrival
+                // (an arrival made by the copies themselves would leave the
+                // writes unfenced)
+                asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+                fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[b]);
             }
