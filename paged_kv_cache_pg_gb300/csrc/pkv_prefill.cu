@@ -2,10 +2,14 @@
 //
 // Rows: the (query, head) pairs of one KV head, 128 to an M-tile (16 queries
 // x 8 heads for the pages' 16/2 heads).  A CTA takes one M-tile and one split
-// of the keys and runs, per tile of 32 keys:
-//   S = Q K^T  -> TMEM (128 lanes x 32 columns, two buffers)   [MMA warp]
+// of the keys and runs, per tile of 64 keys:
+//   S = Q K^T  -> TMEM (128 lanes x 64 columns, two buffers)   [MMA warp]
 //   softmax of S with the causal mask, P = hi + lo bf16 parts   [4 warps]
 //   O += P_hi V + P_lo V -> TMEM (128 lanes x 256 columns)      [MMA warp]
+// A tcgen05 MMA with M = 128 costs about the same for every N up to 128, so
+// the S product of a 64-key tile takes the time a 32-key one would.  P has
+// one buffer: the softmax computes tile n+1's weights while the PV product
+// of tile n reads P, and stores them once that product is done.
 // Q, K, V and P sit in shared memory in the 128-byte-swizzled layouts the
 // MMA reads through matrix descriptors.  K and V tiles have rings of their
 // own, each filled by its own producer warp: a K slot is free as soon as its
@@ -14,7 +18,8 @@
 // out a whole load latency).  Tiles arrive by 2D TMA copies of whole 16-row
 // page runs (the rows of 16 consecutive positions are contiguous in a page
 // whose size is a multiple of 16) or, for a ragged tail or other page sizes,
-// by cp.async from one row lookup per key.  The max of a row is rescaled
+// by cp.async from one row lookup per key, fenced by the copying threads
+// before the tensor cores read them.  The max of a row is rescaled
 // lazily: O in TMEM is corrected only when the running max grows by more
 // than 2^8.  Split partials use the decode layout and its combine kernel.
 #include <algorithm>
@@ -26,17 +31,17 @@ namespace pkv {
 namespace {
 
 constexpr int kM = 128;              // rows of an M-tile
-constexpr int kN = 32;               // keys a tile
-constexpr int kKS = 4;               // K tile buffers
-constexpr int kVS = 4;               // V tile buffers
+constexpr int kN = 64;               // keys a tile
+constexpr int kKS = 2;               // K tile buffers
+constexpr int kVS = 2;               // V tile buffers
 constexpr int kPThreads = 224;       // warps 0-3 softmax, 4 K producer, 5 MMA, 6 V producer
 constexpr uint32_t kTmemCols = 512;  // S buffers at columns 0 and 32, O at 256
 constexpr uint32_t kOCol = 256;
 constexpr int kQBytes = kM * 512;    // four 64-dim regions of 128 rows x 128 B
-constexpr int kKVBytes = kN * 512;   // four 64-dim regions of 32 rows x 128 B
+constexpr int kKVBytes = kN * 512;   // four 64-dim regions of 64 rows x 128 B
 constexpr int kRegionQ = kM * 128;   // bytes of one 64-dim region of Q
 constexpr int kRegionKV = kN * 128;  // bytes of one 64-dim region of a K or V tile
-constexpr int kPBytes = kM * 128;    // 128 rows x 128 B: tile n's 32 keys in half n & 1
+constexpr int kPBytes = kM * 128;    // 128 rows x 128 B: one tile's 64 keys
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kKS * kKVBytes;
@@ -244,27 +249,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sv[32];
+            uint32_t sv[32], sw[32];
             tmem_ld32(lane_base + sb * kN, sv);
+            tmem_ld32(lane_base + sb * kN + 32, sw);
             tc_fence_before();
             mbar_arrive(&bars[kBarSEmpty + sb]);
             const int kt = key0 + n * kN;
             // raw scores; the causal and split bounds cut into a tile only near
             // the diagonal and at the split's end
-            float x[32];
+            float x[kN];
             if (__all_sync(0xffffffffu, kt + kN <= key1 && kt + kN - 1 <= qpos)) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(sv[i]);
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = __uint_as_float(sv[i]);
+                    x[32 + i] = __uint_as_float(sw[i]);
+                }
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int kp = kt + i;
+                    const int kp = kt + i, kq = kt + 32 + i;
                     x[i] = (kp < key1 && kp <= qpos) ? __uint_as_float(sv[i]) : -INFINITY;
+                    x[32 + i] = (kq < key1 && kq <= qpos) ? __uint_as_float(sw[i]) : -INFINITY;
                 }
             }
             float mx = x[0];
 #pragma unroll
-            for (int i = 1; i < 32; ++i) mx = fmaxf(mx, x[i]);
+            for (int i = 1; i < kN; ++i) mx = fmaxf(mx, x[i]);
             mx *= kScaleLog2;  // in log2 units; -inf when the whole tile is masked
             const bool grow = m_used != -INFINITY && mx > m_used + kRescale;
             if (__any_sync(0xffffffffu, grow)) {
@@ -295,9 +305,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // offset is 0 while every score so far was masked)
             const float m_off = m_used == -INFINITY ? 0.f : m_used;
             float psum = 0.f;
-            uint32_t hi[16], lo[16];
+            uint32_t hi[kN / 2], lo[kN / 2];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+            for (int i = 0; i < kN; i += 2) {
                 const float p0 = ex2(fmaf(x[i], kScaleLog2, -m_off));
                 const float p1 = ex2(fmaf(x[i + 1], kScaleLog2, -m_off));
                 psum += p0 + p1;
@@ -311,17 +321,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 lo[i / 2] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
             }
             l += psum;
-            // this tile's half of the P rows is free once tile n-2's products are done
-            if (n > 1 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + (n & 1)],
-                                                             ((n - 2) >> 1) & 1, c.status))) {
+            // the P rows are free once the last tile's products are done
+            if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + ((n - 1) & 1)],
+                                                             ((n - 1) >> 1) & 1, c.status))) {
                 *abort_flag = 1;
                 break;
             }
-            // row r of the P operands: 32 keys = 64 bytes = chunks 4h .. 4h+3
-            const int h4 = 4 * (n & 1);
+            // row r of the P operands: 64 keys = 128 bytes = chunks 0 .. 7
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const uint32_t off = r * 128 + ((((ch + h4) ^ (r & 7))) << 4);
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint32_t off = r * 128 + (((ch ^ (r & 7))) << 4);
                 *reinterpret_cast<uint4 *>(p_hi + off) =
                     make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
                 *reinterpret_cast<uint4 *>(p_lo + off) =
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // page ids in registers: lane i holds pages win + i (cur) and
         // win + 32 + i (nxt); the window slides by 32 once a tile starts past
         // its first half, so the next half is loading long before it is read
-        // and no table read waits in the issue loop (a tile spans at most 9
+        // and no table read waits in the issue loop (a tile spans at most 17
         // pages, so its pages always lie in the 64-page window)
         auto page_id = [&](int p) -> int {
             return (sd.table && p < sd.n_table) ? __ldg(sd.table + p) : 0;
@@ -413,50 +422,64 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             const int kt = key0 + n * kN;
             uint8_t *dst = ring + b * kKVBytes;
-            // this lane's key (one lookup per key per tile): clamped into the split
-            const int key = min(kt + lane, key1 - 1);
-            int row = key;
-            int64_t pg = 0;
+            // this lane's keys kt + lane and kt + 32 + lane (one lookup per key
+            // per tile), clamped into the split
             if (sd.table) {
-                const int page = key / sd.ptok;
-                row = key - page * sd.ptok;
-                const int first = __shfl_sync(0xffffffffu, page, 0);  // the tile's lowest page
+                const int first = min(kt, key1 - 1) / sd.ptok;  // the tile's lowest page
                 while (first >= win + 32) {
                     win += 32;
                     cur = nxt;
                     nxt = page_id(win + 32 + lane);
                 }
-                const int idx = page - win;  // 0 .. 63
-                const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
-                const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
-                const int id = idx < 32 ? a0 : a1;
-                if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
-                    pg = (int64_t)id * sd.ps;
-                } else if (c.status && !is_v) {
-                    atomicOr(c.status, PKV_DEV_BAD_PAGE);
-                }
             }
-            const int64_t krow = pg + off_k(sd.ptok, kvh, row) + gap;
+            int64_t krow[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int key = min(kt + 32 * h + lane, key1 - 1);
+                int row = key;
+                int64_t pg = 0;
+                if (sd.table) {
+                    const int page = key / sd.ptok;
+                    row = key - page * sd.ptok;
+                    const int idx = page - win;  // 0 .. 63: a tile spans at most 17 pages
+                    const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
+                    const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
+                    const int id = idx < 32 ? a0 : a1;
+                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
+                        pg = (int64_t)id * sd.ps;
+                    } else if (c.status && !is_v) {
+                        atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                    }
+                }
+                krow[h] = pg + off_k(sd.ptok, kvh, row) + gap;
+            }
             if (map != nullptr && kt + kN <= key1) {
-                // two 16-row page runs, four 64-dim chunks each
-                const int y0 = static_cast<int>(sd.layer_row + shfl64(krow, 0) / kHeadDim);
-                const int y1 = static_cast<int>(sd.layer_row + shfl64(krow, 16) / kHeadDim);
+                // four 16-row page runs, four 64-dim chunks each
+                const int y0 = static_cast<int>(sd.layer_row + shfl64(krow[0], 0) / kHeadDim);
+                const int y1 = static_cast<int>(sd.layer_row + shfl64(krow[0], 16) / kHeadDim);
+                const int y2 = static_cast<int>(sd.layer_row + shfl64(krow[1], 0) / kHeadDim);
+                const int y3 = static_cast<int>(sd.layer_row + shfl64(krow[1], 16) / kHeadDim);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[b], kKVBytes);
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
                         tma_load_2d(dst + ch * kRegionKV, map, 64 * ch, y0, &full[b], pol);
                         tma_load_2d(dst + ch * kRegionKV + 2048, map, 64 * ch, y1, &full[b], pol);
+                        tma_load_2d(dst + ch * kRegionKV + 4096, map, 64 * ch, y2, &full[b], pol);
+                        tma_load_2d(dst + ch * kRegionKV + 6144, map, 64 * ch, y3, &full[b], pol);
                     }
                 }
             } else {
-                // key r's row from lane r's lookup; keys past the split repeat its last row
+                // key r's row from its lane's lookup; keys past the split repeat its last row
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
 #pragma unroll 8
-                for (int rr = 0; rr < kN; ++rr)
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                                     smem_u32(dst + swz128(kRegionKV, rr, lane))),
-                                 "l"(sd.layer_base + shfl64(krow, rr) + lane * 8)
-                                 : "memory");
+                    for (int rr = 0; rr < 32; ++rr)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                         smem_u32(dst + swz128(kRegionKV, 32 * h + rr, lane))),
+                                     "l"(sd.layer_base + shfl64(krow[h], rr) + lane * 8)
+                                     : "memory");
+                }
                 // these are generic-proxy writes and the tensor cores read the
                 // tile through the async proxy: each lane waits for its own
                 // copies and fences the proxies before the warp's one arrival
@@ -510,7 +533,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t vb = sbase + kOffV + b * kKVBytes;
 #pragma unroll
             for (int kk = 0; kk < kN / 16; ++kk) {
-                const uint32_t pa = sbase + kOffP + (n & 1) * 64 + kk * 32;
+                const uint32_t pa = sbase + kOffP + kk * 32;
                 const uint32_t va = vb + kk * 2048;  // 16 keys = two 8-row groups
                 tc_mma(tmem + kOCol, smem_desc(pa, 16, 1024), smem_desc(va, kRegionKV, 1024), idesc_o,
                        (n > 0 || kk > 0) ? 1u : 0u);
@@ -540,7 +563,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // Work items: (KV head, M-tile, split) per stream, splits fastest.  A stream
 // is split only as far as filling the SMs needs, from its own shape alone.
 // Split model of plan_prefill, in hundredths of a microsecond.
-constexpr int64_t kTileCost = 126;   // a 32-key tile of one 128-row M-tile
+constexpr int64_t kTileCost = 150;   // a 64-key tile of one 128-row M-tile
 constexpr int64_t kCtaCost = 1200;   // a CTA's fixed cost
 constexpr int64_t kPartialCost = 4;  // a (unit, split) partial written and read back
 constexpr int kMaxPrefillSplits = 64;
@@ -564,7 +587,7 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         // Splits: the count with the least modelled time for this stream's
         // grid on nsm SMs, waves x (tiles a CTA x a tile's time + a CTA's
         // fixed cost) + the split partials' round trip through HBM.  The
-        // costs are this kernel's on GB300: about 1.26 us a 32-key tile of
+        // costs are this kernel's on GB300: about 1.5 us a 64-key tile of
         // 128 rows, 12 us a CTA (Q load, TMEM, pipeline fill, epilogue) and
         // 0.04 us a (unit, split) partial of 128 rows written and read back.
         // For 512 queries on 31,000 keys it picks 7 splits, 448 CTAs in
