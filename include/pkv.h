@@ -290,10 +290,11 @@ int pkv_pool(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int3
  * one ws per in-flight call.  q and out 16-byte aligned.
  * A bf16 call in which some stream has more than 16 query columns a unit
  * (n_new * n_q_heads / H > 16: a draft window of several tokens) runs on
- * the tensor cores instead, as pkv_prefill does (the new rows stored first
- * when k_new is given; nothing read before the wait); the result agrees with
- * the warp-MMA path within the attention tolerance, and paged output still
- * equals contiguous output bit for bit. */
+ * the tensor cores instead, as pkv_prefill does (with k_new, the new
+ * positions' keys and values read from the inputs and stored into their
+ * pages by the same kernel; nothing read before the wait); the result agrees
+ * with the warp-MMA path within the attention tolerance, and paged output
+ * still equals contiguous output bit for bit. */
 int pkv_decode_ws_size(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
                        int32_t n_q_heads, size_t *bytes);
 int pkv_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,

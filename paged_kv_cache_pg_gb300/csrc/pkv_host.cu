@@ -351,24 +351,21 @@ static int decode_common(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seq
     return route ? plan_prefill(*c, nsm, plan) : plan_decode(*c, sparse, k, nsm, plan);
 }
 
-// The tensor-core route of a dense decode call: the new rows (when given)
-// are stored, then the chunk kernel attends them (its split partials merged
-// by the decode combine).
+// The tensor-core route of a dense decode call: the chunk kernel attends the
+// window, reading the new rows (when given) from the inputs and storing them
+// into their pages itself; its split partials are merged by the decode
+// combine.
 static int launch_tensor_route(const pkv_layout *L, const pkv_seq *seqs, const Common &c,
                                const DecodePlan &plan, const void *q, const void *k_new,
                                const void *v_new, const void *ik_new, void *out, float *ws,
                                cudaStream_t stream) {
-    if (k_new) {
-        const int rc = launch_store(c, total_new(c), static_cast<const uint16_t *>(k_new),
-                                    static_cast<const uint16_t *>(v_new),
-                                    static_cast<const uint16_t *>(ik_new), stream);
-        if (rc) return rc;
-    }
     DecodeMaps maps;
     Common cc = c;
     plan_maps(cc, L, seqs, maps);
     return launch_prefill(cc, plan, maps, static_cast<const uint16_t *>(q),
-                          static_cast<uint16_t *>(out), ws, stream);
+                          static_cast<uint16_t *>(out), ws, static_cast<const uint16_t *>(k_new),
+                          static_cast<const uint16_t *>(v_new), static_cast<const uint16_t *>(ik_new),
+                          stream);
 }
 
 extern "C" int pkv_decode_ws_size(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,
@@ -524,7 +521,8 @@ extern "C" int pkv_prefill(const pkv_layout *L, const pkv_seq *seqs, int32_t n_s
     DecodeMaps maps;
     plan_maps(c, L, seqs, maps);
     return launch_prefill(c, plan, maps, static_cast<const uint16_t *>(q),
-                          static_cast<uint16_t *>(out), static_cast<float *>(ws), stream);
+                          static_cast<uint16_t *>(out), static_cast<float *>(ws), nullptr, nullptr,
+                          nullptr, stream);
 }
 
 extern "C" int pkv_block_scores(const pkv_layout *L, const pkv_seq *seqs, int32_t n_seqs,

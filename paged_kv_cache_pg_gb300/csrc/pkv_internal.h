@@ -179,8 +179,12 @@ int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &map
 // Chunked prefill (pkv_prefill.cu): plan and launch; split partials use the
 // decode layout and are merged by the decode combine kernel.
 int plan_prefill(Common &c, int nsm, DecodePlan *plan);
+// With k_new (a decode call's new rows, [token][KV head][256], and ik_new
+// [token][Di] or null), the kernel reads the new positions' K and V from there
+// and stores them (and the indexer-key rows) into their pages.
 int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
-                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream);
+                   const uint16_t *q, uint16_t *out, float *ws, const uint16_t *k_new,
+                   const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream);
 // CTAs the combine gives one (unit, query column) of a stream with ns splits:
 // two (each half the dims, the splits in two groups) past 32 splits, where
 // one thread would need a second round of loads; one otherwise.  It depends

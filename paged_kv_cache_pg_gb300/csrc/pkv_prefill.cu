@@ -127,6 +127,9 @@ struct PrefillArgs {
     const uint16_t *q;
     uint16_t *out;
     float *ws;
+    // a decode call's new rows [token][KV head][256] (and [token][Di]), read
+    // from here and stored into their pages by the kernel, or null
+    const uint16_t *k_new, *v_new, *ik_new;
 };
 
 // Byte offset of 16-byte chunk c (0..31) of row r in a 128-byte-swizzled
@@ -206,6 +209,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(smem);
+    // the next kernel (the split combine, or the next call) may start once
+    // every CTA is running: it waits for this grid before reading anything
+    // this grid writes, except cached rows more than 32 positions below its
+    // own new tokens, which the rows stored here (a decode call's at most 32
+    // new rows a stream) are not
+    if (tid == 0) pdl_trigger();
 
     if (warp < 4) {
         // ---------------- softmax: thread r owns row r (TMEM lane r) ----------------
@@ -403,6 +412,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint64_t pol = policy_evict_normal();  // every M-tile of the head reads these rows
         // V rows sit H * ptok rows after the K rows of the same page
         const int64_t gap = is_v ? (int64_t)H * sd.ptok * kHeadDim : 0;
+        const bool fuse = a.k_new != nullptr;
+        const uint16_t *const new_rows = is_v ? a.v_new : a.k_new;
         // page ids in registers: lane i holds pages win + i (cur) and
         // win + 32 + i (nxt); the window slides by 32 once a tile starts past
         // its first half, so the next half is loading long before it is read
@@ -433,6 +444,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
             int64_t krow[2];
+            bool bad[2] = {false, false};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int key = min(kt + 32 * h + lane, key1 - 1);
@@ -447,13 +459,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const int id = idx < 32 ? a0 : a1;
                     if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
                         pg = (int64_t)id * sd.ps;
-                    } else if (c.status && !is_v) {
-                        atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                    } else {
+                        bad[h] = true;
+                        if (c.status && !is_v) atomicOr(c.status, PKV_DEV_BAD_PAGE);
                     }
                 }
                 krow[h] = pg + off_k(sd.ptok, kvh, row) + gap;
             }
-            if (map != nullptr && kt + kN <= key1) {
+            // with a decode call's new rows, keys from qbase on come from the
+            // input, not the cache (which this kernel stores them into)
+            const bool fresh_tile = fuse && min(kt + kN, key1) > qbase;
+            if (map != nullptr && kt + kN <= key1 && !fresh_tile) {
                 // four 16-row page runs, four 64-dim chunks each
                 const int y0 = static_cast<int>(sd.layer_row + shfl64(krow[0], 0) / kHeadDim);
                 const int y1 = static_cast<int>(sd.layer_row + shfl64(krow[0], 16) / kHeadDim);
@@ -473,11 +489,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // key r's row from its lane's lookup; keys past the split repeat its last row
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
+                    const int key = min(kt + 32 * h + lane, key1 - 1);
+                    const uint16_t *src = sd.layer_base + krow[h];
+                    if (fresh_tile && key >= qbase)
+                        src = new_rows + (((int64_t)sd.tok_off + (key - qbase)) * H + kvh) * kHeadDim;
+                    const int64_t sp = reinterpret_cast<int64_t>(src);
 #pragma unroll 8
                     for (int rr = 0; rr < 32; ++rr)
                         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
                                          smem_u32(dst + swz128(kRegionKV, 32 * h + rr, lane))),
-                                     "l"(sd.layer_base + shfl64(krow[h], rr) + lane * 8)
+                                     "l"(reinterpret_cast<const uint16_t *>(shfl64(sp, rr)) + lane * 8)
                                      : "memory");
                 }
                 // these are generic-proxy writes and the tensor cores read the
@@ -489,6 +510,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[b]);
+                if (fresh_tile) {
+                    // store the tile's new rows (K or V of this KV head, and the
+                    // indexer-key row once, with KV head 0) into their pages
+                    for (int i = max(kt, qbase); i < min(kt + kN, key1); ++i) {
+                        const int h = (i - kt) >> 5, l = (i - kt) & 31;
+                        const int64_t kr = shfl64(h ? krow[1] : krow[0], l);
+                        if (__shfl_sync(0xffffffffu, h ? bad[1] : bad[0], l)) continue;
+                        const int64_t r = (int64_t)sd.tok_off + (i - qbase);
+                        uint16_t *row = const_cast<uint16_t *>(sd.layer_base) + kr;
+                        reinterpret_cast<uint4 *>(row)[lane] =
+                            __ldg(reinterpret_cast<const uint4 *>(new_rows + (r * H + kvh) * kHeadDim) + lane);
+                        if (!is_v && kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
+                            const int prow = sd.table ? i % sd.ptok : i;
+                            const int64_t page_start = kr - (int64_t)prow * kHeadDim;
+                            uint16_t *idst = const_cast<uint16_t *>(sd.layer_base) + page_start +
+                                             off_ik(H, c.idx_dim, sd.ptok, prow);
+                            reinterpret_cast<uint4 *>(idst)[lane] =
+                                __ldg(reinterpret_cast<const uint4 *>(a.ik_new + r * c.idx_dim) + lane);
+                        }
+                    }
+                }
             }
         }
     } else if (warp == 5 && lane == 0) {
@@ -548,7 +590,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    pdl_trigger();
     if (warp == 5) {
         __syncwarp();  // lane 0 issued the MMAs, lanes 1-31 went straight here
         tc_fence_after();
@@ -645,7 +686,8 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
 }
 
 int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &maps,
-                   const uint16_t *q, uint16_t *out, float *ws, cudaStream_t stream) {
+                   const uint16_t *q, uint16_t *out, float *ws, const uint16_t *k_new,
+                   const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     if (once_per_device(attr_done, [] {
             return cuda_rc(cudaFuncSetAttribute(prefill_partial,
@@ -653,7 +695,7 @@ int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
                                                 static_cast<int>(kPSmem)));
         }) != PKV_OK)
         return PKV_ECUDA;
-    PrefillArgs a{q, out, ws};
+    PrefillArgs a{q, out, ws, k_new, v_new, ik_new};
     cudaError_t e = launch_pdl(prefill_partial, plan.total_items, kPThreads, kPSmem, stream, c, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;
     if (plan.total_comb > 0) return launch_combine(c, plan, q, out, ws, stream);
