@@ -194,7 +194,7 @@ def test_status_word_stays_clear_on_good_input(multi):
     assert np.array_equal(out, base)
 
 
-@pytest.mark.parametrize("ptok", [16, 48, None])
+@pytest.mark.parametrize("ptok", [4, 16, 48, None])
 def test_fused_store_decode_equals_store_then_decode(ptok):
     # Lengths put a split boundary (multiples of 256 keys) inside the 4-token
     # window of the first stream; the second stream's window starts a split.

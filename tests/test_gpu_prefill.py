@@ -57,6 +57,24 @@ def test_small_chunks_match_oracle_and_contiguous(ptok):
     assert np.array_equal(_prefill(cont, lens, n_new, 1, 16, q), got)
 
 
+@pytest.mark.parametrize("ptok", [4, 8])
+def test_small_pages_many_pages_a_tile(ptok):
+    # Pages of 4 and 8 positions: a 64-key tile spans 9 to 17 pages, so the
+    # producers' 64-page window of ids slides within the split, and every
+    # tile goes key by key.  Lengths give splits and a ragged tail.
+    lay = pkv.layout(1, 2, 256, 128)
+    lens = [1500, 644]
+    n_new = [36, 100]
+    streams = [synth.make_stream(1800 + i, 1, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q = [synth.queries(1900 + i, n, 16, 256) for i, n in enumerate(n_new)]
+    pl = place(lay, streams, ptok, seed=ptok)
+    got = _prefill(pl, lens, n_new, 0, 16, q)
+    ok, report = within_tol(got, oracle_decode(pl, 0, 16, q))
+    assert ok, report
+    cont = place(lay, streams, None)
+    assert np.array_equal(_prefill(cont, lens, n_new, 0, 16, q), got)
+
+
 def test_prefill_of_a_short_window_agrees_with_decode():
     t = torch()
     lay = pkv.layout(1, 2, 256, 128)
