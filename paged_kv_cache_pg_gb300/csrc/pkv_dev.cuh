@@ -140,6 +140,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, int x, i
         : "memory");
 }
 
+// One 3D tensor-map box (x, y, z) -> shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, int y, int z,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (L1 bypassed).
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t policy) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),

@@ -123,20 +123,24 @@ struct MapKey {
     uintptr_t base;
     uint64_t rows;
     bool bytes8;
+    bool tile;
+    int box_rows;
 };
 std::mutex g_map_mu;
 std::vector<std::pair<MapKey, RowMap>> g_maps;  // encoded maps, most recent last
 }  // namespace
 
-int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool bytes8) {
+int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool bytes8,
+            bool tile, int box_rows) {
     if (rows == 0 || rows > (1ull << 31) || !aligned16(base)) return -1;
+    if ((box_rows != 16 && box_rows != 64) || (bytes8 && tile) || (!tile && box_rows != 16)) return -1;
     RowMap m;
     bool have = false;
     {
         std::lock_guard<std::mutex> g(g_map_mu);
         for (auto &e : g_maps)
             if (e.first.base == reinterpret_cast<uintptr_t>(base) && e.first.rows == rows &&
-                e.first.bytes8 == bytes8) {
+                e.first.bytes8 == bytes8 && e.first.tile == tile && e.first.box_rows == box_rows) {
                 m = e.second;
                 have = true;
                 break;
@@ -146,20 +150,29 @@ int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool
         auto fn = encode_fn();
         if (!fn) return -1;
         // bf16 rows: 256 elements (512 B), boxes of 64 x 16; e4m3 code rows:
-        // 256 bytes, boxes of 128 x 16 (both 128-byte inner boxes)
-        cuuint64_t dims[2] = {256, rows};
-        cuuint64_t strides[1] = {bytes8 ? 256u : 512u};
-        cuuint32_t box[2] = {bytes8 ? 128u : 64u, 16};
-        cuuint32_t estr[2] = {1, 1};
+        // 256 bytes, boxes of 128 x 16 (both 128-byte inner boxes).  The tile
+        // view: dims {64, rows, 4 column chunks}, strides 512 B (a row) and
+        // 128 B (a chunk), boxes of {64, box_rows, 4}.
+        cuuint64_t dims[3] = {256, rows, 1};
+        cuuint64_t strides[2] = {bytes8 ? 256u : 512u, 0};
+        cuuint32_t box[3] = {bytes8 ? 128u : 64u, 16, 1};
+        if (tile) {
+            dims[0] = 64;
+            dims[2] = 4;
+            strides[1] = 128;
+            box[1] = static_cast<cuuint32_t>(box_rows);
+            box[2] = 4;
+        }
+        cuuint32_t estr[3] = {1, 1, 1};
         CUresult r = fn(reinterpret_cast<CUtensorMap *>(m.bytes),
-                        bytes8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                        const_cast<void *>(base), dims, strides, box, estr,
+                        bytes8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        tile ? 3 : 2, const_cast<void *>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return -1;
         std::lock_guard<std::mutex> g(g_map_mu);
         if (g_maps.size() >= 256) g_maps.erase(g_maps.begin());
-        g_maps.push_back({{reinterpret_cast<uintptr_t>(base), rows, bytes8}, m});
+        g_maps.push_back({{reinterpret_cast<uintptr_t>(base), rows, bytes8, tile, box_rows}, m});
     }
     for (int i = 0; i < n_maps; ++i)
         if (std::memcmp(maps.map[i].bytes, m.bytes, sizeof(m.bytes)) == 0) return i;
@@ -168,11 +181,11 @@ int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool
     return n_maps++;
 }
 
-void plan_maps(Common &c, const pkv_layout *L, const pkv_seq *seqs, DecodeMaps &maps) {
+void plan_maps(Common &c, const pkv_layout *L, const pkv_seq *seqs, DecodeMaps &maps, bool tiles) {
     int n_maps = 0;
     for (int s = 0; s < c.n_seqs; ++s) {
         SeqDev &d = c.seq[s];
-        d.tma = -1;
+        d.tma = d.tma64 = -1;
         const pkv_pg &pg = seqs[s].pg;
         const int64_t layer_off =
             (int64_t)c.layer * layer_elems_f(fp8_of(L), L->n_kv_heads, L->idx_dim, pg.page_pos);
@@ -192,6 +205,12 @@ void plan_maps(Common &c, const pkv_layout *L, const pkv_seq *seqs, DecodeMaps &
         d.tma = row_map(maps, n_maps, pg.base, rows, false);
         d.layer_row = layer_off / 256;
         d.page_rows = pg.page_elems / 256;
+        // a chunk kernel's 64-key tile starts on a multiple of 64 positions, so
+        // with pages of a multiple of 64 it is one 64-row run: one copy.  (A
+        // decode tile stays four 2D copies of 16 rows: one 3D copy of its 8 KB
+        // made the decode chain about 3 % slower, its rows arriving later.)
+        if (tiles && d.tma >= 0 && pg.page_pos % 64 == 0)
+            d.tma64 = row_map(maps, n_maps, pg.base, rows, false, true, 64);
     }
 }
 
@@ -361,7 +380,7 @@ static int launch_tensor_route(const pkv_layout *L, const pkv_seq *seqs, const C
                                cudaStream_t stream) {
     DecodeMaps maps;
     Common cc = c;
-    plan_maps(cc, L, seqs, maps);
+    plan_maps(cc, L, seqs, maps, true);
     return launch_prefill(cc, plan, maps, static_cast<const uint16_t *>(q),
                           static_cast<uint16_t *>(out), ws, static_cast<const uint16_t *>(k_new),
                           static_cast<const uint16_t *>(v_new), static_cast<const uint16_t *>(ik_new),
@@ -402,7 +421,7 @@ extern "C" int pkv_decode(const pkv_layout *L, const pkv_seq *seqs, int32_t n_se
         return launch_tensor_route(L, seqs, c, plan, q, k_new, v_new, L->idx_dim ? ik_new : nullptr,
                                    out, static_cast<float *>(ws), stream);
     DecodeMaps maps;  // copied into the launch's parameters
-    plan_maps(c, L, seqs, maps);
+    plan_maps(c, L, seqs, maps, false);
     if (c.kv_fp8)
         return launch_decode8(c, plan, maps, static_cast<const uint16_t *>(q),
                               static_cast<uint16_t *>(out), static_cast<float *>(ws),
@@ -439,7 +458,7 @@ extern "C" int pkv_decode_static(const pkv_layout *L, const pkv_seq *seqs, int32
         return launch_tensor_route(L, seqs, c, plan, q, k_new, v_new, L->idx_dim ? ik_new : nullptr,
                                    out, static_cast<float *>(scratch), stream);
     DecodeMaps maps;
-    plan_maps(c, L, seqs, maps);
+    plan_maps(c, L, seqs, maps, false);
     if (c.kv_fp8)
         return launch_decode8(c, plan, maps, static_cast<const uint16_t *>(q),
                               static_cast<uint16_t *>(out), static_cast<float *>(scratch),
@@ -477,7 +496,8 @@ extern "C" int pkv_sparse_decode(const pkv_layout *L, const pkv_seq *seqs, int32
     if (plan.ws_bytes > 0 &&
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
-    for (int s = 0; s < c.n_seqs; ++s) c.seq[s].tma = -1;  // selected blocks: cp.async path
+    for (int s = 0; s < c.n_seqs; ++s)  // selected blocks: cp.async path
+        c.seq[s].tma = c.seq[s].tma64 = -1;
     DecodeMaps maps;
     return launch_decode(c, plan, maps, true, static_cast<const uint16_t *>(q), ids, k,
                          static_cast<uint16_t *>(out), static_cast<float *>(ws), nullptr, nullptr,
@@ -519,7 +539,7 @@ extern "C" int pkv_prefill(const pkv_layout *L, const pkv_seq *seqs, int32_t n_s
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
     DecodeMaps maps;
-    plan_maps(c, L, seqs, maps);
+    plan_maps(c, L, seqs, maps, true);
     return launch_prefill(c, plan, maps, static_cast<const uint16_t *>(q),
                           static_cast<uint16_t *>(out), static_cast<float *>(ws), nullptr, nullptr,
                           nullptr, stream);

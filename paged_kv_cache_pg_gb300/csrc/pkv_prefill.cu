@@ -15,11 +15,15 @@
 // own, each filled by its own producer warp: a K slot is free as soon as its
 // S product is done, so the next K tiles load while the softmax and the PV
 // product of earlier tiles run (with one ring for both, every tile waited
-// out a whole load latency).  Tiles arrive by 2D TMA copies of whole 16-row
-// page runs (the rows of 16 consecutive positions are contiguous in a page
-// whose size is a multiple of 16) or, for a ragged tail or other page sizes,
-// by cp.async from one row lookup per key, fenced by the copying threads
-// before the tensor cores read them.  The max of a row is rescaled
+// out a whole load latency).  Tiles arrive by 2D TMA copies of whole page
+// runs: the rows of consecutive positions are contiguous inside a page, so a
+// tile in one page of a multiple of 64 positions is one 64-row run (one 3D
+// copy of all four 64-dim chunks) and in pages of a multiple of 16 four
+// 16-row runs (sixteen 2D copies; each copy costs the issuing thread about
+// 40 ns, whatever its size).  A ragged tail or other
+// page sizes go by cp.async from one row lookup per key, fenced by the
+// copying threads before the tensor cores read them.  A producer looks up a
+// tile's rows before its slot is free.  The max of a row is rescaled
 // lazily: O in TMEM is corrected only when the running max grows by more
 // than 2^8.  Split partials use the decode layout and its combine kernel.
 #include <algorithm>
@@ -109,6 +113,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 64 consecutive 32-bit TMEM columns of this thread's lane: one load and one
+// wait for a whole S tile.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -258,9 +273,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sv[32], sw[32];
-            tmem_ld32(lane_base + sb * kN, sv);
-            tmem_ld32(lane_base + sb * kN + 32, sw);
+            uint32_t sv[kN];
+            tmem_ld64(lane_base + sb * kN, sv);
             tc_fence_before();
             mbar_arrive(&bars[kBarSEmpty + sb]);
             const int kt = key0 + n * kN;
@@ -269,21 +283,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
             float x[kN];
             if (__all_sync(0xffffffffu, kt + kN <= key1 && kt + kN - 1 <= qpos)) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    x[i] = __uint_as_float(sv[i]);
-                    x[32 + i] = __uint_as_float(sw[i]);
-                }
+                for (int i = 0; i < kN; ++i) x[i] = __uint_as_float(sv[i]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int kp = kt + i, kq = kt + 32 + i;
+                for (int i = 0; i < kN; ++i) {
+                    const int kp = kt + i;
                     x[i] = (kp < key1 && kp <= qpos) ? __uint_as_float(sv[i]) : -INFINITY;
-                    x[32 + i] = (kq < key1 && kq <= qpos) ? __uint_as_float(sw[i]) : -INFINITY;
                 }
             }
-            float mx = x[0];
+            // the max as eight interleaved chains (it is exact in any order)
+            float m8[8];
 #pragma unroll
-            for (int i = 1; i < kN; ++i) mx = fmaxf(mx, x[i]);
+            for (int i = 0; i < 8; ++i) m8[i] = x[i];
+#pragma unroll
+            for (int i = 8; i < kN; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             mx *= kScaleLog2;  // in log2 units; -inf when the whole tile is masked
             const bool grow = m_used != -INFINITY && mx > m_used + kRescale;
             if (__any_sync(0xffffffffu, grow)) {
@@ -313,13 +328,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // p = 2^(s * scale - m); a masked score is -inf and gives 0 (the
             // offset is 0 while every score so far was masked)
             const float m_off = m_used == -INFINITY ? 0.f : m_used;
-            float psum = 0.f;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum as four chains
             uint32_t hi[kN / 2], lo[kN / 2];
 #pragma unroll
             for (int i = 0; i < kN; i += 2) {
                 const float p0 = ex2(fmaf(x[i], kScaleLog2, -m_off));
                 const float p1 = ex2(fmaf(x[i + 1], kScaleLog2, -m_off));
-                psum += p0 + p1;
+                ps[(i >> 1) & 3] += p0 + p1;
                 // p = hi + lo: hi is p's top 16 bits (exact), lo the top 16 bits
                 // of the exact remainder, so hi + lo is p to 2^-15 relative;
                 // bit selects keep the split off the conversion pipe
@@ -329,7 +344,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const float r1 = p1 - __uint_as_float(u1 & 0xffff0000u);
                 lo[i / 2] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
             }
-            l += psum;
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             // the P rows are free once the last tile's products are done
             if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + ((n - 1) & 1)],
                                                              ((n - 1) >> 1) & 1, c.status))) {
@@ -408,10 +423,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
         uint8_t *const ring = smem + (is_v ? kOffV : kOffK);
         uint64_t *const full = &bars[is_v ? kBarVFull : kBarKFull];
         uint64_t *const empty = &bars[is_v ? kBarVEmpty : kBarKEmpty];
-        const void *map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;
+        // the stream's fields in registers: read from the launch parameters
+        // with a per-CTA index, each costs a constant-cache round trip, and
+        // the issue loop would reread them every tile
+        const int ptok = sd.ptok, n_pages = sd.n_pages, n_table = sd.n_table, tok_off = sd.tok_off;
+        const int32_t *const table = sd.table;
+        const int64_t ps = sd.ps, layer_row = sd.layer_row;
+        const uint16_t *const layer_base = sd.layer_base;
+        const void *const map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;        // 16 x 64 boxes
+        const void *const map64 = sd.tma64 >= 0 ? &maps.map[sd.tma64] : nullptr;  // 64-row tiles
         const uint64_t pol = policy_evict_normal();  // every M-tile of the head reads these rows
         // V rows sit H * ptok rows after the K rows of the same page
-        const int64_t gap = is_v ? (int64_t)H * sd.ptok * kHeadDim : 0;
+        const int64_t gap = is_v ? (int64_t)H * ptok * kHeadDim : 0;
         const bool fuse = a.k_new != nullptr;
         const uint16_t *const new_rows = is_v ? a.v_new : a.k_new;
         // page ids in registers: lane i holds pages win + i (cur) and
@@ -419,24 +442,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // its first half, so the next half is loading long before it is read
         // and no table read waits in the issue loop (a tile spans at most 17
         // pages, so its pages always lie in the 64-page window)
-        auto page_id = [&](int p) -> int {
-            return (sd.table && p < sd.n_table) ? __ldg(sd.table + p) : 0;
-        };
-        int win = sd.table ? key0 / sd.ptok : 0;
+        auto page_id = [&](int p) -> int { return (table && p < n_table) ? __ldg(table + p) : 0; };
+        int win = table ? key0 / ptok : 0;
         int cur = page_id(win + lane), nxt = page_id(win + 32 + lane);
         for (int n = 0; n < ntiles; ++n) {
             const int b = n % nbuf;
-            if (__any_sync(0xffffffffu, *abort_flag) ||
-                (n >= nbuf && !__all_sync(0xffffffffu, mbar_wait(&empty[b], ((n / nbuf) - 1) & 1, c.status)))) {
-                *abort_flag = 1;
-                break;
-            }
             const int kt = key0 + n * kN;
-            uint8_t *dst = ring + b * kKVBytes;
-            // this lane's keys kt + lane and kt + 32 + lane (one lookup per key
-            // per tile), clamped into the split
-            if (sd.table) {
-                const int first = min(kt, key1 - 1) / sd.ptok;  // the tile's lowest page
+            // the tile's rows are looked up before its slot is free: this
+            // lane's keys kt + lane and kt + 32 + lane, clamped into the split
+            if (table) {
+                const int first = min(kt, key1 - 1) / ptok;  // the tile's lowest page
                 while (first >= win + 32) {
                     win += 32;
                     cur = nxt;
@@ -450,31 +465,45 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const int key = min(kt + 32 * h + lane, key1 - 1);
                 int row = key;
                 int64_t pg = 0;
-                if (sd.table) {
-                    const int page = key / sd.ptok;
-                    row = key - page * sd.ptok;
+                if (table) {
+                    const int page = key / ptok;
+                    row = key - page * ptok;
                     const int idx = page - win;  // 0 .. 63: a tile spans at most 17 pages
                     const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
                     const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
                     const int id = idx < 32 ? a0 : a1;
-                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(sd.n_pages)) {
-                        pg = (int64_t)id * sd.ps;
+                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
+                        pg = (int64_t)id * ps;
                     } else {
                         bad[h] = true;
                         if (c.status && !is_v) atomicOr(c.status, PKV_DEV_BAD_PAGE);
                     }
                 }
-                krow[h] = pg + off_k(sd.ptok, kvh, row) + gap;
+                krow[h] = pg + off_k(ptok, kvh, row) + gap;
             }
             // with a decode call's new rows, keys from qbase on come from the
             // input, not the cache (which this kernel stores them into)
             const bool fresh_tile = fuse && min(kt + kN, key1) > qbase;
-            if (map != nullptr && kt + kN <= key1 && !fresh_tile) {
-                // four 16-row page runs, four 64-dim chunks each
-                const int y0 = static_cast<int>(sd.layer_row + shfl64(krow[0], 0) / kHeadDim);
-                const int y1 = static_cast<int>(sd.layer_row + shfl64(krow[0], 16) / kHeadDim);
-                const int y2 = static_cast<int>(sd.layer_row + shfl64(krow[1], 0) / kHeadDim);
-                const int y3 = static_cast<int>(sd.layer_row + shfl64(krow[1], 16) / kHeadDim);
+            const bool whole = kt + kN <= key1 && !fresh_tile;
+            // a whole tile in one page (pages of a multiple of 64): one 64-row
+            // run of all 256 dims, one copy; else four 16-row page runs of four
+            // 64-dim chunks, sixteen copies
+            const int y0 = static_cast<int>(layer_row + shfl64(krow[0], 0) / kHeadDim);
+            const int y1 = static_cast<int>(layer_row + shfl64(krow[0], 16) / kHeadDim);
+            const int y2 = static_cast<int>(layer_row + shfl64(krow[1], 0) / kHeadDim);
+            const int y3 = static_cast<int>(layer_row + shfl64(krow[1], 16) / kHeadDim);
+            if (__any_sync(0xffffffffu, *abort_flag) ||
+                (n >= nbuf && !__all_sync(0xffffffffu, mbar_wait(&empty[b], ((n / nbuf) - 1) & 1, c.status)))) {
+                *abort_flag = 1;
+                break;
+            }
+            uint8_t *dst = ring + b * kKVBytes;
+            if (whole && map64 != nullptr) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[b], kKVBytes);
+                    tma_load_3d(dst, map64, 0, y0, 0, &full[b], pol);
+                }
+            } else if (whole && map != nullptr) {
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[b], kKVBytes);
 #pragma unroll
@@ -490,9 +519,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int key = min(kt + 32 * h + lane, key1 - 1);
-                    const uint16_t *src = sd.layer_base + krow[h];
+                    const uint16_t *src = layer_base + krow[h];
                     if (fresh_tile && key >= qbase)
-                        src = new_rows + (((int64_t)sd.tok_off + (key - qbase)) * H + kvh) * kHeadDim;
+                        src = new_rows + (((int64_t)tok_off + (key - qbase)) * H + kvh) * kHeadDim;
                     const int64_t sp = reinterpret_cast<int64_t>(src);
 #pragma unroll 8
                     for (int rr = 0; rr < 32; ++rr)
@@ -517,15 +546,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         const int h = (i - kt) >> 5, l = (i - kt) & 31;
                         const int64_t kr = shfl64(h ? krow[1] : krow[0], l);
                         if (__shfl_sync(0xffffffffu, h ? bad[1] : bad[0], l)) continue;
-                        const int64_t r = (int64_t)sd.tok_off + (i - qbase);
-                        uint16_t *row = const_cast<uint16_t *>(sd.layer_base) + kr;
+                        const int64_t r = (int64_t)tok_off + (i - qbase);
+                        uint16_t *row = const_cast<uint16_t *>(layer_base) + kr;
                         reinterpret_cast<uint4 *>(row)[lane] =
                             __ldg(reinterpret_cast<const uint4 *>(new_rows + (r * H + kvh) * kHeadDim) + lane);
                         if (!is_v && kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
-                            const int prow = sd.table ? i % sd.ptok : i;
+                            const int prow = table ? i % ptok : i;
                             const int64_t page_start = kr - (int64_t)prow * kHeadDim;
-                            uint16_t *idst = const_cast<uint16_t *>(sd.layer_base) + page_start +
-                                             off_ik(H, c.idx_dim, sd.ptok, prow);
+                            uint16_t *idst = const_cast<uint16_t *>(layer_base) + page_start +
+                                             off_ik(H, c.idx_dim, ptok, prow);
                             reinterpret_cast<uint4 *>(idst)[lane] =
                                 __ldg(reinterpret_cast<const uint4 *>(a.ik_new + r * c.idx_dim) + lane);
                         }
@@ -538,13 +567,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t idesc_s = mma_idesc(kN, false);
         const uint32_t idesc_o = mma_idesc(kHeadDim, true);
         bool ok = mbar_wait(&bars[kBarQFull], 0, c.status);
-        fence_async_smem();
         tc_fence_after();
+        // operands written by threads (Q, P, key-by-key tiles) were fenced to
+        // the async proxy by their writers before they arrived
         auto issue_s = [&](int n) -> bool {
             const int b = n % kKS, sb = n & 1;
             if (!mbar_wait(&bars[kBarKFull + b], (n / kKS) & 1, c.status)) return false;
             if (n >= 2 && !mbar_wait(&bars[kBarSEmpty + sb], ((n - 2) >> 1) & 1, c.status)) return false;
-            fence_async_smem();
             tc_fence_after();
             const uint32_t kb = sbase + kOffK + b * kKVBytes;
 #pragma unroll
@@ -570,7 +599,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 ok = false;
                 break;
             }
-            fence_async_smem();
             tc_fence_after();
             const uint32_t vb = sbase + kOffV + b * kKVBytes;
 #pragma unroll
