@@ -124,23 +124,26 @@ struct MapKey {
     uint64_t rows;
     bool bytes8;
     bool tile;
-    int box_rows;
+    int box_rows, box_chunks;
 };
 std::mutex g_map_mu;
 std::vector<std::pair<MapKey, RowMap>> g_maps;  // encoded maps, most recent last
 }  // namespace
 
 int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool bytes8,
-            bool tile, int box_rows) {
+            bool tile, int box_rows, int box_chunks) {
     if (rows == 0 || rows > (1ull << 31) || !aligned16(base)) return -1;
-    if ((box_rows != 16 && box_rows != 64) || (bytes8 && tile) || (!tile && box_rows != 16)) return -1;
+    if (tile ? (bytes8 || (box_rows != 64 && box_rows != 128) || (box_chunks != 2 && box_chunks != 4))
+             : (box_rows != 16 || box_chunks != 1))
+        return -1;
     RowMap m;
     bool have = false;
     {
         std::lock_guard<std::mutex> g(g_map_mu);
         for (auto &e : g_maps)
             if (e.first.base == reinterpret_cast<uintptr_t>(base) && e.first.rows == rows &&
-                e.first.bytes8 == bytes8 && e.first.tile == tile && e.first.box_rows == box_rows) {
+                e.first.bytes8 == bytes8 && e.first.tile == tile && e.first.box_rows == box_rows &&
+                e.first.box_chunks == box_chunks) {
                 m = e.second;
                 have = true;
                 break;
@@ -152,7 +155,7 @@ int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool
         // bf16 rows: 256 elements (512 B), boxes of 64 x 16; e4m3 code rows:
         // 256 bytes, boxes of 128 x 16 (both 128-byte inner boxes).  The tile
         // view: dims {64, rows, 4 column chunks}, strides 512 B (a row) and
-        // 128 B (a chunk), boxes of {64, box_rows, 4}.
+        // 128 B (a chunk), boxes of {64, box_rows, box_chunks}.
         cuuint64_t dims[3] = {256, rows, 1};
         cuuint64_t strides[2] = {bytes8 ? 256u : 512u, 0};
         cuuint32_t box[3] = {bytes8 ? 128u : 64u, 16, 1};
@@ -161,7 +164,7 @@ int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool
             dims[2] = 4;
             strides[1] = 128;
             box[1] = static_cast<cuuint32_t>(box_rows);
-            box[2] = 4;
+            box[2] = static_cast<cuuint32_t>(box_chunks);
         }
         cuuint32_t estr[3] = {1, 1, 1};
         CUresult r = fn(reinterpret_cast<CUtensorMap *>(m.bytes),
@@ -172,7 +175,7 @@ int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool
         if (r != CUDA_SUCCESS) return -1;
         std::lock_guard<std::mutex> g(g_map_mu);
         if (g_maps.size() >= 256) g_maps.erase(g_maps.begin());
-        g_maps.push_back({{reinterpret_cast<uintptr_t>(base), rows, bytes8, tile, box_rows}, m});
+        g_maps.push_back({{reinterpret_cast<uintptr_t>(base), rows, bytes8, tile, box_rows, box_chunks}, m});
     }
     for (int i = 0; i < n_maps; ++i)
         if (std::memcmp(maps.map[i].bytes, m.bytes, sizeof(m.bytes)) == 0) return i;
@@ -185,7 +188,8 @@ void plan_maps(Common &c, const pkv_layout *L, const pkv_seq *seqs, DecodeMaps &
     int n_maps = 0;
     for (int s = 0; s < c.n_seqs; ++s) {
         SeqDev &d = c.seq[s];
-        d.tma = d.tma64 = -1;
+        d.tma = -1;
+        d.tma_k = d.tma_v = -1;
         const pkv_pg &pg = seqs[s].pg;
         const int64_t layer_off =
             (int64_t)c.layer * layer_elems_f(fp8_of(L), L->n_kv_heads, L->idx_dim, pg.page_pos);
@@ -205,12 +209,17 @@ void plan_maps(Common &c, const pkv_layout *L, const pkv_seq *seqs, DecodeMaps &
         d.tma = row_map(maps, n_maps, pg.base, rows, false);
         d.layer_row = layer_off / 256;
         d.page_rows = pg.page_elems / 256;
-        // a chunk kernel's 64-key tile starts on a multiple of 64 positions, so
-        // with pages of a multiple of 64 it is one 64-row run: one copy.  (A
-        // decode tile stays four 2D copies of 16 rows: one 3D copy of its 8 KB
-        // made the decode chain about 3 % slower, its rows arriving later.)
-        if (tiles && d.tma >= 0 && pg.page_pos % 64 == 0)
-            d.tma64 = row_map(maps, n_maps, pg.base, rows, false, true, 64);
+        // a chunk kernel's K slot (a 128-key tile over 128 dims) and V slot
+        // (64 keys over 256 dims) start on multiples of their key counts, so
+        // in pages of a multiple of those counts each is one run: one copy.
+        // (A decode tile stays four 2D copies of 16 rows: one 3D copy of its
+        // 8 KB made the decode chain about 3 % slower, its rows arriving later.)
+        if (tiles && d.tma >= 0) {
+            if (pg.page_pos % 128 == 0)
+                d.tma_k = static_cast<int16_t>(row_map(maps, n_maps, pg.base, rows, false, true, 128, 2));
+            if (pg.page_pos % 64 == 0)
+                d.tma_v = static_cast<int16_t>(row_map(maps, n_maps, pg.base, rows, false, true, 64, 4));
+        }
     }
 }
 
@@ -496,8 +505,10 @@ extern "C" int pkv_sparse_decode(const pkv_layout *L, const pkv_seq *seqs, int32
     if (plan.ws_bytes > 0 &&
         (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return PKV_EINVAL;
-    for (int s = 0; s < c.n_seqs; ++s)  // selected blocks: cp.async path
-        c.seq[s].tma = c.seq[s].tma64 = -1;
+    for (int s = 0; s < c.n_seqs; ++s) {  // selected blocks: cp.async path
+        c.seq[s].tma = -1;
+        c.seq[s].tma_k = c.seq[s].tma_v = -1;
+    }
     DecodeMaps maps;
     return launch_decode(c, plan, maps, true, static_cast<const uint16_t *>(q), ids, k,
                          static_cast<uint16_t *>(out), static_cast<float *>(ws), nullptr, nullptr,

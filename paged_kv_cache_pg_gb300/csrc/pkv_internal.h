@@ -37,8 +37,8 @@ struct SeqDev {
     int32_t ncols;         // query columns of one unit: n_new * group (decode)
     int64_t ws_off;        // float offset of this stream's partials in ws
     int32_t tma;           // index of the stream's 2D row map (16-row boxes of 64 dims), or -1
-    int32_t tma64;         // bf16: its 3D tile map, one copy a 64-row run of all 256 dims
-                           // (pages of a multiple of 64 positions), or -1
+    int16_t tma_k;         // bf16, chunk kernel: its 3D map of 128-row runs over 128 dims, or -1
+    int16_t tma_v;         // bf16, chunk kernel: its 3D map of 64-row runs over 256 dims, or -1
     int64_t layer_row;     // row (256 elements) of layer_base from the map's base
     int64_t page_rows;     // rows in a page (page_elems / 256)
 };
@@ -47,9 +47,9 @@ struct SeqDev {
 // elements with 128-byte swizzle: one box is 16 consecutive key (or value)
 // rows of one 64-element column chunk.  The 3D tile view of the same rows
 // adds the four column chunks as the outer dimension (dims {64, rows, 4},
-// strides 512 B and 128 B): one box of {64, R, 4} lands as four swizzled
-// planes of R rows x 128 B, chunk after chunk, the layout four 2D boxes
-// give, in one copy.
+// strides 512 B and 128 B): one box of {64, R, C} lands as C swizzled planes
+// of R rows x 128 B, chunk after chunk, the layout R/16 x C 2D boxes give,
+// in one copy.
 constexpr int kMaxMaps = 16;
 struct alignas(64) RowMap {
     unsigned char bytes[128];  // CUtensorMap
@@ -61,9 +61,9 @@ struct DecodeMaps {
 // or -1 when none can be made (no driver entry point, or maps full).
 // bytes8: rows of 256 bytes (e4m3 codes, boxes of 128 x 16) instead of 256
 // bf16 elements (boxes of 64 x 16); tile: the 3D tile view of bf16 rows,
-// boxes of {64, box_rows, 4} (box_rows 16 or 64).
+// boxes of {64, box_rows, box_chunks} (box_rows 64 or 128, box_chunks 2 or 4).
 int row_map(DecodeMaps &maps, int &n_maps, const void *base, uint64_t rows, bool bytes8,
-            bool tile = false, int box_rows = 16);
+            bool tile = false, int box_rows = 16, int box_chunks = 1);
 
 struct Common {
     int32_t n_seqs;
@@ -178,7 +178,9 @@ struct DecodePlan {
 int plan_decode(Common &c, bool sparse, int32_t k, int nsm, DecodePlan *plan);
 // Give each eligible dense stream its row map (page size a multiple of 16,
 // rows of 256 elements aligned to the buffer base), and with `tiles` (a
-// chunk-kernel call) its 64-row tile map where pages hold a multiple of 64.
+// chunk-kernel call) its tile maps: 64-row runs of V where pages hold a
+// multiple of 64 positions, 128-row runs of K where they hold a multiple of
+// 128.
 void plan_maps(Common &c, const pkv_layout *layout, const pkv_seq *seqs, DecodeMaps &maps,
                bool tiles);
 int launch_decode(const Common &c, const DecodePlan &plan, const DecodeMaps &maps, bool sparse,

@@ -2,30 +2,30 @@
 //
 // Rows: the (query, head) pairs of one KV head, 128 to an M-tile (16 queries
 // x 8 heads for the pages' 16/2 heads).  A CTA takes one M-tile and one split
-// of the keys and runs, per tile of 64 keys:
-//   S = Q K^T  -> TMEM (128 lanes x 64 columns, two buffers)   [MMA warp]
-//   softmax of S with the causal mask, P = hi + lo bf16 parts   [4 warps]
-//   O += P_hi V + P_lo V -> TMEM (128 lanes x 256 columns)      [MMA warp]
+// of the keys and runs, per tile of 128 keys:
+//   S = Q K^T  -> TMEM (128 lanes x 128 columns)               [MMA thread]
+//   softmax of S with the causal mask, P = hi + lo bf16 parts   [8 warps]
+//   O += P_hi V + P_lo V -> TMEM (128 lanes x 256 columns)      [MMA thread]
 // A tcgen05 MMA with M = 128 costs about the same for every N up to 128, so
-// the S product of a 64-key tile takes the time a 32-key one would.  P has
-// one buffer: the softmax computes tile n+1's weights while the PV product
-// of tile n reads P, and stores them once that product is done.
-// Q, K, V and P sit in shared memory in the 128-byte-swizzled layouts the
-// MMA reads through matrix descriptors.  K and V tiles have rings of their
-// own, each filled by its own producer warp: a K slot is free as soon as its
-// S product is done, so the next K tiles load while the softmax and the PV
-// product of earlier tiles run (with one ring for both, every tile waited
-// out a whole load latency).  Tiles arrive by 2D TMA copies of whole page
-// runs: the rows of consecutive positions are contiguous inside a page, so a
-// tile in one page of a multiple of 64 positions is one 64-row run (one 3D
-// copy of all four 64-dim chunks) and in pages of a multiple of 16 four
-// 16-row runs (sixteen 2D copies; each copy costs the issuing thread about
-// 40 ns, whatever its size).  A ragged tail or other
-// page sizes go by cp.async from one row lookup per key, fenced by the
-// copying threads before the tensor cores read them.  A producer looks up a
-// tile's rows before its slot is free.  The max of a row is rescaled
-// lazily: O in TMEM is corrected only when the running max grows by more
-// than 2^8.  Split partials use the decode layout and its combine kernel.
+// a 128-key S product takes the instructions a 64-key one did.  Q sits in
+// TMEM (columns 0-127, bf16 pairs) and is the S product's A operand there;
+// that leaves shared memory for P (hi and lo, 64 KB), two K slots (a tile's
+// keys over 128 of the dims each) and two V slots (64 of a tile's keys over
+// all dims each).  The softmax takes two threads a row (TMEM lane), each on
+// 64 of the tile's keys and 128 of O's columns; the pair agrees on the row
+// maximum through shared memory.  S has one TMEM buffer: the next S product
+// starts once the softmax threads have read S, and P has one buffer, which
+// the softmax fills once the previous tile's PV product is done.
+// K and V arrive through rings of their own, each filled by its own producer
+// warp, which looks a unit's rows up before its slot is free.  A unit in one
+// page comes by one 3D TMA copy (pages of a multiple of 128 positions for K,
+// 64 for V), or by 2D copies of 16-row page runs (pages of a multiple of 16;
+// each copy costs the issuing thread about 40 ns, whatever its size), or,
+// for a ragged tail or other page sizes, by cp.async from one row lookup per
+// key, fenced by the copying threads before the tensor cores read it.  The
+// max of a row is rescaled lazily: O in TMEM is corrected only when the
+// running max grows by more than 2^8.  Split partials use the decode layout
+// and its combine kernel.
 #include <algorithm>
 #include <climits>
 
@@ -35,27 +35,31 @@ namespace pkv {
 namespace {
 
 constexpr int kM = 128;              // rows of an M-tile
-constexpr int kN = 64;               // keys a tile
-constexpr int kKS = 2;               // K tile buffers
-constexpr int kVS = 2;               // V tile buffers
-constexpr int kPThreads = 224;       // warps 0-3 softmax, 4 K producer, 5 MMA, 6 V producer
-constexpr uint32_t kTmemCols = 512;  // S buffers at columns 0 and 32, O at 256
-constexpr uint32_t kOCol = 256;
-constexpr int kQBytes = kM * 512;    // four 64-dim regions of 128 rows x 128 B
-constexpr int kKVBytes = kN * 512;   // four 64-dim regions of 64 rows x 128 B
-constexpr int kRegionQ = kM * 128;   // bytes of one 64-dim region of Q
-constexpr int kRegionKV = kN * 128;  // bytes of one 64-dim region of a K or V tile
-constexpr int kPBytes = kM * 128;    // 128 rows x 128 B: one tile's 64 keys
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + kKS * kKVBytes;
-constexpr int kOffP = kOffV + kVS * kKVBytes;  // P hi, then P lo
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-// barriers (a pair wherever the producing side may run a tile ahead)
-constexpr int kBarKFull = 0, kBarVFull = kBarKFull + kKS, kBarKEmpty = kBarVFull + kVS;
-constexpr int kBarVEmpty = kBarKEmpty + kKS, kBarSFull = kBarVEmpty + kVS, kBarSEmpty = kBarSFull + 2;
-constexpr int kBarPFull = kBarSEmpty + 2, kBarODone = kBarPFull + 2, kBarQFull = kBarODone + 2;
-constexpr int kNumBars = kBarQFull + 1;
+constexpr int kN = 128;              // keys a tile
+constexpr int kSoftWarps = 8;        // two threads a row, each on 64 keys of a tile
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+constexpr int kPThreads = 352;       // warps 0-7 softmax, 8 K producer, 9 MMA, 10 V producer
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kQCol = 0;        // Q: 256 dims as bf16 pairs
+constexpr uint32_t kSCol = 128;      // S: 128 keys
+constexpr uint32_t kOCol = 256;      // O: 256 dims
+constexpr int kKRegion = kN * 128;   // one 64-dim region of 128 K rows
+constexpr int kKHalf = 2 * kKRegion; // a K slot: the tile's 128 keys over 128 dims
+constexpr int kVRegion = 64 * 128;   // one 64-dim region of 64 V rows
+constexpr int kVHalf = 4 * kVRegion; // a V slot: 64 of the tile's keys over 256 dims
+constexpr int kPRegion = kM * 128;   // 64 keys of the 128 P rows
+constexpr int kPPart = 2 * kPRegion; // P hi (or lo): the tile's 128 keys
+constexpr int kOffP = 0;             // P hi, then P lo
+constexpr int kOffK = kOffP + 2 * kPPart;
+constexpr int kOffV = kOffK + 2 * kKHalf;
+constexpr int kOffRed = kOffV + 2 * kVHalf;       // [tile parity][half][row] floats
+constexpr int kOffBar = kOffRed + 2 * 2 * kM * 4;
+// barriers: a pair for each ring's two slots, one for each single buffer
+constexpr int kBarKFull = 0, kBarKEmpty = 2, kBarVFull = 4, kBarVEmpty = 6;
+constexpr int kBarSFull = 8, kBarSEmpty = 9, kBarPFull = 10, kBarODone = 11, kBarQFull = 12;
+constexpr int kBarRed = 13;
+constexpr int kNumBars = 14;
 constexpr size_t kPSmem = 1024 + kOffBar + kNumBars * 8 + 16;
 static_assert(kPSmem <= 232448, "prefill shared memory above the 227 KB a CTA may hold");
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
@@ -82,6 +86,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A from TMEM (the TS form): a_tmem is the address of A's
+// first column, 16 bf16 elements of each row in 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -190,28 +205,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int ntiles = key1 > key0 ? (key1 - key0 + kN - 1) / kN : 0;
 
     if (tid == 0) {
-        for (int i = 0; i < kKS; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[kBarKFull + i], 1);
             mbar_init(&bars[kBarKEmpty + i], 1);
-        }
-        for (int i = 0; i < kVS; ++i) {
             mbar_init(&bars[kBarVFull + i], 1);
             mbar_init(&bars[kBarVEmpty + i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[kBarSFull + i], 1);
-            mbar_init(&bars[kBarSEmpty + i], kM);
-            mbar_init(&bars[kBarPFull + i], kM);
-            mbar_init(&bars[kBarODone + i], 1);
-        }
-        mbar_init(&bars[kBarQFull], kM);
+        mbar_init(&bars[kBarSFull], 1);
+        mbar_init(&bars[kBarSEmpty], kSoftThreads);
+        mbar_init(&bars[kBarPFull], kSoftThreads);
+        mbar_init(&bars[kBarODone], 1);
+        mbar_init(&bars[kBarQFull], kSoftThreads);
+        mbar_init(&bars[kBarRed], kSoftThreads);
         *abort_flag = 0;
         fence_mbar_init();
     }
     // tcgen05 alloc, dealloc, ld and st are warp-collective (.sync.aligned):
     // every one below follows a __syncwarp, because a CTA barrier does not
     // reconverge a warp whose lanes took different paths before it
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
@@ -231,80 +243,92 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // new rows a stream) are not
     if (tid == 0) pdl_trigger();
 
-    if (warp < 4) {
-        // ---------------- softmax: thread r owns row r (TMEM lane r) ----------------
+    if (warp < kSoftWarps) {
+        // ------- softmax: row r (TMEM lane r) by two threads, keys 64 hf .. 64 hf + 63 of a tile -------
         pdl_wait();
-        const int r = tid;
+        const int r = lane + 32 * (warp & 3);
+        const int hf = warp >> 2;
         const int col = col0 + r;
         const bool row_ok = r < rows;
         const int j = row_ok ? col / G : 0;
         // rows past the M-tile's end take no mask: their Q rows are zero, so
         // their scores are finite, and their outputs are never written
         const int qpos = row_ok ? qbase + j : INT_MAX;
-        // Q row into the swizzled A operand
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        float *const red = reinterpret_cast<float *>(smem + kOffRed);
+        // Q dims 128 hf .. 128 hf + 127 into TMEM columns 64 hf .. 64 hf + 63 (bf16 pairs)
         {
-            uint8_t *qs = smem + kOffQ;
-            if (row_ok) {
-                const uint16_t *src =
-                    a.q + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
-#pragma unroll 8
-                for (int ch = 0; ch < 32; ++ch)
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                                     smem_u32(qs + swz128(kRegionQ, r, ch))),
-                                 "l"(src + ch * 8)
-                                 : "memory");
-                asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-            } else {
-#pragma unroll 8
-                for (int ch = 0; ch < 32; ++ch)
-                    *reinterpret_cast<uint4 *>(qs + swz128(kRegionQ, r, ch)) = make_uint4(0, 0, 0, 0);
+            const uint16_t *src =
+                a.q + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim + 128 * hf;
+#pragma unroll 1
+            for (int h32 = 0; h32 < 2; ++h32) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(src + 64 * h32 + 2 * i))
+                                           : make_uint4(0, 0, 0, 0);
+                    qv[i] = v.x;
+                    qv[i + 1] = v.y;
+                    qv[i + 2] = v.z;
+                    qv[i + 3] = v.w;
+                }
+                __syncwarp();
+                tmem_st32(lane_base + kQCol + 64 * hf + 32 * h32, qv);
             }
-            fence_async_smem();
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
             mbar_arrive(&bars[kBarQFull]);
         }
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         float m_used = -INFINITY, l = 0.f;
-        uint8_t *p_hi = smem + kOffP, *p_lo = smem + kOffP + kPBytes;
+        uint8_t *const p_hi = smem + kOffP + hf * kPRegion, *const p_lo = p_hi + kPPart;
         for (int n = 0; n < ntiles; ++n) {
-            const int sb = n & 1;
             // every exit is warp-uniform: the TMEM loads below are .sync.aligned
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarSFull + sb], (n >> 1) & 1, c.status))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarSFull], n & 1, c.status))) {
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            uint32_t sv[kN];
-            tmem_ld64(lane_base + sb * kN, sv);
+            uint32_t sv[64];
+            tmem_ld64(lane_base + kSCol + 64 * hf, sv);
             tc_fence_before();
-            mbar_arrive(&bars[kBarSEmpty + sb]);
-            const int kt = key0 + n * kN;
+            mbar_arrive(&bars[kBarSEmpty]);
+            const int kt = key0 + n * kN + 64 * hf;  // this thread's first key
             // raw scores; the causal and split bounds cut into a tile only near
             // the diagonal and at the split's end
-            float x[kN];
-            if (__all_sync(0xffffffffu, kt + kN <= key1 && kt + kN - 1 <= qpos)) {
+            float x[64];
+            if (__all_sync(0xffffffffu, kt + 64 <= key1 && kt + 63 <= qpos)) {
 #pragma unroll
-                for (int i = 0; i < kN; ++i) x[i] = __uint_as_float(sv[i]);
+                for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(sv[i]);
             } else {
 #pragma unroll
-                for (int i = 0; i < kN; ++i) {
+                for (int i = 0; i < 64; ++i) {
                     const int kp = kt + i;
                     x[i] = (kp < key1 && kp <= qpos) ? __uint_as_float(sv[i]) : -INFINITY;
                 }
             }
-            // the max as eight interleaved chains (it is exact in any order)
+            // this half's max as eight interleaved chains (exact in any order),
+            // then the row's from the partner thread
             float m8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) m8[i] = x[i];
 #pragma unroll
-            for (int i = 8; i < kN; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            mx *= kScaleLog2;  // in log2 units; -inf when the whole tile is masked
+            for (int i = 8; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
+            const float lmx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                    fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            red[((n & 1) * 2 + hf) * kM + r] = lmx;
+            mbar_arrive(&bars[kBarRed]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarRed], n & 1, c.status))) {
+                *abort_flag = 1;
+                break;
+            }
+            // in log2 units; -inf when the whole row of the tile is masked
+            const float mx = fmaxf(lmx, red[((n & 1) * 2 + (hf ^ 1)) * kM + r]) * kScaleLog2;
+            // both threads of a row see the same maximum, so they decide alike
             const bool grow = m_used != -INFINITY && mx > m_used + kRescale;
             if (__any_sync(0xffffffffu, grow)) {
-                // correct O: the previous tile's products must be in it first
-                if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + ((n - 1) & 1)],
-                                                                 ((n - 1) >> 1) & 1, c.status))) {
+                // correct this thread's half of O: the previous tile's products
+                // must be in it first
+                if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone], (n - 1) & 1, c.status))) {
                     *abort_flag = 1;
                     break;
                 }
@@ -312,12 +336,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const float m_new = fmaxf(m_used, mx);
                 const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
 #pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int ch = 0; ch < 4; ++ch) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + kOCol + ch * 32, o);
+                    tmem_ld32(lane_base + kOCol + 128 * hf + ch * 32, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(lane_base + kOCol + ch * 32, o);
+                    tmem_st32(lane_base + kOCol + 128 * hf + ch * 32, o);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 l *= alpha;
@@ -328,10 +352,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // p = 2^(s * scale - m); a masked score is -inf and gives 0 (the
             // offset is 0 while every score so far was masked)
             const float m_off = m_used == -INFINITY ? 0.f : m_used;
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum as four chains
-            uint32_t hi[kN / 2], lo[kN / 2];
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};  // this half's sum as four chains
+            uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int i = 0; i < kN; i += 2) {
+            for (int i = 0; i < 64; i += 2) {
                 const float p0 = ex2(fmaf(x[i], kScaleLog2, -m_off));
                 const float p1 = ex2(fmaf(x[i + 1], kScaleLog2, -m_off));
                 ps[(i >> 1) & 3] += p0 + p1;
@@ -346,12 +370,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             // the P rows are free once the last tile's products are done
-            if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + ((n - 1) & 1)],
-                                                             ((n - 1) >> 1) & 1, c.status))) {
+            if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone], (n - 1) & 1, c.status))) {
                 *abort_flag = 1;
                 break;
             }
-            // row r of the P operands: 64 keys = 128 bytes = chunks 0 .. 7
+            // row r of this half's P region: 64 keys = 128 bytes = chunks 0 .. 7
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
                 const uint32_t off = r * 128 + (((ch ^ (r & 7))) << 4);
@@ -362,15 +385,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars[kBarPFull + (n & 1)]);
+            mbar_arrive(&bars[kBarPFull]);
         }
         // ---------------- epilogue ----------------
         bool ok = __all_sync(0xffffffffu, !*abort_flag);
         if (ok && ntiles > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone + ((ntiles - 1) & 1)],
-                                               ((ntiles - 1) >> 1) & 1, c.status))) {
+            !__all_sync(0xffffffffu, mbar_wait(&bars[kBarODone], (ntiles - 1) & 1, c.status))) {
             *abort_flag = 1;
             ok = false;
+        }
+        // the row's sum: this thread's keys and its partner's
+        if (ok) {
+            red[((ntiles & 1) * 2 + hf) * kM + r] = l;
+            mbar_arrive(&bars[kBarRed]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarRed], ntiles & 1, c.status))) {
+                *abort_flag = 1;
+                ok = false;
+            } else {
+                l += red[((ntiles & 1) * 2 + (hf ^ 1)) * kM + r];
+            }
         }
         tc_fence_after();
         if (ok) {
@@ -381,11 +414,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint16_t *orow = a.out + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
 #pragma unroll 1
-            for (int ch = 0; ch < 8; ++ch) {
+            for (int ch = 0; ch < 4; ++ch) {
+                const int d0 = 128 * hf + 32 * ch;  // the chunk's first dim
                 uint32_t o[32];
                 __syncwarp();  // rows past the tile's end skipped the stores below
                 if (ntiles > 0) {
-                    tmem_ld32(lane_base + kOCol + ch * 32, o);
+                    tmem_ld32(lane_base + kOCol + d0, o);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
@@ -399,10 +433,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         v.y = pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
                         v.z = pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
                         v.w = pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + ch * 32 + i) = v;
+                        *reinterpret_cast<uint4 *>(orow + d0 + i) = v;
                     }
                 } else {
-                    float *dst = part_acc + prow * kHeadDim + ch * 32;
+                    float *dst = part_acc + prow * kHeadDim + d0;
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
                         *reinterpret_cast<float4 *>(dst + i) =
@@ -410,181 +444,219 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                         __uint_as_float(o[i + 2]), __uint_as_float(o[i + 3]));
                 }
             }
-            if (row_ok && !single) {
+            if (row_ok && !single && hf == 0) {
                 part_ml[prow * 2 + 0] = m_used;
                 part_ml[prow * 2 + 1] = l;
             }
         }
-    } else if (warp == 4 || warp == 6) {
-        // ---------------- producers: K tiles (warp 4), V tiles (warp 6) ----------------
+    } else if (warp == kWarpK || warp == kWarpV) {
+        // ------- producers: K (warp 8) in dim halves, V (warp 10) in key halves -------
         pdl_wait();  // the chunk's rows are stored by the previous kernel
-        const bool is_v = warp == 6;
-        const int nbuf = is_v ? kVS : kKS;
+        const bool is_v = warp == kWarpV;
         uint8_t *const ring = smem + (is_v ? kOffV : kOffK);
         uint64_t *const full = &bars[is_v ? kBarVFull : kBarKFull];
         uint64_t *const empty = &bars[is_v ? kBarVEmpty : kBarKEmpty];
+        const int half_bytes = is_v ? kVHalf : kKHalf;
+        const int region = is_v ? kVRegion : kKRegion;  // bytes of one 64-dim region of a slot
+        const int nk = is_v ? 64 : kN;                  // keys a slot
         // the stream's fields in registers: read from the launch parameters
         // with a per-CTA index, each costs a constant-cache round trip, and
-        // the issue loop would reread them every tile
+        // the issue loop would reread them every unit
         const int ptok = sd.ptok, n_pages = sd.n_pages, n_table = sd.n_table, tok_off = sd.tok_off;
         const int32_t *const table = sd.table;
         const int64_t ps = sd.ps, layer_row = sd.layer_row;
         const uint16_t *const layer_base = sd.layer_base;
-        const void *const map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;        // 16 x 64 boxes
-        const void *const map64 = sd.tma64 >= 0 ? &maps.map[sd.tma64] : nullptr;  // 64-row tiles
+        const void *const map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;  // 16 x 64 boxes
+        // one copy a slot: 128 rows x 128 dims (K) or 64 rows x 256 dims (V)
+        const int tmap = is_v ? sd.tma_v : sd.tma_k;
+        const void *const map_t = tmap >= 0 ? &maps.map[tmap] : nullptr;
         const uint64_t pol = policy_evict_normal();  // every M-tile of the head reads these rows
         // V rows sit H * ptok rows after the K rows of the same page
         const int64_t gap = is_v ? (int64_t)H * ptok * kHeadDim : 0;
         const bool fuse = a.k_new != nullptr;
         const uint16_t *const new_rows = is_v ? a.v_new : a.k_new;
         // page ids in registers: lane i holds pages win + i (cur) and
-        // win + 32 + i (nxt); the window slides by 32 once a tile starts past
+        // win + 32 + i (nxt); the window slides by 32 once a unit starts past
         // its first half, so the next half is loading long before it is read
-        // and no table read waits in the issue loop (a tile spans at most 17
-        // pages, so its pages always lie in the 64-page window)
+        // and no table read waits in the issue loop (a unit of 128 keys spans
+        // at most 33 pages, so its pages always lie in the 64-page window)
         auto page_id = [&](int p) -> int { return (table && p < n_table) ? __ldg(table + p) : 0; };
         int win = table ? key0 / ptok : 0;
         int cur = page_id(win + lane), nxt = page_id(win + 32 + lane);
         for (int n = 0; n < ntiles; ++n) {
-            const int b = n % nbuf;
-            const int kt = key0 + n * kN;
-            // the tile's rows are looked up before its slot is free: this
-            // lane's keys kt + lane and kt + 32 + lane, clamped into the split
-            if (table) {
-                const int first = min(kt, key1 - 1) / ptok;  // the tile's lowest page
-                while (first >= win + 32) {
-                    win += 32;
-                    cur = nxt;
-                    nxt = page_id(win + 32 + lane);
-                }
-            }
-            int64_t krow[2];
-            bool bad[2] = {false, false};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int key = min(kt + 32 * h + lane, key1 - 1);
-                int row = key;
-                int64_t pg = 0;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                // a unit: K, the tile's keys over dims 128 hh ..; V, keys 64 hh .. of the tile
+                const int kb = key0 + n * kN + (is_v ? 64 * hh : 0);
+                // its rows are looked up before its slot is free: this lane's
+                // keys kb + 32 g + lane, clamped into the split
                 if (table) {
-                    const int page = key / ptok;
-                    row = key - page * ptok;
-                    const int idx = page - win;  // 0 .. 63: a tile spans at most 17 pages
-                    const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
-                    const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
-                    const int id = idx < 32 ? a0 : a1;
-                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
-                        pg = (int64_t)id * ps;
-                    } else {
-                        bad[h] = true;
-                        if (c.status && !is_v) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                    const int first = min(kb, key1 - 1) / ptok;  // the unit's lowest page
+                    while (first >= win + 32) {
+                        win += 32;
+                        cur = nxt;
+                        nxt = page_id(win + 32 + lane);
                     }
                 }
-                krow[h] = pg + off_k(ptok, kvh, row) + gap;
-            }
-            // with a decode call's new rows, keys from qbase on come from the
-            // input, not the cache (which this kernel stores them into)
-            const bool fresh_tile = fuse && min(kt + kN, key1) > qbase;
-            const bool whole = kt + kN <= key1 && !fresh_tile;
-            // a whole tile in one page (pages of a multiple of 64): one 64-row
-            // run of all 256 dims, one copy; else four 16-row page runs of four
-            // 64-dim chunks, sixteen copies
-            const int y0 = static_cast<int>(layer_row + shfl64(krow[0], 0) / kHeadDim);
-            const int y1 = static_cast<int>(layer_row + shfl64(krow[0], 16) / kHeadDim);
-            const int y2 = static_cast<int>(layer_row + shfl64(krow[1], 0) / kHeadDim);
-            const int y3 = static_cast<int>(layer_row + shfl64(krow[1], 16) / kHeadDim);
-            if (__any_sync(0xffffffffu, *abort_flag) ||
-                (n >= nbuf && !__all_sync(0xffffffffu, mbar_wait(&empty[b], ((n / nbuf) - 1) & 1, c.status)))) {
-                *abort_flag = 1;
-                break;
-            }
-            uint8_t *dst = ring + b * kKVBytes;
-            if (whole && map64 != nullptr) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[b], kKVBytes);
-                    tma_load_3d(dst, map64, 0, y0, 0, &full[b], pol);
-                }
-            } else if (whole && map != nullptr) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[b], kKVBytes);
+                int64_t krow[4];
+                bool bad[4];
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        tma_load_2d(dst + ch * kRegionKV, map, 64 * ch, y0, &full[b], pol);
-                        tma_load_2d(dst + ch * kRegionKV + 2048, map, 64 * ch, y1, &full[b], pol);
-                        tma_load_2d(dst + ch * kRegionKV + 4096, map, 64 * ch, y2, &full[b], pol);
-                        tma_load_2d(dst + ch * kRegionKV + 6144, map, 64 * ch, y3, &full[b], pol);
+                for (int g = 0; g < 4; ++g) {
+                    krow[g] = 0;
+                    bad[g] = false;
+                    if (g * 32 >= nk) continue;
+                    const int key = min(kb + 32 * g + lane, key1 - 1);
+                    int row = key;
+                    int64_t pg = 0;
+                    if (table) {
+                        const int page = key / ptok;
+                        row = key - page * ptok;
+                        const int idx = page - win;  // 0 .. 63
+                        const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
+                        const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
+                        const int id = idx < 32 ? a0 : a1;
+                        if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
+                            pg = (int64_t)id * ps;
+                        } else {
+                            bad[g] = true;
+                            if (c.status && !is_v) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                        }
                     }
+                    krow[g] = pg + off_k(ptok, kvh, row) + gap;
                 }
-            } else {
-                // key r's row from its lane's lookup; keys past the split repeat its last row
+                // with a decode call's new rows, keys from qbase on come from the
+                // input, not the cache (which this kernel stores them into)
+                const bool fresh = fuse && min(kb + nk, key1) > qbase;
+                const bool whole = kb + nk <= key1 && !fresh;
+                const int chunk0 = is_v ? 0 : 2 * hh;  // first 64-dim chunk of the slot
+                const int y0 = static_cast<int>(layer_row + shfl64(krow[0], 0) / kHeadDim);
+                if (__any_sync(0xffffffffu, *abort_flag) ||
+                    (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&empty[hh], (n - 1) & 1, c.status)))) {
+                    *abort_flag = 1;
+                    break;
+                }
+                uint8_t *dst = ring + hh * half_bytes;
+                if (whole && map_t != nullptr) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[hh], half_bytes);
+                        tma_load_3d(dst, map_t, 0, y0, chunk0, &full[hh], pol);
+                    }
+                } else if (whole && map != nullptr) {
+                    // 16-row page runs: 8 (K) or 4 (V), two or four chunks each
+                    int yr[8];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int key = min(kt + 32 * h + lane, key1 - 1);
-                    const uint16_t *src = layer_base + krow[h];
-                    if (fresh_tile && key >= qbase)
-                        src = new_rows + (((int64_t)tok_off + (key - qbase)) * H + kvh) * kHeadDim;
-                    const int64_t sp = reinterpret_cast<int64_t>(src);
+                    for (int rn = 0; rn < 8; ++rn) {
+                        const int64_t kr = shfl64(krow[rn >> 1], (rn & 1) * 16);
+                        yr[rn] = static_cast<int>(layer_row + kr / kHeadDim);
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[hh], half_bytes);
+#pragma unroll
+                        for (int rn = 0; rn < 8; ++rn) {
+                            if (rn * 16 >= nk) break;
+#pragma unroll
+                            for (int ch = 0; ch < 4; ++ch) {
+                                if (!is_v && ch >= 2) break;
+                                tma_load_2d(dst + ch * region + rn * 2048, map, 64 * (chunk0 + ch), yr[rn],
+                                            &full[hh], pol);
+                            }
+                        }
+                    }
+                } else {
+                    // key by key: each row's 16-byte chunks of the slot's dims
+                    int64_t sp[4];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int key = min(kb + 32 * g + lane, key1 - 1);
+                        const uint16_t *src = layer_base + krow[g];
+                        if (fresh && key >= qbase)
+                            src = new_rows + (((int64_t)tok_off + (key - qbase)) * H + kvh) * kHeadDim;
+                        sp[g] = reinterpret_cast<int64_t>(src + 64 * chunk0);
+                    }
+                    if (is_v) {
+                        // 64 rows of 32 chunks: a row a pass, a chunk a lane
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
 #pragma unroll 8
-                    for (int rr = 0; rr < 32; ++rr)
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                                         smem_u32(dst + swz128(kRegionKV, 32 * h + rr, lane))),
-                                     "l"(reinterpret_cast<const uint16_t *>(shfl64(sp, rr)) + lane * 8)
-                                     : "memory");
-                }
-                // these are generic-proxy writes and the tensor cores read the
-                // tile through the async proxy: each lane waits for its own
-                // copies and fences the proxies before the warp's one arrival
-                // (an arrival made by the copies themselves would leave the
-                // writes unfenced)
-                asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[b]);
-                if (fresh_tile) {
-                    // store the tile's new rows (K or V of this KV head, and the
-                    // indexer-key row once, with KV head 0) into their pages
-                    for (int i = max(kt, qbase); i < min(kt + kN, key1); ++i) {
-                        const int h = (i - kt) >> 5, l = (i - kt) & 31;
-                        const int64_t kr = shfl64(h ? krow[1] : krow[0], l);
-                        if (__shfl_sync(0xffffffffu, h ? bad[1] : bad[0], l)) continue;
-                        const int64_t r = (int64_t)tok_off + (i - qbase);
-                        uint16_t *row = const_cast<uint16_t *>(layer_base) + kr;
-                        reinterpret_cast<uint4 *>(row)[lane] =
-                            __ldg(reinterpret_cast<const uint4 *>(new_rows + (r * H + kvh) * kHeadDim) + lane);
-                        if (!is_v && kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
-                            const int prow = table ? i % ptok : i;
-                            const int64_t page_start = kr - (int64_t)prow * kHeadDim;
-                            uint16_t *idst = const_cast<uint16_t *>(layer_base) + page_start +
-                                             off_ik(H, c.idx_dim, ptok, prow);
-                            reinterpret_cast<uint4 *>(idst)[lane] =
-                                __ldg(reinterpret_cast<const uint4 *>(a.ik_new + r * c.idx_dim) + lane);
+                            for (int rr = 0; rr < 32; ++rr)
+                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                                 smem_u32(dst + swz128(kVRegion, 32 * g + rr, lane))),
+                                             "l"(reinterpret_cast<const uint16_t *>(shfl64(sp[g], rr)) + lane * 8)
+                                             : "memory");
+                    } else {
+                        // 128 rows of 16 chunks: two rows a pass, a chunk a lane
+                        const int hl = lane >> 4, cl = lane & 15;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+#pragma unroll 4
+                            for (int rr = 0; rr < 32; rr += 2)
+                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                                 smem_u32(dst + swz128(kKRegion, 32 * g + rr + hl, cl))),
+                                             "l"(reinterpret_cast<const uint16_t *>(shfl64(sp[g], rr + hl)) + cl * 8)
+                                             : "memory");
+                    }
+                    // these are generic-proxy writes and the tensor cores read the
+                    // slot through the async proxy: each lane waits for its own
+                    // copies and fences the proxies before the warp's one arrival
+                    // (an arrival made by the copies themselves would leave the
+                    // writes unfenced)
+                    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[hh]);
+                    if (fresh && (is_v || hh == 0)) {
+                        // store the unit's new rows (K or V of this KV head, and the
+                        // indexer-key row once, with KV head 0) into their pages
+                        for (int i = max(kb, qbase); i < min(kb + nk, key1); ++i) {
+                            const int g = (i - kb) >> 5, ln = (i - kb) & 31;
+                            const int64_t kg = g == 0 ? krow[0] : g == 1 ? krow[1] : g == 2 ? krow[2] : krow[3];
+                            const bool bg = g == 0 ? bad[0] : g == 1 ? bad[1] : g == 2 ? bad[2] : bad[3];
+                            const int64_t kr = shfl64(kg, ln);
+                            if (__shfl_sync(0xffffffffu, bg, ln)) continue;
+                            const int64_t rw = (int64_t)tok_off + (i - qbase);
+                            uint16_t *row = const_cast<uint16_t *>(layer_base) + kr;
+                            reinterpret_cast<uint4 *>(row)[lane] =
+                                __ldg(reinterpret_cast<const uint4 *>(new_rows + (rw * H + kvh) * kHeadDim) + lane);
+                            if (!is_v && kvh == 0 && a.ik_new != nullptr && lane < c.idx_dim / 8) {
+                                const int prow = table ? i % ptok : i;
+                                const int64_t page_start = kr - (int64_t)prow * kHeadDim;
+                                uint16_t *idst = const_cast<uint16_t *>(layer_base) + page_start +
+                                                 off_ik(H, c.idx_dim, ptok, prow);
+                                reinterpret_cast<uint4 *>(idst)[lane] =
+                                    __ldg(reinterpret_cast<const uint4 *>(a.ik_new + rw * c.idx_dim) + lane);
+                            }
                         }
                     }
                 }
             }
+            if (__any_sync(0xffffffffu, *abort_flag)) break;
         }
-    } else if (warp == 5 && lane == 0) {
+    } else if (warp == kWarpMma && lane == 0) {
         // ---------------- MMA issue ----------------
+        // operands written by threads (Q, P, key-by-key slots) were fenced by
+        // their writers before they arrived
         const uint32_t idesc_s = mma_idesc(kN, false);
         const uint32_t idesc_o = mma_idesc(kHeadDim, true);
         bool ok = mbar_wait(&bars[kBarQFull], 0, c.status);
         tc_fence_after();
-        // operands written by threads (Q, P, key-by-key tiles) were fenced to
-        // the async proxy by their writers before they arrived
+        // S = Q K^T: Q (A) from TMEM, 8 columns (16 dims) a step; K (B) from
+        // the two dim-half slots
         auto issue_s = [&](int n) -> bool {
-            const int b = n % kKS, sb = n & 1;
-            if (!mbar_wait(&bars[kBarKFull + b], (n / kKS) & 1, c.status)) return false;
-            if (n >= 2 && !mbar_wait(&bars[kBarSEmpty + sb], ((n - 2) >> 1) & 1, c.status)) return false;
-            tc_fence_after();
-            const uint32_t kb = sbase + kOffK + b * kKVBytes;
+            if (n > 0 && !mbar_wait(&bars[kBarSEmpty], (n - 1) & 1, c.status)) return false;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                if (!mbar_wait(&bars[kBarKFull + hh], n & 1, c.status)) return false;
+                tc_fence_after();
+                const uint32_t kb = sbase + kOffK + hh * kKHalf;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                const uint32_t qa = sbase + kOffQ + (kk >> 2) * kRegionQ + (kk & 3) * 32;
-                const uint32_t kbb = kb + (kk >> 2) * kRegionKV + (kk & 3) * 32;
-                tc_mma(tmem + sb * kN, smem_desc(qa, 16, 1024), smem_desc(kbb, 16, 1024), idesc_s,
-                       kk > 0);
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    const uint32_t kbb = kb + (k8 >> 2) * kKRegion + (k8 & 3) * 32;
+                    tc_mma_ts(tmem + kSCol, tmem + kQCol + (8 * hh + k8) * 8, smem_desc(kbb, 16, 1024),
+                              idesc_s, (hh > 0 || k8 > 0) ? 1u : 0u);
+                }
+                tc_commit(&bars[kBarKEmpty + hh]);  // the slot is free once its half is done
             }
-            tc_commit(&bars[kBarSFull + sb]);
-            tc_commit(&bars[kBarKEmpty + b]);  // the K slot is free once S is computed
+            tc_commit(&bars[kBarSFull]);
             return true;
         };
         if (ok && ntiles > 0) ok = issue_s(0);
@@ -593,32 +665,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 ok = false;
                 break;
             }
-            const int b = n % kVS;
-            if (!mbar_wait(&bars[kBarVFull + b], (n / kVS) & 1, c.status) ||
-                !mbar_wait(&bars[kBarPFull + (n & 1)], (n >> 1) & 1, c.status)) {
+            if (!mbar_wait(&bars[kBarPFull], n & 1, c.status)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            const uint32_t vb = sbase + kOffV + b * kKVBytes;
+#pragma unroll 1
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+                if (!mbar_wait(&bars[kBarVFull + hh], n & 1, c.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t vb = sbase + kOffV + hh * kVHalf;
 #pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk) {
-                const uint32_t pa = sbase + kOffP + kk * 32;
-                const uint32_t va = vb + kk * 2048;  // 16 keys = two 8-row groups
-                tc_mma(tmem + kOCol, smem_desc(pa, 16, 1024), smem_desc(va, kRegionKV, 1024), idesc_o,
-                       (n > 0 || kk > 0) ? 1u : 0u);
-                tc_mma(tmem + kOCol, smem_desc(pa + kPBytes, 16, 1024), smem_desc(va, kRegionKV, 1024),
-                       idesc_o, 1u);
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const uint32_t pa = sbase + kOffP + hh * kPRegion + k4 * 32;
+                    const uint32_t va = vb + k4 * 2048;  // 16 keys = two 8-row groups
+                    tc_mma(tmem + kOCol, smem_desc(pa, 16, 1024), smem_desc(va, kVRegion, 1024), idesc_o,
+                           (n > 0 || hh > 0 || k4 > 0) ? 1u : 0u);
+                    tc_mma(tmem + kOCol, smem_desc(pa + kPPart, 16, 1024), smem_desc(va, kVRegion, 1024),
+                           idesc_o, 1u);
+                }
+                tc_commit(&bars[kBarVEmpty + hh]);
             }
-            tc_commit(&bars[kBarODone + (n & 1)]);
-            tc_commit(&bars[kBarVEmpty + b]);
+            if (!ok) break;
+            tc_commit(&bars[kBarODone]);
         }
         if (!ok) *abort_flag = 1;
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         __syncwarp();  // lane 0 issued the MMAs, lanes 1-31 went straight here
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -632,7 +710,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // Work items: (KV head, M-tile, split) per stream, splits fastest.  A stream
 // is split only as far as filling the SMs needs, from its own shape alone.
 // Split model of plan_prefill, in hundredths of a microsecond.
-constexpr int64_t kTileCost = 150;   // a 64-key tile of one 128-row M-tile
+constexpr int64_t kTileCost = 175;   // a 128-key tile of one 128-row M-tile
 constexpr int64_t kCtaCost = 1200;   // a CTA's fixed cost
 constexpr int64_t kPartialCost = 4;  // a (unit, split) partial written and read back
 constexpr int kMaxPrefillSplits = 64;
@@ -667,7 +745,7 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         // the SM count enter, so paged and contiguous caches get the same
         // splits.
         const int64_t units = (int64_t)H * mtiles, tiles = (d.len + kN - 1) / kN;
-        const int max_ns = std::max(1, std::min(kMaxPrefillSplits, d.len / (4 * kN)));
+        const int max_ns = std::max(1, std::min(kMaxPrefillSplits, d.len / 256));  // 256 keys a split at least
         int ns = 1;
         int64_t best = INT64_MAX;
         for (int n = 1; n <= max_ns; ++n) {
