@@ -72,6 +72,8 @@ extern "C" {
 /* ---- bits a kernel ORs into *dev_status ---------------------------------- */
 #define PKV_DEV_BAD_PAGE 1u /* a table entry was outside [0, n_pages)     */
 #define PKV_DEV_TIMEOUT 2u  /* a pipeline wait ran past its time limit     */
+#define PKV_DEV_SMEM 4u     /* a kernel's shared memory was not at the
+                               alignment its layout needs; it did nothing  */
 
 /* kinds of rows (pkv_pg_row, pkv_gather) */
 #define PKV_K 0

@@ -37,30 +37,33 @@ namespace {
 constexpr int kM = 128;              // rows of an M-tile
 constexpr int kN = 128;              // keys a tile
 constexpr int kSoftWarps = 8;        // two threads a row, each on 64 keys of a tile
-constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
-constexpr int kPThreads = 352;       // warps 0-7 softmax, 8 K producer, 9 MMA, 10 V producer
+constexpr int kWarpLoad = 8, kWarpMma = 9;
+constexpr int kPThreads = 320;       // warps 0-7 softmax, 8 producer, 9 MMA
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kQCol = 0;        // Q: 256 dims as bf16 pairs
 constexpr uint32_t kSCol = 128;      // S: 128 keys
 constexpr uint32_t kOCol = 256;      // O: 256 dims
 constexpr int kKRegion = kN * 128;   // one 64-dim region of 128 K rows
-constexpr int kKHalf = 2 * kKRegion; // a K slot: the tile's 128 keys over 128 dims
 constexpr int kVRegion = 64 * 128;   // one 64-dim region of 64 V rows
-constexpr int kVHalf = 4 * kVRegion; // a V slot: 64 of the tile's keys over 256 dims
+constexpr int kSlotBytes = 2 * kKRegion;  // a K slot (the tile's keys over 128 dims) or
+                                          // a V slot (64 of its keys over 256 dims)
+static_assert(kSlotBytes == 4 * kVRegion, "K and V slots share one ring");
+constexpr int kSlots = 5;            // the ring, taken in the MMAs' order
 constexpr int kPRegion = kM * 128;   // 64 keys of the 128 P rows
 constexpr int kPPart = 2 * kPRegion; // P hi (or lo): the tile's 128 keys
 constexpr int kOffP = 0;             // P hi, then P lo
-constexpr int kOffK = kOffP + 2 * kPPart;
-constexpr int kOffV = kOffK + 2 * kKHalf;
-constexpr int kOffRed = kOffV + 2 * kVHalf;       // [tile parity][half][row] floats
+constexpr int kOffRing = kOffP + 2 * kPPart;
+constexpr int kOffRed = kOffRing + kSlots * kSlotBytes;  // [tile parity][half][row] floats
 constexpr int kOffBar = kOffRed + 2 * 2 * kM * 4;
-// barriers: a pair for each ring's two slots, one for each single buffer
-constexpr int kBarKFull = 0, kBarKEmpty = 2, kBarVFull = 4, kBarVEmpty = 6;
-constexpr int kBarSFull = 8, kBarSEmpty = 9, kBarPFull = 10, kBarODone = 11, kBarQFull = 12;
-constexpr int kBarRed = 13;
-constexpr int kNumBars = 14;
-constexpr size_t kPSmem = 1024 + kOffBar + kNumBars * 8 + 16;
+// barriers: a pair for each ring slot, one for each single buffer
+constexpr int kBarFull = 0, kBarEmpty = kSlots;
+constexpr int kBarSFull = 2 * kSlots, kBarSEmpty = kBarSFull + 1, kBarPFull = kBarSFull + 2;
+constexpr int kBarODone = kBarSFull + 3, kBarQFull = kBarSFull + 4, kBarRed = kBarSFull + 5;
+constexpr int kNumBars = kBarRed + 1;
+// no alignment slack: the dynamic shared memory is declared 1024-byte aligned
+// (checked at entry), and five slots leave no room for it
+constexpr size_t kPSmem = kOffBar + kNumBars * 8 + 16;
 static_assert(kPSmem <= 232448, "prefill shared memory above the 227 KB a CTA may hold");
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 constexpr float kRescale = 8.f;  // rescale O when the max grows by more than 2^8
@@ -171,14 +174,24 @@ __device__ __forceinline__ uint32_t swz128(int region, int r, int c) {
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
                     const PrefillArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // the 128-byte swizzle of the TMA copies and the MMA operands repeats
+    // every 1024 bytes from a 1024-byte boundary
+    extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    {
+        // the address as the hardware gives it (an asm result the compiler
+        // cannot fold from the declared alignment)
+        uint32_t base;
+        asm volatile("mov.u32 %0, %1;" : "=r"(base) : "r"(smem_u32(smem)));
+        if (base & 1023u) {  // uniform: every thread returns before any barrier
+            if (tid == 0 && c.status) atomicOr(c.status, PKV_DEV_SMEM);
+            return;
+        }
+    }
     const int H = c.n_kv_heads, G = c.group;
     // the stream whose block of work items holds this CTA (the blocks are
     // laid out longest CTA first, not in stream order)
@@ -205,11 +218,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int ntiles = key1 > key0 ? (key1 - key0 + kN - 1) / kN : 0;
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[kBarKFull + i], 1);
-            mbar_init(&bars[kBarKEmpty + i], 1);
-            mbar_init(&bars[kBarVFull + i], 1);
-            mbar_init(&bars[kBarVEmpty + i], 1);
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&bars[kBarFull + i], 1);
+            mbar_init(&bars[kBarEmpty + i], 1);
         }
         mbar_init(&bars[kBarSFull], 1);
         mbar_init(&bars[kBarSEmpty], kSoftThreads);
@@ -449,108 +460,178 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 part_ml[prow * 2 + 1] = l;
             }
         }
-    } else if (warp == kWarpK || warp == kWarpV) {
-        // ------- producers: K (warp 8) in dim halves, V (warp 10) in key halves -------
+    } else if (warp == kWarpLoad) {
+        // ------- producer: K and V slots through one ring, in the order the MMAs take them -------
+        // Per tile m the MMAs take K(m) over dims 0-127 and 128-255, then
+        // V(m-1) keys 0-63 and 64-127 (the PV product of the tile before);
+        // after the last tile, V(ntiles-1).  The slots go round robin, so a
+        // slot is refilled four slots after it was taken.
         pdl_wait();  // the chunk's rows are stored by the previous kernel
-        const bool is_v = warp == kWarpV;
-        uint8_t *const ring = smem + (is_v ? kOffV : kOffK);
-        uint64_t *const full = &bars[is_v ? kBarVFull : kBarKFull];
-        uint64_t *const empty = &bars[is_v ? kBarVEmpty : kBarKEmpty];
-        const int half_bytes = is_v ? kVHalf : kKHalf;
-        const int region = is_v ? kVRegion : kKRegion;  // bytes of one 64-dim region of a slot
-        const int nk = is_v ? 64 : kN;                  // keys a slot
         // the stream's fields in registers: read from the launch parameters
         // with a per-CTA index, each costs a constant-cache round trip, and
-        // the issue loop would reread them every unit
+        // the issue loop would reread them every slot
         const int ptok = sd.ptok, n_pages = sd.n_pages, n_table = sd.n_table, tok_off = sd.tok_off;
         const int32_t *const table = sd.table;
         const int64_t ps = sd.ps, layer_row = sd.layer_row;
         const uint16_t *const layer_base = sd.layer_base;
-        const void *const map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;  // 16 x 64 boxes
-        // one copy a slot: 128 rows x 128 dims (K) or 64 rows x 256 dims (V)
-        const int tmap = is_v ? sd.tma_v : sd.tma_k;
-        const void *const map_t = tmap >= 0 ? &maps.map[tmap] : nullptr;
+        const void *const map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;          // 16 x 64 boxes
+        const void *const map_k = sd.tma_k >= 0 ? &maps.map[sd.tma_k] : nullptr;    // a K slot
+        const void *const map_v = sd.tma_v >= 0 ? &maps.map[sd.tma_v] : nullptr;    // a V slot
         const uint64_t pol = policy_evict_normal();  // every M-tile of the head reads these rows
         // V rows sit H * ptok rows after the K rows of the same page
-        const int64_t gap = is_v ? (int64_t)H * ptok * kHeadDim : 0;
+        const int64_t vgap = (int64_t)H * ptok * kHeadDim;
         const bool fuse = a.k_new != nullptr;
-        const uint16_t *const new_rows = is_v ? a.v_new : a.k_new;
         // page ids in registers: lane i holds pages win + i (cur) and
-        // win + 32 + i (nxt); the window slides by 32 once a unit starts past
+        // win + 32 + i (nxt); the window slides by 32 once a tile starts past
         // its first half, so the next half is loading long before it is read
-        // and no table read waits in the issue loop (a unit of 128 keys spans
+        // and no table read waits in the issue loop (a tile of 128 keys spans
         // at most 33 pages, so its pages always lie in the 64-page window)
         auto page_id = [&](int p) -> int { return (table && p < n_table) ? __ldg(table + p) : 0; };
         int win = table ? key0 / ptok : 0;
         int cur = page_id(win + lane), nxt = page_id(win + 32 + lane);
-        for (int n = 0; n < ntiles; ++n) {
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                // a unit: K, the tile's keys over dims 128 hh ..; V, keys 64 hh .. of the tile
-                const int kb = key0 + n * kN + (is_v ? 64 * hh : 0);
-                // its rows are looked up before its slot is free: this lane's
-                // keys kb + 32 g + lane, clamped into the split
+        // A whole cached tile in one page (pages of a multiple of 128) needs
+        // only its first row: yk, the map row of its first K row (-1 for any
+        // other tile).  Any other tile: the K row offsets of this lane's keys
+        // m kN + 32 g + lane (clamped into the split), and which of them had
+        // a bad page id.  (The producer shares its sub-partition with two
+        // softmax warps: its per-tile instructions are on the pipeline's
+        // critical path.)
+        int64_t rk[4], rv[4];
+        uint32_t bk = 0, bv = 0;
+        int yk = -1, yv = -1;
+        const int vrows = H * ptok;  // V rows sit this many map rows after K's
+        auto lookup = [&](int m) {
+            const int kb = key0 + m * kN;
+            if (table) {
+                const int first = min(kb, key1 - 1) / ptok;  // the tile's lowest page
+                while (first >= win + 32) {
+                    win += 32;
+                    cur = nxt;
+                    nxt = page_id(win + 32 + lane);
+                }
+            }
+            bk = 0;
+            yk = -1;
+            if (map_k != nullptr && map_v != nullptr && kb + kN <= key1 && !(fuse && kb + kN > qbase)) {
+                int row = kb;
+                int64_t pg = 0;
                 if (table) {
-                    const int first = min(kb, key1 - 1) / ptok;  // the unit's lowest page
-                    while (first >= win + 32) {
-                        win += 32;
-                        cur = nxt;
-                        nxt = page_id(win + 32 + lane);
+                    const int page = kb / ptok;
+                    row = kb - page * ptok;
+                    const int idx = page - win;  // 0 .. 31
+                    const int id = __shfl_sync(0xffffffffu, idx < 32 ? cur : nxt, idx & 31);
+                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
+                        pg = (int64_t)id * ps;
+                    } else if (lane == 0 && c.status) {
+                        atomicOr(c.status, PKV_DEV_BAD_PAGE);
                     }
                 }
-                int64_t krow[4];
-                bool bad[4];
+                yk = static_cast<int>(layer_row + (pg + off_k(ptok, kvh, row)) / kHeadDim);
+                return;
+            }
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    krow[g] = 0;
-                    bad[g] = false;
-                    if (g * 32 >= nk) continue;
-                    const int key = min(kb + 32 * g + lane, key1 - 1);
-                    int row = key;
-                    int64_t pg = 0;
-                    if (table) {
-                        const int page = key / ptok;
-                        row = key - page * ptok;
-                        const int idx = page - win;  // 0 .. 63
-                        const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
-                        const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
-                        const int id = idx < 32 ? a0 : a1;
-                        if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
-                            pg = (int64_t)id * ps;
-                        } else {
-                            bad[g] = true;
-                            if (c.status && !is_v) atomicOr(c.status, PKV_DEV_BAD_PAGE);
-                        }
+            for (int g = 0; g < 4; ++g) {
+                const int key = min(kb + 32 * g + lane, key1 - 1);
+                int row = key;
+                int64_t pg = 0;
+                if (table) {
+                    const int page = key / ptok;
+                    row = key - page * ptok;
+                    const int idx = page - win;  // 0 .. 63
+                    const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
+                    const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
+                    const int id = idx < 32 ? a0 : a1;
+                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
+                        pg = (int64_t)id * ps;
+                    } else {
+                        bk |= 1u << g;
+                        if (c.status) atomicOr(c.status, PKV_DEV_BAD_PAGE);
                     }
-                    krow[g] = pg + off_k(ptok, kvh, row) + gap;
+                }
+                rk[g] = pg + off_k(ptok, kvh, row);
+            }
+        };
+        if (ntiles > 0) lookup(0);
+        uint32_t q = 0;  // slots issued
+        bool ok = true;
+        for (int m = 0; m <= ntiles && ok; ++m) {
+#pragma unroll 1
+            for (int it = 0; it < 4; ++it) {
+                const bool is_v = it >= 2;
+                const int hh = it & 1;
+                const int tm = is_v ? m - 1 : m;  // the slot's tile
+                if (tm < 0 || tm >= ntiles) continue;
+                const int slot = q % kSlots;
+                uint64_t *const full = &bars[kBarFull + slot];
+                uint8_t *const dst = smem + kOffRing + slot * kSlotBytes;
+                const int yt = is_v ? yv : yk;
+                if (yt >= 0) {
+                    // the tile lies in one page: the slot is one copy
+                    if (__any_sync(0xffffffffu, *abort_flag) ||
+                        (q >= kSlots && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarEmpty + slot],
+                                                                             ((q / kSlots) - 1) & 1, c.status)))) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full, kSlotBytes);
+                        if (is_v)
+                            tma_load_3d(dst, map_v, 0, yt + vrows + 64 * hh, 0, full, pol);
+                        else
+                            tma_load_3d(dst, map_k, 0, yt, 2 * hh, full, pol);
+                    }
+                    ++q;
+                    continue;
+                }
+                // the slot's keys: K, the tile's 128 (four groups of 32); V, 64
+                // of them (two groups), over all dims
+                const int kb = key0 + tm * kN + (is_v ? 64 * hh : 0);
+                const int nk = is_v ? 64 : kN;
+                const int64_t gap = is_v ? vgap : 0;
+                int64_t r[4];
+                uint32_t bm;
+                if (is_v) {
+                    r[0] = (hh ? rv[2] : rv[0]) + gap;
+                    r[1] = (hh ? rv[3] : rv[1]) + gap;
+                    r[2] = r[3] = 0;
+                    bm = (bv >> (2 * hh)) & 3u;
+                } else {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) r[g] = rk[g];
+                    bm = bk;
                 }
                 // with a decode call's new rows, keys from qbase on come from the
                 // input, not the cache (which this kernel stores them into)
                 const bool fresh = fuse && min(kb + nk, key1) > qbase;
                 const bool whole = kb + nk <= key1 && !fresh;
                 const int chunk0 = is_v ? 0 : 2 * hh;  // first 64-dim chunk of the slot
-                const int y0 = static_cast<int>(layer_row + shfl64(krow[0], 0) / kHeadDim);
+                const int region = is_v ? kVRegion : kKRegion;
+                const void *const map_t = is_v ? map_v : map_k;
                 if (__any_sync(0xffffffffu, *abort_flag) ||
-                    (n > 0 && !__all_sync(0xffffffffu, mbar_wait(&empty[hh], (n - 1) & 1, c.status)))) {
+                    (q >= kSlots && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarEmpty + slot],
+                                                                         ((q / kSlots) - 1) & 1, c.status)))) {
                     *abort_flag = 1;
+                    ok = false;
                     break;
                 }
-                uint8_t *dst = ring + hh * half_bytes;
                 if (whole && map_t != nullptr) {
+                    // the slot's keys lie in one page: one copy
+                    const int y0 = static_cast<int>(layer_row + shfl64(r[0], 0) / kHeadDim);
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&full[hh], half_bytes);
-                        tma_load_3d(dst, map_t, 0, y0, chunk0, &full[hh], pol);
+                        mbar_arrive_expect_tx(full, kSlotBytes);
+                        tma_load_3d(dst, map_t, 0, y0, chunk0, full, pol);
                     }
                 } else if (whole && map != nullptr) {
                     // 16-row page runs: 8 (K) or 4 (V), two or four chunks each
                     int yr[8];
 #pragma unroll
                     for (int rn = 0; rn < 8; ++rn) {
-                        const int64_t kr = shfl64(krow[rn >> 1], (rn & 1) * 16);
+                        const int64_t kr = shfl64(r[rn >> 1], (rn & 1) * 16);
                         yr[rn] = static_cast<int>(layer_row + kr / kHeadDim);
                     }
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&full[hh], half_bytes);
+                        mbar_arrive_expect_tx(full, kSlotBytes);
 #pragma unroll
                         for (int rn = 0; rn < 8; ++rn) {
                             if (rn * 16 >= nk) break;
@@ -558,17 +639,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             for (int ch = 0; ch < 4; ++ch) {
                                 if (!is_v && ch >= 2) break;
                                 tma_load_2d(dst + ch * region + rn * 2048, map, 64 * (chunk0 + ch), yr[rn],
-                                            &full[hh], pol);
+                                            full, pol);
                             }
                         }
                     }
                 } else {
                     // key by key: each row's 16-byte chunks of the slot's dims
+                    const uint16_t *const new_rows = is_v ? a.v_new : a.k_new;
                     int64_t sp[4];
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         const int key = min(kb + 32 * g + lane, key1 - 1);
-                        const uint16_t *src = layer_base + krow[g];
+                        const uint16_t *src = layer_base + r[g];
                         if (fresh && key >= qbase)
                             src = new_rows + (((int64_t)tok_off + (key - qbase)) * H + kvh) * kHeadDim;
                         sp[g] = reinterpret_cast<int64_t>(src + 64 * chunk0);
@@ -603,16 +685,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
                     fence_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&full[hh]);
+                    if (lane == 0) mbar_arrive(full);
                     if (fresh && (is_v || hh == 0)) {
-                        // store the unit's new rows (K or V of this KV head, and the
+                        // store the slot's new rows (K or V of this KV head, and the
                         // indexer-key row once, with KV head 0) into their pages
                         for (int i = max(kb, qbase); i < min(kb + nk, key1); ++i) {
                             const int g = (i - kb) >> 5, ln = (i - kb) & 31;
-                            const int64_t kg = g == 0 ? krow[0] : g == 1 ? krow[1] : g == 2 ? krow[2] : krow[3];
-                            const bool bg = g == 0 ? bad[0] : g == 1 ? bad[1] : g == 2 ? bad[2] : bad[3];
-                            const int64_t kr = shfl64(kg, ln);
-                            if (__shfl_sync(0xffffffffu, bg, ln)) continue;
+                            const int64_t rg = g == 0 ? r[0] : g == 1 ? r[1] : g == 2 ? r[2] : r[3];
+                            const int64_t kr = shfl64(rg, ln);
+                            if ((bm >> g) & 1u) continue;
                             const int64_t rw = (int64_t)tok_off + (i - qbase);
                             uint16_t *row = const_cast<uint16_t *>(layer_base) + kr;
                             reinterpret_cast<uint4 *>(row)[lane] =
@@ -628,8 +709,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         }
                     }
                 }
+                ++q;
             }
-            if (__any_sync(0xffffffffu, *abort_flag)) break;
+            // tile m's rows serve its V next; look the next tile's up
+#pragma unroll
+            for (int g = 0; g < 4; ++g) rv[g] = rk[g];
+            bv = bk;
+            yv = yk;
+            if (m + 1 < ntiles) lookup(m + 1);
         }
     } else if (warp == kWarpMma && lane == 0) {
         // ---------------- MMA issue ----------------
@@ -639,22 +726,33 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t idesc_o = mma_idesc(kHeadDim, true);
         bool ok = mbar_wait(&bars[kBarQFull], 0, c.status);
         tc_fence_after();
+        uint32_t q = 0;  // slots taken, in the producer's order
+        auto take = [&](uint32_t &addr) -> bool {
+            const uint32_t slot = q % kSlots;
+            if (!mbar_wait(&bars[kBarFull + slot], (q / kSlots) & 1, c.status)) return false;
+            tc_fence_after();
+            addr = sbase + kOffRing + slot * kSlotBytes;
+            return true;
+        };
+        auto give = [&]() {
+            tc_commit(&bars[kBarEmpty + q % kSlots]);  // free once these MMAs are done
+            ++q;
+        };
         // S = Q K^T: Q (A) from TMEM, 8 columns (16 dims) a step; K (B) from
-        // the two dim-half slots
+        // the tile's two dim-half slots
         auto issue_s = [&](int n) -> bool {
             if (n > 0 && !mbar_wait(&bars[kBarSEmpty], (n - 1) & 1, c.status)) return false;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
-                if (!mbar_wait(&bars[kBarKFull + hh], n & 1, c.status)) return false;
-                tc_fence_after();
-                const uint32_t kb = sbase + kOffK + hh * kKHalf;
+                uint32_t kb;
+                if (!take(kb)) return false;
 #pragma unroll
                 for (int k8 = 0; k8 < 8; ++k8) {
                     const uint32_t kbb = kb + (k8 >> 2) * kKRegion + (k8 & 3) * 32;
                     tc_mma_ts(tmem + kSCol, tmem + kQCol + (8 * hh + k8) * 8, smem_desc(kbb, 16, 1024),
                               idesc_s, (hh > 0 || k8 > 0) ? 1u : 0u);
                 }
-                tc_commit(&bars[kBarKEmpty + hh]);  // the slot is free once its half is done
+                give();
             }
             tc_commit(&bars[kBarSFull]);
             return true;
@@ -669,14 +767,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 ok = false;
                 break;
             }
+            // O += P V over the tile's two key-half slots
 #pragma unroll 1
             for (int hh = 0; hh < 2 && ok; ++hh) {
-                if (!mbar_wait(&bars[kBarVFull + hh], n & 1, c.status)) {
+                uint32_t vb;
+                if (!take(vb)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t vb = sbase + kOffV + hh * kVHalf;
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
                     const uint32_t pa = sbase + kOffP + hh * kPRegion + k4 * 32;
@@ -686,7 +784,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     tc_mma(tmem + kOCol, smem_desc(pa + kPPart, 16, 1024), smem_desc(va, kVRegion, 1024),
                            idesc_o, 1u);
                 }
-                tc_commit(&bars[kBarVEmpty + hh]);
+                give();
             }
             if (!ok) break;
             tc_commit(&bars[kBarODone]);
