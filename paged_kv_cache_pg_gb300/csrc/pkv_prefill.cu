@@ -37,8 +37,8 @@ namespace {
 constexpr int kM = 128;              // rows of an M-tile
 constexpr int kN = 128;              // keys a tile
 constexpr int kSoftWarps = 8;        // two threads a row, each on 64 keys of a tile
-constexpr int kWarpLoad = 8, kWarpMma = 9;
-constexpr int kPThreads = 320;       // warps 0-7 softmax, 8 producer, 9 MMA
+constexpr int kWarpMma = 9;         // warps 8 and 10-12 produce: K and V slots of dims or keys 0..,
+constexpr int kPThreads = 416;       // then of the second half; warps 0-7 softmax
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kQCol = 0;        // Q: 256 dims as bf16 pairs
@@ -460,13 +460,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 part_ml[prow * 2 + 1] = l;
             }
         }
-    } else if (warp == kWarpLoad) {
-        // ------- producer: K and V slots through one ring, in the order the MMAs take them -------
-        // Per tile m the MMAs take K(m) over dims 0-127 and 128-255, then
-        // V(m-1) keys 0-63 and 64-127 (the PV product of the tile before);
-        // after the last tile, V(ntiles-1).  The slots go round robin, so a
-        // slot is refilled four slots after it was taken.
+    } else if (warp >= kSoftWarps && warp != kWarpMma) {
+        // ------- producers: K slots (warps 8, 11) and V slots (10, 12) of one ring -------
+        // The MMAs take the slots in the order K(0) over dims 0-127 and
+        // 128-255, then per tile m >= 1: K(m) halves, V(m-1) keys 0-63 and
+        // 64-127 (the PV product of the tile before), and last V(ntiles-1).
+        // Each producer takes one half (warps 8 and 10 the first, 11 and 12
+        // the second) and knows its slots' places in that order, so the four
+        // fill the ring side by side; a slot is refilled five places after it
+        // was taken.
         pdl_wait();  // the chunk's rows are stored by the previous kernel
+        const bool is_v = warp == 10 || warp == 12;
+        const int hh = warp >= 11;  // which half of the tile's dims (K) or keys (V)
         // the stream's fields in registers: read from the launch parameters
         // with a per-CTA index, each costs a constant-cache round trip, and
         // the issue loop would reread them every slot
@@ -477,10 +482,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const void *const map = sd.tma >= 0 ? &maps.map[sd.tma] : nullptr;          // 16 x 64 boxes
         const void *const map_k = sd.tma_k >= 0 ? &maps.map[sd.tma_k] : nullptr;    // a K slot
         const void *const map_v = sd.tma_v >= 0 ? &maps.map[sd.tma_v] : nullptr;    // a V slot
+        const void *const map_t = is_v ? map_v : map_k;
         const uint64_t pol = policy_evict_normal();  // every M-tile of the head reads these rows
         // V rows sit H * ptok rows after the K rows of the same page
-        const int64_t vgap = (int64_t)H * ptok * kHeadDim;
+        const int64_t gap = is_v ? (int64_t)H * ptok * kHeadDim : 0;
+        const int vrows = is_v ? H * ptok : 0;
         const bool fuse = a.k_new != nullptr;
+        const uint16_t *const new_rows = is_v ? a.v_new : a.k_new;
+        const int nk = is_v ? 64 : kN;       // keys a slot
+        const int region = is_v ? kVRegion : kKRegion;
         // page ids in registers: lane i holds pages win + i (cur) and
         // win + 32 + i (nxt); the window slides by 32 once a tile starts past
         // its first half, so the next half is loading long before it is read
@@ -489,49 +499,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
         auto page_id = [&](int p) -> int { return (table && p < n_table) ? __ldg(table + p) : 0; };
         int win = table ? key0 / ptok : 0;
         int cur = page_id(win + lane), nxt = page_id(win + 32 + lane);
-        // A whole cached tile in one page (pages of a multiple of 128) needs
-        // only its first row: yk, the map row of its first K row (-1 for any
-        // other tile).  Any other tile: the K row offsets of this lane's keys
-        // m kN + 32 g + lane (clamped into the split), and which of them had
-        // a bad page id.  (The producer shares its sub-partition with two
-        // softmax warps: its per-tile instructions are on the pipeline's
-        // critical path.)
-        int64_t rk[4], rv[4];
-        uint32_t bk = 0, bv = 0;
-        int yk = -1, yv = -1;
-        const int vrows = H * ptok;  // V rows sit this many map rows after K's
-        auto lookup = [&](int m) {
-            const int kb = key0 + m * kN;
+        bool ok = true;
+        for (int m = 0; m < ntiles && ok; ++m) {
+            const int kt = key0 + m * kN;
             if (table) {
-                const int first = min(kb, key1 - 1) / ptok;  // the tile's lowest page
+                const int first = min(kt, key1 - 1) / ptok;  // the tile's lowest page
                 while (first >= win + 32) {
                     win += 32;
                     cur = nxt;
                     nxt = page_id(win + 32 + lane);
                 }
             }
-            bk = 0;
-            yk = -1;
-            if (map_k != nullptr && map_v != nullptr && kb + kN <= key1 && !(fuse && kb + kN > qbase)) {
-                int row = kb;
-                int64_t pg = 0;
-                if (table) {
-                    const int page = kb / ptok;
-                    row = kb - page * ptok;
-                    const int idx = page - win;  // 0 .. 31
-                    const int id = __shfl_sync(0xffffffffu, idx < 32 ? cur : nxt, idx & 31);
-                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
-                        pg = (int64_t)id * ps;
-                    } else if (lane == 0 && c.status) {
-                        atomicOr(c.status, PKV_DEV_BAD_PAGE);
-                    }
-                }
-                yk = static_cast<int>(layer_row + (pg + off_k(ptok, kvh, row)) / kHeadDim);
-                return;
-            }
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const int key = min(kb + 32 * g + lane, key1 - 1);
+            // A whole cached tile in one page (pages of a multiple of 128)
+            // needs only its first row (yt, the map row of its first K row);
+            // a whole cached tile in pages of a multiple of 16 only the first
+            // rows of its eight 16-row runs (lane i < 8: yrun, the map row of
+            // run i, V's for the V producer).  Any other tile: the row offsets
+            // of this lane's keys kt + 32 g + lane (clamped into the split),
+            // and which of them had a bad page id.  The lookups come before
+            // the slots' waits.
+            const bool cached = kt + kN <= key1 && !(fuse && kt + kN > qbase);
+            int yt = -1, yrun = -1;
+            int64_t r[4] = {0, 0, 0, 0};
+            uint32_t bm = 0;
+            if (cached && map != nullptr && !(map_k != nullptr && map_v != nullptr)) {
+                const int key = kt + 16 * (lane & 7);
                 int row = key;
                 int64_t pg = 0;
                 if (table) {
@@ -543,71 +535,56 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const int id = idx < 32 ? a0 : a1;
                     if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
                         pg = (int64_t)id * ps;
-                    } else {
-                        bk |= 1u << g;
-                        if (c.status) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                    } else if (lane < 8 && !is_v && c.status) {
+                        atomicOr(c.status, PKV_DEV_BAD_PAGE);
                     }
                 }
-                rk[g] = pg + off_k(ptok, kvh, row);
+                yrun = static_cast<int>(layer_row + (pg + off_k(ptok, kvh, row) + gap) / kHeadDim);
+            } else if (cached && map_k != nullptr && map_v != nullptr) {
+                int row = kt;
+                int64_t pg = 0;
+                if (table) {
+                    const int page = kt / ptok;
+                    row = kt - page * ptok;
+                    const int id = __shfl_sync(0xffffffffu, cur, (page - win) & 31);  // page - win < 32
+                    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
+                        pg = (int64_t)id * ps;
+                    } else if (lane == 0 && !is_v && c.status) {
+                        atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                    }
+                }
+                yt = static_cast<int>(layer_row + (pg + off_k(ptok, kvh, row)) / kHeadDim);
+            } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (is_v && (g >> 1) != hh) continue;  // a V slot holds two of the groups
+                    const int key = min(kt + 32 * g + lane, key1 - 1);
+                    int row = key;
+                    int64_t pg = 0;
+                    if (table) {
+                        const int page = key / ptok;
+                        row = key - page * ptok;
+                        const int idx = page - win;  // 0 .. 63
+                        const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
+                        const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
+                        const int id = idx < 32 ? a0 : a1;
+                        if (static_cast<uint32_t>(id) < static_cast<uint32_t>(n_pages)) {
+                            pg = (int64_t)id * ps;
+                        } else {
+                            bm |= 1u << g;
+                            if (c.status && !is_v) atomicOr(c.status, PKV_DEV_BAD_PAGE);
+                        }
+                    }
+                    r[g] = pg + off_k(ptok, kvh, row) + gap;
+                }
             }
-        };
-        if (ntiles > 0) lookup(0);
-        uint32_t q = 0;  // slots issued
-        bool ok = true;
-        for (int m = 0; m <= ntiles && ok; ++m) {
-#pragma unroll 1
-            for (int it = 0; it < 4; ++it) {
-                const bool is_v = it >= 2;
-                const int hh = it & 1;
-                const int tm = is_v ? m - 1 : m;  // the slot's tile
-                if (tm < 0 || tm >= ntiles) continue;
+            {
+                // the slot's place in the MMAs' order
+                const uint32_t q = is_v ? (m + 1 < ntiles ? 4 * m + 4 + hh : 4 * m + 2 + hh)
+                                        : (m == 0 ? hh : 4 * m - 2 + hh);
                 const int slot = q % kSlots;
                 uint64_t *const full = &bars[kBarFull + slot];
                 uint8_t *const dst = smem + kOffRing + slot * kSlotBytes;
-                const int yt = is_v ? yv : yk;
-                if (yt >= 0) {
-                    // the tile lies in one page: the slot is one copy
-                    if (__any_sync(0xffffffffu, *abort_flag) ||
-                        (q >= kSlots && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarEmpty + slot],
-                                                                             ((q / kSlots) - 1) & 1, c.status)))) {
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(full, kSlotBytes);
-                        if (is_v)
-                            tma_load_3d(dst, map_v, 0, yt + vrows + 64 * hh, 0, full, pol);
-                        else
-                            tma_load_3d(dst, map_k, 0, yt, 2 * hh, full, pol);
-                    }
-                    ++q;
-                    continue;
-                }
-                // the slot's keys: K, the tile's 128 (four groups of 32); V, 64
-                // of them (two groups), over all dims
-                const int kb = key0 + tm * kN + (is_v ? 64 * hh : 0);
-                const int nk = is_v ? 64 : kN;
-                const int64_t gap = is_v ? vgap : 0;
-                int64_t r[4];
-                uint32_t bm;
-                if (is_v) {
-                    r[0] = (hh ? rv[2] : rv[0]) + gap;
-                    r[1] = (hh ? rv[3] : rv[1]) + gap;
-                    r[2] = r[3] = 0;
-                    bm = (bv >> (2 * hh)) & 3u;
-                } else {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) r[g] = rk[g];
-                    bm = bk;
-                }
-                // with a decode call's new rows, keys from qbase on come from the
-                // input, not the cache (which this kernel stores them into)
-                const bool fresh = fuse && min(kb + nk, key1) > qbase;
-                const bool whole = kb + nk <= key1 && !fresh;
-                const int chunk0 = is_v ? 0 : 2 * hh;  // first 64-dim chunk of the slot
-                const int region = is_v ? kVRegion : kKRegion;
-                const void *const map_t = is_v ? map_v : map_k;
                 if (__any_sync(0xffffffffu, *abort_flag) ||
                     (q >= kSlots && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarEmpty + slot],
                                                                          ((q / kSlots) - 1) & 1, c.status)))) {
@@ -615,9 +592,59 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ok = false;
                     break;
                 }
+                if (yt >= 0) {
+                    // the tile lies in one page: the slot is one copy
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full, kSlotBytes);
+                        if (is_v)
+                            tma_load_3d(dst, map_v, 0, yt + vrows + 64 * hh, 0, full, pol);
+                        else
+                            tma_load_3d(dst, map_k, 0, yt, 2 * hh, full, pol);
+                    }
+                    continue;
+                }
+                if (yrun >= 0) {  // uniform: every lane looked a run up
+                    // 16-row page runs of a cached tile: a V slot in one page is
+                    // one copy; else 8 (K) or 4 (V) runs of two or four chunks
+                    const int rn0 = is_v ? 4 * hh : 0;
+                    const int y0 = __shfl_sync(0xffffffffu, yrun, rn0);
+                    if (is_v && map_v != nullptr) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(full, kSlotBytes);
+                            tma_load_3d(dst, map_v, 0, y0, 0, full, pol);
+                        }
+                        continue;
+                    }
+                    int yr[8];
+#pragma unroll
+                    for (int rn = 0; rn < 8; ++rn) yr[rn] = __shfl_sync(0xffffffffu, yrun, (rn0 + rn) & 7);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full, kSlotBytes);
+#pragma unroll
+                        for (int rn = 0; rn < 8; ++rn) {
+                            if (rn * 16 >= nk) break;
+#pragma unroll
+                            for (int ch = 0; ch < 4; ++ch) {
+                                if (!is_v && ch >= 2) break;
+                                tma_load_2d(dst + ch * region + rn * 2048, map, 64 * ((is_v ? 0 : 2 * hh) + ch),
+                                            yr[rn], full, pol);
+                            }
+                        }
+                    }
+                    continue;
+                }
+                // the slot's keys: K, the tile's 128 (four groups of 32) over
+                // dims 128 hh ..; V, keys 64 hh .. (two groups) over all dims
+                const int kb = kt + (is_v ? 64 * hh : 0);
+                const int g0 = is_v ? 2 * hh : 0;  // the slot's first key group
+                const int64_t ra = is_v ? (hh ? r[2] : r[0]) : r[0];
+                const int64_t rb = is_v ? (hh ? r[3] : r[1]) : r[1];
+                const bool fresh = fuse && min(kb + nk, key1) > qbase;
+                const bool whole = kb + nk <= key1 && !fresh;
+                const int chunk0 = is_v ? 0 : 2 * hh;  // first 64-dim chunk of the slot
                 if (whole && map_t != nullptr) {
                     // the slot's keys lie in one page: one copy
-                    const int y0 = static_cast<int>(layer_row + shfl64(r[0], 0) / kHeadDim);
+                    const int y0 = static_cast<int>(layer_row + shfl64(ra, 0) / kHeadDim);
                     if (lane == 0) {
                         mbar_arrive_expect_tx(full, kSlotBytes);
                         tma_load_3d(dst, map_t, 0, y0, chunk0, full, pol);
@@ -627,8 +654,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     int yr[8];
 #pragma unroll
                     for (int rn = 0; rn < 8; ++rn) {
-                        const int64_t kr = shfl64(r[rn >> 1], (rn & 1) * 16);
-                        yr[rn] = static_cast<int>(layer_row + kr / kHeadDim);
+                        const int gg = rn >> 1;
+                        const int64_t rg = is_v ? (gg == 0 ? ra : rb) : (gg == 0 ? r[0] : gg == 1 ? r[1] : gg == 2 ? r[2] : r[3]);
+                        yr[rn] = static_cast<int>(layer_row + shfl64(rg, (rn & 1) * 16) / kHeadDim);
                     }
                     if (lane == 0) {
                         mbar_arrive_expect_tx(full, kSlotBytes);
@@ -645,12 +673,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     }
                 } else {
                     // key by key: each row's 16-byte chunks of the slot's dims
-                    const uint16_t *const new_rows = is_v ? a.v_new : a.k_new;
                     int64_t sp[4];
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
-                        const int key = min(kb + 32 * g + lane, key1 - 1);
-                        const uint16_t *src = layer_base + r[g];
+                        const int gk = g0 + g;  // key group within the tile
+                        const int key = min(kt + 32 * gk + lane, key1 - 1);
+                        const int64_t rg = gk == 0 ? r[0] : gk == 1 ? r[1] : gk == 2 ? r[2] : r[3];
+                        const uint16_t *src = layer_base + rg;
                         if (fresh && key >= qbase)
                             src = new_rows + (((int64_t)tok_off + (key - qbase)) * H + kvh) * kHeadDim;
                         sp[g] = reinterpret_cast<int64_t>(src + 64 * chunk0);
@@ -690,10 +719,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         // store the slot's new rows (K or V of this KV head, and the
                         // indexer-key row once, with KV head 0) into their pages
                         for (int i = max(kb, qbase); i < min(kb + nk, key1); ++i) {
-                            const int g = (i - kb) >> 5, ln = (i - kb) & 31;
-                            const int64_t rg = g == 0 ? r[0] : g == 1 ? r[1] : g == 2 ? r[2] : r[3];
+                            const int gk = (i - kt) >> 5, ln = (i - kt) & 31;
+                            const int64_t rg = gk == 0 ? r[0] : gk == 1 ? r[1] : gk == 2 ? r[2] : r[3];
                             const int64_t kr = shfl64(rg, ln);
-                            if ((bm >> g) & 1u) continue;
+                            if ((bm >> gk) & 1u) continue;
                             const int64_t rw = (int64_t)tok_off + (i - qbase);
                             uint16_t *row = const_cast<uint16_t *>(layer_base) + kr;
                             reinterpret_cast<uint4 *>(row)[lane] =
@@ -709,14 +738,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         }
                     }
                 }
-                ++q;
             }
-            // tile m's rows serve its V next; look the next tile's up
-#pragma unroll
-            for (int g = 0; g < 4; ++g) rv[g] = rk[g];
-            bv = bk;
-            yv = yk;
-            if (m + 1 < ntiles) lookup(m + 1);
         }
     } else if (warp == kWarpMma && lane == 0) {
         // ---------------- MMA issue ----------------
@@ -808,7 +830,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // Work items: (KV head, M-tile, split) per stream, splits fastest.  A stream
 // is split only as far as filling the SMs needs, from its own shape alone.
 // Split model of plan_prefill, in hundredths of a microsecond.
-constexpr int64_t kTileCost = 175;   // a 128-key tile of one 128-row M-tile
+constexpr int64_t kTileCost = 220;   // a 128-key tile of one 128-row M-tile
 constexpr int64_t kCtaCost = 1200;   // a CTA's fixed cost
 constexpr int64_t kPartialCost = 4;  // a (unit, split) partial written and read back
 constexpr int kMaxPrefillSplits = 64;
@@ -832,16 +854,15 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         // Splits: the count with the least modelled time for this stream's
         // grid on nsm SMs, waves x (tiles a CTA x a tile's time + a CTA's
         // fixed cost) + the split partials' round trip through HBM.  The
-        // costs are this kernel's on GB300: about 1.5 us a 64-key tile of
-        // 128 rows, 12 us a CTA (Q load, TMEM, pipeline fill, epilogue) and
-        // 0.04 us a (unit, split) partial of 128 rows written and read back.
-        // For 512 queries on 31,000 keys it picks 7 splits, 448 CTAs in
-        // three nearly full waves (2 splits would give one wave of 128 CTAs
-        // with 24 SMs idle).  For 2,048 queries at 16,384 (256 units) it
-        // picks 4 splits, 7 nearly full waves, against 2 waves unsplit, the
-        // second two-thirds full.  Only the stream's own length and rows and
-        // the SM count enter, so paged and contiguous caches get the same
-        // splits.
+        // costs are this kernel's on GB300: about 2.2 us a 128-key tile of
+        // 128 rows, 12 us a CTA (Q into TMEM, pipeline fill, epilogue, the
+        // next CTA's entry) and 0.04 us a (unit, split) partial of 128 rows
+        // written and read back.  For 512 queries on 31,000 keys it picks 7
+        // splits, 448 CTAs in three nearly full waves (295 us; 2 splits, one
+        // wave of 128 CTAs, measured the same, 3 to 19 splits 310-395 us).
+        // For 2,048 queries at 16,384 (256 units) it picks 1 split, 2 waves.
+        // Only the stream's own length and rows and the SM count enter, so
+        // paged and contiguous caches get the same splits.
         const int64_t units = (int64_t)H * mtiles, tiles = (d.len + kN - 1) / kN;
         const int max_ns = std::max(1, std::min(kMaxPrefillSplits, d.len / 256));  // 256 keys a split at least
         int ns = 1;
