@@ -857,10 +857,11 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         // costs are this kernel's on GB300: about 2.2 us a 128-key tile of
         // 128 rows, 12 us a CTA (Q into TMEM, pipeline fill, epilogue, the
         // next CTA's entry) and 0.04 us a (unit, split) partial of 128 rows
-        // written and read back.  For 512 queries on 31,000 keys it picks 7
-        // splits, 448 CTAs in three nearly full waves (295 us; 2 splits, one
-        // wave of 128 CTAs, measured the same, 3 to 19 splits 310-395 us).
-        // For 2,048 queries at 16,384 (256 units) it picks 1 split, 2 waves.
+        // written and read back.  For 512 queries at 31,000 (64 units) it
+        // picks 2 splits, one wave of 128 CTAs (296 us; 7 splits, three
+        // nearly full waves, measured the same, 3-6 and 8-19 splits 310-395
+        // us).  For 2,048 queries at 16,384 (256 units) it picks 1 split, 2
+        // waves.
         // Only the stream's own length and rows and the SM count enter, so
         // paged and contiguous caches get the same splits.
         const int64_t units = (int64_t)H * mtiles, tiles = (d.len + kN - 1) / kN;
