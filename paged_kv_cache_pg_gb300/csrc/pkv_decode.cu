@@ -417,6 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u.key0 + (ks + j * ks_n) * kTile + kTile <= early_end)
                     prefetch_tile(c, sd, u, x, ks + j * ks_n, lane);
     }
+    // the query row's address from the launch parameters before the wait
+    // (an asm use the compiler cannot move past it): only its load waits
+    const int bcol = cg * 8 + (lane >> 2);
+    const uint16_t *const qr =
+        (active && bcol < ncols) ? a.q + q_row<kSparse>(c, sd, u, bcol) * kHeadDim : nullptr;
+    asm volatile("" ::"l"(qr));
     if (!waited) pdl_wait();
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -425,11 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
     if (active) {
-        const int bcol = cg * 8 + (lane >> 2);
         uint32_t qf[16][2];
         {
-            const uint16_t *qr =
-                bcol < ncols ? a.q + q_row<kSparse>(c, sd, u, bcol) * kHeadDim : nullptr;
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk) {
                 const int d = kk * 16 + 2 * (lane & 3);
@@ -616,7 +619,9 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     // the next kernel may start now: it waits for this grid before reading
     // anything this grid writes, and its CTAs stream their cached rows meanwhile
     pdl_trigger();
-    pdl_wait();
+    // everything below up to the partials' loads reads the launch parameters
+    // only: done before the wait, its constant-cache misses (the stream
+    // search, the stream's fields) overlap the partial kernel's tail
     const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
     const SeqDev &sd = c.seq[s];
     const int ns = sd.nsplit;
@@ -638,6 +643,11 @@ __global__ void __launch_bounds__(kCombThreads, 4)
     const int i1 = halves == 2 && !grp ? (ns + 1) >> 1 : ns;
     const float *col_acc = part_acc + p0 * kHeadDim + d;
     const int warp = tid >> 5;
+    const int64_t orow = q_row<kSparse>(c, sd, Unit{0, unit, 0, kSparse ? unit / c.group : unit, 0, 0, 0}, col);
+    // the addresses are in registers before the wait (an asm use the compiler
+    // cannot move past it)
+    asm volatile("" ::"l"(col_acc), "l"(col_ml), "l"(stride), "l"(orow), "r"(i0), "r"(i1), "r"(ns));
+    pdl_wait();
     float xs[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) xs[j] = i0 + j < i1 ? __ldcg(col_acc + (i0 + j) * stride) : 0.f;
@@ -678,10 +688,7 @@ __global__ void __launch_bounds__(kCombThreads, 4)
         O += sh_o[dd];
     }
     const float o = L > 0.f ? O / L : 0.f;
-    Unit u;
-    u.unit = unit;
-    u.kvh = kSparse ? unit / c.group : unit;
-    a.out[q_row<kSparse>(c, sd, u, col) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+    a.out[orow * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
 }
 static_assert(kCombThreads == kHeadDim, "a thread a dim (one group), or two groups of half the dims");
 
@@ -695,8 +702,7 @@ static_assert(kCombThreads == kHeadDim, "a thread a dim (one group), or two grou
 __global__ void __launch_bounds__(kCombThreads)
     combine_cols(const __grid_constant__ Common c, const DecodeArgs a) {
     constexpr int kB = 8;  // splits loaded at a time
-    pdl_wait();
-    pdl_trigger();
+    // the setup reads the launch parameters only: before the wait
     const int s = find_seq(c.n_seqs, blockIdx.x, [&](int t) { return c.seq[t].comb_off; });
     const SeqDev &sd = c.seq[s];
     const int ns = sd.nsplit;
@@ -711,6 +717,9 @@ __global__ void __launch_bounds__(kCombThreads)
     const int64_t p0 = (int64_t)unit * ns * sd.ncols + col;  // split i at p0 + i * ncols
     const float *col_acc = part_acc + p0 * kHeadDim + 8 * lane;
     const int64_t stride = (int64_t)sd.ncols * kHeadDim;
+    asm volatile("" ::"l"(col_acc), "l"(col_ml), "l"(stride), "r"(ns));
+    pdl_wait();
+    pdl_trigger();
     const float2 none = make_float2(-INFINITY, 0.f);
     const float2 ml0 = lane < ns ? __ldcg(col_ml + (int64_t)lane * sd.ncols) : none;
     const float2 ml1 = lane + 32 < ns ? __ldcg(col_ml + (int64_t)(lane + 32) * sd.ncols) : none;

@@ -287,6 +287,17 @@ __global__ void __maxnreg__(192)
         if (kt + kT8 > qbase - 32) break;
         issue(issued);
     }
+    // the query row's address from the launch parameters before the wait
+    // (an asm use the compiler cannot move past it): only its load waits
+    const uint16_t *qr = nullptr;
+    {
+        const int col = cg * 8 + g;
+        if (active && col < ncols) {
+            const int j = col / G;
+            qr = a.q + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
+        }
+    }
+    asm volatile("" ::"l"(qr));
     pdl_wait();
     __syncthreads();
     for (; issued < kDepth8 && issued < my_tiles; ++issued) issue(issued);
@@ -294,12 +305,6 @@ __global__ void __maxnreg__(192)
     // the queries of this thread's B-operand column, in the permuted dim order
     uint32_t qf[16][2];
     {
-        const int col = cg * 8 + g;
-        const uint16_t *qr = nullptr;
-        if (active && col < ncols) {
-            const int j = col / G;
-            qr = a.q + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
-        }
         // dims 64 c4 .. 64 c4 + 63 of the row: eight 16-byte loads, two steps each
         uint4 u[8];
 #pragma unroll

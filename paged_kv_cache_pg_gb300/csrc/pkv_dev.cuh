@@ -278,9 +278,18 @@ __device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
 // Stream of the work item / token: the last s with off(s) <= i.
 template <typename F>
 __device__ __forceinline__ int find_seq(int n, int32_t i, F off) {
+    // four streams' offsets are loaded before any is compared: read from the
+    // launch parameters with a computed index, their constant-cache misses
+    // then overlap instead of following one another
     int s = 0;
-    for (int t = 1; t < n; ++t)
-        if (off(t) <= i) s = t;
+    for (int t0 = 1; t0 < n; t0 += 4) {
+        int32_t v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = t0 + k < n ? off(t0 + k) : INT32_MAX;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (v[k] <= i) s = t0 + k;
+    }
     return s;
 }
 
