@@ -39,15 +39,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __shared__ __align__(16) float ps[kScoreBlocks * kPStride];
     __shared__ int64_t prow[kScoreBlocks];  // each block's pooled row (-1 past the end)
     extern __shared__ float4 qs4[];  // [n_q_heads][Di / 4]
-    pdl_wait();
-    pdl_trigger();
     const int s = blockIdx.x / tiles_per_seq;
     const int b0 = (blockIdx.x - s * tiles_per_seq) * kScoreBlocks;
     const SeqDev &sd = c.seq[s];
     const int nb = sd.len / 4;
     const int H = c.n_kv_heads, Di = c.idx_dim, Hq = c.n_q_heads;
     const int tid = threadIdx.x;
-    // pooled rows of blocks b0 .. b0+63: one lookup per block, then the rows
+    // pooled rows of blocks b0 .. b0+63: one lookup per block.  The launch
+    // parameters and the page table are not written by the kernels before
+    // this one, so the lookups run before the grid-dependency wait; the
+    // pooled rows and the queries (which those kernels write) after it.
     if (tid < kScoreBlocks) {
         const int b = b0 + tid;
         int64_t off = -1;
@@ -58,6 +59,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         prow[tid] = off;
     }
+    pdl_wait();
+    pdl_trigger();
     // indexer queries of this stream's one decode token, 8 a thread and load
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(qi + (int64_t)sd.tok_off * Hq * Di);
@@ -128,14 +131,19 @@ __global__ void __launch_bounds__(kTopThreads)
     __shared__ int2 warp_tot2[kTopThreads / 32];
     __shared__ int vars[4];
     extern __shared__ uint32_t skeys[];  // the row's order keys, when it fits
+    // the row and its length from the launch parameters before the wait (an
+    // asm use the compiler cannot move past it): only the scores wait
+    const int s = blockIdx.x / c.n_q_heads, h = blockIdx.x - s * c.n_q_heads;
+    const int nb = c.seq[s].len / 4;
+    const float *row = scores + ((int64_t)s * c.n_q_heads + h) * ld;
+    int32_t *out = ids + ((int64_t)s * c.n_q_heads + h) * k;
+    asm volatile("" ::"r"(nb), "l"(row), "l"(out));
     pdl_wait();
     pdl_trigger();
-    const int s = blockIdx.x / c.n_q_heads, h = blockIdx.x - s * c.n_q_heads;
     // the launch sized the key array for every row, or gave it none
     const TopkSmem sm{hist, hist11, cand, warp_tot, warp_tot2, vars,
                       keys_in_smem != 0 ? skeys : nullptr};
-    topk_block(scores + ((int64_t)s * c.n_q_heads + h) * ld, c.seq[s].len / 4, k,
-               ids + ((int64_t)s * c.n_q_heads + h) * k, sm);
+    topk_block(row, nb, k, out, sm);
 }
 
 }  // namespace
