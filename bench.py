@@ -55,9 +55,9 @@ ROWS = ["prefill", "sparse", "mix", "decode_layer", "prompt_cache", "decode_e4m3
 # combine kernels), from one ncu capture of the decode kernels (summary under
 # profiles/), valid while the decode sources hash to the value the capture
 # was taken with; reported as null, with the capture date, otherwise.
-DECODE_TRAFFIC = {"bytes": 40377600, "captured": "2026-12-02",
+DECODE_TRAFFIC = {"bytes": 40379904, "captured": "2026-12-02",
                   "sources": ["pkv_decode.cu", "pkv_dev.cuh", "pkv_internal.h", "pkv_host.cu"],
-                  "sha256": "d62ae8c36d134c262964745bf422293a38a24faa106ff76a496dd4c0cffad9aa"}
+                  "sha256": "3d0c281022d012bc7f95eec7324822942159e464c695fbcdf299834a54e6561d"}
 FLUSH_BYTES = 256 << 20                  # written between timed calls: twice the L2
 
 
