@@ -9,23 +9,27 @@
 // A tcgen05 MMA with M = 128 costs about the same for every N up to 128, so
 // a 128-key S product takes the instructions a 64-key one did.  Q sits in
 // TMEM (columns 0-127, bf16 pairs) and is the S product's A operand there;
-// that leaves shared memory for P (hi and lo, 64 KB), two K slots (a tile's
-// keys over 128 of the dims each) and two V slots (64 of a tile's keys over
-// all dims each).  The softmax takes two threads a row (TMEM lane), each on
-// 64 of the tile's keys and 128 of O's columns; the pair agrees on the row
-// maximum through shared memory.  S has one TMEM buffer: the next S product
-// starts once the softmax threads have read S, and P has one buffer, which
-// the softmax fills once the previous tile's PV product is done.
-// K and V arrive through rings of their own, each filled by its own producer
-// warp, which looks a unit's rows up before its slot is free.  A unit in one
-// page comes by one 3D TMA copy (pages of a multiple of 128 positions for K,
-// 64 for V), or by 2D copies of 16-row page runs (pages of a multiple of 16;
-// each copy costs the issuing thread about 40 ns, whatever its size), or,
-// for a ragged tail or other page sizes, by cp.async from one row lookup per
-// key, fenced by the copying threads before the tensor cores read it.  The
-// max of a row is rescaled lazily: O in TMEM is corrected only when the
-// running max grows by more than 2^8.  Split partials use the decode layout
-// and its combine kernel.
+// that leaves shared memory for P (hi and lo, 64 KB) and one ring of five
+// 32 KB slots: a K slot holds the tile's keys over 128 of the dims, a V slot
+// 64 of its keys over all dims.  The softmax takes two threads a row (TMEM
+// lane), each on 64 of the tile's keys and 128 of O's columns; the pair
+// agrees on the row maximum through shared memory.  S has one TMEM buffer:
+// the next S product starts once the softmax threads have read S, and P has
+// one buffer, which the softmax fills once the previous tile's PV product is
+// done.
+// Four producer warps, one for each slot kind (K over the first or second
+// dims, V over the first or second keys), fill the ring in the order the
+// MMAs take the slots, looking a tile's rows up before its slots are free: a
+// cached tile inside one page needs one page lookup and comes by one 3D TMA
+// copy a slot (pages of a multiple of 128 positions), a cached tile in pages
+// of a multiple of 16 needs its eight 16-row run starts and comes by 2D
+// copies of the runs (each copy costs the issuing thread about 40 ns,
+// whatever its size), and any other tile (a ragged tail, new rows, other page
+// sizes) comes key by key by cp.async from one row lookup per key, fenced by
+// the copying threads before the tensor cores read it.  The max of a row is
+// rescaled lazily: O in TMEM is corrected only when the running max grows by
+// more than 2^8.  Split partials use the decode layout and its combine
+// kernel.
 #include <algorithm>
 #include <climits>
 
