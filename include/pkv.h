@@ -74,6 +74,11 @@ extern "C" {
 #define PKV_DEV_TIMEOUT 2u  /* a pipeline wait ran past its time limit     */
 #define PKV_DEV_SMEM 4u     /* a kernel's shared memory was not at the
                                alignment its layout needs; it did nothing  */
+#define PKV_DEV_RANGE 8u    /* the tensor-core attention (pkv_prefill, and
+                               a decode call's tensor-core route) summed a
+                               non-finite value: a V entry beyond fp16's
+                               range (|v| > 65,504) in a call whose PV
+                               product runs in fp16, or non-finite inputs */
 
 /* kinds of rows (pkv_pg_row, pkv_gather) */
 #define PKV_K 0
@@ -314,9 +319,16 @@ int pkv_decode(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, in
  * cache already (pkv_store, and pkv_pool for its blocks).  QK^T and PV run as
  * tcgen05 MMAs with float32 accumulation in tensor memory (P in two bf16
  * parts).  Whole 16-position page runs are read by TMA when the page size is
- * a multiple of 16; other tiles key by key.  q, out: [tokens][n_q_heads][D].
- * ws: device, >= pkv_prefill_ws_size bytes, 256-byte aligned.  Paged output
- * equals contiguous output bit for bit. */
+ * a multiple of 16; other tiles key by key.  When every stream of the call
+ * has more than 32 queries and at least 8 blocks of 128 query columns a KV
+ * head (n_new * n_q_heads / H >= 897), a first kernel converts the streams'
+ * V rows to fp16 in ws (their bytes are part of pkv_prefill_ws_size) and the
+ * PV product runs in fp16 (P rounded to 11 significant bits, one MMA where
+ * the two bf16 parts take two): exact for V entries of magnitude 2^-14 to
+ * 65,280, rounded to fp16's 2^-24 grid below that, and a V entry beyond
+ * 65,504 makes the output non-finite and sets PKV_DEV_RANGE.  q, out:
+ * [tokens][n_q_heads][D].  ws: device, >= pkv_prefill_ws_size bytes,
+ * 256-byte aligned.  Paged output equals contiguous output bit for bit. */
 int pkv_prefill_ws_size(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs,
                         int32_t n_q_heads, size_t *bytes);
 int pkv_prefill(const pkv_layout *layout, const pkv_seq *seqs, int32_t n_seqs, int32_t layer,

@@ -6,6 +6,8 @@
 //   S = Q K^T  -> TMEM (128 lanes x 128 columns)               [MMA thread]
 //   softmax of S with the causal mask, P = hi + lo bf16 parts   [8 warps]
 //   O += P_hi V + P_lo V -> TMEM (128 lanes x 256 columns)      [MMA thread]
+// or, in the fp16 V mode (long chunks; below), P in fp16 and O += P V on V
+// rows converted to fp16 once a call by v16_gather.
 // A tcgen05 MMA with M = 128 costs about the same for every N up to 128, so
 // a 128-key S product takes the instructions a 64-key one did.  Q sits in
 // TMEM (columns 0-127, bf16 pairs) and is the S product's A operand there;
@@ -72,11 +74,49 @@ static_assert(kPSmem <= 232448, "prefill shared memory above the 227 KB a CTA ma
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 constexpr float kRescale = 8.f;  // rescale O when the max grows by more than 2^8
 
-// Instruction descriptor, kind::f16: D float32, A and B bf16, A K-major, B
-// K-major (S = Q K^T) or MN-major (O += P V), M = 128.
-__host__ __device__ constexpr uint32_t mma_idesc(int n, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// Instruction descriptor, kind::f16: D float32, A and B both bf16 or both
+// fp16, A K-major, B K-major (S = Q K^T) or MN-major (O += P V), M = 128.
+__host__ __device__ constexpr uint32_t mma_idesc(int n, bool b_mn_major, bool f16 = false) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+}
+
+// Two floats to an fp16 pair, round to nearest even, lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+
+// A bf16 pair to an fp16 pair (each bf16 value is exactly a float): exact
+// for magnitudes 2^-14 to 65,280, rounded to fp16's 2^-24 grid below, and
+// infinite above 65,504.
+__device__ __forceinline__ uint32_t f16_of_bf16(uint32_t w) {
+    return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// The fp16 V mode.  A launch whose streams each have a chunk of more than
+// 32 queries and at least eight M-tiles a KV head reads V rows converted
+// once a call by v16_gather into the workspace (each KV head's rows padded
+// with zeros to a multiple of the key tile) instead of the cache's bf16
+// rows: the PV product runs in fp16 on one P part, half the MMAs of the
+// bf16 hi and lo parts (A and B of one MMA share a type, and P needs more
+// than bf16's 8 significant bits).  The conversion costs a read and a write
+// of the V rows; each M-tile's CTA would otherwise convert every V tile
+// again.  Decode calls (at most 32 new rows a stream) never take it.
+constexpr int kV16MinTiles = 8;
+constexpr int kV16MinNew = 33;
+__host__ __device__ inline int v16_stride(int len) { return (len + kN - 1) / kN * kN; }
+// Rows of the launch's converted V (0: the launch reads bf16 V).
+inline int64_t v16_rows(const Common &c) {
+    int64_t rows = 0;
+    for (int s = 0; s < c.n_seqs; ++s) {
+        const SeqDev &d = c.seq[s];
+        if (d.ncols == 0) continue;
+        if (d.n_new < kV16MinNew || (d.ncols + kM - 1) / kM < kV16MinTiles) return 0;
+        rows += (int64_t)c.n_kv_heads * v16_stride(d.len);
+    }
+    return rows <= ((int64_t)1 << 30) ? rows : 0;
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
@@ -167,6 +207,11 @@ struct PrefillArgs {
     // a decode call's new rows [token][KV head][256] (and [token][Di]), read
     // from here and stored into their pages by the kernel, or null
     const uint16_t *k_new, *v_new, *ik_new;
+    // the fp16 V mode: the converted rows (in the workspace), their map, and
+    // each stream's first row there (KV head 0; -1: the stream reads bf16 V)
+    uint16_t *v16;
+    int32_t v16_map;
+    int32_t v16_row[PKV_MAX_SEQS];
 };
 
 // Byte offset of 16-byte chunk c (0..31) of row r in a 128-byte-swizzled
@@ -175,9 +220,10 @@ __device__ __forceinline__ uint32_t swz128(int region, int r, int c) {
     return (c >> 3) * region + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
 }
 
+template <bool kV16>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_partial(const __grid_constant__ Common c, const __grid_constant__ DecodeMaps maps,
-                    const PrefillArgs a) {
+                    const __grid_constant__ PrefillArgs a) {
     // the 128-byte swizzle of the TMA copies and the MMA operands repeats
     // every 1024 bytes from a 1024-byte boundary
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -220,6 +266,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int key0 = split * sd.split_len;
     const int key1 = min(min(sd.len, key0 + sd.split_len), last_q + 1);
     const int ntiles = key1 > key0 ? (key1 - key0 + kN - 1) / kN : 0;
+    constexpr bool v16 = kV16;  // the PV product in fp16 on converted V rows
 
     if (tid == 0) {
         for (int i = 0; i < kSlots; ++i) {
@@ -369,19 +416,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const float m_off = m_used == -INFINITY ? 0.f : m_used;
             float ps[4] = {0.f, 0.f, 0.f, 0.f};  // this half's sum as four chains
             uint32_t hi[32], lo[32];
+            if (v16) {
+                // P in fp16: 11 significant bits (weights at most 2^8 with the
+                // lazy rescale; below 2^-14 on fp16's 2^-24 grid)
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                const float p0 = ex2(fmaf(x[i], kScaleLog2, -m_off));
-                const float p1 = ex2(fmaf(x[i + 1], kScaleLog2, -m_off));
-                ps[(i >> 1) & 3] += p0 + p1;
-                // p = hi + lo: hi is p's top 16 bits (exact), lo the top 16 bits
-                // of the exact remainder, so hi + lo is p to 2^-15 relative;
-                // bit selects keep the split off the conversion pipe
-                const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-                hi[i / 2] = __byte_perm(u0, u1, 0x7632);
-                const float r0 = p0 - __uint_as_float(u0 & 0xffff0000u);
-                const float r1 = p1 - __uint_as_float(u1 & 0xffff0000u);
-                lo[i / 2] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+                for (int i = 0; i < 64; i += 2) {
+                    const float p0 = ex2(fmaf(x[i], kScaleLog2, -m_off));
+                    const float p1 = ex2(fmaf(x[i + 1], kScaleLog2, -m_off));
+                    ps[(i >> 1) & 3] += p0 + p1;
+                    hi[i / 2] = pack_f16(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; i += 2) {
+                    const float p0 = ex2(fmaf(x[i], kScaleLog2, -m_off));
+                    const float p1 = ex2(fmaf(x[i + 1], kScaleLog2, -m_off));
+                    ps[(i >> 1) & 3] += p0 + p1;
+                    // p = hi + lo: hi is p's top 16 bits (exact), lo the top 16
+                    // bits of the exact remainder, so hi + lo is p to 2^-15
+                    // relative; bit selects keep the split off the conversion pipe
+                    const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+                    hi[i / 2] = __byte_perm(u0, u1, 0x7632);
+                    const float r0 = p0 - __uint_as_float(u0 & 0xffff0000u);
+                    const float r1 = p1 - __uint_as_float(u1 & 0xffff0000u);
+                    lo[i / 2] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+                }
             }
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             // the P rows are free once the last tile's products are done
@@ -395,8 +454,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const uint32_t off = r * 128 + (((ch ^ (r & 7))) << 4);
                 *reinterpret_cast<uint4 *>(p_hi + off) =
                     make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
-                *reinterpret_cast<uint4 *>(p_lo + off) =
-                    make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+                if (!v16)
+                    *reinterpret_cast<uint4 *>(p_lo + off) =
+                        make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
             }
             fence_async_smem();
             tc_fence_before();
@@ -428,6 +488,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int64_t prow = ((int64_t)kvh * sd.nsplit + split) * sd.ncols + col;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint16_t *orow = a.out + (((int64_t)sd.tok_off + j) * c.n_q_heads + kvh * G + (col - j * G)) * kHeadDim;
+            bool finite = true;  // a V entry beyond fp16's range makes O infinite or NaN
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 const int d0 = 128 * hf + 32 * ch;  // the chunk's first dim
@@ -440,6 +501,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
                 }
                 if (!row_ok) continue;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) finite &= fabsf(__uint_as_float(o[i])) <= 3.402823466e38f;
                 if (single) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
@@ -463,6 +526,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 part_ml[prow * 2 + 0] = m_used;
                 part_ml[prow * 2 + 1] = l;
             }
+            if (!finite && c.status) atomicOr(c.status, PKV_DEV_RANGE);
         }
     } else if (warp >= kSoftWarps && warp != kWarpMma) {
         // ------- producers: K slots (warps 8, 11) and V slots (10, 12) of one ring -------
@@ -487,6 +551,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const void *const map_k = sd.tma_k >= 0 ? &maps.map[sd.tma_k] : nullptr;    // a K slot
         const void *const map_v = sd.tma_v >= 0 ? &maps.map[sd.tma_v] : nullptr;    // a V slot
         const void *const map_t = is_v ? map_v : map_k;
+        // fp16 V mode: each V slot is one copy of converted rows
+        const bool v16v = v16 && is_v;
+        const void *const map16 = v16v ? &maps.map[a.v16_map] : nullptr;
+        const int y16 = v16v ? a.v16_row[s] + kvh * v16_stride(sd.len) : 0;
         const uint64_t pol = policy_evict_normal();  // every M-tile of the head reads these rows
         // V rows sit H * ptok rows after the K rows of the same page
         const int64_t gap = is_v ? (int64_t)H * ptok * kHeadDim : 0;
@@ -526,7 +594,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             int yt = -1, yrun = -1;
             int64_t r[4] = {0, 0, 0, 0};
             uint32_t bm = 0;
-            if (cached && map != nullptr && !(map_k != nullptr && map_v != nullptr)) {
+            if (v16v) {
+                // no lookups: the converted rows are contiguous
+            } else if (cached && map != nullptr && !(map_k != nullptr && map_v != nullptr)) {
                 const int key = kt + 16 * (lane & 7);
                 int row = key;
                 int64_t pg = 0;
@@ -595,6 +665,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     *abort_flag = 1;
                     ok = false;
                     break;
+                }
+                if (v16v) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full, kSlotBytes);
+                        tma_load_3d(dst, map16, 0, y16 + kt + 64 * hh, 0, full, pol);
+                    }
+                    continue;
                 }
                 if (yt >= 0) {
                     // the tile lies in one page: the slot is one copy
@@ -749,7 +826,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // operands written by threads (Q, P, key-by-key slots) were fenced by
         // their writers before they arrived
         const uint32_t idesc_s = mma_idesc(kN, false);
-        const uint32_t idesc_o = mma_idesc(kHeadDim, true);
+        const uint32_t idesc_o = mma_idesc(kHeadDim, true, v16);
         bool ok = mbar_wait(&bars[kBarQFull], 0, c.status);
         tc_fence_after();
         uint32_t q = 0;  // slots taken, in the producer's order
@@ -807,8 +884,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const uint32_t va = vb + k4 * 2048;  // 16 keys = two 8-row groups
                     tc_mma(tmem + kOCol, smem_desc(pa, 16, 1024), smem_desc(va, kVRegion, 1024), idesc_o,
                            (n > 0 || hh > 0 || k4 > 0) ? 1u : 0u);
-                    tc_mma(tmem + kOCol, smem_desc(pa + kPPart, 16, 1024), smem_desc(va, kVRegion, 1024),
-                           idesc_o, 1u);
+                    if (!v16)
+                        tc_mma(tmem + kOCol, smem_desc(pa + kPPart, 16, 1024), smem_desc(va, kVRegion, 1024),
+                               idesc_o, 1u);
                 }
                 give();
             }
@@ -826,6 +904,45 @@ __global__ void __launch_bounds__(kPThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
+    }
+}
+
+// The fp16 V mode's rows: a warp a group of four rows (one KV head's key of
+// a stream each), a lane 16 bytes of a row; keys past the stream's length
+// are zeros.  A table entry outside [0, n_pages) is reported and read as
+// page 0, as the chunk kernel does.
+constexpr int kV16Threads = 256;
+constexpr int kV16RowsWarp = 4;
+constexpr int kV16RowsBlock = kV16Threads / 32 * kV16RowsWarp;
+static_assert(kN % kV16RowsBlock == 0, "a stream's rows fill whole blocks");
+
+__global__ void __launch_bounds__(kV16Threads)
+    v16_gather(const __grid_constant__ Common c, const __grid_constant__ PrefillArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * (kV16Threads / 32) + (threadIdx.x >> 5)) * kV16RowsWarp;
+    // the stream holding these rows (a block's rows lie in one stream: each
+    // stream's rows are a multiple of the key tile)
+    int s = 0;
+    for (int t = 0; t < c.n_seqs; ++t)
+        if (a.v16_row[t] >= 0 && row0 >= a.v16_row[t]) s = t;
+    const SeqDev &sd = c.seq[s];
+    const int stride = v16_stride(sd.len);
+    const int local = row0 - a.v16_row[s];
+    const int kvh = local / stride, key0 = local - kvh * stride;
+    pdl_trigger();  // the chunk kernel waits for this grid before it reads the rows
+    pdl_wait();     // the rows were stored by an earlier kernel
+    uint4 v[kV16RowsWarp];
+#pragma unroll
+    for (int i = 0; i < kV16RowsWarp; ++i) {
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (key0 + i < sd.len)
+            v[i] = __ldg(reinterpret_cast<const uint4 *>(v_row(sd, c.n_kv_heads, kvh, key0 + i, c.status)) + lane);
+    }
+#pragma unroll
+    for (int i = 0; i < kV16RowsWarp; ++i) {
+        const uint4 h = make_uint4(f16_of_bf16(v[i].x), f16_of_bf16(v[i].y), f16_of_bf16(v[i].z),
+                                   f16_of_bf16(v[i].w));
+        reinterpret_cast<uint4 *>(a.v16 + (int64_t)(row0 + i) * kHeadDim)[lane] = h;
     }
 }
 
@@ -909,9 +1026,11 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         d.work_off = items;
         items += H * ((d.ncols + kM - 1) / kM) * d.nsplit;
     }
+    // the fp16 V mode's rows, after the partials
+    const int64_t rows16 = v16_rows(c);
     plan->total_items = items;
     plan->total_comb = comb;
-    plan->ws_bytes = static_cast<size_t>(floats) * 4;
+    plan->ws_bytes = static_cast<size_t>(floats) * 4 + static_cast<size_t>(rows16) * kHeadDim * 2;
     return PKV_OK;
 }
 
@@ -920,13 +1039,48 @@ int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
                    const uint16_t *v_new, const uint16_t *ik_new, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     if (once_per_device(attr_done, [] {
-            return cuda_rc(cudaFuncSetAttribute(prefill_partial,
+            const int rc = cuda_rc(cudaFuncSetAttribute(prefill_partial<false>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        static_cast<int>(kPSmem)));
+            if (rc != PKV_OK) return rc;
+            return cuda_rc(cudaFuncSetAttribute(prefill_partial<true>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 static_cast<int>(kPSmem)));
         }) != PKV_OK)
         return PKV_ECUDA;
-    PrefillArgs a{q, out, ws, k_new, v_new, ik_new};
-    cudaError_t e = launch_pdl(prefill_partial, plan.total_items, kPThreads, kPSmem, stream, c, maps, a);
+    PrefillArgs a{q, out, ws, k_new, v_new, ik_new, nullptr, -1, {}};
+    for (int s = 0; s < PKV_MAX_SEQS; ++s) a.v16_row[s] = -1;
+    // the fp16 V mode (chunks only: a decode call's new rows are not in
+    // their pages yet): rows at the end of the workspace, as planned
+    DecodeMaps m16 = maps;
+    int64_t rows16 = k_new == nullptr ? v16_rows(c) : 0;
+    const size_t bytes16 = static_cast<size_t>(rows16) * kHeadDim * 2;
+    if (plan.ws_bytes < bytes16) rows16 = 0;
+    for (int s = 0, r = 0; s < c.n_seqs && rows16 > 0; ++s)
+        if (c.seq[s].ncols > 0) {
+            a.v16_row[s] = r;
+            r += c.n_kv_heads * v16_stride(c.seq[s].len);
+        }
+    if (rows16 > 0) {
+        int n_maps = 0;
+        for (int s = 0; s < c.n_seqs; ++s)
+            n_maps = std::max(n_maps, std::max<int>(c.seq[s].tma, std::max<int>(c.seq[s].tma_k, c.seq[s].tma_v)) + 1);
+        a.v16 = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(ws) + (plan.ws_bytes - bytes16));
+        a.v16_map = row_map(m16, n_maps, a.v16, static_cast<uint64_t>(rows16), false, true, 64, 4);
+        if (a.v16_map < 0) rows16 = 0;  // no map to be had: bf16 V
+    }
+    if (rows16 == 0) {
+        a.v16 = nullptr;
+        a.v16_map = -1;
+        for (int s = 0; s < PKV_MAX_SEQS; ++s) a.v16_row[s] = -1;
+    } else {
+        cudaError_t e = launch_pdl(v16_gather, static_cast<unsigned>(rows16 / kV16RowsBlock), kV16Threads, 0,
+                                   stream, c, a);
+        if (e != cudaSuccess) return PKV_ECUDA;
+    }
+    cudaError_t e = rows16 > 0
+                        ? launch_pdl(prefill_partial<true>, plan.total_items, kPThreads, kPSmem, stream, c, m16, a)
+                        : launch_pdl(prefill_partial<false>, plan.total_items, kPThreads, kPSmem, stream, c, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;
     if (plan.total_comb > 0) return launch_combine(c, plan, q, out, ws, stream);
     return PKV_OK;

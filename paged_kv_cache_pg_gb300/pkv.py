@@ -17,7 +17,7 @@ from . import build as _build
 K, V, IK, P, KS, VS = 0, 1, 2, 3, 4, 5
 KV_BF16, KV_E4M3 = 0, 1
 OK, EINVAL, EAGAIN, ECUDA, EDEVICE = 0, 1, 2, 3, 4
-DEV_BAD_PAGE, DEV_TIMEOUT, DEV_SMEM = 1, 2, 4
+DEV_BAD_PAGE, DEV_TIMEOUT, DEV_SMEM, DEV_RANGE = 1, 2, 4, 8
 MAX_SEQS = 64
 _NAMES = {EINVAL: "PKV_EINVAL", EAGAIN: "PKV_EAGAIN", ECUDA: "PKV_ECUDA", EDEVICE: "PKV_EDEVICE"}
 

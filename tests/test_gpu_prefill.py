@@ -127,3 +127,63 @@ def test_pages_chunk_31000_plus_512_sampled():
         assert ok, (j, h, report)
     cont = place(lay, [s], None)
     assert np.array_equal(_prefill(cont, [T], [C], 0, 16, [q]).reshape(C, 16, 256), got)
+
+
+
+def _bf16_bits(x: float) -> int:
+    return int(np.array([x], np.float32).view(np.uint32)[0] >> 16)
+
+
+def _prefill_status(pl, lens, n_new, layer, hq, q_list):
+    t = torch()
+    seqs = pl.seqs(lens, n_new)
+    q = dev_u16(np.concatenate(q_list))
+    out = t.zeros_like(q)
+    ws = t.zeros(max(64, pkv.prefill_ws_size(pl.lay, seqs, hq) // 4 + 64), dtype=t.float32,
+                 device="cuda")
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    pkv.prefill(pl.lay, seqs, layer, hq, q, out, ws, status=status)
+    t.cuda.synchronize()
+    return host_u16(out), int(status.item())
+
+
+@pytest.mark.parametrize("ptok", [16, 48, 256, None, 20])
+def test_fp16_v_chunks_match_oracle_and_contiguous(ptok):
+    # chunks of more than 32 queries and at least 8 M-tiles a KV head in
+    # every stream: the PV product runs in fp16 on V rows converted once
+    lay = pkv.layout(2, 2, 256, 128)
+    lens = [460, 150]
+    n_new = [130, 150]          # 1,040 and 1,200 query columns a KV head
+    streams = [synth.make_stream(1900 + i, 2, T, 2, 256, 128) for i, T in enumerate(lens)]
+    q = [synth.queries(1910 + i, n, 16, 256) for i, n in enumerate(n_new)]
+    pl = place(lay, streams, ptok, seed=9) if ptok else place(lay, streams, None)
+    got = _prefill(pl, lens, n_new, 1, 16, q)
+    ok, report = within_tol(got, oracle_decode(pl, 1, 16, q))
+    assert ok, report
+    cont = place(lay, streams, None)
+    assert np.array_equal(_prefill(cont, lens, n_new, 1, 16, q), got)
+
+
+@pytest.mark.parametrize("big, n_new, reported", [(65280.0, 128, False), (131072.0, 128, True),
+                                                  (131072.0, 60, False)])
+def test_v_at_and_beyond_fp16_range(big, n_new, reported):
+    # A chunk of 128 queries (8 M-tiles a KV head) runs the PV product in
+    # fp16.  65,280 is the largest bf16 value fp16 holds exactly: the rows
+    # stay within tolerance and nothing is reported.  2^17 overflows fp16:
+    # the kernel reports a non-finite accumulator.  A chunk of 60 queries
+    # keeps bf16 V: 2^17 is an ordinary value there.
+    lay = pkv.layout(1, 2, 256, 128)
+    T = 400
+    s = synth.make_stream(1800, 1, T, 2, 256, 128)
+    v = s.v.copy()
+    v[0, 37, 1, 5] = _bf16_bits(big)
+    v[0, 350, 0, 200] = _bf16_bits(-big)
+    s = synth.Stream(T, s.k, v, s.ik)
+    q = synth.queries(1801, n_new, 16, 256)
+    pl = place(lay, [s], 48, seed=8)
+    got, st = _prefill_status(pl, [T], [n_new], 0, 16, [q])
+    assert bool(st & pkv.DEV_RANGE) == reported, st
+    assert st & ~pkv.DEV_RANGE == 0, st
+    if not reported:
+        ok, report = within_tol(got, oracle_decode(pl, 0, 16, [q]))
+        assert ok, report
