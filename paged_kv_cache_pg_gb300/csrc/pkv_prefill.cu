@@ -907,10 +907,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
 }
 
-// The fp16 V mode's rows: a warp a group of four rows (one KV head's key of
-// a stream each), a lane 16 bytes of a row; keys past the stream's length
-// are zeros.  A table entry outside [0, n_pages) is reported and read as
-// page 0, as the chunk kernel does.
+// The fp16 V mode's rows: a warp a group of four rows (consecutive keys of
+// one KV head of a stream), a lane 16 bytes of each, all four loads issued
+// before any store; keys past the stream's length are zeros.  The rows'
+// addresses (page lookups) come before the grid-dependency wait, their
+// loads after it.  A table entry outside [0, n_pages) is reported and read
+// as page 0, as the chunk kernel does.
 constexpr int kV16Threads = 256;
 constexpr int kV16RowsWarp = 4;
 constexpr int kV16RowsBlock = kV16Threads / 32 * kV16RowsWarp;
@@ -930,14 +932,23 @@ __global__ void __launch_bounds__(kV16Threads)
     const int local = row0 - a.v16_row[s];
     const int kvh = local / stride, key0 = local - kvh * stride;
     pdl_trigger();  // the chunk kernel waits for this grid before it reads the rows
-    pdl_wait();     // the rows were stored by an earlier kernel
+    const uint4 *src[kV16RowsWarp];
+#pragma unroll
+    for (int i = 0; i < kV16RowsWarp; ++i)
+        src[i] = key0 + i < sd.len
+                     ? reinterpret_cast<const uint4 *>(v_row(sd, c.n_kv_heads, kvh, key0 + i, c.status)) + lane
+                     : nullptr;
+    pdl_wait();  // the rows were stored by an earlier kernel
     uint4 v[kV16RowsWarp];
 #pragma unroll
     for (int i = 0; i < kV16RowsWarp; ++i) {
         v[i] = make_uint4(0, 0, 0, 0);
-        if (key0 + i < sd.len)
-            v[i] = __ldg(reinterpret_cast<const uint4 *>(v_row(sd, c.n_kv_heads, kvh, key0 + i, c.status)) + lane);
+        if (src[i])  // volatile: the loads stay ahead of the stores
+            asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
+                         : "l"(src[i]));
     }
+    asm volatile("" ::: "memory");
 #pragma unroll
     for (int i = 0; i < kV16RowsWarp; ++i) {
         const uint4 h = make_uint4(f16_of_bf16(v[i].x), f16_of_bf16(v[i].y), f16_of_bf16(v[i].z),
@@ -951,7 +962,8 @@ __global__ void __launch_bounds__(kV16Threads)
 // Work items: (KV head, M-tile, split) per stream, splits fastest.  A stream
 // is split only as far as filling the SMs needs, from its own shape alone.
 // Split model of plan_prefill, in hundredths of a microsecond.
-constexpr int64_t kTileCost = 220;   // a 128-key tile of one 128-row M-tile
+constexpr int64_t kTileCost = 220;   // a 128-key tile of one 128-row M-tile (bf16 V)
+constexpr int64_t kTileCost16 = 175; // the same in the fp16 V mode
 constexpr int64_t kCtaCost = 1200;   // a CTA's fixed cost
 constexpr int64_t kPartialCost = 4;  // a (unit, split) partial written and read back
 constexpr int kMaxPrefillSplits = 64;
@@ -960,6 +972,8 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
     int32_t items = 0, comb = 0;
     int64_t floats = 0;
     const int H = c.n_kv_heads;
+    for (int s = 0; s < c.n_seqs; ++s) c.seq[s].ncols = c.seq[s].n_new * c.group;
+    const int64_t tile_cost = v16_rows(c) > 0 ? kTileCost16 : kTileCost;
     for (int s = 0; s < c.n_seqs; ++s) {
         SeqDev &d = c.seq[s];
         d.work_off = 0;
@@ -976,13 +990,13 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         // grid on nsm SMs, waves x (tiles a CTA x a tile's time + a CTA's
         // fixed cost) + the split partials' round trip through HBM.  The
         // costs are this kernel's on GB300: about 2.2 us a 128-key tile of
-        // 128 rows, 12 us a CTA (Q into TMEM, pipeline fill, epilogue, the
-        // next CTA's entry) and 0.04 us a (unit, split) partial of 128 rows
-        // written and read back.  For 512 queries at 31,000 (64 units) it
-        // picks 2 splits, one wave of 128 CTAs (296 us; 7 splits, three
-        // nearly full waves, measured the same, 3-6 and 8-19 splits 310-395
-        // us).  For 2,048 queries at 16,384 (256 units) it picks 1 split, 2
-        // waves.
+        // 128 rows (1.75 us in the fp16 V mode), 12 us a CTA (Q into TMEM,
+        // pipeline fill, epilogue, the next CTA's entry) and 0.04 us a
+        // (unit, split) partial of 128 rows written and read back.  For 512
+        // queries at 31,000 (64 units) it picks 2 splits, one wave of 128
+        // CTAs (bf16 V: 296 us; 7 splits, three nearly full waves, measured
+        // the same, 3-6 and 8-19 splits 310-395 us).  For 2,048 queries at
+        // 16,384 (256 units) it picks 1 split, 2 waves.
         // Only the stream's own length and rows and the SM count enter, so
         // paged and contiguous caches get the same splits.
         const int64_t units = (int64_t)H * mtiles, tiles = (d.len + kN - 1) / kN;
@@ -991,7 +1005,7 @@ int plan_prefill(Common &c, int nsm, DecodePlan *plan) {
         int64_t best = INT64_MAX;
         for (int n = 1; n <= max_ns; ++n) {
             const int64_t waves = (units * n + nsm - 1) / nsm;
-            const int64_t cost = waves * (((tiles + n - 1) / n) * kTileCost + kCtaCost) +
+            const int64_t cost = waves * (((tiles + n - 1) / n) * tile_cost + kCtaCost) +
                                  (n > 1 ? n * units * kPartialCost : 0);
             if (cost < best) {
                 best = cost;
