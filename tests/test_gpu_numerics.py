@@ -36,7 +36,7 @@ from gpu_setup import decode, dev_u16, host_u16, oracle_decode, place, torch, wi
 pytestmark = pytest.mark.gpu
 
 LOG2E = 1.4426950408889634
-TILE = 32          # keys a prefill S tile
+TILE = 128         # keys a prefill S tile (the chunk kernel's 128-key tiles)
 RESCALE = 8.0      # log2 units of growth before the prefill rescales O
 
 
@@ -150,9 +150,12 @@ def test_prefill_mid_chunk_every_row_several_splits_and_mtiles(qscale):
     q = synth.scale_pow2(synth.queries(4300 + qscale, C, 16, 256), qscale)
     pl = place(lay, [s], 48, seed=12)
     got, ws_bytes = _prefill(pl, [T], [C], 0, 16, [q])
-    # partials of several splits: 2 heads x ns x 2,048 columns x (256 + 2) floats
-    ns = ws_bytes // 4 // (2 * C * 8 * 258)
-    assert ns >= 2, ws_bytes
+    # a 256-query chunk takes the fp16 V mode: the workspace holds the V rows
+    # in fp16 (2 heads x T rounded up to 128 x 512 B) after the partials of
+    # several splits (2 heads x ns x 2,048 columns x (256 + 2) floats)
+    v16 = 2 * (-(-T // TILE) * TILE) * 256 * 2
+    ns = (ws_bytes - v16) // 4 // (2 * C * 8 * 258)
+    assert ns >= 2 and v16 + ns * 2 * C * 8 * 258 * 4 == ws_bytes, ws_bytes
     ok, report = within_tol(got, oracle_decode(pl, 0, 16, [q]))
     assert ok, report
     cont = place(lay, [s], None)
@@ -161,6 +164,7 @@ def test_prefill_mid_chunk_every_row_several_splits_and_mtiles(qscale):
         # the split lengths the plan can have used for ns splits
         lens_ok = {-(-(-(-T // n)) // TILE) * TILE for n in range(1, 65)}
         lens_ok = [sl for sl in lens_ok if -(-T // sl) == ns]
+        assert lens_ok, ns
         lg = _logits_log2(s, 0, q, P0, 8)
         for sl in lens_ok:
             assert _rescale_rows(lg, sl) > 0, sl
