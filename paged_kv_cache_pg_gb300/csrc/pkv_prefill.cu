@@ -1080,6 +1080,9 @@ int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
         for (int s = 0; s < c.n_seqs; ++s)
             n_maps = std::max(n_maps, std::max<int>(c.seq[s].tma, std::max<int>(c.seq[s].tma_k, c.seq[s].tma_v)) + 1);
         a.v16 = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(ws) + (plan.ws_bytes - bytes16));
+        // the V slots' tile view (boxes of {64, 64, 4}) over the fp16 rows:
+        // the map's element type is bf16, and a TMA copy moves the 2-byte
+        // elements' bits unchanged, so fp16 rows come through as they are
         a.v16_map = row_map(m16, n_maps, a.v16, static_cast<uint64_t>(rows16), false, true, 64, 4);
         if (a.v16_map < 0) rows16 = 0;  // no map to be had: bf16 V
     }
