@@ -12,10 +12,11 @@
 // a 128-key S product takes the instructions a 64-key one did.  Q sits in
 // TMEM (columns 0-127, bf16 pairs) and is the S product's A operand there;
 // that leaves shared memory for P (hi and lo, 64 KB) and one ring of five
-// 32 KB slots: a K slot holds the tile's keys over 128 of the dims, a V slot
-// 64 of its keys over all dims.  The softmax takes two threads a row (TMEM
-// lane), each on 64 of the tile's keys and 128 of O's columns; the pair
-// agrees on the row maximum through shared memory.  S has one TMEM buffer:
+// 32 KB slots (P in fp16, 32 KB, and six slots in the fp16 V mode): a K slot
+// holds the tile's keys over 128 of the dims, a V slot 64 of its keys over
+// all dims.  The softmax takes two threads a row (TMEM lane), each on 64 of
+// the tile's keys and 128 of O's columns; the pair agrees on the row maximum
+// through shared memory.  S has one TMEM buffer:
 // the next S product starts once the softmax threads have read S, and P has
 // one buffer, which the softmax fills once the previous tile's PV product is
 // done.
@@ -55,22 +56,32 @@ constexpr int kVRegion = 64 * 128;   // one 64-dim region of 64 V rows
 constexpr int kSlotBytes = 2 * kKRegion;  // a K slot (the tile's keys over 128 dims) or
                                           // a V slot (64 of its keys over 256 dims)
 static_assert(kSlotBytes == 4 * kVRegion, "K and V slots share one ring");
-constexpr int kSlots = 5;            // the ring, taken in the MMAs' order
 constexpr int kPRegion = kM * 128;   // 64 keys of the 128 P rows
-constexpr int kPPart = 2 * kPRegion; // P hi (or lo): the tile's 128 keys
-constexpr int kOffP = 0;             // P hi, then P lo
-constexpr int kOffRing = kOffP + 2 * kPPart;
-constexpr int kOffRed = kOffRing + kSlots * kSlotBytes;  // [tile parity][half][row] floats
-constexpr int kOffBar = kOffRed + 2 * 2 * kM * 4;
-// barriers: a pair for each ring slot, one for each single buffer
-constexpr int kBarFull = 0, kBarEmpty = kSlots;
-constexpr int kBarSFull = 2 * kSlots, kBarSEmpty = kBarSFull + 1, kBarPFull = kBarSFull + 2;
-constexpr int kBarODone = kBarSFull + 3, kBarQFull = kBarSFull + 4, kBarRed = kBarSFull + 5;
-constexpr int kNumBars = kBarRed + 1;
-// no alignment slack: the dynamic shared memory is declared 1024-byte aligned
-// (checked at entry), and five slots leave no room for it
-constexpr size_t kPSmem = kOffBar + kNumBars * 8 + 16;
-static_assert(kPSmem <= 232448, "prefill shared memory above the 227 KB a CTA may hold");
+constexpr int kPPart = 2 * kPRegion; // P (or its hi or lo part): the tile's 128 keys
+constexpr int kOffP = 0;             // P, or P hi then P lo
+
+// Shared-memory layout of each V mode: P, the ring (taken in the MMAs'
+// order), the row-maximum exchange, the barriers.  The fp16 V mode's P is
+// one part, and the 32 KB the lo part takes in the bf16 mode is a sixth
+// ring slot: a slot is refilled six places after it was taken, which
+// covers the about 2 us a slot's copy takes to land at the fp16 mode's
+// pace (five slots left the MMA thread waiting about 0.3 us a tile).
+template <bool kV16>
+struct PLayout {
+    static constexpr int slots = kV16 ? 6 : 5;
+    static constexpr int off_ring = kOffP + (kV16 ? 1 : 2) * kPPart;
+    static constexpr int off_red = off_ring + slots * kSlotBytes;  // [tile parity][half][row] floats
+    static constexpr int off_bar = off_red + 2 * 2 * kM * 4;
+    // barriers: a pair for each ring slot, one for each single buffer
+    static constexpr int bar_full = 0, bar_empty = slots;
+    static constexpr int bar_sfull = 2 * slots, bar_sempty = bar_sfull + 1, bar_pfull = bar_sfull + 2;
+    static constexpr int bar_odone = bar_sfull + 3, bar_qfull = bar_sfull + 4, bar_red = bar_sfull + 5;
+    static constexpr int num_bars = bar_red + 1;
+    // no alignment slack: the dynamic shared memory is declared 1024-byte
+    // aligned (checked at entry), and the ring leaves no room for it
+    static constexpr size_t smem = off_bar + num_bars * 8 + 16;
+    static_assert(smem <= 232448, "prefill shared memory above the 227 KB a CTA may hold");
+};
 constexpr float kScaleLog2 = 0.0625f * 1.4426950408889634f;  // log2(e) / sqrt(256)
 constexpr float kRescale = 8.f;  // rescale O when the max grows by more than 2^8
 
@@ -227,8 +238,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // the 128-byte swizzle of the TMA copies and the MMA operands repeats
     // every 1024 bytes from a 1024-byte boundary
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    using L = PLayout<kV16>;
+    constexpr int kSlots = L::slots, kOffRing = L::off_ring, kOffRed = L::off_red;
+    constexpr int kBarFull = L::bar_full, kBarEmpty = L::bar_empty, kBarSFull = L::bar_sfull;
+    constexpr int kBarSEmpty = L::bar_sempty, kBarPFull = L::bar_pfull, kBarODone = L::bar_odone;
+    constexpr int kBarQFull = L::bar_qfull, kBarRed = L::bar_red;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::num_bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -535,8 +551,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // 64-127 (the PV product of the tile before), and last V(ntiles-1).
         // Each producer takes one half (warps 8 and 10 the first, 11 and 12
         // the second) and knows its slots' places in that order, so the four
-        // fill the ring side by side; a slot is refilled five places after it
-        // was taken.
+        // fill the ring side by side; a slot is refilled five (bf16 V) or six
+        // (fp16 V) places after it was taken.
         pdl_wait();  // the chunk's rows are stored by the previous kernel
         const bool is_v = warp == 10 || warp == 12;
         const int hh = warp >= 11;  // which half of the tile's dims (K) or keys (V)
@@ -1055,11 +1071,11 @@ int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
     if (once_per_device(attr_done, [] {
             const int rc = cuda_rc(cudaFuncSetAttribute(prefill_partial<false>,
                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                        static_cast<int>(kPSmem)));
+                                                        static_cast<int>(PLayout<false>::smem)));
             if (rc != PKV_OK) return rc;
             return cuda_rc(cudaFuncSetAttribute(prefill_partial<true>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                static_cast<int>(kPSmem)));
+                                                static_cast<int>(PLayout<true>::smem)));
         }) != PKV_OK)
         return PKV_ECUDA;
     PrefillArgs a{q, out, ws, k_new, v_new, ik_new, nullptr, -1, {}};
@@ -1096,8 +1112,10 @@ int launch_prefill(const Common &c, const DecodePlan &plan, const DecodeMaps &ma
         if (e != cudaSuccess) return PKV_ECUDA;
     }
     cudaError_t e = rows16 > 0
-                        ? launch_pdl(prefill_partial<true>, plan.total_items, kPThreads, kPSmem, stream, c, m16, a)
-                        : launch_pdl(prefill_partial<false>, plan.total_items, kPThreads, kPSmem, stream, c, maps, a);
+                        ? launch_pdl(prefill_partial<true>, plan.total_items, kPThreads, PLayout<true>::smem,
+                                     stream, c, m16, a)
+                        : launch_pdl(prefill_partial<false>, plan.total_items, kPThreads, PLayout<false>::smem,
+                                     stream, c, maps, a);
     if (e != cudaSuccess) return PKV_ECUDA;
     if (plan.total_comb > 0) return launch_combine(c, plan, q, out, ws, stream);
     return PKV_OK;
