@@ -42,6 +42,26 @@ def test_library_exports_every_declared_function(lib):
     assert set(pkv.EXPORTS) <= declared
 
 
+def test_binding_constants_match_the_header():
+    """Every numeric #define of include/pkv.h that the binding mirrors has
+    the header's value there (status codes, device status bits, row kinds,
+    formats)."""
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "pkv.h")).read()
+    defs = {m.group(1): int(m.group(2))
+            for m in re.finditer(r"^#define PKV_(\w+) (\d+)u?\b", hdr, re.M)}
+    mirrored = {"OK": pkv.OK, "EINVAL": pkv.EINVAL, "EAGAIN": pkv.EAGAIN, "ECUDA": pkv.ECUDA,
+                "EDEVICE": pkv.EDEVICE, "DEV_BAD_PAGE": pkv.DEV_BAD_PAGE,
+                "DEV_TIMEOUT": pkv.DEV_TIMEOUT, "DEV_SMEM": pkv.DEV_SMEM, "DEV_RANGE": pkv.DEV_RANGE,
+                "K": pkv.K, "V": pkv.V, "IK": pkv.IK, "P": pkv.P, "KS": pkv.KS, "VS": pkv.VS,
+                "KV_BF16": pkv.KV_BF16, "KV_E4M3": pkv.KV_E4M3}
+    for name, value in mirrored.items():
+        assert defs.get(name) == value, (name, defs.get(name), value)
+    # the device status bits are distinct single bits
+    bits = [defs[n] for n in defs if n.startswith("DEV_")]
+    assert len(bits) == 4 and all(b and b & (b - 1) == 0 for b in bits) and len(set(bits)) == 4
+
+
 def test_page_elems_match_oracle(lib, orc):
     for hkv, di, ptok in [(2, 128, 256), (1, 128, 16), (4, 0, 48), (2, 128, 4)]:
         lay = pkv.layout(13, hkv, 256, di)
