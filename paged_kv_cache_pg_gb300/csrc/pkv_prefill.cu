@@ -923,14 +923,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
 }
 
-// The fp16 V mode's rows: a warp a group of four rows (consecutive keys of
-// one KV head of a stream), a lane 16 bytes of each, all four loads issued
-// before any store; keys past the stream's length are zeros.  The rows'
-// addresses (page lookups) come before the grid-dependency wait, their
-// loads after it.  A table entry outside [0, n_pages) is reported and read
-// as page 0, as the chunk kernel does.
-constexpr int kV16Threads = 256;
-constexpr int kV16RowsWarp = 4;
+// The fp16 V mode's rows: a warp a run of 16 consecutive keys of one KV
+// head of a stream, a lane 16 bytes of each row, the 16 loads issued before
+// any store.  A run inside one page (pages of a multiple of 16 positions, or
+// a contiguous stream) takes one page lookup, any other run one a row; keys
+// past the stream's length are zeros.  The lookups come before the
+// grid-dependency wait, the loads after it.  A table entry outside
+// [0, n_pages) is reported and read as page 0, as the chunk kernel does.
+constexpr int kV16Threads = 128;
+constexpr int kV16RowsWarp = 16;
 constexpr int kV16RowsBlock = kV16Threads / 32 * kV16RowsWarp;
 static_assert(kN % kV16RowsBlock == 0, "a stream's rows fill whole blocks");
 
@@ -948,12 +949,21 @@ __global__ void __launch_bounds__(kV16Threads)
     const int local = row0 - a.v16_row[s];
     const int kvh = local / stride, key0 = local - kvh * stride;
     pdl_trigger();  // the chunk kernel waits for this grid before it reads the rows
+    const int n = min(kV16RowsWarp, sd.len - key0);  // rows with data (<= 0: none)
+    const bool one = sd.table == nullptr || sd.ptok % kV16RowsWarp == 0;
     const uint4 *src[kV16RowsWarp];
+    if (one) {
+        // consecutive positions of one head in a page are consecutive rows
+        const uint4 *r0 = n > 0 ? reinterpret_cast<const uint4 *>(v_row(sd, c.n_kv_heads, kvh, key0, c.status)) + lane
+                                : nullptr;
 #pragma unroll
-    for (int i = 0; i < kV16RowsWarp; ++i)
-        src[i] = key0 + i < sd.len
-                     ? reinterpret_cast<const uint4 *>(v_row(sd, c.n_kv_heads, kvh, key0 + i, c.status)) + lane
-                     : nullptr;
+        for (int i = 0; i < kV16RowsWarp; ++i) src[i] = i < n ? r0 + i * (kHeadDim / 8) : nullptr;
+    } else {
+#pragma unroll
+        for (int i = 0; i < kV16RowsWarp; ++i)
+            src[i] = i < n ? reinterpret_cast<const uint4 *>(v_row(sd, c.n_kv_heads, kvh, key0 + i, c.status)) + lane
+                           : nullptr;
+    }
     pdl_wait();  // the rows were stored by an earlier kernel
     uint4 v[kV16RowsWarp];
 #pragma unroll
@@ -965,10 +975,18 @@ __global__ void __launch_bounds__(kV16Threads)
                          : "l"(src[i]));
     }
     asm volatile("" ::: "memory");
+    // volatile too, so that no conversion (and the wait for its row) is
+    // placed between the loads
+    auto cvt = [](uint32_t w) {
+        uint32_t h;
+        asm volatile("cvt.rn.f16x2.f32 %0, %1, %2;"
+                     : "=r"(h)
+                     : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+        return h;
+    };
 #pragma unroll
     for (int i = 0; i < kV16RowsWarp; ++i) {
-        const uint4 h = make_uint4(f16_of_bf16(v[i].x), f16_of_bf16(v[i].y), f16_of_bf16(v[i].z),
-                                   f16_of_bf16(v[i].w));
+        const uint4 h = make_uint4(cvt(v[i].x), cvt(v[i].y), cvt(v[i].z), cvt(v[i].w));
         reinterpret_cast<uint4 *>(a.v16 + (int64_t)(row0 + i) * kHeadDim)[lane] = h;
     }
 }
