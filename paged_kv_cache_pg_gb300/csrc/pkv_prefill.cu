@@ -16,13 +16,14 @@
 // holds the tile's keys over 128 of the dims, a V slot 64 of its keys over
 // all dims.  The softmax takes two threads a row (TMEM lane), each on 64 of
 // the tile's keys and 128 of O's columns; the pair agrees on the row maximum
-// through shared memory.  S has one TMEM buffer:
-// the next S product starts once the softmax threads have read S, and P has
-// one buffer, which the softmax fills once the previous tile's PV product is
-// done.
+// through shared memory.  S has one TMEM buffer: the next S product starts
+// once the softmax threads have read S, and P has one buffer, which the
+// softmax fills once the previous tile's PV product is done.
 // Four producer warps, one for each slot kind (K over the first or second
 // dims, V over the first or second keys), fill the ring in the order the
-// MMAs take the slots, looking a tile's rows up before its slots are free: a
+// MMAs take the slots.  In the fp16 V mode a V slot is one 3D copy of the
+// converted rows (contiguous: no page lookups).  Otherwise the producers
+// look a tile's rows up before its slots are free: a
 // cached tile inside one page needs one page lookup and comes by one 3D TMA
 // copy a slot (pages of a multiple of 128 positions), a cached tile in pages
 // of a multiple of 16 needs its eight 16-row run starts and comes by 2D
