@@ -271,11 +271,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const SeqDev &sd = c.seq[s];
     const int mtiles = (sd.ncols + kM - 1) / kM;
     // consecutive CTAs share a (KV head, split): the M-tiles that read the
-    // same key range run in the same wave and find its tiles in L2
+    // same key range run in the same wave and find its tiles in L2.  The
+    // M-tiles with the most keys (the last ones of a causal chunk) come
+    // first, so that in a grid of several waves the SMs freed first take the
+    // shortest CTAs of the last one (the serving mix's 2,048-query lane, 256
+    // CTAs: 488 us against 506 in ascending order).  The order changes which
+    // SM runs a CTA, never its result.
     const int item = blockIdx.x - sd.work_off;
     const int kvh = item / (mtiles * sd.nsplit);
     const int split = (item / mtiles) % sd.nsplit;
-    const int mt = item % mtiles;
+    const int mt = mtiles - 1 - item % mtiles;
     const int col0 = mt * kM;
     const int rows = min(kM, sd.ncols - col0);
     const int qbase = sd.len - sd.n_new;
