@@ -187,3 +187,22 @@ def test_v_at_and_beyond_fp16_range(big, n_new, reported):
     if not reported:
         ok, report = within_tol(got, oracle_decode(pl, 0, 16, [q]))
         assert ok, report
+
+
+def test_fp16_v_mode_starts_at_eight_m_tiles():
+    # 250 positions: one split, so the workspace holds no partials, only the
+    # fp16 V mode's converted rows (2 KV heads x 256 padded keys x 512 B).
+    # 113 queries are 904 query columns a KV head (8 M-tiles): the mode
+    # applies; 112 are 896 (7 M-tiles): bf16 V, no workspace.  Both match
+    # the oracle.
+    lay = pkv.layout(1, 2, 256, 128)
+    T = 250
+    s = synth.make_stream(2000, 1, T, 2, 256, 128)
+    pl = place(lay, [s], 48, seed=10)
+    assert pkv.prefill_ws_size(pl.lay, pl.seqs([T], [113]), 16) == 2 * 256 * 512
+    assert pkv.prefill_ws_size(pl.lay, pl.seqs([T], [112]), 16) == 0
+    for n in (112, 113):
+        q = synth.queries(2001, n, 16, 256)
+        got = _prefill(pl, [T], [n], 0, 16, [q])
+        ok, report = within_tol(got, oracle_decode(pl, 0, 16, [q]))
+        assert ok, (n, report)
